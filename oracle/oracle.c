@@ -1,0 +1,172 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for the wide-row reduce-then-reuse
+ * operators (row softmax, LayerNorm, RMSNorm).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: it is used by the tests, by the package smoke check and by
+ * the CPU-baseline leg of the benchmark.  It shares no code, header, constant
+ * or helper with the CUDA library.
+ *
+ * Source of the operators.  The CREDIT summary page ("CREDIT: Cost-guided
+ * Reduction-reuse with Efficient DSMEM Inter-CTA Tiling", arXiv 2609.01864v1),
+ * section "B. Reduction-Reuse Transformation", models a row as per-element
+ * inputs that feed scalar reductions, after which an elementwise function h
+ * produces every output element.  The clustered transformation (section
+ * "C. Cluster Reduction and Reuse Protocol") only changes where the partial
+ * statistics live; the outputs are those of the plain definitions below
+ * ("D. Traffic Validation": output traffic and h are unchanged).  So the
+ * oracle is the textbook definition of each operator, written out row by
+ * row, two passes per statistic, every sum in fp64 in column order:
+ *
+ *   softmax   m = max_j x_j,  s = sum_j exp(x_j - m),  y_j = exp(x_j - m) / s
+ *   LayerNorm mu = sum_j x_j / N,  var = sum_j (x_j - mu)^2 / N   (biased)
+ *             y_j = (x_j - mu) / sqrt(var + eps) * gamma_j + beta_j
+ *   RMSNorm   ms = sum_j x_j^2 / N,  y_j = x_j / sqrt(ms + eps) * w_j
+ *
+ * gamma / beta / w absent (NULL) mean gamma = 1, beta = 0, w = 1.
+ *
+ * Readings where the pages are silent: the variance is biased (divide by N)
+ * and eps sits inside the square root for both norms; RMSNorm is not on the
+ * pages and follows the usual definition above.
+ *
+ * Inputs are the exact bytes the GPU receives: dtype 0 = fp32, 1 = bf16
+ * (raw 16-bit patterns), 2 = fp64.  Every widening to double is exact.
+ * Outputs are fp64; no rounding to the GPU's output type happens here.
+ *
+ * Build: gcc -O2 -fPIC -shared (no -ffast-math: the order and rounding of
+ * every operation is the one written).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define OR_F32 0
+#define OR_BF16 1
+#define OR_F64 2
+
+#define OR_OK 0
+#define OR_BAD_ARG 1
+
+/* Widen element i of a typed buffer to double.  bf16 is the upper half of an
+ * IEEE-754 binary32 word, so its value is that word with 16 zero low bits. */
+static double or_load(const void *p, int dtype, int64_t i)
+{
+    if (dtype == OR_F32) {
+        float f;
+        memcpy(&f, (const unsigned char *)p + 4 * i, 4);
+        return (double)f;
+    }
+    if (dtype == OR_BF16) {
+        uint16_t h;
+        uint32_t u;
+        float f;
+        memcpy(&h, (const unsigned char *)p + 2 * i, 2);
+        u = ((uint32_t)h) << 16;
+        memcpy(&f, &u, 4);
+        return (double)f;
+    }
+    {
+        double d;
+        memcpy(&d, (const unsigned char *)p + 8 * i, 8);
+        return d;
+    }
+}
+
+static int or_dtype_ok(int dtype)
+{
+    return dtype == OR_F32 || dtype == OR_BF16 || dtype == OR_F64;
+}
+
+/* Decode n elements of a typed buffer into doubles (used by the tests to read
+ * back bf16 / fp32 bytes through the same widening the oracle uses). */
+int oracle_widen(const void *x, int dtype, int64_t n, double *out)
+{
+    int64_t i;
+    if (!x || !out || n < 0 || !or_dtype_ok(dtype))
+        return OR_BAD_ARG;
+    for (i = 0; i < n; ++i)
+        out[i] = or_load(x, dtype, i);
+    return OR_OK;
+}
+
+/* Row softmax over `rows` rows of `cols` contiguous elements. */
+int oracle_softmax(const void *x, int dtype, int64_t rows, int64_t cols,
+                   double *y)
+{
+    int64_t r, j;
+    if (!x || !y || rows < 0 || cols <= 0 || !or_dtype_ok(dtype))
+        return OR_BAD_ARG;
+    for (r = 0; r < rows; ++r) {
+        int64_t base = r * cols;
+        double m = -INFINITY, s = 0.0;
+        for (j = 0; j < cols; ++j) {
+            double v = or_load(x, dtype, base + j);
+            if (v > m)
+                m = v;
+        }
+        for (j = 0; j < cols; ++j)
+            s += exp(or_load(x, dtype, base + j) - m);
+        for (j = 0; j < cols; ++j)
+            y[base + j] = exp(or_load(x, dtype, base + j) - m) / s;
+    }
+    return OR_OK;
+}
+
+/* Row LayerNorm.  gamma / beta: length-cols vectors of dtype pdtype, or NULL.
+ * If z is not NULL it receives the normalised value (x - mu)/sqrt(var + eps)
+ * before the affine step (the tests use it to size the cancellation bound). */
+int oracle_layernorm(const void *x, int dtype, int64_t rows, int64_t cols,
+                     const void *gamma, const void *beta, int pdtype,
+                     double eps, double *y, double *z)
+{
+    int64_t r, j;
+    if (!x || !y || rows < 0 || cols <= 0 || !or_dtype_ok(dtype) ||
+        ((gamma || beta) && !or_dtype_ok(pdtype)) || !(eps >= 0.0))
+        return OR_BAD_ARG;
+    for (r = 0; r < rows; ++r) {
+        int64_t base = r * cols;
+        double sum = 0.0, ssd = 0.0, mu, var, inv;
+        for (j = 0; j < cols; ++j)
+            sum += or_load(x, dtype, base + j);
+        mu = sum / (double)cols;
+        for (j = 0; j < cols; ++j) {
+            double d = or_load(x, dtype, base + j) - mu;
+            ssd += d * d;
+        }
+        var = ssd / (double)cols;
+        inv = 1.0 / sqrt(var + eps);
+        for (j = 0; j < cols; ++j) {
+            double zj = (or_load(x, dtype, base + j) - mu) * inv;
+            double g = gamma ? or_load(gamma, pdtype, j) : 1.0;
+            double b = beta ? or_load(beta, pdtype, j) : 0.0;
+            if (z)
+                z[base + j] = zj;
+            y[base + j] = zj * g + b;
+        }
+    }
+    return OR_OK;
+}
+
+/* Row RMSNorm.  w: length-cols vector of dtype pdtype, or NULL. */
+int oracle_rmsnorm(const void *x, int dtype, int64_t rows, int64_t cols,
+                   const void *w, int pdtype, double eps, double *y)
+{
+    int64_t r, j;
+    if (!x || !y || rows < 0 || cols <= 0 || !or_dtype_ok(dtype) ||
+        (w && !or_dtype_ok(pdtype)) || !(eps >= 0.0))
+        return OR_BAD_ARG;
+    for (r = 0; r < rows; ++r) {
+        int64_t base = r * cols;
+        double ss = 0.0, inv;
+        for (j = 0; j < cols; ++j) {
+            double v = or_load(x, dtype, base + j);
+            ss += v * v;
+        }
+        inv = 1.0 / sqrt(ss / (double)cols + eps);
+        for (j = 0; j < cols; ++j) {
+            double g = w ? or_load(w, pdtype, j) : 1.0;
+            y[base + j] = or_load(x, dtype, base + j) * inv * g;
+        }
+    }
+    return OR_OK;
+}
