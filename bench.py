@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark of the clustered DSMEM reduce-reuse path on one GB300.
+
+A step is one library call over the whole workload: bf16 LayerNorm with fp32
+gamma/beta, 1024 rows x 262144 columns (512 KiB per row), eps 1e-5, x drawn
+from N(0.5, 2) with seed 1.  `value` is the algorithmic HBM rate of the timed
+steps: one read plus one write of the matrix, gamma/beta once, divided by the
+device time per step (CUDA events on the launching stream).  The input (512
+MiB) is larger than the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints ONE JSON line.  Under torchrun (N > 1) every rank runs its own replica
+of the workload on its own GPU (rows are independent: weak scaling, no
+collective on the data path); the time is the max over ranks.
+`--impl reference` times the fp64 CPU oracle on this host's cores instead.
+Other workloads (`--workload`) and forced plans (`--variant`) are for local
+studies; the default is the headline line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "wide-row reduce-reuse HBM GB/s and % of GB300 peak; DRAM bytes vs 1R+1W ideal"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _workloads():
+    from dsmem_thread_block_gb300 import workloads as wl
+    table = {w.name: w for w in wl.ALL}
+    for c in wl.SWEEP_COLS:
+        w = wl.sweep_point(c)
+        table[w.name] = w
+    return wl, table
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dsmem_thread_block_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str, variant_key: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None if the
+    kernels changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    e = d.get("entries", {}).get(f"{workload}|{variant_key}")
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi SM clock and throttle-reason samples, host-timestamped."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str | None, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        self.error = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", str(period_ms)]
+        if device_id:
+            cmd += ["-i", device_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception as e:  # no nvidia-smi
+            self.error = str(e)
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if self.error or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": self.error or "no samples"}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        note = "sampled during the timed region"
+        if not inside:  # timed region shorter than the sampling period
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:2]
+            note = "nearest samples to a short timed region"
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for _, p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for _, p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in inside for i in range(4)
+                          if p[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "note": note}
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_oracle_rate(w, inputs, rows: int, threads: int):
+    """Time the oracle (as it stands) over the first `rows` rows; return
+    (GB/s of algorithmic bytes, seconds)."""
+    import oracle
+    sub = dict(inputs)
+    sub["x"] = inputs["x"][:rows]
+    t0 = time.perf_counter()
+    if w.op == "softmax":
+        oracle.run_rows(oracle.softmax, sub["x"], threads=threads)
+    elif w.op == "layernorm":
+        oracle.run_rows(oracle.layernorm, sub["x"], sub.get("gamma"), sub.get("beta"),
+                        threads=threads, eps=w.eps)
+    else:
+        oracle.run_rows(oracle.rmsnorm, sub["x"], sub.get("weight"), threads=threads, eps=w.eps)
+    dt = time.perf_counter() - t0
+    return w.with_rows(rows).ideal_bytes() / dt / 1e9, dt
+
+
+def cpu_sample_rows(w, inputs, threads: int, budget_s: float) -> int:
+    """Rows of the workload the oracle finishes in about `budget_s`."""
+    _, dt1 = cpu_oracle_rate(w, inputs, min(threads, w.rows), threads)
+    per_row = dt1 / min(threads, w.rows) * 1.0
+    return int(max(1, min(w.rows, budget_s / max(per_row, 1e-9))))
+
+
+def run_reference(args, w, rank: int):
+    """--impl reference: the fp64 oracle on the host cores, same metric."""
+    if rank != 0:
+        return
+    cores = len(os.sched_getaffinity(0))
+    inputs = w.generate()
+    total_budget = 90.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    rows = cpu_sample_rows(w, inputs, cores, per_step)
+    for _ in range(args.warmup):
+        cpu_oracle_rate(w, inputs, rows, cores)
+    times = [cpu_oracle_rate(w, inputs, rows, cores)[1] for _ in range(args.steps)]
+    tot = sum(times)
+    value = w.with_rows(rows).ideal_bytes() * len(times) / tot / 1e9
+    sample = f"first {rows} of {w.rows} rows per step (full width {w.cols})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="layernorm_bf16_1024x262144")
+    ap.add_argument("--variant", default="auto", help="auto | cluster:P | two_pass")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-budget", type=float, default=20.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    wl, table = _workloads()
+    w = table[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from dsmem_thread_block_gb300 import _credit as C
+
+    torch.cuda.set_device(local)
+    dev = torch.cuda.current_device()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    C.load(build_if_missing=True)
+
+    inputs = w.generate()
+    DT = {"f32": C.F32, "bf16": C.BF16}
+    OPS = {"softmax": C.SOFTMAX, "layernorm": C.LAYERNORM, "rmsnorm": C.RMSNORM}
+
+    def to_device(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to("cuda")
+        return torch.from_numpy(a).to("cuda")
+    dx = to_device(inputs["x"])
+    dy = torch.empty_like(dx)
+    params = {k: to_device(v) for k, v in inputs.items() if k != "x"}
+
+    if args.variant == "auto":
+        plan = C.credit_plan(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev)
+    elif args.variant == "two_pass":
+        plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.TWO_PASS, 1)
+    else:
+        P = int(args.variant.split(":")[1])
+        plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.CLUSTER, P)
+    ws = None
+    if plan.workspace_bytes:
+        ws = torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=dx.device)
+    wptr, wbytes = (ws.data_ptr(), int(plan.workspace_bytes)) if ws is not None else (0, 0)
+    stream = torch.cuda.Stream()
+    sptr = stream.cuda_stream
+    pdt = DT[w.param_dtype] if w.param_dtype else C.F32
+    lib = C.load()
+    pp = C._plan_ptr(plan)
+
+    def launch(xp, yp):
+        if w.op == "softmax":
+            return lib.credit_softmax(xp, yp, w.rows, w.cols, DT[w.dtype], pp, wptr or None,
+                                      wbytes, sptr)
+        if w.op == "layernorm":
+            g, b = params.get("gamma"), params.get("beta")
+            return lib.credit_layernorm(xp, yp, w.rows, w.cols, DT[w.dtype],
+                                        g.data_ptr() if g is not None else None,
+                                        b.data_ptr() if b is not None else None, pdt, w.eps,
+                                        pp, wptr or None, wbytes, sptr)
+        wt = params.get("weight")
+        return lib.credit_rmsnorm(xp, yp, w.rows, w.cols, DT[w.dtype],
+                                  wt.data_ptr() if wt is not None else None, pdt, w.eps, pp,
+                                  wptr or None, wbytes, sptr)
+
+    xp, yp = dx.data_ptr(), dy.data_ptr()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            st = launch(xp, yp)
+            if st != C.OK:
+                raise C.CreditError(st, "warmup launch")
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)  # let the sampler start before the timed region
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        launch(xp, yp)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    time.sleep(0.1)
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+    assert C.credit_get_device_error(dev) == C.OK
+
+    t = torch.tensor([ms_total], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    bytes_step = w.ideal_bytes()
+    value = bytes_step * world / (ms_step * 1e-3) / 1e9
+
+    # ---- end to end: pinned host buffers, H2D + call + D2H every step
+    hx = torch.empty(dx.shape, dtype=dx.dtype, pin_memory=True)
+    hx.copy_(dx)
+    hparams = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v)
+               for k, v in params.items()}
+    hy = torch.empty(dy.shape, dtype=dy.dtype, pin_memory=True)
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    h2d = hx.numel() * hx.element_size() + sum(v.numel() * v.element_size()
+                                               for v in hparams.values())
+    d2h = hy.numel() * hy.element_size()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        f0.record(stream)
+        for _ in range(e2e_steps):
+            dx.copy_(hx, non_blocking=True)
+            for k, v in hparams.items():
+                params[k].copy_(v, non_blocking=True)
+            launch(xp, yp)
+            hy.copy_(dy, non_blocking=True)
+        f1.record(stream)
+    torch.cuda.synchronize()
+    te = torch.tensor([f0.elapsed_time(f1)], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = bytes_step * world / (float(te.item()) / e2e_steps * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peak()
+    variant_key = ("two_pass" if plan.variant == C.TWO_PASS else f"cluster:{plan.cluster_size}")
+    launches_per_step = 2 if plan.variant == C.TWO_PASS else 1
+    traffic = stored_traffic(w.name, variant_key)
+    # the dominant kernel is the only kernel of a clustered step
+    achieved = bytes_step / (ms_step * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                "ideal_bytes": bytes_step}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cores = len(os.sched_getaffinity(0))
+        rows = cpu_sample_rows(w, inputs, cores, args.cpu_budget)
+        rate, dt = cpu_oracle_rate(w, inputs, rows, cores)
+        cpu = {"value": rate, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"first {rows} of {w.rows} rows (full width {w.cols}), "
+                         f"{dt:.1f} s on {cores} threads"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "io_dtype": w.dtype,
+                       "param_dtype": w.param_dtype, "variant": variant_key,
+                       "threads": plan.threads, "smem_bytes": int(plan.smem_bytes),
+                       "parallelism": f"replicas x{world}",
+                       "l2": "input larger than L2 (no flush)",
+                       "pct_of_nominal_8TBps": 100 * achieved / 8000.0},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

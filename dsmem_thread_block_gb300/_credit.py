@@ -1,0 +1,148 @@
+"""ctypes binding of libcredit.so -- argument marshalling only.
+
+The functions here carry the C ABI's names and arguments (include/credit.h):
+raw device pointers as ints, sizes, dtype codes, a ``Plan`` structure and a
+stream handle.  Every step of the computation runs in the library's CUDA
+kernels; if the library is missing this module raises instead of falling
+back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_LEGAL_PLAN, ERR_CUDA, \
+    ERR_DEVICE_TIMEOUT, ERR_NOT_CALIBRATED = range(7)
+F32, BF16 = 0, 1
+SOFTMAX, LAYERNORM, RMSNORM = 0, 1, 2
+AUTO, CLUSTER, TWO_PASS = 0, 1, 2
+
+_vp, _i64, _i32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                              ctypes.c_float, ctypes.c_size_t)
+
+
+class Plan(ctypes.Structure):
+    """Mirror of credit_plan_t."""
+    _fields_ = [("variant", ctypes.c_int32), ("cluster_size", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("waves", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+                ("slice_elems", ctypes.c_int64), ("active_clusters", ctypes.c_int32),
+                ("reserved0", ctypes.c_int32), ("pred_us", ctypes.c_float),
+                ("pred_two_pass_us", ctypes.c_float)]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved0"}
+
+    def __repr__(self):
+        return f"Plan({self.as_dict()})"
+
+
+class CreditError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+# C signatures: name -> (restype, argtypes)
+SIGNATURES = {
+    "credit_plan": (_i32, [_i32, _i64, _i64, _i32, _i32, ctypes.POINTER(Plan)]),
+    "credit_plan_for": (_i32, [_i32, _i64, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(Plan)]),
+    "credit_softmax": (_i32, [_vp, _vp, _i64, _i64, _i32, ctypes.POINTER(Plan), _vp, _sz, _vp]),
+    "credit_layernorm": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _i32, _f32,
+                                ctypes.POINTER(Plan), _vp, _sz, _vp]),
+    "credit_rmsnorm": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _i32, _f32,
+                              ctypes.POINTER(Plan), _vp, _sz, _vp]),
+    "credit_status_string": (ctypes.c_char_p, [_i32]),
+    "credit_get_device_error": (_i32, [_i32]),
+    "credit_version": (ctypes.c_char_p, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libcredit.so (building it first only if asked)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                if not build_if_missing:
+                    raise RuntimeError(
+                        f"libcredit.so is not built ({path}); run "
+                        "`python -c 'import __graft_entry__ as g; g.build()'`")
+                _build.build()
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(lib, name)
+                f.restype, f.argtypes = res, args
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().credit_status_string(status).decode()
+    except Exception:  # library not loadable: still give a readable message
+        return f"status {status}"
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise CreditError(status, where)
+
+
+def _plan_ptr(plan):
+    return None if plan is None else ctypes.byref(plan)
+
+
+def credit_plan(op: int, rows: int, cols: int, dtype: int, device: int) -> Plan:
+    p = Plan()
+    _check(load().credit_plan(op, rows, cols, dtype, device, ctypes.byref(p)), "credit_plan")
+    return p
+
+
+def credit_plan_for(op: int, rows: int, cols: int, dtype: int, device: int,
+                    variant: int, cluster_size: int = 1) -> Plan:
+    p = Plan()
+    _check(load().credit_plan_for(op, rows, cols, dtype, device, variant, cluster_size,
+                                  ctypes.byref(p)), "credit_plan_for")
+    return p
+
+
+def credit_softmax(x: int, y: int, rows: int, cols: int, dtype: int, plan=None,
+                   workspace: int = 0, workspace_bytes: int = 0, stream: int = 0) -> int:
+    return load().credit_softmax(x, y, rows, cols, dtype, _plan_ptr(plan), workspace or None,
+                                 workspace_bytes, stream or None)
+
+
+def credit_layernorm(x: int, y: int, rows: int, cols: int, dtype: int, gamma: int, beta: int,
+                     param_dtype: int, eps: float, plan=None, workspace: int = 0,
+                     workspace_bytes: int = 0, stream: int = 0) -> int:
+    return load().credit_layernorm(x, y, rows, cols, dtype, gamma or None, beta or None,
+                                   param_dtype, eps, _plan_ptr(plan), workspace or None,
+                                   workspace_bytes, stream or None)
+
+
+def credit_rmsnorm(x: int, y: int, rows: int, cols: int, dtype: int, weight: int,
+                   param_dtype: int, eps: float, plan=None, workspace: int = 0,
+                   workspace_bytes: int = 0, stream: int = 0) -> int:
+    return load().credit_rmsnorm(x, y, rows, cols, dtype, weight or None, param_dtype, eps,
+                                 _plan_ptr(plan), workspace or None, workspace_bytes,
+                                 stream or None)
+
+
+def credit_get_device_error(device: int) -> int:
+    return load().credit_get_device_error(device)
+
+
+def credit_version() -> str:
+    return load().credit_version().decode()

@@ -1,0 +1,289 @@
+// api.cu -- the C ABI of libcredit (see include/credit.h): argument checks,
+// the planner (legality + candidate choice) and dispatch to the kernels.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/credit.h"
+#include "common.cuh"
+#include "internal.h"
+#include "planner.h"
+
+namespace credit {
+
+__device__ unsigned g_device_error;
+
+namespace {
+
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+std::unordered_map<uint64_t, KernelInfo> g_kinfo;  // (device, kernel) -> info
+
+struct DeviceGuard {  // switch device for a host query, restore on exit
+    int old = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&old) != cudaSuccess) { cudaGetLastError(); return; }
+        ok = old == dev || cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        if (old >= 0) cudaSetDevice(old);
+    }
+};
+
+}  // namespace
+
+const DevInfo* device_info(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.valid) {
+        int n = 0;
+        if (cudaGetDeviceCount(&n) != cudaSuccess || dev >= n) { cudaGetLastError(); return nullptr; }
+        cudaDeviceProp p;
+        if (cudaGetDeviceProperties(&p, dev) != cudaSuccess) { cudaGetLastError(); return nullptr; }
+        d.sms = p.multiProcessorCount;
+        d.smem_optin = (int)p.sharedMemPerBlockOptin;
+        d.smem_per_sm = (int)p.sharedMemPerMultiprocessor;
+        d.reserved_smem = (int)p.reservedSharedMemPerBlock;
+        d.l2_bytes = p.l2CacheSize;
+        d.major = p.major;
+        d.minor = p.minor;
+        d.max_threads_sm = p.maxThreadsPerMultiProcessor;
+        d.regs_per_sm = p.regsPerMultiprocessor;
+        d.valid = true;
+    }
+    return &d;
+}
+
+// Per-(device, kernel) attributes, set once: the dynamic-SMEM opt-in up to the
+// device limit and (cluster kernels) non-portable cluster sizes up to 16.
+const KernelInfo* kernel_info(int dev, const void* fn, bool cluster) {
+    const DevInfo* d = device_info(dev);
+    if (!d || !fn) return nullptr;
+    const uint64_t key = ((uint64_t)dev << 56) ^ (uint64_t)(uintptr_t)fn;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_kinfo.find(key);
+    if (it != g_kinfo.end()) return &it->second;
+    DeviceGuard g(dev);
+    if (!g.ok) return nullptr;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) { cudaGetLastError(); return nullptr; }
+    KernelInfo ki;
+    ki.static_smem = (int)fa.sharedSizeBytes;
+    ki.regs = fa.numRegs;
+    ki.max_dyn_smem = d->smem_optin - ki.static_smem;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.max_dyn_smem) !=
+        cudaSuccess) { cudaGetLastError(); return nullptr; }
+    if (cluster &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return &g_kinfo.emplace(key, ki).first->second;
+}
+
+unsigned* device_error_word() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) { cudaGetLastError(); return nullptr; }
+    return static_cast<unsigned*>(p);
+}
+
+int occupancy_clusters(int dev, const void* fn, int P, int threads, size_t smem, int64_t rows) {
+    const DevInfo* d = device_info(dev);
+    if (!d) return 0;
+    DeviceGuard g(dev);
+    if (!g.ok) return 0;
+    if (P == 1) {
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        return nb * d->sms;
+    }
+    cudaLaunchConfig_t cfg = {};
+    const int64_t r = std::min<int64_t>(rows, 1 << 20);
+    cfg.gridDim = dim3((unsigned)(r * P), 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)P;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int nc = 0;
+    if (cudaOccupancyMaxActiveClusters(&nc, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return nc;
+}
+
+}  // namespace credit
+
+using namespace credit;
+
+namespace {
+
+bool dtype_ok(credit_dtype_t d) { return d == CREDIT_F32 || d == CREDIT_BF16; }
+size_t esize(credit_dtype_t d) { return d == CREDIT_F32 ? 4 : 2; }
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+credit_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CREDIT_OK : CREDIT_ERR_CUDA; }
+
+struct OpCall {
+    credit_op_t op;
+    const void* x;
+    void* y;
+    int64_t rows, cols;
+    credit_dtype_t dtype;
+    const void* p0;
+    const void* p1;
+    credit_dtype_t pdtype;
+    float eps;
+    const credit_plan_t* plan;
+    void* ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+credit_status_t run(const OpCall& c) {
+    if (!c.x || !c.y || c.rows < 1 || c.cols < 1) return CREDIT_ERR_INVALID_ARG;
+    if (!dtype_ok(c.dtype)) return CREDIT_ERR_UNSUPPORTED;
+    if ((c.p0 || c.p1) && !dtype_ok(c.pdtype)) return CREDIT_ERR_UNSUPPORTED;
+    if (c.op != CREDIT_SOFTMAX && !(c.eps >= 0.f)) return CREDIT_ERR_INVALID_ARG;
+    if (c.rows > INT64_MAX / c.cols) return CREDIT_ERR_INVALID_ARG;
+    const size_t es = esize(c.dtype);
+    const int64_t n = c.rows * c.cols;
+    if (n > INT64_MAX / (int64_t)es) return CREDIT_ERR_INVALID_ARG;
+    // in place is fine (each element is read before it is written, by the
+    // same CTA); any other overlap is rejected
+    const uintptr_t xb = (uintptr_t)c.x, yb = (uintptr_t)c.y, bytes = (uintptr_t)(n * (int64_t)es);
+    if (xb != yb && xb < yb + bytes && yb < xb + bytes) return CREDIT_ERR_INVALID_ARG;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return CREDIT_ERR_CUDA; }
+    credit_plan_t plan;
+    credit_status_t st;
+    if (c.plan && c.plan->variant != CREDIT_AUTO) {
+        // re-derive the launch shape from (variant, P, threads) so a stale or
+        // hand-edited plan can never launch an illegal configuration
+        st = make_plan(dev, c.op, c.rows, c.cols, c.dtype, (credit_variant_t)c.plan->variant,
+                       c.plan->cluster_size, c.plan->threads, &plan);
+    } else {
+        st = auto_plan(dev, c.op, c.rows, c.cols, c.dtype, &plan);
+    }
+    if (st != CREDIT_OK) return st;
+
+    const bool vec = aligned16(c.x) && aligned16(c.y) && ((int64_t)(c.cols * es) % 16 == 0) &&
+                     (!c.p0 || aligned16(c.p0)) && (!c.p1 || aligned16(c.p1));
+    KernelKey key{(int)c.op, (int)c.dtype, (c.p0 || c.p1) ? (int)c.pdtype : 0, vec};
+    unsigned* err = device_error_word();
+    if (!err) return CREDIT_ERR_CUDA;
+
+    if (plan.variant == CREDIT_CLUSTER) {
+        ClusterArgs a;
+        a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;
+        a.cols = c.cols;
+        a.slice = plan.slice_elems;
+        a.chunk_elems = (int32_t)bulk_chunk_elems(plan.slice_elems, (int)es);
+        a.eps = c.eps;
+        a.err = err;
+        const void* fn = cluster_kernel(key);
+        if (!kernel_info(dev, fn, true)) return CREDIT_ERR_CUDA;
+        return from_cuda(launch_cluster(key, a, c.rows, plan.cluster_size, plan.threads,
+                                        (size_t)plan.smem_bytes, c.stream));
+    }
+    // two-pass baseline
+    if (!c.ws || c.ws_bytes < (size_t)plan.workspace_bytes || !aligned16(c.ws))
+        return CREDIT_ERR_INVALID_ARG;
+    TwoPassArgs a;
+    a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;
+    a.cols = c.cols;
+    a.chunk = (int32_t)plan.slice_elems;
+    a.nch = (int32_t)((c.cols + plan.slice_elems - 1) / plan.slice_elems);
+    a.eps = c.eps;
+    a.ws = static_cast<float*>(c.ws);
+    return from_cuda(launch_two_pass(key, a, c.rows, plan.threads, c.stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+credit_status_t credit_plan(credit_op_t op, int64_t rows, int64_t cols, credit_dtype_t dtype,
+                            int device, credit_plan_t* out) {
+    if (!out) return CREDIT_ERR_INVALID_ARG;
+    return auto_plan(device, op, rows, cols, dtype, out);
+}
+
+credit_status_t credit_plan_for(credit_op_t op, int64_t rows, int64_t cols, credit_dtype_t dtype,
+                                int device, credit_variant_t variant, int cluster_size,
+                                credit_plan_t* out) {
+    if (!out) return CREDIT_ERR_INVALID_ARG;
+    if (variant != CREDIT_CLUSTER && variant != CREDIT_TWO_PASS) return CREDIT_ERR_INVALID_ARG;
+    return make_plan(device, op, rows, cols, dtype, variant, cluster_size, 0, out);
+}
+
+credit_status_t credit_softmax(const void* x, void* y, int64_t rows, int64_t cols,
+                               credit_dtype_t dtype, const credit_plan_t* plan, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    OpCall c{CREDIT_SOFTMAX, x, y, rows, cols, dtype, nullptr, nullptr, CREDIT_F32, 0.f,
+             plan, workspace, workspace_bytes, (cudaStream_t)stream};
+    return run(c);
+}
+
+credit_status_t credit_layernorm(const void* x, void* y, int64_t rows, int64_t cols,
+                                 credit_dtype_t dtype, const void* gamma, const void* beta,
+                                 credit_dtype_t param_dtype, float eps, const credit_plan_t* plan,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+    OpCall c{CREDIT_LAYERNORM, x, y, rows, cols, dtype, gamma, beta, param_dtype, eps,
+             plan, workspace, workspace_bytes, (cudaStream_t)stream};
+    return run(c);
+}
+
+credit_status_t credit_rmsnorm(const void* x, void* y, int64_t rows, int64_t cols,
+                               credit_dtype_t dtype, const void* weight, credit_dtype_t param_dtype,
+                               float eps, const credit_plan_t* plan, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    OpCall c{CREDIT_RMSNORM, x, y, rows, cols, dtype, weight, nullptr, param_dtype, eps,
+             plan, workspace, workspace_bytes, (cudaStream_t)stream};
+    return run(c);
+}
+
+const char* credit_status_string(credit_status_t s) {
+    switch (s) {
+        case CREDIT_OK: return "ok";
+        case CREDIT_ERR_INVALID_ARG: return "invalid argument";
+        case CREDIT_ERR_UNSUPPORTED: return "unsupported dtype or op";
+        case CREDIT_ERR_NO_LEGAL_PLAN: return "no legal plan (shared-memory or residency limit)";
+        case CREDIT_ERR_CUDA: return "CUDA runtime error";
+        case CREDIT_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+        case CREDIT_ERR_NOT_CALIBRATED: return "device not calibrated";
+    }
+    return "unknown status";
+}
+
+credit_status_t credit_get_device_error(int device) {
+    DeviceGuard g(device);
+    if (!g.ok) return CREDIT_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) { cudaGetLastError(); return CREDIT_ERR_CUDA; }
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
+    return (v & kErrTimeout) ? CREDIT_ERR_DEVICE_TIMEOUT : CREDIT_OK;
+}
+
+const char* credit_version(void) { return "0.1.0"; }
+
+}  // extern "C"

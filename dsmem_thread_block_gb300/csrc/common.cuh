@@ -1,0 +1,190 @@
+// common.cuh -- element traits, per-operator statistics and CTA-level
+// reductions shared by the clustered and the two-pass kernels.
+//
+// Operators (CREDIT summary page, arXiv 2609.01864v1, "B. Reduction-Reuse
+// Transformation": per-element inputs feed scalar statistics, then an
+// elementwise h writes every output):
+//   softmax   partial (m, s):      m = max x, s = sum exp(x - m)
+//             combine:             m = max m_q, s = sum s_q exp(m_q - m)
+//             h:                   y = exp(x - m) / s
+//   LayerNorm partial (n, mu, M2): count, mean, sum of squared deviations
+//             combine (Chan et al.): d = mu_b - mu_a, n = n_a + n_b,
+//                                    mu = mu_a + d n_b / n,
+//                                    M2 = M2_a + M2_b + d^2 n_a n_b / n
+//             h:                   y = (x - mu) / sqrt(M2 / N + eps) g + b
+//   RMSNorm   partial (ss):        sum x^2;  combine: sum
+//             h:                   y = x / sqrt(ss / N + eps) w
+// Partials are fp32; they are combined in rank order so every CTA of a
+// cluster rebuilds bit-identical statistics.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace credit {
+
+enum Op : int { kSoftmax = 0, kLayerNorm = 1, kRMSNorm = 2 };
+
+constexpr int kMaxCluster = 16;   // non-portable cluster size limit
+constexpr int kMaxThreads = 512;
+constexpr int kMaxWarps = kMaxThreads / 32;
+constexpr int kMaxChunks = 16;    // mbarriers per CTA for the staged slice
+constexpr int kSlotStride = 4;    // floats per pushed partial (16 bytes)
+
+// Device error word bits.
+constexpr unsigned kErrTimeout = 1u;
+
+// Bounded waits give up after this long (a second or so).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------- element traits
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kVec = 4;  // elements per 16-byte vector
+    __device__ static float to_f(float v) { return v; }
+    __device__ static float from_f(float v) { return v; }
+    __device__ static void unpack(uint4 v, float* f) {
+        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+    }
+    __device__ static uint4 pack(const float* f) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                          __float_as_uint(f[2]), __float_as_uint(f[3]));
+    }
+};
+template <> struct Elem<bf16> {
+    static constexpr int kVec = 8;
+    __device__ static float to_f(bf16 v) { return __bfloat162float(v); }
+    __device__ static bf16 from_f(float v) { return __float2bfloat16_rn(v); }
+    __device__ static float lo(uint32_t w) { return __uint_as_float(w << 16); }
+    __device__ static float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+    __device__ static void unpack(uint4 v, float* f) {
+        f[0] = lo(v.x); f[1] = hi(v.x); f[2] = lo(v.y); f[3] = hi(v.y);
+        f[4] = lo(v.z); f[5] = hi(v.z); f[6] = lo(v.w); f[7] = hi(v.w);
+    }
+    __device__ static uint32_t pack2(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __device__ static uint4 pack(const float* f) {
+        return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]),
+                          pack2(f[4], f[5]), pack2(f[6], f[7]));
+    }
+};
+
+// Load VEC per-column parameters starting at column j0 (j0 % VEC == 0, the
+// vector 16-byte aligned when PT is the element type, 8-byte otherwise).
+template <typename PT, int VEC>
+__device__ __forceinline__ void load_params(const PT* p, int64_t j0, float* out) {
+    if constexpr (sizeof(PT) == 4) {
+        const float4* q = reinterpret_cast<const float4*>(p + j0);
+#pragma unroll
+        for (int k = 0; k < VEC / 4; ++k) {
+            float4 v = __ldg(q + k);
+            out[4 * k] = v.x; out[4 * k + 1] = v.y;
+            out[4 * k + 2] = v.z; out[4 * k + 3] = v.w;
+        }
+    } else {
+        if constexpr (VEC == 8) {
+            uint4 v = __ldg(reinterpret_cast<const uint4*>(p + j0));
+            Elem<bf16>::unpack(v, out);
+        } else {
+            uint2 v = __ldg(reinterpret_cast<const uint2*>(p + j0));
+            out[0] = Elem<bf16>::lo(v.x); out[1] = Elem<bf16>::hi(v.x);
+            out[2] = Elem<bf16>::lo(v.y); out[3] = Elem<bf16>::hi(v.y);
+        }
+    }
+}
+
+template <typename PT>
+__device__ __forceinline__ float load_param1(const PT* p, int64_t j) {
+    if constexpr (sizeof(PT) == 4) return __ldg(reinterpret_cast<const float*>(p) + j);
+    else return __bfloat162float(p[j]);
+}
+
+// ------------------------------------------------------------ exponentials
+constexpr float kLog2e = 1.4426950408889634f;
+
+// fp32 outputs use CUDA's expf (max 2 ulp); bf16 outputs use the hardware
+// base-2 exponential on a pre-scaled argument, ample for a 2^-7 tolerance.
+template <typename T>
+__device__ __forceinline__ float exp_shift(float x, float m, float m_log2e) {
+    if constexpr (sizeof(T) == 4) {
+        return expf(x - m);
+    } else {
+        return fast_ex2(fmaf(x, kLog2e, -m_log2e));
+    }
+}
+
+// ---------------------------------------------------------- statistics
+struct SoftmaxPart { float m, s; };
+struct NormPart { float n, mu, m2; };
+
+// exp(a - b) * s, with s == 0 -> 0 even when a == b == -inf.
+__device__ __forceinline__ float rescale(float s, float a, float b) {
+    return s == 0.f ? 0.f : s * expf(a - b);
+}
+
+__device__ __forceinline__ SoftmaxPart softmax_merge(SoftmaxPart a, SoftmaxPart b) {
+    float m = fmaxf(a.m, b.m);
+    return {m, rescale(a.s, a.m, m) + rescale(b.s, b.m, m)};
+}
+
+__device__ __forceinline__ NormPart chan_merge(NormPart a, NormPart b) {
+    if (b.n == 0.f) return a;
+    if (a.n == 0.f) return b;
+    float n = a.n + b.n;
+    float d = b.mu - a.mu;
+    float f = b.n / n;
+    return {n, fmaf(d, f, a.mu), a.m2 + b.m2 + d * d * a.n * f};
+}
+
+// ------------------------------------------------------ CTA reductions
+// Every thread returns the same value: lane 0 of each warp publishes its
+// warp's result and every thread folds the per-warp values in warp order.
+// `buf` alternates between two scratch arrays so back-to-back reductions
+// need one __syncthreads each.
+template <typename F>
+__device__ __forceinline__ float warp_allreduce(float v, F f) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = f(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+struct SumOp { __device__ float operator()(float a, float b) const { return a + b; } };
+struct MaxOp { __device__ float operator()(float a, float b) const { return fmaxf(a, b); } };
+
+template <typename F>
+__device__ __forceinline__ float block_allreduce(float v, float* buf, F f, float init) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+    v = warp_allreduce(v, f);
+    if (lane == 0) buf[warp] = v;
+    __syncthreads();
+    float r = init;
+    for (int w = 0; w < nw; ++w) r = f(r, buf[w]);
+    return r;
+}
+
+// Bounded mbarrier wait: spins on try_wait; after kWaitLimitNs sets the
+// device error word and returns false (the caller carries on so that every
+// cluster barrier is still reached).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned* err) {
+    for (int i = 0; i < 256; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+}  // namespace credit

@@ -1,0 +1,56 @@
+// internal.h -- declarations shared between the host API (api.cu) and the
+// translation units that own the kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace credit {
+
+// Arguments of the clustered reduce-reuse kernel (one launch = all rows).
+struct ClusterArgs {
+    const void* x;
+    void* y;
+    const void* p0;       // gamma (LayerNorm) or weight (RMSNorm), may be null
+    const void* p1;       // beta (LayerNorm), may be null
+    int64_t cols;
+    int64_t slice;        // elements owned by one CTA (multiple of the vector width)
+    int32_t chunk_elems;  // elements per bulk copy / mbarrier
+    float eps;
+    unsigned* err;        // device error word
+};
+
+// Arguments of the two-pass (global re-read) kernel pair.
+struct TwoPassArgs {
+    const void* x;
+    void* y;
+    const void* p0;
+    const void* p1;
+    int64_t cols;
+    int32_t chunk;        // elements per block (threads * kTwoPassVpt * vector)
+    int32_t nch;          // chunks per row
+    float eps;
+    float* ws;            // rows * nch * 4 floats
+};
+
+constexpr int kTwoPassVpt = 4;  // 16-byte vectors per thread per chunk
+
+// Kernel selector: op 0..2, dtype 0 = fp32 / 1 = bf16, pdtype likewise,
+// vec = aligned 16-byte path.
+struct KernelKey {
+    int op, dtype, pdtype;
+    bool vec;
+};
+
+const void* cluster_kernel(KernelKey k);
+const void* two_pass_stats_kernel(KernelKey k);
+const void* two_pass_apply_kernel(KernelKey k);
+
+cudaError_t launch_cluster(KernelKey k, const ClusterArgs& a, int64_t rows,
+                           int P, int threads, size_t smem, cudaStream_t s);
+cudaError_t launch_two_pass(KernelKey k, const TwoPassArgs& a, int64_t rows,
+                            int threads, cudaStream_t s);
+
+unsigned* device_error_word();  // address of this device's error word
+
+}  // namespace credit

@@ -1,0 +1,139 @@
+// plan.cu -- plan legality and candidate selection.
+//
+// Legality (CREDIT summary page, arXiv 2609.01864v1, "B. Reduction-Reuse
+// Transformation", resource constraint): a cluster size P is legal when the
+// retained slice (ceil(N / P) elements rounded up to a 16-byte vector, times
+// the element size) plus the kernel's fixed per-CTA scratch fits the
+// dynamic-shared-memory opt-in limit, and the device can keep at least one
+// such cluster resident (cudaOccupancyMaxActiveClusters; clusters must fit
+// in one GPC, so the page's floor(S / P) is replaced by the runtime's count).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+#include "planner.h"
+
+namespace credit {
+
+namespace {
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+bool op_ok(credit_op_t op) {
+    return op == CREDIT_SOFTMAX || op == CREDIT_LAYERNORM || op == CREDIT_RMSNORM;
+}
+
+int cluster_threads(int64_t slice_vecs) {
+    // about four 16-byte vectors per thread, warp multiples, 64..512
+    int64_t t = round_up(std::max<int64_t>(1, slice_vecs / 4), 32);
+    return (int)std::min<int64_t>(512, std::max<int64_t>(64, t));
+}
+
+// Static model used until the device is calibrated: one HBM stream at a
+// nominal rate, derated when fewer than two CTAs share an SM (nothing hides
+// a CTA's load -> reduce -> barrier -> store sequence), plus a fixed cost per
+// wave of resident clusters.
+constexpr double kNominalBytesPerUs = 6.0e6;
+constexpr double kWaveUsCluster = 1.5;
+constexpr double kWaveUsSingle = 0.5;
+constexpr double kLaunchUs = 3.0;
+
+}  // namespace
+
+int64_t bulk_chunk_elems(int64_t slice_elems, int elem_bytes) {
+    const int64_t vec = 16 / elem_bytes;
+    const int64_t target = 16384 / elem_bytes;
+    return round_up(std::max(target, ceil_div(slice_elems, kMaxChunks)), vec);
+}
+
+credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
+                          credit_dtype_t dtype, credit_variant_t variant, int P,
+                          int threads, credit_plan_t* out) {
+    if (!out || rows < 1 || cols < 1) return CREDIT_ERR_INVALID_ARG;
+    if (!op_ok(op)) return CREDIT_ERR_UNSUPPORTED;
+    if (dtype != CREDIT_F32 && dtype != CREDIT_BF16) return CREDIT_ERR_UNSUPPORTED;
+    if (threads != 0 && (threads < 32 || threads > kMaxThreads || threads % 32 != 0))
+        return CREDIT_ERR_INVALID_ARG;
+    const DevInfo* d = device_info(dev);
+    if (!d) return CREDIT_ERR_CUDA;
+    const int es = dtype == CREDIT_F32 ? 4 : 2;
+    const int64_t vec = 16 / es;
+    credit_plan_t p;
+    std::memset(&p, 0, sizeof(p));
+    p.variant = variant;
+    const double bytes = 2.0 * (double)rows * (double)cols * es;
+
+    if (variant == CREDIT_CLUSTER) {
+        if (P < 1 || P > kMaxCluster) return CREDIT_ERR_NO_LEGAL_PLAN;
+        const int64_t slice = round_up(ceil_div(cols, P), vec);
+        const int64_t smem = round_up(slice * es, 16);
+        const void* fn = cluster_kernel(KernelKey{(int)op, (int)dtype, 0, true});
+        const KernelInfo* ki = kernel_info(dev, fn, true);
+        if (!ki) return CREDIT_ERR_CUDA;
+        if (smem > ki->max_dyn_smem) return CREDIT_ERR_NO_LEGAL_PLAN;
+        const int t = threads ? threads : cluster_threads(slice / vec);
+        const int active = occupancy_clusters(dev, fn, P, t, (size_t)smem, rows);
+        if (active < 1) return CREDIT_ERR_NO_LEGAL_PLAN;
+        p.cluster_size = P;
+        p.threads = t;
+        p.smem_bytes = smem;
+        p.slice_elems = slice;
+        p.active_clusters = active;
+        p.waves = (int32_t)std::min<int64_t>(ceil_div(rows, active), INT32_MAX);
+        const double ctas_per_sm = (double)active * P / d->sms;
+        const double eff = ctas_per_sm >= 2.0 ? 0.9 : 0.7;
+        p.pred_us = (float)(bytes / (kNominalBytesPerUs * eff) +
+                            p.waves * (P > 1 ? kWaveUsCluster : kWaveUsSingle));
+    } else if (variant == CREDIT_TWO_PASS) {
+        const int64_t per_thread = kTwoPassVpt * vec;
+        int t = threads;
+        if (!t) {
+            t = cols >= (int64_t)kMaxThreads * per_thread
+                    ? kMaxThreads
+                    : (int)std::max<int64_t>(32, round_up(ceil_div(cols, per_thread), 32));
+        }
+        const int64_t chunk = (int64_t)t * per_thread;
+        const int64_t nch = ceil_div(cols, chunk);
+        if (nch > INT32_MAX) return CREDIT_ERR_INVALID_ARG;
+        const void* fn = two_pass_stats_kernel(KernelKey{(int)op, (int)dtype, 0, true});
+        const KernelInfo* ki = kernel_info(dev, fn, false);
+        if (!ki) return CREDIT_ERR_CUDA;
+        const int active = occupancy_clusters(dev, fn, 1, t, 0, rows);
+        if (active < 1) return CREDIT_ERR_NO_LEGAL_PLAN;
+        p.cluster_size = 1;
+        p.threads = t;
+        p.slice_elems = chunk;
+        p.workspace_bytes = rows * nch * 4 * (int64_t)sizeof(float);
+        p.active_clusters = active;
+        p.waves = (int32_t)std::min<int64_t>(ceil_div(rows * nch, active), INT32_MAX);
+        p.pred_us = (float)(1.5 * bytes / (kNominalBytesPerUs * 0.9) + 2 * kLaunchUs);
+        p.pred_two_pass_us = p.pred_us;
+    } else {
+        return CREDIT_ERR_INVALID_ARG;
+    }
+    *out = p;
+    return CREDIT_OK;
+}
+
+credit_status_t auto_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
+                          credit_dtype_t dtype, credit_plan_t* out) {
+    if (!out || rows < 1 || cols < 1) return CREDIT_ERR_INVALID_ARG;
+    credit_plan_t base;
+    credit_status_t st = make_plan(dev, op, rows, cols, dtype, CREDIT_TWO_PASS, 0, 0, &base);
+    if (st != CREDIT_OK) return st;
+    credit_plan_t best = base;
+    for (int P = 1; P <= kMaxCluster; ++P) {
+        credit_plan_t c;
+        if (make_plan(dev, op, rows, cols, dtype, CREDIT_CLUSTER, P, 0, &c) != CREDIT_OK) continue;
+        if (P > 1 && (int64_t)(P - 1) * c.slice_elems >= cols) continue;  // an idle CTA
+        if (c.pred_us < best.pred_us) best = c;
+    }
+    best.pred_two_pass_us = base.pred_us;
+    *out = best;
+    return CREDIT_OK;
+}
+
+}  // namespace credit

@@ -1,0 +1,46 @@
+// planner.h -- device facts, per-kernel facts and the plan builders.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/credit.h"
+
+namespace credit {
+
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+    bool valid = false;
+    int sms = 0;
+    int smem_optin = 0;      // max dynamic + static shared memory per block
+    int smem_per_sm = 0;
+    int reserved_smem = 0;   // shared memory the system reserves per block
+    int l2_bytes = 0;
+    int major = 0, minor = 0;
+    int max_threads_sm = 0;
+    int regs_per_sm = 0;
+};
+
+struct KernelInfo {
+    int static_smem = 0;
+    int max_dyn_smem = 0;
+    int regs = 0;
+};
+
+const DevInfo* device_info(int dev);
+const KernelInfo* kernel_info(int dev, const void* fn, bool cluster);
+int occupancy_clusters(int dev, const void* fn, int P, int threads, size_t smem, int64_t rows);
+
+// Elements per bulk copy (one mbarrier each) for a staged slice.
+int64_t bulk_chunk_elems(int64_t slice_elems, int elem_bytes);
+
+// Build the plan of a given variant (threads == 0: choose).
+credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
+                          credit_dtype_t dtype, credit_variant_t variant, int P,
+                          int threads, credit_plan_t* out);
+
+// Enumerate legal candidates and keep the predicted-fastest.
+credit_status_t auto_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
+                          credit_dtype_t dtype, credit_plan_t* out);
+
+}  // namespace credit

@@ -1,0 +1,184 @@
+/*
+ * credit.h -- C ABI of libcredit: CREDIT's DSMEM reduction-reuse
+ * transformation for wide-row reduce-then-reuse operators (row softmax,
+ * LayerNorm, RMSNorm) on GB300 (sm_103a).
+ *
+ * Operation (CREDIT summary page, arXiv 2609.01864v1, "B. Reduction-Reuse
+ * Transformation" and "C. Cluster Reduction and Reuse Protocol"): each row is
+ * split into P contiguous slices owned by the P CTAs of one thread-block
+ * cluster.  Every CTA stages its slice in shared memory once, reduces it to a
+ * compact partial statistic, pushes that partial into a slot that each peer
+ * CTA owns (distributed shared memory), waits on a cluster barrier, combines
+ * the P slots with local reads only, and writes its output slice straight
+ * from shared memory.  The row is read from HBM once and written once.
+ * The non-clustered two-pass kernel (partials to a global workspace, then a
+ * second kernel that re-reads the row) ships alongside as the in-library
+ * baseline ("A. Experimental Setup and Baselines": a non-DSMEM CUDA baseline
+ * that either stages locally or re-reads global memory).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named x, y, gamma, beta, weight, workspace are DEVICE pointers
+ *    on the current CUDA device; the caller owns them.  Nothing on the call
+ *    path allocates memory.
+ *  - Matrices are row-major with row stride == cols (contiguous rows).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous on that stream and never synchronise
+ *    the host; a launch error is returned as CREDIT_ERR_CUDA.
+ *  - y == x (in place) is allowed; any other overlap of x and y is rejected.
+ *  - Errors are returned as credit_status_t; nothing is thrown.
+ *  - Calls are thread-safe.  The only state is a per-device cache of kernel
+ *    attributes and of the calibration profile.
+ */
+#ifndef CREDIT_H
+#define CREDIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CREDIT_OK = 0,
+    CREDIT_ERR_INVALID_ARG = 1,     /* null / overlapping / misaligned / bad size */
+    CREDIT_ERR_UNSUPPORTED = 2,     /* dtype or op not supported */
+    CREDIT_ERR_NO_LEGAL_PLAN = 3,   /* forced plan breaks the SMEM legality rule */
+    CREDIT_ERR_CUDA = 4,            /* a CUDA runtime call failed */
+    CREDIT_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device-side wait gave up */
+    CREDIT_ERR_NOT_CALIBRATED = 6   /* the cost model has no profile yet */
+} credit_status_t;
+
+typedef enum { CREDIT_F32 = 0, CREDIT_BF16 = 1 } credit_dtype_t;
+
+typedef enum {
+    CREDIT_SOFTMAX = 0,
+    CREDIT_LAYERNORM = 1,
+    CREDIT_RMSNORM = 2
+} credit_op_t;
+
+typedef enum {
+    CREDIT_AUTO = 0,       /* let credit_plan decide */
+    CREDIT_CLUSTER = 1,    /* clustered DSMEM kernel, cluster_size = P (1..16) */
+    CREDIT_TWO_PASS = 2    /* non-clustered two-pass re-read kernel pair */
+} credit_variant_t;
+
+/*
+ * A launch plan.  Produced by credit_plan / credit_plan_for; may be passed to
+ * the operator calls (NULL there means "plan automatically").
+ *   variant          CREDIT_CLUSTER or CREDIT_TWO_PASS (never AUTO once planned)
+ *   cluster_size     P, CTAs per row (1..16; 1 = one CTA stages the whole row)
+ *   threads          threads per CTA
+ *   smem_bytes       dynamic shared memory per CTA (the staged slice)
+ *   workspace_bytes  device workspace the call needs (TWO_PASS only, else 0)
+ *   slice_elems      elements of a row owned by one CTA (CLUSTER) or one
+ *                    chunk (TWO_PASS)
+ *   waves            predicted waves of resident clusters, ceil(rows / active)
+ *   active_clusters  clusters resident at once (cudaOccupancyMaxActiveClusters)
+ *   pred_us          predicted time of this plan, microseconds (0 = none)
+ *   pred_two_pass_us predicted / measured time of the two-pass baseline
+ */
+typedef struct {
+    int32_t variant;
+    int32_t cluster_size;
+    int32_t threads;
+    int32_t waves;
+    int64_t smem_bytes;
+    int64_t workspace_bytes;
+    int64_t slice_elems;
+    int32_t active_clusters;
+    int32_t reserved0;
+    float pred_us;
+    float pred_two_pass_us;
+} credit_plan_t;
+
+/*
+ * Plan an operator call automatically (CREDIT "D. Profitability and Candidate
+ * Selection": enumerate the legal cluster sizes -- retained slice plus fixed
+ * scratch must fit the dynamic-SMEM limit ("B. ... Resource Constraint") --
+ * predict each one's time and the two-pass baseline's, and keep the fastest).
+ * Uses the calibration profile of `device` if credit_calibrate has run on it,
+ * else a static bandwidth model.  Host only; does not launch kernels.
+ * Returns CREDIT_ERR_INVALID_ARG for rows < 1, cols < 1 or a null `out`.
+ */
+credit_status_t credit_plan(credit_op_t op, int64_t rows, int64_t cols,
+                            credit_dtype_t dtype, int device,
+                            credit_plan_t *out);
+
+/*
+ * Build a plan for a forced variant: CREDIT_CLUSTER with the given
+ * cluster_size (1..16), or CREDIT_TWO_PASS (cluster_size ignored).
+ * Returns CREDIT_ERR_NO_LEGAL_PLAN if the slice does not fit in shared memory
+ * or no cluster of that size can be resident.
+ */
+credit_status_t credit_plan_for(credit_op_t op, int64_t rows, int64_t cols,
+                                credit_dtype_t dtype, int device,
+                                credit_variant_t variant, int cluster_size,
+                                credit_plan_t *out);
+
+/*
+ * Row softmax: y[r, j] = exp(x[r, j] - max_r) / sum_k exp(x[r, k] - max_r).
+ * (CREDIT "B. Workload-by-Workload Scaling": softmax-logits.)  The partial a
+ * CTA pushes is (running max, sum of exp relative to it).
+ *   x, y       device, rows x cols of `dtype` (fp32 or bf16); y may equal x
+ *   plan       NULL = credit_plan; else a plan from credit_plan[_for] made
+ *              for the same op/rows/cols/dtype
+ *   workspace  device scratch of >= plan.workspace_bytes (TWO_PASS only;
+ *              may be NULL for CLUSTER plans)
+ * Fast path: x, y 16-byte aligned and cols*sizeof(dtype) a multiple of 16
+ * (bulk copies into shared memory); otherwise an element-wise staging path.
+ */
+credit_status_t credit_softmax(const void *x, void *y, int64_t rows,
+                               int64_t cols, credit_dtype_t dtype,
+                               const credit_plan_t *plan, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/*
+ * Row LayerNorm: y = (x - mean) / sqrt(var + eps) * gamma[j] + beta[j], with
+ * the biased variance.  (CREDIT "A. Experimental Setup": LayerNorm workload.)
+ * The partial a CTA pushes is (count, mean, M2) and the P partials are merged
+ * with Chan et al.'s pairwise update in rank order.
+ *   gamma, beta  device vectors of `cols` elements of param_dtype, or NULL
+ *                (gamma = 1, beta = 0)
+ *   eps          >= 0
+ * Other arguments as credit_softmax.
+ */
+credit_status_t credit_layernorm(const void *x, void *y, int64_t rows,
+                                 int64_t cols, credit_dtype_t dtype,
+                                 const void *gamma, const void *beta,
+                                 credit_dtype_t param_dtype, float eps,
+                                 const credit_plan_t *plan, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/*
+ * Row RMSNorm: y = x / sqrt(mean(x^2) + eps) * weight[j].  Not on the CREDIT
+ * page; it is the same one-statistic reduce-then-reuse class as LayerNorm.
+ * The partial a CTA pushes is its sum of squares.
+ *   weight  device vector of `cols` elements of param_dtype, or NULL (= 1)
+ * Other arguments as credit_softmax.
+ */
+credit_status_t credit_rmsnorm(const void *x, void *y, int64_t rows,
+                               int64_t cols, credit_dtype_t dtype,
+                               const void *weight, credit_dtype_t param_dtype,
+                               float eps, const credit_plan_t *plan,
+                               void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *credit_status_string(credit_status_t status);
+
+/*
+ * Read and clear the device error word of `device`.  Bounded device waits
+ * that give up set it; the result is CREDIT_ERR_DEVICE_TIMEOUT in that case,
+ * else CREDIT_OK.  Synchronises the device.
+ */
+credit_status_t credit_get_device_error(int device);
+
+/* Library version as "major.minor.patch" (static storage). */
+const char *credit_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CREDIT_H */

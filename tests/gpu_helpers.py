@@ -1,0 +1,125 @@
+"""Shared helpers for the GPU parity tests: move seeded inputs to the device,
+call the library through its C ABI, read results back, and compare them with
+the fp64 oracle under the stated tolerances.
+
+Tolerances (per element, o = oracle value in fp64, g = GPU value widened):
+  fp32 outputs   |g - o| <= 1e-5   * |o|
+  bf16 outputs   |g - o| <= 2^-7   * |o|        (one bf16 ulp at a binade top)
+LayerNorm adds a cancellation term for its final y = z * gamma + beta: when
+the two terms nearly cancel, the fp32 rounding of the mean and of z (~1e-7 of
+|z * gamma|) dominates a tiny |o|, so its bound is
+  |g - o| <= rtol * |o| + 1e-5 * (|z * gamma| + |beta|)
+and the tests report how many elements pass only through that term.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from dsmem_thread_block_gb300 import _credit as C
+from dsmem_thread_block_gb300 import workloads as wl
+
+RTOL = {"f32": 1e-5, "bf16": 2.0 ** -7}
+LN_CANCEL = 1e-5
+OPS = {wl.SOFTMAX: C.SOFTMAX, wl.LAYERNORM: C.LAYERNORM, wl.RMSNORM: C.RMSNORM}
+DT = {"f32": C.F32, "bf16": C.BF16}
+
+
+def to_device(a: np.ndarray, dev="cuda") -> torch.Tensor:
+    """numpy fp32 / uint16(bf16 bits) -> CUDA tensor of the same bytes."""
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(a)
+    return t.to(dev)
+
+
+def to_host(t: torch.Tensor) -> np.ndarray:
+    """CUDA tensor -> numpy with the same bytes (bf16 as uint16 bits)."""
+    t = t.cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def make_plan(w: wl.Workload, variant=None, P=1, rows=None):
+    rows = w.rows if rows is None else rows
+    dev = torch.cuda.current_device()
+    if variant is None:
+        return C.credit_plan(OPS[w.op], rows, w.cols, DT[w.dtype], dev)
+    return C.credit_plan_for(OPS[w.op], rows, w.cols, DT[w.dtype], dev, variant, P)
+
+
+def call(w: wl.Workload, dx: torch.Tensor, dy: torch.Tensor, params: dict, plan,
+         rows=None, stream=None) -> int:
+    """One library call through the C ABI on device tensors; returns status."""
+    rows = w.rows if rows is None else rows
+    ws = None
+    if plan is not None and plan.workspace_bytes:
+        ws = torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=dx.device)
+    wptr = ws.data_ptr() if ws is not None else 0
+    wbytes = int(plan.workspace_bytes) if ws is not None else 0
+    s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    pdt = DT[w.param_dtype] if w.param_dtype else C.F32
+    if w.op == wl.SOFTMAX:
+        return C.credit_softmax(dx.data_ptr(), dy.data_ptr(), rows, w.cols, DT[w.dtype], plan,
+                                wptr, wbytes, s)
+    if w.op == wl.LAYERNORM:
+        g, b = params.get("gamma"), params.get("beta")
+        return C.credit_layernorm(dx.data_ptr(), dy.data_ptr(), rows, w.cols, DT[w.dtype],
+                                  g.data_ptr() if g is not None else 0,
+                                  b.data_ptr() if b is not None else 0, pdt, w.eps, plan,
+                                  wptr, wbytes, s)
+    wt = params.get("weight")
+    return C.credit_rmsnorm(dx.data_ptr(), dy.data_ptr(), rows, w.cols, DT[w.dtype],
+                            wt.data_ptr() if wt is not None else 0, pdt, w.eps, plan, wptr,
+                            wbytes, s)
+
+
+def run(w: wl.Workload, inputs: dict, plan, in_place=False) -> np.ndarray:
+    """Run the library on host inputs; return the output bytes (numpy)."""
+    dx = to_device(inputs["x"])
+    dy = dx if in_place else torch.empty_like(dx)
+    params = {k: to_device(v) for k, v in inputs.items() if k != "x"}
+    st = call(w, dx, dy, params, plan, rows=inputs["x"].shape[0])
+    assert st == C.OK, C.status_string(st)
+    torch.cuda.synchronize()
+    assert C.credit_get_device_error(torch.cuda.current_device()) == C.OK
+    return to_host(dy)
+
+
+def oracle_rows(w: wl.Workload, inputs: dict, rows=None, want_z=False):
+    """fp64 oracle on all rows (or the listed row indices)."""
+    x = inputs["x"] if rows is None else inputs["x"][rows]
+    if w.op == wl.SOFTMAX:
+        return oracle.softmax(x), None
+    if w.op == wl.LAYERNORM:
+        y, z = oracle.layernorm(x, inputs.get("gamma"), inputs.get("beta"), eps=w.eps,
+                                want_z=True)
+        return y, z
+    return oracle.rmsnorm(x, inputs.get("weight"), eps=w.eps), None
+
+
+def check(w: wl.Workload, got: np.ndarray, inputs: dict, rows=None, scale=1.0) -> dict:
+    """Compare GPU output bytes with the oracle; assert the tolerance."""
+    want, z = oracle_rows(w, inputs, rows)
+    g = oracle.widen(got if rows is None else got[rows])
+    rtol = RTOL[w.dtype] * scale
+    err = np.abs(g - want)
+    bound = rtol * np.abs(want)
+    only_cancel = 0
+    if w.op == wl.LAYERNORM:
+        gam = oracle.widen(inputs["gamma"]) if "gamma" in inputs else 1.0
+        bet = oracle.widen(inputs["beta"]) if "beta" in inputs else 0.0
+        extra = LN_CANCEL * scale * (np.abs(z * gam) + np.abs(bet))
+        only_cancel = int(((err > bound) & (err <= bound + extra)).sum())
+        bound = bound + extra
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(
+            f"{w.name}: {int(bad.sum())} of {err.size} elements out of tolerance; worst at "
+            f"{i}: got {g[i]!r} want {want[i]!r} err {err[i]:.3e} bound {bound[i]:.3e}")
+    rel = err / np.maximum(np.abs(want), 1e-300)
+    return {"max_rel": float(rel.max()), "only_cancel": only_cancel, "n": int(err.size)}

@@ -1,0 +1,80 @@
+"""The C ABI library builds, loads and exports every symbol include/credit.h
+declares, and its host-side argument checks behave (no GPU needed: nothing
+here launches a kernel)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from dsmem_thread_block_gb300 import _credit as C
+from dsmem_thread_block_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        text = open(os.path.join(inc, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(credit_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return C.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "credit_softmax" in names and "credit_plan" in names
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (credit_[a-z0-9_]+)\b", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for n in names:
+        getattr(lib, n)
+
+
+def test_binding_covers_the_abi(lib):
+    for n in declared_functions():
+        assert n in C.SIGNATURES, f"{n} has no ctypes signature"
+
+
+def test_plan_struct_layout_matches_header():
+    # int32 x4, int64 x3, int32 x2, float x2 -> 56 bytes, no padding surprises
+    assert ctypes.sizeof(C.Plan) == 56
+    assert C.Plan.smem_bytes.offset == 16 and C.Plan.pred_us.offset == 48
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert C.status_string(s)
+    assert C.status_string(C.ERR_NO_LEGAL_PLAN).startswith("no legal plan")
+    assert C.credit_version().count(".") == 2
+
+
+def test_host_side_argument_checks_need_no_gpu(lib):
+    # null pointers and bad shapes are rejected before any CUDA call
+    assert C.credit_softmax(0, 0, 4, 4, C.F32) == C.ERR_INVALID_ARG
+    assert C.credit_softmax(16, 32, 0, 4, C.F32) == C.ERR_INVALID_ARG
+    assert C.credit_softmax(16, 32, 4, 0, C.F32) == C.ERR_INVALID_ARG
+    assert C.credit_softmax(16, 32, 4, 4, 7) == C.ERR_UNSUPPORTED
+    assert C.credit_layernorm(16, 1024, 1, 4, C.F32, 0, 0, C.F32, -1.0) == C.ERR_INVALID_ARG
+    # partial overlap of x and y (in place x == y is allowed)
+    assert C.credit_rmsnorm(4096, 4100, 1, 64, C.F32, 0, C.F32, 1e-6) == C.ERR_INVALID_ARG
+    assert lib.credit_plan(C.SOFTMAX, 4, 4, C.F32, 0, None) == C.ERR_INVALID_ARG
+    assert lib.credit_plan_for(C.SOFTMAX, 4, 4, C.F32, 0, 9, 1, None) == C.ERR_INVALID_ARG
+
+
+def test_library_fails_loudly_when_missing(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "LIB", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(C, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        C.load()

@@ -1,0 +1,200 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the fp64
+oracle on the same seeded inputs, element by element.
+
+Covers the five workloads' shapes at reduced row counts for every legal
+cluster size and the two-pass baseline, the full-size workloads on sampled
+rows in the launch configuration the benchmark uses, cluster-size invariance,
+and the edge cases: ragged widths (element-wise staging path), slices that are
+empty, a single row, in-place calls, misaligned pointers, absent parameters,
+bf16 parameters and constant rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+from dsmem_thread_block_gb300 import _credit as C
+from dsmem_thread_block_gb300 import workloads as wl
+
+from gpu_helpers import check, make_plan, oracle_rows, run, to_device, to_host, call
+
+pytestmark = pytest.mark.gpu
+
+TWO = ("two_pass", 0)
+
+
+def _plans(w, cluster_sizes, rows=None):
+    out = []
+    for P in cluster_sizes:
+        out.append(make_plan(w, C.CLUSTER, P, rows=rows))
+    out.append(make_plan(w, C.TWO_PASS, rows=rows))
+    return out
+
+
+# ----------------------------------------------------------- workload shapes
+def test_softmax_f32_64x4096_all_cluster_sizes():
+    w = wl.SOFTMAX_F32_64x4096
+    inp = w.generate()
+    for P in (1, 2, 3, 4, 8, 16):
+        got = run(w, inp, make_plan(w, C.CLUSTER, P))
+        check(w, got, inp)
+    got = run(w, inp, make_plan(w, C.TWO_PASS))
+    check(w, got, inp)
+
+
+@pytest.mark.parametrize("w,sizes", [
+    (wl.LAYERNORM_BF16_1024x262144.with_rows(3), (4, 5, 8, 16)),
+    (wl.SOFTMAX_F32_512x131072_SPIKES.with_rows(3), (4, 6, 8, 16)),
+    (wl.RMSNORM_BF16_2048x786432.with_rows(2), (8, 12, 16)),
+])
+def test_wide_rows_every_legal_cluster_size(w, sizes):
+    inp = w.generate()
+    outs = []
+    for p in _plans(w, sizes):
+        got = run(w, inp, p)
+        check(w, got, inp)
+        outs.append(oracle_widen(got))
+    # cluster-size invariance: variants agree pairwise within 2x the tolerance
+    rtol = 1e-5 if w.dtype == "f32" else 2.0 ** -7
+    ref = outs[0]
+    for o in outs[1:]:
+        d = np.abs(o - ref)
+        lim = 2 * rtol * np.abs(ref)
+        if w.op == wl.LAYERNORM:
+            lim = lim + 2e-5 * (np.abs(ref) + 1.0)
+        assert (d <= lim).all()
+
+
+def oracle_widen(a):
+    import oracle
+    return oracle.widen(a)
+
+
+@pytest.mark.parametrize("cols", [1 << k for k in range(10, 21, 2)])
+def test_bf16_softmax_sweep_shapes(cols):
+    w = wl.sweep_point(cols).with_rows(2)
+    inp = w.generate()
+    # every power-of-two cluster size that is legal at this width, and two-pass
+    for P in (1, 2, 4, 8, 16):
+        try:
+            p = make_plan(w, C.CLUSTER, P)
+        except C.CreditError as e:
+            assert e.status == C.ERR_NO_LEGAL_PLAN
+            continue
+        check(w, run(w, inp, p), inp)
+    check(w, run(w, inp, make_plan(w, C.TWO_PASS)), inp)
+
+
+# ---------------------------------------------------------------- edge cases
+def _custom(op, dtype, rows, cols, seed, **kw):
+    return wl.Workload(f"{op}_{dtype}_{rows}x{cols}", op, dtype, rows, cols, seed, **kw)
+
+
+EDGE = [
+    _custom(wl.SOFTMAX, "f32", 3, 4099, 5, x_std=3.0),            # ragged: element path
+    _custom(wl.SOFTMAX, "bf16", 2, 1001, 6),                       # ragged bf16
+    _custom(wl.SOFTMAX, "bf16", 2, 1000, 7),                       # 16B rows, ragged slices
+    _custom(wl.SOFTMAX, "f32", 2, 8, 8),                           # empty CTAs, bulk path
+    _custom(wl.SOFTMAX, "f32", 2, 5, 9),                           # cols < P*vec, element path
+    _custom(wl.SOFTMAX, "f32", 1, 1, 10),                          # one element
+    _custom(wl.LAYERNORM, "f32", 2, 3001, 11, x_mean=1.0, x_std=2.0, eps=1e-5, param_dtype="f32"),
+    _custom(wl.LAYERNORM, "bf16", 2, 4096, 12, x_mean=0.5, x_std=2.0, eps=1e-5, param_dtype="bf16"),
+    _custom(wl.LAYERNORM, "f32", 2, 4096, 13, x_mean=-3.0, x_std=0.5, eps=1e-5),  # no params
+    _custom(wl.RMSNORM, "f32", 2, 5003, 14, eps=1e-6, param_dtype="f32"),
+    _custom(wl.RMSNORM, "bf16", 2, 777, 15, eps=1e-6),                            # no weight
+    _custom(wl.RMSNORM, "bf16", 1, 65536, 16, eps=1e-6, param_dtype="f32"),
+]
+
+
+@pytest.mark.parametrize("w", EDGE, ids=[w.name for w in EDGE])
+def test_edge_shapes(w):
+    inp = w.generate()
+    for P in (1, 2, 3, 4, 7, 16):
+        try:
+            p = make_plan(w, C.CLUSTER, P)
+        except C.CreditError as e:
+            assert e.status == C.ERR_NO_LEGAL_PLAN
+            continue
+        check(w, run(w, inp, p), inp)
+    check(w, run(w, inp, make_plan(w, C.TWO_PASS)), inp)
+    check(w, run(w, inp, None), inp)  # automatic plan
+
+
+@pytest.mark.parametrize("variant,P", [(C.CLUSTER, 1), (C.CLUSTER, 4), (C.TWO_PASS, 1)])
+def test_in_place(variant, P):
+    for w in (_custom(wl.SOFTMAX, "f32", 4, 16384, 20, x_std=2.0),
+              _custom(wl.LAYERNORM, "bf16", 4, 16384, 21, eps=1e-5, param_dtype="f32"),
+              _custom(wl.RMSNORM, "f32", 4, 16387, 22, eps=1e-6, param_dtype="bf16")):
+        inp = w.generate()
+        got = run(w, inp, make_plan(w, variant, P), in_place=True)
+        check(w, got, inp)
+
+
+@pytest.mark.parametrize("variant,P", [(C.CLUSTER, 1), (C.CLUSTER, 4), (C.TWO_PASS, 1)])
+def test_misaligned_pointers_take_element_path(variant, P):
+    w = _custom(wl.LAYERNORM, "bf16", 3, 8192, 23, eps=1e-5, param_dtype="f32")
+    inp = w.generate()
+    # place x and y one element past a 16-byte boundary
+    xs = to_device(np.concatenate([np.zeros(1, np.uint16), inp["x"].reshape(-1)]))
+    dx = xs[1:]
+    dy_full = torch.empty(dx.numel() + 1, dtype=dx.dtype, device=dx.device)
+    dy = dy_full[1:]
+    params = {k: to_device(v) for k, v in inp.items() if k != "x"}
+    assert call(w, dx, dy, params, make_plan(w, variant, P)) == C.OK
+    torch.cuda.synchronize()
+    got = to_host(dy).reshape(w.rows, w.cols)
+    check(w, got, inp)
+
+
+def test_constant_rows():
+    # LayerNorm of a constant row is exactly beta (sums of -1.5 are exact)
+    w = _custom(wl.LAYERNORM, "f32", 2, 65536, 24, eps=1e-5, param_dtype="f32")
+    inp = w.generate()
+    inp["x"] = np.full((2, 65536), -1.5, np.float32)
+    for p in _plans(w, (1, 4)):
+        got = run(w, inp, p)
+        assert np.array_equal(got, np.broadcast_to(inp["beta"], got.shape))
+    # softmax of a constant row is uniform
+    w = _custom(wl.SOFTMAX, "f32", 2, 65536, 25)
+    inp = {"x": np.full((2, 65536), 0.25, np.float32)}
+    for p in _plans(w, (1, 4)):
+        got = run(w, inp, p)
+        np.testing.assert_allclose(got, 1.0 / 65536, rtol=1e-6)
+
+
+def test_auto_plan_is_legal_and_clustered_for_wide_rows():
+    for w in (wl.LAYERNORM_BF16_1024x262144, wl.SOFTMAX_F32_512x131072_SPIKES,
+              wl.RMSNORM_BF16_2048x786432):
+        p = make_plan(w)
+        assert p.variant == C.CLUSTER
+        assert p.slice_elems * p.cluster_size >= w.cols
+        assert p.smem_bytes <= 232448
+
+
+# ------------------------------------------------- full size, sampled rows
+FULL = [wl.SOFTMAX_F32_64x4096, wl.LAYERNORM_BF16_1024x262144,
+        wl.SOFTMAX_F32_512x131072_SPIKES, wl.RMSNORM_BF16_2048x786432]
+
+
+@pytest.mark.parametrize("w", FULL, ids=[w.name for w in FULL])
+def test_full_size_sampled_rows(w):
+    inp = w.generate()
+    p = make_plan(w)  # the launch configuration the benchmark times
+    dx = to_device(inp["x"])
+    dy = torch.empty_like(dx)
+    params = {k: to_device(v) for k, v in inp.items() if k != "x"}
+    assert call(w, dx, dy, params, p) == C.OK
+    torch.cuda.synchronize()
+    assert C.credit_get_device_error(torch.cuda.current_device()) == C.OK
+    rng = np.random.default_rng(99)
+    rows = sorted({0, w.rows - 1, *rng.integers(0, w.rows, 6).tolist()})
+    got = to_host(dy[rows])
+    sub = dict(inp)
+    sub["x"] = inp["x"][rows]
+    check(w, got, sub)
+    # every row, at any size: finite, and softmax rows sum to one
+    yf = dy.float()
+    assert bool(torch.isfinite(yf).all())
+    if w.op == wl.SOFTMAX:
+        tol = 1e-4 if w.dtype == "f32" else 2e-2
+        sums = yf.double().sum(dim=1)
+        assert float((sums - 1).abs().max()) <= tol
