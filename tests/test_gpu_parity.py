@@ -150,13 +150,13 @@ def test_constant_rows():
     w = _custom(wl.LAYERNORM, "f32", 2, 65536, 24, eps=1e-5, param_dtype="f32")
     inp = w.generate()
     inp["x"] = np.full((2, 65536), -1.5, np.float32)
-    for p in _plans(w, (1, 4)):
+    for p in _plans(w, (2, 4)):  # a 256 KiB fp32 row needs P >= 2
         got = run(w, inp, p)
         assert np.array_equal(got, np.broadcast_to(inp["beta"], got.shape))
     # softmax of a constant row is uniform
     w = _custom(wl.SOFTMAX, "f32", 2, 65536, 25)
     inp = {"x": np.full((2, 65536), 0.25, np.float32)}
-    for p in _plans(w, (1, 4)):
+    for p in _plans(w, (2, 4)):
         got = run(w, inp, p)
         np.testing.assert_allclose(got, 1.0 / 65536, rtol=1e-6)
 
@@ -198,3 +198,20 @@ def test_full_size_sampled_rows(w):
         tol = 1e-4 if w.dtype == "f32" else 2e-2
         sums = yf.double().sum(dim=1)
         assert float((sums - 1).abs().max()) <= tol
+
+
+def test_illegal_cluster_sizes_are_rejected():
+    # a 256 KiB fp32 row cannot be staged by one CTA (227 KiB limit)
+    w = _custom(wl.SOFTMAX, "f32", 2, 65536, 26)
+    with pytest.raises(C.CreditError) as e:
+        make_plan(w, C.CLUSTER, 1)
+    assert e.value.status == C.ERR_NO_LEGAL_PLAN
+    with pytest.raises(C.CreditError) as e:
+        make_plan(w, C.CLUSTER, 17)
+    assert e.value.status == C.ERR_NO_LEGAL_PLAN
+    # a forced plan passed to a call is re-derived and checked the same way
+    p = make_plan(w, C.CLUSTER, 2)
+    p.cluster_size = 1
+    inp = w.generate()
+    dx = to_device(inp["x"])
+    assert call(w, dx, torch.empty_like(dx), {}, p) == C.ERR_NO_LEGAL_PLAN
