@@ -55,6 +55,8 @@ SIGNATURES = {
                                 ctypes.POINTER(Plan), _vp, _sz, _vp]),
     "credit_rmsnorm": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _i32, _f32,
                               ctypes.POINTER(Plan), _vp, _sz, _vp]),
+    "credit_two_pass_noalloc": (_i32, [_i32, _vp, _vp, _i64, _i64, _i32, _vp, _vp, _i32, _f32,
+                                       _vp]),
     "credit_status_string": (ctypes.c_char_p, [_i32]),
     "credit_get_device_error": (_i32, [_i32]),
     "credit_version": (ctypes.c_char_p, []),
@@ -138,6 +140,15 @@ def credit_rmsnorm(x: int, y: int, rows: int, cols: int, dtype: int, weight: int
     return load().credit_rmsnorm(x, y, rows, cols, dtype, weight or None, param_dtype, eps,
                                  _plan_ptr(plan), workspace or None, workspace_bytes,
                                  stream or None)
+
+
+def credit_two_pass_noalloc(op: int, x: int, y: int, rows: int, cols: int, dtype: int,
+                            p0: int = 0, p1: int = 0, param_dtype: int = F32, eps: float = 0.0,
+                            stream: int = 0) -> int:
+    """Two-pass call for callers that cannot allocate device memory: the
+    partials live in the library's own fixed 2 MiB device array."""
+    return load().credit_two_pass_noalloc(op, x, y, rows, cols, dtype, p0 or None, p1 or None,
+                                          param_dtype, eps, stream or None)
 
 
 def credit_get_device_error(device: int) -> int:

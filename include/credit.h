@@ -164,6 +164,37 @@ credit_status_t credit_rmsnorm(const void *x, void *y, int64_t rows,
                                void *workspace, size_t workspace_bytes,
                                void *stream);
 
+/*
+ * Two-pass call that needs no workspace and allocates no device memory.
+ * The CREDIT paper has no counterpart to this entry point; it exists for
+ * callers that cannot allocate: programs that gave all device memory to their
+ * own pool at start-up, hot loops where cudaMalloc / cudaFree would
+ * synchronise the device, plug-in hosts that give the plug-in no allocator.
+ * It runs the same two-pass kernels as a CREDIT_TWO_PASS plan, with the
+ * per-chunk partials kept in a fixed 2 MiB array inside the library (131072
+ * (row, chunk) partials of 16 bytes; every device that loads the library
+ * holds the array until the process exits).
+ *   op            CREDIT_SOFTMAX, CREDIT_LAYERNORM or CREDIT_RMSNORM
+ *   p0, p1        LayerNorm gamma / beta; RMSNorm weight in p0 (p1 ignored);
+ *                 softmax ignores both; NULL as in the other entry points
+ *   other arguments as credit_layernorm
+ * Returns CREDIT_ERR_INVALID_ARG when the call would need more partials than
+ * the array holds (rows * ceil(cols / chunk) * 16 bytes > 2 MiB; the chunk
+ * is the plan's slice_elems from credit_plan_for(..., CREDIT_TWO_PASS, ...)).
+ * The first call on a device looks up the array's device address and sets
+ * kernel attributes for that device; make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents (nothing in it needs clearing: every partial is written before it
+ * is read); calls whose executions overlap on the GPU, e.g. on two streams,
+ * race on it and must be serialised by the caller.
+ */
+credit_status_t credit_two_pass_noalloc(credit_op_t op, const void *x, void *y,
+                                        int64_t rows, int64_t cols,
+                                        credit_dtype_t dtype, const void *p0,
+                                        const void *p1,
+                                        credit_dtype_t param_dtype, float eps,
+                                        void *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *credit_status_string(credit_status_t status);
 
