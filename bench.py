@@ -210,7 +210,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="layernorm_bf16_1024x262144")
-    ap.add_argument("--variant", default="auto", help="auto | cluster:P | two_pass")
+    ap.add_argument("--variant", default="auto", help="auto | cluster:P | persist:P | two_pass")
+    ap.add_argument("--cps", type=int, default=0, help="persistent CTAs per SM (0 = planner)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the cpu_baseline sample")
@@ -255,8 +256,12 @@ def main():
     elif args.variant == "two_pass":
         plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.TWO_PASS, 1)
     else:
-        P = int(args.variant.split(":")[1])
-        plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.CLUSTER, P)
+        kind, P = args.variant.split(":")
+        var = C.CLUSTER if kind == "cluster" else C.CLUSTER_PERSISTENT
+        plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, var, int(P))
+    if args.cps:
+        plan.ctas_per_sm = args.cps
+        plan = C.Plan.from_buffer_copy(plan)
     ws = None
     if plan.workspace_bytes:
         ws = torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=dx.device)
@@ -354,7 +359,8 @@ def main():
     e2e_value = bytes_step * world / (float(te.item()) / e2e_steps * 1e-3) / 1e9
 
     peak, peak_kind = measured_peak()
-    variant_key = ("two_pass" if plan.variant == C.TWO_PASS else f"cluster:{plan.cluster_size}")
+    variant_key = {C.TWO_PASS: "two_pass", C.CLUSTER: f"cluster:{plan.cluster_size}",
+                   C.CLUSTER_PERSISTENT: f"persist:{plan.cluster_size}"}[plan.variant]
     launches_per_step = 2 if plan.variant == C.TWO_PASS else 1
     traffic = stored_traffic(w.name, variant_key)
     # the dominant kernel is the only kernel of a clustered step
@@ -381,6 +387,7 @@ def main():
             "config": {"workload": w.name, "rows": w.rows, "cols": w.cols, "io_dtype": w.dtype,
                        "param_dtype": w.param_dtype, "variant": variant_key,
                        "threads": plan.threads, "smem_bytes": int(plan.smem_bytes),
+                       "ctas_per_sm": plan.ctas_per_sm, "clusters": plan.active_clusters,
                        "parallelism": f"replicas x{world}",
                        "l2": "input larger than L2 (no flush)",
                        "pct_of_nominal_8TBps": 100 * achieved / 8000.0},

@@ -18,7 +18,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_LEGAL_PLAN, ERR_CUDA, \
     ERR_DEVICE_TIMEOUT, ERR_NOT_CALIBRATED = range(7)
 F32, BF16 = 0, 1
 SOFTMAX, LAYERNORM, RMSNORM = 0, 1, 2
-AUTO, CLUSTER, TWO_PASS = 0, 1, 2
+AUTO, CLUSTER, TWO_PASS, CLUSTER_PERSISTENT = 0, 1, 2, 3
 
 _vp, _i64, _i32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                               ctypes.c_float, ctypes.c_size_t)
@@ -30,14 +30,34 @@ class Plan(ctypes.Structure):
                 ("threads", ctypes.c_int32), ("waves", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("slice_elems", ctypes.c_int64), ("active_clusters", ctypes.c_int32),
-                ("reserved0", ctypes.c_int32), ("pred_us", ctypes.c_float),
+                ("ctas_per_sm", ctypes.c_int32), ("chunk_elems", ctypes.c_int32),
+                ("ring_slots", ctypes.c_int32), ("pred_us", ctypes.c_float),
                 ("pred_two_pass_us", ctypes.c_float)]
 
     def as_dict(self) -> dict:
-        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved0"}
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
     def __repr__(self):
         return f"Plan({self.as_dict()})"
+
+
+class BenchResult(ctypes.Structure):
+    """Mirror of credit_bench_result_t."""
+    _fields_ = [("kind", ctypes.c_int32), ("cluster_size", ctypes.c_int32),
+                ("runs", ctypes.c_int32), ("smids", ctypes.c_int32 * 16),
+                ("median_cycles", ctypes.c_double), ("median_ns", ctypes.c_double),
+                ("iqr_cycles", ctypes.c_double), ("bytes_per_cycle", ctypes.c_double),
+                ("gbps", ctypes.c_double)]
+
+    def as_dict(self) -> dict:
+        d = {f: getattr(self, f) for f, _ in self._fields_ if f != "smids"}
+        d["smids"] = list(self.smids)[: self.cluster_size]
+        return d
+
+
+BENCH_BARRIER, BENCH_EXCHANGE, BENCH_REMOTE_LOAD_LATENCY, BENCH_LOCAL_LOAD_LATENCY, \
+    BENCH_REMOTE_STORE_BW, BENCH_REMOTE_LOAD_BW, BENCH_LOCAL_STORE_BW, \
+    BENCH_LOCAL_LOAD_BW = range(8)
 
 
 class CreditError(RuntimeError):
@@ -57,6 +77,9 @@ SIGNATURES = {
                               ctypes.POINTER(Plan), _vp, _sz, _vp]),
     "credit_two_pass_noalloc": (_i32, [_i32, _vp, _vp, _i64, _i64, _i32, _vp, _vp, _i32, _f32,
                                        _vp]),
+    "credit_bench_dsmem": (_i32, [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(BenchResult)]),
+    "credit_control_time": (_i32, [_i32, _i64, _i32, _i32, _i64, _i32, _i32, _i32,
+                                   ctypes.POINTER(ctypes.c_double)]),
     "credit_status_string": (ctypes.c_char_p, [_i32]),
     "credit_get_device_error": (_i32, [_i32]),
     "credit_version": (ctypes.c_char_p, []),
@@ -149,6 +172,24 @@ def credit_two_pass_noalloc(op: int, x: int, y: int, rows: int, cols: int, dtype
     partials live in the library's own fixed 2 MiB device array."""
     return load().credit_two_pass_noalloc(op, x, y, rows, cols, dtype, p0 or None, p1 or None,
                                           param_dtype, eps, stream or None)
+
+
+def credit_bench_dsmem(device: int, kind: int, cluster_size: int = 2, iters: int = 1000,
+                       runs: int = 15) -> BenchResult:
+    r = BenchResult()
+    _check(load().credit_bench_dsmem(device, kind, cluster_size, iters, runs, ctypes.byref(r)),
+           "credit_bench_dsmem")
+    return r
+
+
+def credit_control_time(device: int, nclusters: int, cluster_size: int, threads: int,
+                        smem_bytes: int, rows_per_cluster: int, barriers_per_row: int,
+                        runs: int = 15) -> float:
+    t = ctypes.c_double()
+    _check(load().credit_control_time(device, nclusters, cluster_size, threads, smem_bytes,
+                                      rows_per_cluster, barriers_per_row, runs, ctypes.byref(t)),
+           "credit_control_time")
+    return t.value
 
 
 def credit_get_device_error(device: int) -> int:

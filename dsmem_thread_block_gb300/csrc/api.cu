@@ -8,7 +8,7 @@
 #include <mutex>
 #include <unordered_map>
 
-#include "../../include/credit.h"
+#include "credit.h"
 #include "common.cuh"
 #include "internal.h"
 #include "planner.h"
@@ -175,8 +175,10 @@ credit_status_t run(const OpCall& c) {
     if (c.plan && c.plan->variant != CREDIT_AUTO) {
         // re-derive the launch shape from (variant, P, threads) so a stale or
         // hand-edited plan can never launch an illegal configuration
+        const bool pers = c.plan->variant == CREDIT_CLUSTER_PERSISTENT;
         st = make_plan(dev, c.op, c.rows, c.cols, c.dtype, (credit_variant_t)c.plan->variant,
-                       c.plan->cluster_size, c.plan->threads, &plan);
+                       c.plan->cluster_size, c.plan->threads, pers ? c.plan->ctas_per_sm : 0,
+                       &plan, pers ? c.plan->chunk_elems : 0);
     } else {
         st = auto_plan(dev, c.op, c.rows, c.cols, c.dtype, &plan);
     }
@@ -187,6 +189,29 @@ credit_status_t run(const OpCall& c) {
     KernelKey key{(int)c.op, (int)c.dtype, (c.p0 || c.p1) ? (int)c.pdtype : 0, vec};
     unsigned* err = device_error_word();
     if (!err) return CREDIT_ERR_CUDA;
+    if (plan.variant == CREDIT_CLUSTER_PERSISTENT && !vec) {
+        // the ring is filled by bulk copies: misaligned or ragged rows take
+        // the one-row-per-cluster kernel's element path instead
+        st = make_plan(dev, c.op, c.rows, c.cols, c.dtype, CREDIT_CLUSTER, plan.cluster_size, 0, 0,
+                       &plan);
+        if (st != CREDIT_OK) return st;
+    }
+    if (plan.variant == CREDIT_CLUSTER_PERSISTENT) {
+        PersistArgs a;
+        a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;
+        a.rows = c.rows;
+        a.cols = c.cols;
+        a.slice = (int32_t)plan.slice_elems;
+        a.chunk = plan.chunk_elems;
+        a.nslots = plan.ring_slots;
+        a.nclusters = plan.active_clusters;
+        a.eps = c.eps;
+        a.err = err;
+        const void* fn = persistent_kernel(key);
+        if (!kernel_info(dev, fn, true)) return CREDIT_ERR_CUDA;
+        return from_cuda(launch_persistent(key, a, plan.cluster_size, plan.threads,
+                                           (size_t)plan.smem_bytes, c.stream));
+    }
 
     if (plan.variant == CREDIT_CLUSTER) {
         ClusterArgs a;
@@ -228,8 +253,10 @@ credit_status_t credit_plan_for(credit_op_t op, int64_t rows, int64_t cols, cred
                                 int device, credit_variant_t variant, int cluster_size,
                                 credit_plan_t* out) {
     if (!out) return CREDIT_ERR_INVALID_ARG;
-    if (variant != CREDIT_CLUSTER && variant != CREDIT_TWO_PASS) return CREDIT_ERR_INVALID_ARG;
-    return make_plan(device, op, rows, cols, dtype, variant, cluster_size, 0, out);
+    if (variant != CREDIT_CLUSTER && variant != CREDIT_TWO_PASS &&
+        variant != CREDIT_CLUSTER_PERSISTENT)
+        return CREDIT_ERR_INVALID_ARG;
+    return make_plan(device, op, rows, cols, dtype, variant, cluster_size, 0, 0, out);
 }
 
 credit_status_t credit_softmax(const void* x, void* y, int64_t rows, int64_t cols,

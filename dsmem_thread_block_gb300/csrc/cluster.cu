@@ -22,233 +22,110 @@
 // which a one-row-per-cluster launch never does).
 #include "common.cuh"
 #include "internal.h"
+#include "rowops.cuh"
 
 namespace credit {
 
 template <int OP, typename T, typename PT, bool BULK>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+__global__ void __launch_bounds__(kMaxThreads, 2)
 cluster_reduce_reuse(const ClusterArgs a) {
     using E = Elem<T>;
     constexpr int VEC = E::kVec;
     extern __shared__ __align__(128) unsigned char stage[];
     __shared__ __align__(16) float slots[kMaxCluster * kSlotStride];
-    __shared__ float red[2][kMaxWarps];
+    __shared__ __align__(16) float red[2][kMaxWarps * 2];
     __shared__ __align__(8) uint64_t mbar[kMaxChunks];
 
     const uint32_t P = cluster_nctarank();
     const uint32_t rank = cluster_ctarank();
     const int64_t row = blockIdx.x / P;
     const int64_t start = (int64_t)rank * a.slice;
-    const int64_t n = max((int64_t)0, min(a.cols - start, a.slice));
+    const int n = (int)max((int64_t)0, min(a.cols - start, a.slice));
     const T* xs = static_cast<const T*>(a.x) + row * a.cols + start;
     T* ys = static_cast<T*>(a.y) + row * a.cols + start;
     const int tid = threadIdx.x, nt = blockDim.x;
-    const uint32_t st_s = smem_u32(stage);
-    const int64_t nvec = n / VEC;  // whole 16-byte vectors (all of n on the bulk path)
+    const int nvec = n / VEC;  // whole 16-byte vectors (all of n on the bulk path)
 
     if (P > 1) cluster_arrive_relaxed();
 
     // ---------------------------------------------------------- a2 stage
     int nchunks = 1;
-    int64_t vpc = nvec;  // vectors per chunk
+    int vpc = nvec;  // vectors per chunk
     if constexpr (BULK) {
-        nchunks = (int)((n + a.chunk_elems - 1) / a.chunk_elems);
+        nchunks = (n + a.chunk_elems - 1) / a.chunk_elems;
         vpc = a.chunk_elems / VEC;
         if (tid == 0) {
+            const uint32_t st_s = smem_u32(stage);
             for (int c = 0; c < nchunks; ++c) mbar_init(smem_u32(&mbar[c]), 1);
             fence_mbar_init();
             fence_proxy_async_smem();
             const uint64_t pol = l2_policy_evict_first();
             for (int c = 0; c < nchunks; ++c) {
-                const int64_t e0 = (int64_t)c * a.chunk_elems;
-                const uint32_t bytes =
-                    (uint32_t)(min((int64_t)a.chunk_elems, n - e0) * (int64_t)sizeof(T));
+                const int e0 = c * a.chunk_elems;
+                const uint32_t bytes = (uint32_t)(min(a.chunk_elems, n - e0) * (int)sizeof(T));
                 const uint32_t bar = smem_u32(&mbar[c]);
                 mbar_arrive_expect_tx(bar, bytes);
-                bulk_g2s(st_s + (uint32_t)(e0 * sizeof(T)), xs + e0, bytes, bar, pol);
+                bulk_g2s(st_s + (uint32_t)(e0 * (int)sizeof(T)), xs + e0, bytes, bar, pol);
             }
         }
         __syncthreads();
     } else {
         T* st = reinterpret_cast<T*>(stage);
-        for (int64_t i = tid; i < n; i += nt) st[i] = xs[i];
+        for (int i = tid; i < n; i += nt) st[i] = xs[i];
         __syncthreads();
     }
+    auto tail_at = [&](int i) { return E::to_f(reinterpret_cast<const T*>(stage)[i]); };
 
-    auto vec_at = [&](int64_t v, float* f) { E::unpack(ld_shared_v4(st_s + (uint32_t)(v * 16)), f); };
-    auto tail_at = [&](int64_t i) { return E::to_f(reinterpret_cast<const T*>(stage)[i]); };
-
-    // -------------------------------------------- a3 local partial, pass A
-    // max (softmax), sum (LayerNorm) or sum of squares (RMSNorm), consumed
-    // chunk by chunk as the bulk copies land.
-    float acc = (OP == kSoftmax) ? -INFINITY : 0.f;
+    // --------------------------------------------- a3 local partial
+    // each chunk is folded into the threads' statistics as soon as it lands
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
+    Stats<OP, T> st;
     for (int c = 0; c < nchunks; ++c) {
         if constexpr (BULK) mbar_wait_bounded(smem_u32(&mbar[c]), 0, a.err);
-        const int64_t vend = min(nvec, (int64_t)(c + 1) * vpc);
-        for (int64_t v = (int64_t)c * vpc + tid; v < vend; v += nt) {
-            float f[VEC];
-            vec_at(v, f);
-#pragma unroll
-            for (int k = 0; k < VEC; ++k) {
-                if constexpr (OP == kSoftmax) acc = fmaxf(acc, f[k]);
-                else if constexpr (OP == kLayerNorm) acc += f[k];
-                else acc = fmaf(f[k], f[k], acc);
-            }
-        }
+        const int v0 = c * vpc;
+        stats_tiles(st, stage + (size_t)v0 * 16, min(nvec, v0 + vpc) - v0, warp, nwarps, lane);
     }
-    if constexpr (!BULK) {
-        for (int64_t i = nvec * VEC + tid; i < n; i += nt) {
-            const float f = tail_at(i);
-            if constexpr (OP == kSoftmax) acc = fmaxf(acc, f);
-            else if constexpr (OP == kLayerNorm) acc += f;
-            else acc = fmaf(f, f, acc);
-        }
-    }
-    float pv0, pv1 = 0.f, pv2 = 0.f;
-    if constexpr (OP == kSoftmax) pv0 = block_allreduce(acc, red[0], MaxOp{}, -INFINITY);
-    else pv0 = block_allreduce(acc, red[0], SumOp{}, 0.f);
-
-    // -------------------------------------------------------- pass B
-    if constexpr (OP == kSoftmax) {
-        // s_q = sum exp(x - m_q); fp32 keeps t = exp(x - m_q) in place so the
-        // output pass is a single multiply.
-        const float mq = pv0, mq_l2e = mq * kLog2e;
-        float s = 0.f;
-        if (n > 0) {
-            for (int64_t v = tid; v < nvec; v += nt) {
-                float f[VEC];
-                vec_at(v, f);
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) {
-                    f[k] = exp_shift<T>(f[k], mq, mq_l2e);
-                    s += f[k];
-                }
-                if constexpr (sizeof(T) == 4) st_shared_v4(st_s + (uint32_t)(v * 16), E::pack(f));
-            }
-            if constexpr (!BULK) {
-                for (int64_t i = nvec * VEC + tid; i < n; i += nt) {
-                    const float t = exp_shift<T>(tail_at(i), mq, mq_l2e);
-                    s += t;
-                    if constexpr (sizeof(T) == 4) reinterpret_cast<float*>(stage)[i] = t;
-                }
-            }
-        }
-        pv1 = block_allreduce(s, red[1], SumOp{}, 0.f);
-    } else if constexpr (OP == kLayerNorm) {
-        // exact two-pass over the staged slice: (n_q, mean_q, M2_q)
-        const float nq = (float)n;
-        const float mu = n > 0 ? pv0 / nq : 0.f;
-        float m2 = 0.f;
-        for (int64_t v = tid; v < nvec; v += nt) {
-            float f[VEC];
-            vec_at(v, f);
-#pragma unroll
-            for (int k = 0; k < VEC; ++k) {
-                const float d = f[k] - mu;
-                m2 = fmaf(d, d, m2);
-            }
-        }
+    if constexpr (!BULK)
+        for (int i = nvec * VEC + tid; i < n; i += nt) st.add1(tail_at(i));
+    auto stash = [&](float mq) {
+        float s = softmax_stash(stage, nvec, warp, nwarps, lane, mq);
         if constexpr (!BULK) {
-            for (int64_t i = nvec * VEC + tid; i < n; i += nt) {
-                const float d = tail_at(i) - mu;
-                m2 = fmaf(d, d, m2);
+            for (int i = nvec * VEC + tid; i < n; i += nt) {
+                const float t = expf(tail_at(i) - mq);
+                reinterpret_cast<float*>(stage)[i] = t;
+                s += t;
             }
         }
-        pv1 = mu;
-        pv2 = block_allreduce(m2, red[1], SumOp{}, 0.f);
-        pv0 = nq;
-    }
+        return s;
+    };
+    float p0, p1, p2;
+    cta_partial<OP, T>(st, red[0], red[1], nwarps, nt, stash, p0, p1, p2);
 
     // --------------------------------------- a4 push, a5 barrier, a6 combine
-    float st0, st1, st2;  // combined statistics, identical in every CTA
+    float st0 = p0, st1 = p1, st2 = p2;  // combined statistics, identical in every CTA
     if (P > 1) {
         cluster_wait_acquire();  // every peer has started: its slots exist
         if (tid < (int)P) {
             const uint32_t dst = mapa_shared(smem_u32(&slots[rank * kSlotStride]), (uint32_t)tid);
-            st_cluster_v4f32(dst, pv0, pv1, pv2, 0.f);
+            st_cluster_v4f32(dst, p0, p1, p2, 0.f);
         }
         cluster_arrive_release();
         cluster_wait_acquire();
-        if constexpr (OP == kSoftmax) {
-            float m = -INFINITY;
-            for (uint32_t q = 0; q < P; ++q) m = fmaxf(m, slots[q * kSlotStride]);
-            float s = 0.f;
-            for (uint32_t q = 0; q < P; ++q)
-                s += rescale(slots[q * kSlotStride + 1], slots[q * kSlotStride], m);
-            st0 = m; st1 = s; st2 = 0.f;
-        } else if constexpr (OP == kLayerNorm) {
-            NormPart acc2{0.f, 0.f, 0.f};
-            for (uint32_t q = 0; q < P; ++q)
-                acc2 = chan_merge(acc2, NormPart{slots[q * kSlotStride], slots[q * kSlotStride + 1],
-                                                 slots[q * kSlotStride + 2]});
-            st0 = acc2.n; st1 = acc2.mu; st2 = acc2.m2;
-        } else {
-            float ss = 0.f;
-            for (uint32_t q = 0; q < P; ++q) ss += slots[q * kSlotStride];
-            st0 = ss; st1 = st2 = 0.f;
-        }
-    } else {
-        st0 = pv0; st1 = pv1; st2 = pv2;
+        combine_slots<OP>(slots, P, st0, st1, st2);
     }
 
     // ------------------------------------------------------- a7 output
-    const float inv_n = 1.f / (float)a.cols;
-    float c0 = 0.f, c1 = 0.f;
-    if constexpr (OP == kSoftmax) {
-        if constexpr (sizeof(T) == 4) c0 = rescale(1.f, pv0, st0) / st1;  // exp(m_q - m) / s
-        else { c0 = st0 * kLog2e; c1 = 1.f / st1; }
-    } else if constexpr (OP == kLayerNorm) {
-        c0 = st1;                                        // mean
-        c1 = 1.f / sqrtf(fmaxf(st2 * inv_n, 0.f) + a.eps);  // 1 / sqrt(var + eps)
-    } else {
-        c0 = 1.f / sqrtf(st0 * inv_n + a.eps);
-    }
+    const OutputMap<OP, T> h(st0, st1, st2, p0, a.cols, a.eps);
     const PT* g = static_cast<const PT*>(a.p0);
     const PT* b = static_cast<const PT*>(a.p1);
-
-    auto h = [&](float f, float gj, float bj) -> float {
-        if constexpr (OP == kSoftmax) {
-            if constexpr (sizeof(T) == 4) return f * c0;
-            else return fast_ex2(fmaf(f, kLog2e, -c0)) * c1;
-        } else if constexpr (OP == kLayerNorm) {
-            return fmaf((f - c0) * c1, gj, bj);
-        } else {
-            return (f * c0) * gj;
-        }
-    };
-
-    for (int64_t v = tid; v < nvec; v += nt) {
-        float f[VEC], gv[VEC], bv[VEC];
-        vec_at(v, f);
-        const int64_t j0 = start + v * VEC;
-#pragma unroll
-        for (int k = 0; k < VEC; ++k) { gv[k] = 1.f; bv[k] = 0.f; }
-        if constexpr (OP != kSoftmax) {
-            if constexpr (BULK) {
-                if (g) load_params<PT, VEC>(g, j0, gv);
-                if (b) load_params<PT, VEC>(b, j0, bv);
-            } else {
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) {
-                    if (g) gv[k] = load_param1<PT>(g, j0 + k);
-                    if (b) bv[k] = load_param1<PT>(b, j0 + k);
-                }
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < VEC; ++k) f[k] = h(f[k], gv[k], bv[k]);
-        if constexpr (BULK) {
-            st_global_cs_v4(ys + v * VEC, E::pack(f));
-        } else {
-#pragma unroll
-            for (int k = 0; k < VEC; ++k) ys[v * VEC + k] = E::from_f(f[k]);
-        }
-    }
-    if constexpr (!BULK) {
-        for (int64_t i = nvec * VEC + tid; i < n; i += nt) {
+    if constexpr (BULK) {
+        output_tiles<OP, T, PT>(h, stage, ys, g ? g + start : nullptr, b ? b + start : nullptr,
+                                nvec, warp, nwarps, lane);
+    } else {
+        for (int i = tid; i < n; i += nt) {
             const float gj = (OP != kSoftmax && g) ? load_param1<PT>(g, start + i) : 1.f;
             const float bj = (OP != kSoftmax && b) ? load_param1<PT>(b, start + i) : 0.f;
-            ys[i] = E::from_f(h(tail_at(i), gj, bj));
+            ys[i] = E::from_f(h.one(tail_at(i), gj, bj));
         }
     }
 }

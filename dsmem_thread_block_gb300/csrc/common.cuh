@@ -80,6 +80,7 @@ template <> struct Elem<bf16> {
 // vector 16-byte aligned when PT is the element type, 8-byte otherwise).
 template <typename PT, int VEC>
 __device__ __forceinline__ void load_params(const PT* p, int64_t j0, float* out) {
+    static_assert(VEC == 4 || VEC == 8, "4 or 8 parameters per load");
     if constexpr (sizeof(PT) == 4) {
         const float4* q = reinterpret_cast<const float4*>(p + j0);
 #pragma unroll
@@ -186,5 +187,99 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
     return true;
 }
+
+}  // namespace credit
+
+namespace credit {
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+// Barrier among the first `nthreads` threads of the CTA (named barrier 1).
+__device__ __forceinline__ void named_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" :: "r"(nthreads) : "memory");
+}
+
+// Fold the P pushed partials (stride kSlotStride floats) in rank order into
+// the row statistics (st0, st1, st2); identical in every CTA of the cluster.
+//   softmax:   m = max m_q, s = sum s_q exp(m_q - m)
+//   LayerNorm: Chan et al.'s combination in its all-at-once (parallel-axis)
+//              form: n = sum n_q, mean = sum n_q mean_q / n,
+//              M2 = sum (M2_q + n_q (mean_q - mean)^2)
+//   RMSNorm:   ss = sum ss_q
+template <int OP>
+__device__ __forceinline__ void combine_slots(const float* sl, uint32_t P, float& st0,
+                                              float& st1, float& st2) {
+    if constexpr (OP == kSoftmax) {
+        float m = -INFINITY;
+        for (uint32_t q = 0; q < P; ++q) m = fmaxf(m, sl[q * kSlotStride]);
+        float s = 0.f;
+        for (uint32_t q = 0; q < P; ++q)
+            s += rescale(sl[q * kSlotStride + 1], sl[q * kSlotStride], m);
+        st0 = m; st1 = s; st2 = 0.f;
+    } else if constexpr (OP == kLayerNorm) {
+        float n = 0.f, nm = 0.f;
+        for (uint32_t q = 0; q < P; ++q) {
+            n += sl[q * kSlotStride];
+            nm = fmaf(sl[q * kSlotStride], sl[q * kSlotStride + 1], nm);
+        }
+        const float mean = n > 0.f ? nm / n : 0.f;
+        float m2 = 0.f;
+        for (uint32_t q = 0; q < P; ++q) {
+            const float d = sl[q * kSlotStride + 1] - mean;
+            m2 += fmaf(sl[q * kSlotStride] * d, d, sl[q * kSlotStride + 2]);
+        }
+        st0 = n; st1 = mean; st2 = m2;
+    } else {
+        float ss = 0.f;
+        for (uint32_t q = 0; q < P; ++q) ss += sl[q * kSlotStride];
+        st0 = ss; st1 = st2 = 0.f;
+    }
+}
+
+// Block-wide reductions over the first `nthreads` threads (named barrier 1);
+// every participating thread returns the same value (lane 0 of each warp
+// publishes, every thread folds the warps in order).  `red` needs
+// 2 floats per warp and must not be read by any thread from an earlier use.
+__device__ __forceinline__ void block_sum2(float& x, float& y, float* red, int nwarps,
+                                           int nthreads) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+        y += __shfl_xor_sync(0xffffffffu, y, o);
+    }
+    if (lane == 0) { red[2 * warp] = x; red[2 * warp + 1] = y; }
+    named_sync(nthreads);
+    x = 0.f; y = 0.f;
+    for (int w = 0; w < nwarps; ++w) { x += red[2 * w]; y += red[2 * w + 1]; }
+}
+
+__device__ __forceinline__ float block_max1(float x, float* red, int nwarps, int nthreads) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    if (lane == 0) red[2 * warp] = x;
+    named_sync(nthreads);
+    x = -INFINITY;
+    for (int w = 0; w < nwarps; ++w) x = fmaxf(x, red[2 * w]);
+    return x;
+}
+
+// 16-byte shared-memory load the compiler can schedule (and order against
+// the barriers, which are asm volatile with memory clobbers).
+__device__ __forceinline__ uint4 lds16(const unsigned char* p) {
+    return *reinterpret_cast<const uint4*>(p);
+}
+
+// 16-byte streaming global store (evict-first: the output is not re-read).
+__device__ __forceinline__ void stg16_stream(void* p, uint4 v) {
+    __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
+}  // namespace credit
+
+namespace credit {
 
 }  // namespace credit

@@ -35,6 +35,27 @@ struct TwoPassArgs {
 
 constexpr int kTwoPassVpt = 4;  // 16-byte vectors per thread per chunk
 
+// Arguments of the persistent clustered kernel: `nclusters` resident clusters
+// loop over the rows; each CTA streams its slice of every row it owns through
+// a ring of `nslots` shared-memory slots of `chunk` elements.
+struct PersistArgs {
+    const void* x;
+    void* y;
+    const void* p0;
+    const void* p1;
+    int64_t rows;
+    int64_t cols;
+    int32_t slice;        // elements owned by one CTA (multiple of the vector width)
+    int32_t chunk;        // elements per ring slot / bulk copy (multiple of the vector width)
+    int32_t nslots;       // ring slots per CTA (<= kPersistMaxSlots)
+    int32_t nclusters;    // clusters in the grid
+    float eps;
+    unsigned* err;
+};
+
+constexpr int kPersistMaxSlots = 32;
+constexpr int kPersistMaxThreads = 544;  // 16 consumer warps + 1 producer warp
+
 // Kernel selector: op 0..2, dtype 0 = fp32 / 1 = bf16, pdtype likewise,
 // vec = aligned 16-byte path.
 struct KernelKey {
@@ -43,11 +64,14 @@ struct KernelKey {
 };
 
 const void* cluster_kernel(KernelKey k);
+const void* persistent_kernel(KernelKey k);
 const void* two_pass_stats_kernel(KernelKey k);
 const void* two_pass_apply_kernel(KernelKey k);
 
 cudaError_t launch_cluster(KernelKey k, const ClusterArgs& a, int64_t rows,
                            int P, int threads, size_t smem, cudaStream_t s);
+cudaError_t launch_persistent(KernelKey k, const PersistArgs& a, int P, int threads,
+                              size_t smem, cudaStream_t s);
 cudaError_t launch_two_pass(KernelKey k, const TwoPassArgs& a, int64_t rows,
                             int threads, cudaStream_t s);
 

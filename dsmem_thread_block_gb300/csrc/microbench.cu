@@ -1,0 +1,314 @@
+// microbench.cu -- DSMEM primitive characterisation and the control kernel.
+//
+// CREDIT summary page (arXiv 2609.01864v1), "C. Positioning": DSMEM is
+// profiled with latency, throughput and repeated cluster-synchronisation
+// microbenchmarks that place the CTAs on different SMs, reporting the median
+// of 15 runs; "D. Profitability and Candidate Selection": a work-free control
+// kernel with the real kernel's grid, cluster size, dynamic-SMEM footprint
+// and K = 2L barriers measures launch, scheduling, occupancy and
+// synchronisation cost, and its excess over a one-CTA control is T_ctrl.
+//
+// Every benchmark kernel requests more than half of an SM's shared memory
+// (or the caller's footprint) so that no two of its CTAs share an SM; the
+// SM ids are reported so the caller can check.  Timing inside kernels uses
+// clock64 (SM cycles) and %globaltimer (ns); the control kernel is timed
+// with CUDA events.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "credit.h"
+#include "common.cuh"
+#include "internal.h"
+#include "planner.h"
+
+namespace credit {
+namespace {
+
+struct BenchOut {
+    long long cycles;     // measured by rank 0, thread 0
+    long long ns;
+    unsigned smid[kMaxCluster];
+    unsigned sink;
+};
+
+constexpr int kChaseEntries = 4096;      // u32 ring in shared memory
+constexpr int kBwBytes = 64 * 1024;      // remote buffer for the throughput kinds
+
+__device__ __forceinline__ void cluster_sync_all() {
+    cluster_arrive_release();
+    cluster_wait_acquire();
+}
+
+// kind BARRIER: iters x (arrive.release + wait.acquire) on a cluster of P.
+// kind EXCHANGE: iters x (push a 16-byte partial to every peer + barrier),
+// i.e. steps a4 + a5 of the protocol.
+__global__ void bench_barrier(BenchOut* out, int iters, int exchange) {
+    extern __shared__ __align__(16) unsigned char dyn[];
+    __shared__ __align__(16) float slots[kMaxCluster * 4];
+    const uint32_t P = cluster_nctarank(), rank = cluster_ctarank();
+    if (threadIdx.x == 0) out->smid[rank] = smid();
+    if (threadIdx.x == 0) dyn[0] = 0;
+    cluster_sync_all();
+    const long long c0 = clock64();
+    const uint64_t t0 = globaltimer_ns();
+    for (int i = 0; i < iters; ++i) {
+        if (exchange && threadIdx.x < P) {
+            const uint32_t dst = mapa_shared(smem_u32(&slots[rank * 4]), threadIdx.x);
+            st_cluster_v4f32(dst, (float)i, 1.f, 2.f, 3.f);
+        }
+        cluster_sync_all();
+    }
+    const long long c1 = clock64();
+    const uint64_t t1 = globaltimer_ns();
+    if (rank == 0 && threadIdx.x == 0) {
+        out->cycles = c1 - c0;
+        out->ns = (long long)(t1 - t0);
+        out->sink = (unsigned)slots[0];
+    }
+    cluster_sync_all();
+}
+
+// kind LOAD_LATENCY: rank 0 chases a pointer ring that lives in rank 1's
+// shared memory (remote) or in its own (local).
+__global__ void bench_chase(BenchOut* out, int iters, int remote) {
+    __shared__ uint32_t ring[kChaseEntries];
+    const uint32_t rank = cluster_ctarank();
+    if (threadIdx.x == 0) out->smid[rank] = smid();
+    // a stride coprime with the ring size defeats any prefetch
+    for (int i = threadIdx.x; i < kChaseEntries; i += blockDim.x)
+        ring[i] = (uint32_t)((i + 1031) % kChaseEntries);
+    __syncthreads();
+    cluster_sync_all();
+    if (rank == 0 && threadIdx.x == 0) {
+        const uint32_t owner = remote ? 1u : 0u;
+        const uint32_t base = mapa_shared(smem_u32(ring), owner);
+        uint32_t idx = 0;
+        const long long c0 = clock64();
+        const uint64_t t0 = globaltimer_ns();
+        for (int i = 0; i < iters; ++i) idx = ld_cluster_u32(base + idx * 4u);
+        const long long c1 = clock64();
+        const uint64_t t1 = globaltimer_ns();
+        out->cycles = c1 - c0;
+        out->ns = (long long)(t1 - t0);
+        out->sink = idx;
+    }
+    cluster_sync_all();  // rank 1 keeps its shared memory alive until rank 0 is done
+}
+
+// kind STORE_BW / LOAD_BW: every thread of rank 0 moves 16-byte vectors to or
+// from a 64 KiB buffer of rank 1 (remote) or of its own (local), `iters`
+// passes over the buffer.
+__global__ void bench_bw(BenchOut* out, int iters, int remote, int store) {
+    extern __shared__ __align__(16) unsigned char buf[];
+    const uint32_t rank = cluster_ctarank();
+    if (threadIdx.x == 0) out->smid[rank] = smid();
+    for (int i = threadIdx.x; i < kBwBytes / 4; i += blockDim.x)
+        reinterpret_cast<uint32_t*>(buf)[i] = (uint32_t)i;
+    __syncthreads();
+    cluster_sync_all();
+    if (rank == 0) {
+        const uint32_t base = mapa_shared(smem_u32(buf), remote ? 1u : 0u);
+        uint32_t acc = 0;
+        __syncthreads();
+        const long long c0 = clock64();
+        const uint64_t t0 = globaltimer_ns();
+        for (int it = 0; it < iters; ++it) {
+            for (int v = threadIdx.x; v < kBwBytes / 16; v += blockDim.x) {
+                const uint32_t addr = base + (uint32_t)v * 16u;
+                if (store) {
+                    st_cluster_v4f32(addr, (float)it, (float)v, 0.f, 1.f);
+                } else {
+                    uint32_t a0, a1, a2, a3;
+                    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(addr) : "memory");
+                    acc ^= a0 ^ a1 ^ a2 ^ a3;
+                }
+            }
+        }
+        if (store) asm volatile("fence.acq_rel.cluster;" ::: "memory");
+        __syncthreads();
+        const long long c1 = clock64();
+        const uint64_t t1 = globaltimer_ns();
+        if (threadIdx.x == 0) {
+            out->cycles = c1 - c0;
+            out->ns = (long long)(t1 - t0);
+        }
+        if (acc == 0xdeadbeefu) out->sink = acc;
+    }
+    cluster_sync_all();
+}
+
+// The control kernel: the real kernel's grid (nclusters x P CTAs), cluster
+// size, dynamic shared memory and `barriers` cluster barriers per row for
+// `rows_per_cluster` rows, and no work.
+__global__ void control_kernel(int rows_per_cluster, int barriers) {
+    extern __shared__ __align__(16) unsigned char dyn[];
+    const bool clustered = cluster_nctarank() > 1;
+    if (threadIdx.x == 0) dyn[0] = 1;
+    for (int r = 0; r < rows_per_cluster; ++r)
+        for (int b = 0; b < barriers; ++b)
+            if (clustered) cluster_sync_all();
+            else __syncthreads();
+}
+
+cudaError_t launch_cluster_kernel(const void* fn, int P, int ctas, int threads, size_t smem,
+                                  void** args, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)P;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = P > 1 ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+double median(std::vector<double> v) {
+    std::sort(v.begin(), v.end());
+    const size_t n = v.size();
+    return n % 2 ? v[n / 2] : 0.5 * (v[n / 2 - 1] + v[n / 2]);
+}
+
+double quantile(std::vector<double> v, double q) {
+    std::sort(v.begin(), v.end());
+    const double pos = q * (double)(v.size() - 1);
+    const size_t i = (size_t)pos;
+    const double f = pos - (double)i;
+    return i + 1 < v.size() ? v[i] * (1 - f) + v[i + 1] * f : v[i];
+}
+
+}  // namespace
+}  // namespace credit
+
+using namespace credit;
+
+extern "C" credit_status_t credit_bench_dsmem(int device, int kind, int cluster_size, int iters,
+                                              int runs, credit_bench_result_t* out) {
+    if (!out || iters < 1 || runs < 1 || runs > 1000) return CREDIT_ERR_INVALID_ARG;
+    if (cluster_size < 1 || cluster_size > kMaxCluster) return CREDIT_ERR_INVALID_ARG;
+    const bool pair = kind == CREDIT_BENCH_REMOTE_LOAD_LATENCY || kind == CREDIT_BENCH_LOCAL_LOAD_LATENCY ||
+                      kind == CREDIT_BENCH_REMOTE_STORE_BW || kind == CREDIT_BENCH_REMOTE_LOAD_BW ||
+                      kind == CREDIT_BENCH_LOCAL_STORE_BW || kind == CREDIT_BENCH_LOCAL_LOAD_BW;
+    if (!pair && kind != CREDIT_BENCH_BARRIER && kind != CREDIT_BENCH_EXCHANGE)
+        return CREDIT_ERR_INVALID_ARG;
+    const int P = pair ? 2 : cluster_size;
+    const DevInfo* d = device_info(device);
+    if (!d) return CREDIT_ERR_CUDA;
+    int old = 0;
+    if (cudaGetDevice(&old) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
+    credit_status_t status = CREDIT_OK;
+    BenchOut* dout = nullptr;
+    std::vector<double> cyc, ns;
+    BenchOut h;
+    std::memset(&h, 0, sizeof(h));
+    const void* fn = nullptr;
+    int threads = 32;
+    size_t smem = (size_t)d->smem_per_sm / 2 + 4096;  // one CTA per SM
+    int remote = (kind == CREDIT_BENCH_REMOTE_LOAD_LATENCY || kind == CREDIT_BENCH_REMOTE_STORE_BW ||
+                  kind == CREDIT_BENCH_REMOTE_LOAD_BW);
+    int store = (kind == CREDIT_BENCH_REMOTE_STORE_BW || kind == CREDIT_BENCH_LOCAL_STORE_BW);
+    int exchange = kind == CREDIT_BENCH_EXCHANGE;
+    if (kind == CREDIT_BENCH_BARRIER || kind == CREDIT_BENCH_EXCHANGE) {
+        fn = (const void*)bench_barrier;
+        threads = 128;
+    } else if (kind == CREDIT_BENCH_REMOTE_LOAD_LATENCY || kind == CREDIT_BENCH_LOCAL_LOAD_LATENCY) {
+        fn = (const void*)bench_chase;
+        threads = 128;
+    } else {
+        fn = (const void*)bench_bw;
+        threads = 512;
+        smem = std::max<size_t>(smem, kBwBytes);
+    }
+    if (!kernel_info(device, fn, true)) status = CREDIT_ERR_CUDA;
+    if (status == CREDIT_OK && cudaMalloc(&dout, sizeof(BenchOut)) != cudaSuccess) status = CREDIT_ERR_CUDA;
+    for (int r = 0; status == CREDIT_OK && r < runs + 1; ++r) {  // run 0 warms up
+        void* args_barrier[] = {&dout, &iters, &exchange};
+        void* args_chase[] = {&dout, &iters, &remote};
+        void* args_bw[] = {&dout, &iters, &remote, &store};
+        void** args = fn == (const void*)bench_barrier ? args_barrier
+                      : fn == (const void*)bench_chase ? args_chase : args_bw;
+        if (cudaMemset(dout, 0, sizeof(BenchOut)) != cudaSuccess ||
+            launch_cluster_kernel(fn, P, P, threads, smem, args, 0) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess ||
+            cudaMemcpy(&h, dout, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            status = CREDIT_ERR_CUDA;
+            break;
+        }
+        if (r == 0) continue;
+        cyc.push_back((double)h.cycles / iters);
+        ns.push_back((double)h.ns / iters);
+    }
+    if (dout) cudaFree(dout);
+    cudaSetDevice(old);
+    if (status != CREDIT_OK) return status;
+    std::memset(out, 0, sizeof(*out));
+    out->kind = kind;
+    out->cluster_size = P;
+    out->runs = runs;
+    for (int q = 0; q < P; ++q) out->smids[q] = (int32_t)h.smid[q];
+    out->median_cycles = median(cyc);
+    out->median_ns = median(ns);
+    out->iqr_cycles = quantile(cyc, 0.75) - quantile(cyc, 0.25);
+    if (pair && kind != CREDIT_BENCH_REMOTE_LOAD_LATENCY && kind != CREDIT_BENCH_LOCAL_LOAD_LATENCY) {
+        out->bytes_per_cycle = (double)kBwBytes / out->median_cycles;
+        out->gbps = (double)kBwBytes / out->median_ns;
+    }
+    return CREDIT_OK;
+}
+
+extern "C" credit_status_t credit_control_time(int device, int64_t nclusters, int cluster_size,
+                                               int threads, int64_t smem_bytes,
+                                               int rows_per_cluster, int barriers_per_row,
+                                               int runs, double* median_us) {
+    if (!median_us || nclusters < 1 || nclusters * cluster_size > 0x7fffffff || runs < 1 ||
+        cluster_size < 1 || cluster_size > kMaxCluster || threads < 32 || threads > 1024 ||
+        smem_bytes < 0 || rows_per_cluster < 0 || barriers_per_row < 0)
+        return CREDIT_ERR_INVALID_ARG;
+    const DevInfo* d = device_info(device);
+    if (!d) return CREDIT_ERR_CUDA;
+    const KernelInfo* ki = kernel_info(device, (const void*)control_kernel, true);
+    if (!ki) return CREDIT_ERR_CUDA;
+    if (smem_bytes > ki->max_dyn_smem) return CREDIT_ERR_NO_LEGAL_PLAN;
+    int old = 0;
+    if (cudaGetDevice(&old) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
+    credit_status_t status = CREDIT_OK;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    std::vector<double> t;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) status = CREDIT_ERR_CUDA;
+    for (int r = 0; status == CREDIT_OK && r < runs + 1; ++r) {
+        void* args[] = {&rows_per_cluster, &barriers_per_row};
+        float ms = 0.f;
+        if (cudaEventRecord(e0, 0) != cudaSuccess ||
+            launch_cluster_kernel((const void*)control_kernel, cluster_size,
+                                  (int)(nclusters * cluster_size), threads, (size_t)smem_bytes, args,
+                                  0) != cudaSuccess ||
+            cudaEventRecord(e1, 0) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) {
+            cudaGetLastError();
+            status = CREDIT_ERR_CUDA;
+            break;
+        }
+        if (r > 0) t.push_back(1e3 * ms);
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaSetDevice(old);
+    if (status == CREDIT_OK) *median_us = median(t);
+    return status;
+}

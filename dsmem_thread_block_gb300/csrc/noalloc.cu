@@ -13,7 +13,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/credit.h"
+#include "credit.h"
 #include "common.cuh"
 #include "internal.h"
 #include "planner.h"
@@ -74,7 +74,7 @@ extern "C" credit_status_t credit_two_pass_noalloc(credit_op_t op, const void* x
     if (dev < 0 || dev >= kMaxDevices) return CREDIT_ERR_CUDA;
     credit_plan_t plan;
     const credit_status_t st =
-        make_plan(dev, op, rows, cols, dtype, CREDIT_TWO_PASS, 0, 0, &plan);
+        make_plan(dev, op, rows, cols, dtype, CREDIT_TWO_PASS, 0, 0, 0, &plan);
     if (st != CREDIT_OK) return st;
     if ((size_t)plan.workspace_bytes > kStaticScratchBytes) return CREDIT_ERR_INVALID_ARG;
     void* scratch = scratch_address(dev);

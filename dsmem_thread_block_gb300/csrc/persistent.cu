@@ -1,0 +1,198 @@
+// persistent.cu -- the clustered reduce-reuse kernel as a persistent,
+// warp-specialised pipeline.
+//
+// The grid holds only the clusters that can be resident at once; cluster
+// `cid` handles rows cid, cid + G, cid + 2G, ...  Every CTA owns the same
+// column slice of each of those rows (CREDIT summary page, arXiv
+// 2609.01864v1, "B. Reduction-Reuse Transformation": P non-overlapping
+// CTA-owned slices).  Per CTA:
+//   - one producer warp streams the slice of row after row into a ring of
+//     shared-memory slots with non-multicast bulk copies, one "full" mbarrier
+//     per slot (transaction bytes) and one "empty" mbarrier per slot (one
+//     arrival per consumer warp once the slot's output has been written);
+//   - the consumer warps, per row: fold each chunk into per-thread partials
+//     as it lands, merge them into the CTA partial, push it into slot `rank`
+//     of every peer (mapa + st.shared::cluster), pass the cluster barrier,
+//     combine the P slots in rank order, apply h to the whole staged slice
+//     and release the row's slots back to the producer ("C. Cluster
+//     Reduction and Reuse Protocol").
+// The ring holds at least one whole slice, so the row is read from HBM once;
+// when it holds two or more, the next row's copies are in flight while this
+// row reduces, exchanges and writes.
+// Slot arrays are double-buffered by row parity: the cluster barrier of row k
+// orders every read of row k-1's slots before any push of row k+1, which is
+// the job of the page's second barrier.  A relaxed arrive at entry, waited on
+// before the first push, guarantees every peer is running.
+// Every wait on an mbarrier is bounded (a second); the producer warp takes
+// part in each cluster barrier phase one row ahead of the consumers.
+#include "common.cuh"
+#include "internal.h"
+#include "rowops.cuh"
+
+namespace credit {
+
+template <int OP, typename T, typename PT>
+__global__ void __launch_bounds__(kPersistMaxThreads, 1)
+cluster_persistent(const PersistArgs a) {
+    using E = Elem<T>;
+    constexpr int VEC = E::kVec;
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(16) float slots[2][kMaxCluster * kSlotStride];
+    __shared__ __align__(16) float red[2][2][(kPersistMaxThreads / 32) * 2];  // [row parity][stage]
+    __shared__ __align__(8) uint64_t full_bar[kPersistMaxSlots];
+    __shared__ __align__(8) uint64_t empty_bar[kPersistMaxSlots];
+
+    const uint32_t P = cluster_nctarank();
+    const uint32_t rank = cluster_ctarank();
+    const int64_t cid = blockIdx.x / P;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int ncw = (int)(blockDim.x >> 5) - 1;  // consumer warps; the last warp produces
+    const int nct = ncw * 32;
+    const int64_t start = (int64_t)rank * a.slice;
+    const int n = (int)max((int64_t)0, min(a.cols - start, (int64_t)a.slice));
+    const int nvec = n / VEC;
+    const int vpc = a.chunk / VEC;                      // vectors per slot
+    const int cpr_full = (a.slice + a.chunk - 1) / a.chunk;  // slots per row slot
+    const int cpr = (n + a.chunk - 1) / a.chunk;        // chunks this CTA stages per row
+    const int NR = a.nslots / cpr_full;                 // rows the ring holds
+    const uint32_t ring_s = smem_u32(ring);             // shared-window address for the bulk copies
+    const uint32_t slot_bytes = (uint32_t)a.chunk * (uint32_t)sizeof(T);
+    const int64_t nrows = cid < a.rows ? (a.rows - 1 - cid) / a.nclusters + 1 : 0;
+    const bool clustered = P > 1;
+    // Row k of this CTA lives in row slot k mod NR: slots
+    // [rs * cpr_full, rs * cpr_full + cpr), contiguous in shared memory; the
+    // slot's use count is k div NR.  Both are tracked incrementally.
+
+    if (tid == 0) {
+        for (int s = 0; s < NR * cpr_full; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), (uint32_t)ncw);
+        }
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (clustered) cluster_arrive_relaxed();
+
+    // ------------------------------------------------------------ producer
+    if (warp == ncw) {
+        const uint64_t pol = l2_policy_evict_first();
+        int rs = 0;
+        uint32_t use = 0;
+        for (int64_t k = 0; k < nrows; ++k) {
+            if (lane == 0) {
+                const T* src = static_cast<const T*>(a.x) + (cid + k * a.nclusters) * a.cols + start;
+                for (int c = 0; c < cpr; ++c) {
+                    const int slot = rs * cpr_full + c;
+                    if (use > 0) mbar_wait_bounded(smem_u32(&empty_bar[slot]), (use - 1) & 1u, a.err);
+                    const int e0 = c * a.chunk;
+                    const uint32_t bytes = (uint32_t)(min(a.chunk, n - e0) * (int)sizeof(T));
+                    const uint32_t fb = smem_u32(&full_bar[slot]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    bulk_g2s(ring_s + (uint32_t)slot * slot_bytes, src + e0, bytes, fb, pol);
+                }
+            }
+            if (++rs == NR) { rs = 0; ++use; }
+            __syncwarp();
+            if (clustered) {
+                cluster_wait_acquire();   // entry phase (k == 0) or row k-1
+                cluster_arrive_relaxed(); // row k
+            }
+        }
+        if (clustered) cluster_wait_acquire();  // last row (or the entry phase)
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers
+    const PT* gp = static_cast<const PT*>(a.p0);
+    const PT* bp = static_cast<const PT*>(a.p1);
+    int rs = 0;
+    uint32_t use = 0;
+    for (int64_t k = 0; k < nrows; ++k) {
+        const int64_t row = cid + k * a.nclusters;
+        unsigned char* base = ring + (size_t)rs * cpr_full * slot_bytes;  // the staged slice
+
+        // a2 + a3: fold each chunk into the thread's statistics as it lands
+        Stats<OP, T> stt;
+        for (int c = 0; c < cpr; ++c) {
+            mbar_wait_bounded(smem_u32(&full_bar[rs * cpr_full + c]), use & 1u, a.err);
+            const int v0 = c * vpc;
+            stats_tiles(stt, base + (size_t)v0 * 16, min(nvec, v0 + vpc) - v0, warp, ncw, lane);
+        }
+        auto stash = [&](float mq) { return softmax_stash(base, nvec, warp, ncw, lane, mq); };
+        float p0, p1, p2;
+        cta_partial<OP, T>(stt, red[k & 1][0], red[k & 1][1], ncw, nct, stash, p0, p1, p2);
+
+        // a4 + a5 + a6: replicated push, cluster barrier, local combine
+        float st0 = p0, st1 = p1, st2 = p2;
+        if (clustered) {
+            if (k == 0) cluster_wait_acquire();  // every peer is running
+            float* sl = slots[k & 1];
+            if (tid < (int)P) {
+                const uint32_t dst = mapa_shared(smem_u32(&sl[rank * kSlotStride]), (uint32_t)tid);
+                st_cluster_v4f32(dst, p0, p1, p2, 0.f);
+            }
+            cluster_arrive_release();
+            cluster_wait_acquire();
+            combine_slots<OP>(sl, P, st0, st1, st2);
+        }
+
+        // a7: apply h to the staged slice, then release the row's slots
+        const OutputMap<OP, T> h(st0, st1, st2, p0, a.cols, a.eps);
+        T* yrow = static_cast<T*>(a.y) + row * a.cols + start;
+        output_tiles<OP, T, PT>(h, base, yrow, gp ? gp + start : nullptr, bp ? bp + start : nullptr,
+                                nvec, warp, ncw, lane);
+        // the fp32 softmax stash wrote the slots: order those generic-proxy
+        // writes before the bulk copies that will refill them
+        if constexpr (OP == kSoftmax && sizeof(T) == 4) fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+            for (int c = 0; c < cpr; ++c) mbar_arrive(smem_u32(&empty_bar[rs * cpr_full + c]));
+        if (++rs == NR) { rs = 0; ++use; }
+    }
+    if (clustered && nrows == 0) cluster_wait_acquire();  // entry phase
+}
+
+// ----------------------------------------------------------- dispatch
+template <int OP, typename T>
+static const void* pers_param(int pdtype) {
+    return pdtype == 0 ? (const void*)cluster_persistent<OP, T, float>
+                       : (const void*)cluster_persistent<OP, T, bf16>;
+}
+
+const void* persistent_kernel(KernelKey k) {
+    if (!k.vec) return nullptr;  // the ring is filled by bulk copies only
+    switch (k.op) {
+        case kSoftmax: return k.dtype == 0 ? (const void*)cluster_persistent<kSoftmax, float, float>
+                                           : (const void*)cluster_persistent<kSoftmax, bf16, float>;
+        case kLayerNorm: return k.dtype == 0 ? pers_param<kLayerNorm, float>(k.pdtype)
+                                             : pers_param<kLayerNorm, bf16>(k.pdtype);
+        case kRMSNorm: return k.dtype == 0 ? pers_param<kRMSNorm, float>(k.pdtype)
+                                           : pers_param<kRMSNorm, bf16>(k.pdtype);
+    }
+    return nullptr;
+}
+
+cudaError_t launch_persistent(KernelKey k, const PersistArgs& a, int P, int threads,
+                              size_t smem, cudaStream_t s) {
+    const void* fn = persistent_kernel(k);
+    if (!fn) return cudaErrorInvalidDeviceFunction;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.nclusters * P), 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)P;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = P > 1 ? 1 : 0;
+    PersistArgs b = a;
+    void* args[] = {&b};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace credit

@@ -49,13 +49,71 @@ int64_t bulk_chunk_elems(int64_t slice_elems, int elem_bytes) {
     return round_up(std::max(target, ceil_div(slice_elems, kMaxChunks)), vec);
 }
 
+namespace {
+
+// Persistent plan for a given (P, CTAs per SM).
+credit_status_t persistent_plan(int dev, const DevInfo* d, credit_op_t op, int64_t rows,
+                                int64_t cols, credit_dtype_t dtype, int P, int threads,
+                                int cps, int64_t chunk_override, credit_plan_t* p) {
+    const int es = dtype == CREDIT_F32 ? 4 : 2;
+    const int64_t vec = 16 / es;
+    const int64_t slice = round_up(ceil_div(cols, P), vec);
+    if (slice > INT32_MAX / 4) return CREDIT_ERR_NO_LEGAL_PLAN;
+    // a slot holds a power-of-two number of 16-byte vectors: 16 KiB, or the
+    // next power of two above a smaller slice (one slot per row then)
+    int64_t chunk_vecs = 16384 / 16;
+    if (chunk_override > 0) chunk_vecs = chunk_override / vec;
+    if (chunk_vecs < 1 || (chunk_vecs & (chunk_vecs - 1)) != 0 || chunk_vecs * 16 > (1 << 20))
+        return CREDIT_ERR_INVALID_ARG;
+    while (chunk_vecs / 2 * vec >= slice) chunk_vecs /= 2;
+    const int64_t chunk = chunk_vecs * vec;
+    const int64_t chunk_bytes = chunk * es;
+    const int64_t cpr = ceil_div(slice, chunk);
+    const void* fn = persistent_kernel(KernelKey{(int)op, (int)dtype, 0, true});
+    const KernelInfo* ki = kernel_info(dev, fn, true);
+    if (!ki) return CREDIT_ERR_CUDA;
+    const int64_t budget = cps == 1
+        ? ki->max_dyn_smem
+        : (int64_t)d->smem_per_sm / cps - ki->static_smem - d->reserved_smem;
+    const int64_t fit = std::min<int64_t>(kPersistMaxSlots, budget / chunk_bytes);
+    // the ring holds whole row slices (contiguous in shared memory): at least
+    // one, up to three
+    const int64_t nr = std::min<int64_t>(3, fit / cpr);
+    if (nr < 1) return CREDIT_ERR_NO_LEGAL_PLAN;  // a whole slice must fit the ring
+    const int64_t S = nr * cpr;
+    const int t = threads ? threads : (cps == 1 ? kPersistMaxThreads : 288);
+    if (t < 64 || t > kPersistMaxThreads) return CREDIT_ERR_INVALID_ARG;
+    const int64_t smem = S * chunk_bytes;
+    const int active = occupancy_clusters(dev, fn, P, t, (size_t)smem, rows);
+    if (active < 1) return CREDIT_ERR_NO_LEGAL_PLAN;
+    const int64_t G = std::min<int64_t>(active, rows);
+    p->variant = CREDIT_CLUSTER_PERSISTENT;
+    p->cluster_size = P;
+    p->threads = t;
+    p->smem_bytes = smem;
+    p->slice_elems = slice;
+    p->chunk_elems = (int32_t)chunk;
+    p->ring_slots = (int32_t)S;
+    p->active_clusters = (int32_t)G;
+    p->ctas_per_sm = cps;
+    p->waves = (int32_t)std::min<int64_t>(ceil_div(rows, G), INT32_MAX);
+    const double bytes = 2.0 * (double)rows * (double)cols * es;
+    const double coverage = std::min(1.0, (double)G * P / ((double)d->sms * cps));
+    const double pipe = nr >= 2 ? 0.95 : 0.8;
+    p->pred_us = (float)(bytes / (kNominalBytesPerUs * coverage * pipe) + kLaunchUs);
+    return CREDIT_OK;
+}
+
+}  // namespace
+
 credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
                           credit_dtype_t dtype, credit_variant_t variant, int P,
-                          int threads, credit_plan_t* out) {
+                          int threads, int cps, credit_plan_t* out, int64_t chunk) {
     if (!out || rows < 1 || cols < 1) return CREDIT_ERR_INVALID_ARG;
     if (!op_ok(op)) return CREDIT_ERR_UNSUPPORTED;
     if (dtype != CREDIT_F32 && dtype != CREDIT_BF16) return CREDIT_ERR_UNSUPPORTED;
-    if (threads != 0 && (threads < 32 || threads > kMaxThreads || threads % 32 != 0))
+    if (threads != 0 && (threads < 32 || threads % 32 != 0)) return CREDIT_ERR_INVALID_ARG;
+    if (threads > (variant == CREDIT_CLUSTER_PERSISTENT ? kPersistMaxThreads : kMaxThreads))
         return CREDIT_ERR_INVALID_ARG;
     const DevInfo* d = device_info(dev);
     if (!d) return CREDIT_ERR_CUDA;
@@ -64,6 +122,7 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
     credit_plan_t p;
     std::memset(&p, 0, sizeof(p));
     p.variant = variant;
+    p.ctas_per_sm = 1;
     const double bytes = 2.0 * (double)rows * (double)cols * es;
 
     if (variant == CREDIT_CLUSTER) {
@@ -81,12 +140,31 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
         p.threads = t;
         p.smem_bytes = smem;
         p.slice_elems = slice;
+        p.chunk_elems = (int32_t)bulk_chunk_elems(slice, es);
         p.active_clusters = active;
+        p.ctas_per_sm = std::max(1, (int)((int64_t)active * P / d->sms));
         p.waves = (int32_t)std::min<int64_t>(ceil_div(rows, active), INT32_MAX);
         const double ctas_per_sm = (double)active * P / d->sms;
         const double eff = ctas_per_sm >= 2.0 ? 0.9 : 0.7;
         p.pred_us = (float)(bytes / (kNominalBytesPerUs * eff) +
                             p.waves * (P > 1 ? kWaveUsCluster : kWaveUsSingle));
+    } else if (variant == CREDIT_CLUSTER_PERSISTENT) {
+        if (P < 1 || P > kMaxCluster) return CREDIT_ERR_NO_LEGAL_PLAN;
+        if (cps != 0 && cps != 1 && cps != 2) return CREDIT_ERR_INVALID_ARG;
+        credit_status_t best = CREDIT_ERR_NO_LEGAL_PLAN;
+        for (int c = 1; c <= 2; ++c) {
+            if (cps && c != cps) continue;
+            credit_plan_t q;
+            std::memset(&q, 0, sizeof(q));
+            const credit_status_t st =
+                persistent_plan(dev, d, op, rows, cols, dtype, P, threads, c, chunk, &q);
+            if (st == CREDIT_ERR_CUDA || st == CREDIT_ERR_INVALID_ARG) return st;
+            if (st == CREDIT_OK && (best != CREDIT_OK || q.pred_us < p.pred_us)) {
+                p = q;
+                best = CREDIT_OK;
+            }
+        }
+        if (best != CREDIT_OK) return best;
     } else if (variant == CREDIT_TWO_PASS) {
         const int64_t per_thread = kTwoPassVpt * vec;
         int t = threads;
@@ -106,6 +184,7 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
         p.cluster_size = 1;
         p.threads = t;
         p.slice_elems = chunk;
+        p.chunk_elems = (int32_t)chunk;
         p.workspace_bytes = rows * nch * 4 * (int64_t)sizeof(float);
         p.active_clusters = active;
         p.waves = (int32_t)std::min<int64_t>(ceil_div(rows * nch, active), INT32_MAX);
@@ -122,14 +201,17 @@ credit_status_t auto_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
                           credit_dtype_t dtype, credit_plan_t* out) {
     if (!out || rows < 1 || cols < 1) return CREDIT_ERR_INVALID_ARG;
     credit_plan_t base;
-    credit_status_t st = make_plan(dev, op, rows, cols, dtype, CREDIT_TWO_PASS, 0, 0, &base);
+    credit_status_t st = make_plan(dev, op, rows, cols, dtype, CREDIT_TWO_PASS, 0, 0, 0, &base);
     if (st != CREDIT_OK) return st;
     credit_plan_t best = base;
-    for (int P = 1; P <= kMaxCluster; ++P) {
-        credit_plan_t c;
-        if (make_plan(dev, op, rows, cols, dtype, CREDIT_CLUSTER, P, 0, &c) != CREDIT_OK) continue;
-        if (P > 1 && (int64_t)(P - 1) * c.slice_elems >= cols) continue;  // an idle CTA
-        if (c.pred_us < best.pred_us) best = c;
+    for (int v = 0; v < 2; ++v) {
+        const credit_variant_t var = v == 0 ? CREDIT_CLUSTER : CREDIT_CLUSTER_PERSISTENT;
+        for (int P = 1; P <= kMaxCluster; ++P) {
+            credit_plan_t c;
+            if (make_plan(dev, op, rows, cols, dtype, var, P, 0, 0, &c) != CREDIT_OK) continue;
+            if (P > 1 && (int64_t)(P - 1) * c.slice_elems >= cols) continue;  // an idle CTA
+            if (c.pred_us < best.pred_us) best = c;
+        }
     }
     best.pred_two_pass_us = base.pred_us;
     *out = best;

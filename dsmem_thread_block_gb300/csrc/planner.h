@@ -3,7 +3,7 @@
 
 #include <cstdint>
 
-#include "../../include/credit.h"
+#include "credit.h"
 
 namespace credit {
 
@@ -34,10 +34,13 @@ int occupancy_clusters(int dev, const void* fn, int P, int threads, size_t smem,
 // Elements per bulk copy (one mbarrier each) for a staged slice.
 int64_t bulk_chunk_elems(int64_t slice_elems, int elem_bytes);
 
-// Build the plan of a given variant (threads == 0: choose).
+// Build the plan of a given variant (threads == 0 / cps == 0 / chunk == 0:
+// choose).  cps is the number of persistent CTAs meant to share one SM (1 or
+// 2); chunk the persistent ring's slot size in elements (a power-of-two
+// number of 16-byte vectors).
 credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
                           credit_dtype_t dtype, credit_variant_t variant, int P,
-                          int threads, credit_plan_t* out);
+                          int threads, int cps, credit_plan_t* out, int64_t chunk = 0);
 
 // Enumerate legal candidates and keep the predicted-fastest.
 credit_status_t auto_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,

@@ -1,0 +1,393 @@
+// rowops.cuh -- the per-element arithmetic of the three operators, written
+// with Blackwell's packed fp32x2 instructions (fma / add / sub / mul .f32x2)
+// so that two elements cost one floating-point instruction, plus the
+// per-thread statistics, the CTA-level partial and the output map h.
+//
+// Statistics per thread (CREDIT summary page, arXiv 2609.01864v1, "C.
+// Cluster Reduction and Reuse Protocol": thread accumulation, then warp
+// shuffles, then a shared-memory fold):
+//   RMSNorm          sum of squares
+//   LayerNorm        shifted sums around the thread's first element K:
+//                    n, s1 = sum (x - K), s2 = sum (x - K)^2
+//   softmax, bf16    online (m, s): running max, sum of exp relative to it
+//   softmax, fp32    the max only; a second local pass over the staged slice
+//                    then writes t = exp(x - m_q) back in place and sums it,
+//                    so the output pass is a single multiply
+#pragma once
+
+#include "common.cuh"
+
+namespace credit {
+
+// ------------------------------------------------------------ packed math
+// float2 pairs and the sm_100-family packed builtins (one FFMA2 / FADD2 /
+// FMUL2 per two elements, round to nearest).
+using F2 = float2;
+
+__device__ __forceinline__ F2 f2(float v) { return make_float2(v, v); }
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ F2 add2(F2 a, F2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ F2 mul2(F2 a, F2 b) { return __fmul2_rn(a, b); }
+// three-input max
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// ----------------------------------------------------------- warp tiles
+// Work over a contiguous staged range is split into warp tiles of 32 x U
+// items: warp w takes tiles w, w + nwarps, ...; lane l takes items
+// tile + l + 32u.  Lane offsets inside a tile are compile-time constants and
+// only the one partial tile of a warp carries bounds checks.
+template <int U, typename F>
+__device__ __forceinline__ void for_tiles(int n, int warp, int nwarps, int lane, F f) {
+    constexpr int kTile = 32 * U;
+    int t = warp * kTile;
+    for (; t + kTile <= n; t += nwarps * kTile) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) f(t + lane + 32 * u);
+    }
+    if (t < n) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = t + lane + 32 * u;
+            if (i < n) f(i);
+        }
+    }
+}
+
+// 16-byte vector <-> element pairs (VEC / 2 pairs)
+template <typename T> struct Pairs;
+template <> struct Pairs<float> {
+    static constexpr int kN = 2;
+    __device__ static void unpack(uint4 v, F2* p) {
+        p[0] = {__uint_as_float(v.x), __uint_as_float(v.y)};
+        p[1] = {__uint_as_float(v.z), __uint_as_float(v.w)};
+    }
+    __device__ static uint4 pack(const F2* p) {
+        return make_uint4(__float_as_uint(p[0].x), __float_as_uint(p[0].y),
+                          __float_as_uint(p[1].x), __float_as_uint(p[1].y));
+    }
+};
+template <> struct Pairs<bf16> {
+    static constexpr int kN = 4;
+    __device__ static F2 one(uint32_t w) {
+        return {__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)};
+    }
+    __device__ static void unpack(uint4 v, F2* p) {
+        p[0] = one(v.x); p[1] = one(v.y); p[2] = one(v.z); p[3] = one(v.w);
+    }
+    __device__ static uint32_t two(F2 a) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a.x, a.y);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __device__ static uint4 pack(const F2* p) {
+        return make_uint4(two(p[0]), two(p[1]), two(p[2]), two(p[3]));
+    }
+};
+
+// Per-column parameters of one 16-byte vector as pairs (absent = fill).
+template <typename PT, int NP>
+__device__ __forceinline__ void load_param_pairs(const PT* p, int64_t j0, F2* out, float fill) {
+    constexpr int VEC = 2 * NP;
+    if (!p) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) out[i] = f2(fill);
+        return;
+    }
+    float v[VEC];
+    load_params<PT, VEC>(p, j0, v);
+#pragma unroll
+    for (int i = 0; i < NP; ++i) out[i] = {v[2 * i], v[2 * i + 1]};
+}
+
+// ------------------------------------------------------- thread statistics
+template <int OP, typename T> struct Stats;
+
+template <typename T> struct Stats<kRMSNorm, T> {
+    F2 q = {0.f, 0.f};
+    __device__ __forceinline__ void add(uint4 raw) {
+        F2 p[Pairs<T>::kN];
+        Pairs<T>::unpack(raw, p);
+#pragma unroll
+        for (int i = 0; i < Pairs<T>::kN; ++i) q = fma2(p[i], p[i], q);
+    }
+    __device__ __forceinline__ void add1(float f) { q.x = fmaf(f, f, q.x); }
+};
+
+template <typename T> struct Stats<kLayerNorm, T> {
+    F2 nK = {0.f, 0.f}, s1 = {0.f, 0.f}, s2 = {0.f, 0.f};  // nK = -K in both lanes
+    float n = 0.f;
+    __device__ __forceinline__ void add(uint4 raw) {
+        F2 p[Pairs<T>::kN];
+        Pairs<T>::unpack(raw, p);
+        if (n == 0.f) nK = f2(-p[0].x);
+#pragma unroll
+        for (int i = 0; i < Pairs<T>::kN; ++i) {
+            const F2 d = add2(p[i], nK);
+            s1 = add2(s1, d);
+            s2 = fma2(d, d, s2);
+        }
+        n += (float)(2 * Pairs<T>::kN);
+    }
+    __device__ __forceinline__ void add1(float f) {
+        if (n == 0.f) nK = f2(-f);
+        const float d = f + nK.x;
+        s1.x += d;
+        s2.x = fmaf(d, d, s2.x);
+        n += 1.f;
+    }
+};
+
+// bf16 softmax: online max and sum of exp relative to it
+template <> struct Stats<kSoftmax, bf16> {
+    float m = -INFINITY;
+    F2 s = {0.f, 0.f};
+    __device__ __forceinline__ void rebase(float vm) {
+        if (vm > m) {
+            const float sc = (s.x == 0.f && s.y == 0.f) ? 0.f : fast_ex2((m - vm) * kLog2e);
+            s = mul2(s, f2(sc));
+            m = vm;
+        }
+    }
+    __device__ __forceinline__ void add(uint4 raw) {
+        F2 p[4];
+        Pairs<bf16>::unpack(raw, p);
+        const float vm = fmaxf(max3(p[0].x, p[0].y, p[1].x), max3(p[1].y, p[2].x, max3(p[2].y, p[3].x, p[3].y)));
+        rebase(vm);
+        const F2 nm = f2(-m * kLog2e), l2 = f2(kLog2e);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const F2 a = fma2(p[i], l2, nm);
+            s = add2(s, F2{fast_ex2(a.x), fast_ex2(a.y)});
+        }
+    }
+    __device__ __forceinline__ void add1(float f) {
+        rebase(f);
+        s.x += fast_ex2(fmaf(f, kLog2e, -m * kLog2e));
+    }
+};
+
+// fp32 softmax: the max only (the sum comes from the stash pass)
+template <> struct Stats<kSoftmax, float> {
+    float m = -INFINITY;
+    __device__ __forceinline__ void add(uint4 raw) {
+        m = max3(m, max3(__uint_as_float(raw.x), __uint_as_float(raw.y), __uint_as_float(raw.z)),
+                 __uint_as_float(raw.w));
+    }
+    __device__ __forceinline__ void add1(float f) { m = fmaxf(m, f); }
+};
+
+// fp32 softmax stash pass over the staged vectors [0, nvec) at `base`:
+// t = exp(x - mq) written back in place (accurate expf); returns this
+// thread's sum of t.  Vectors are visited in the same warp tiles as the
+// output pass, so each thread re-reads exactly what it wrote.
+__device__ __forceinline__ float softmax_stash(unsigned char* base, int nvec, int warp, int nwarps,
+                                               int lane, float mq) {
+    F2 s = {0.f, 0.f};
+    for_tiles<4>(nvec, warp, nwarps, lane, [&](int v) {
+        unsigned char* a = base + (size_t)v * 16;
+        const uint4 raw = lds16(a);
+        const F2 t0 = {expf(__uint_as_float(raw.x) - mq), expf(__uint_as_float(raw.y) - mq)};
+        const F2 t1 = {expf(__uint_as_float(raw.z) - mq), expf(__uint_as_float(raw.w) - mq)};
+        s = add2(s, add2(t0, t1));
+        *reinterpret_cast<uint4*>(a) = make_uint4(__float_as_uint(t0.x), __float_as_uint(t0.y),
+                                                  __float_as_uint(t1.x), __float_as_uint(t1.y));
+    });
+    return s.x + s.y;
+}
+
+// ---------------------------------------------------------- CTA partial
+// The CTA's compact partial from its threads' statistics: softmax (m, s),
+// LayerNorm (n, mean, M2), RMSNorm (ss).  At most two block reductions and
+// no per-step division: LayerNorm reduces (n, sum n_t mean_t), then
+// sum M2_t + n_t (mean_t - mean)^2 (the parallel-axis form of Chan et al.'s
+// merge); softmax reduces the max, then each thread's sum rescaled to it.
+// redA / redB: 2 floats per warp each.  For fp32 softmax `stash_sum` runs
+// the stash pass with the CTA max and returns the thread's sum.
+template <int OP, typename T, typename StashFn>
+__device__ __forceinline__ void cta_partial(const Stats<OP, T>& st, float* redA, float* redB,
+                                            int nwarps, int nthreads, StashFn stash_sum,
+                                            float& p0, float& p1, float& p2) {
+    p1 = p2 = 0.f;
+    float unused = 0.f;
+    if constexpr (OP == kSoftmax) {
+        const float m = block_max1(st.m, redA, nwarps, nthreads);
+        float s;
+        if constexpr (sizeof(T) == 4) s = m == -INFINITY ? 0.f : stash_sum(m);
+        else s = rescale(st.s.x + st.s.y, st.m, m);
+        block_sum2(s, unused, redB, nwarps, nthreads);
+        p0 = m; p1 = s;
+    } else if constexpr (OP == kLayerNorm) {
+        const float s1 = st.s1.x + st.s1.y, s2 = st.s2.x + st.s2.y;
+        const float mt = st.n > 0.f ? s1 / st.n - st.nK.x : 0.f;
+        const float m2t = st.n > 0.f ? fmaxf(s2 - s1 * (s1 / st.n), 0.f) : 0.f;
+        float n = st.n, nm = st.n * mt;
+        block_sum2(n, nm, redA, nwarps, nthreads);
+        const float mean = n > 0.f ? nm / n : 0.f;
+        const float d = mt - mean;
+        float q = fmaf(st.n * d, d, m2t);
+        block_sum2(q, unused, redB, nwarps, nthreads);
+        p0 = n; p1 = mean; p2 = q;
+    } else {
+        float ss = st.q.x + st.q.y;
+        block_sum2(ss, unused, redA, nwarps, nthreads);
+        p0 = ss;
+    }
+}
+
+// ------------------------------------------------------------ output map
+// h from the combined statistics (st0, st1, st2) of a row of N columns and
+// (fp32 softmax) the CTA's own max mq:
+//   softmax bf16  y = 2^(x log2 e - m log2 e) / s
+//   softmax fp32  y = t * (exp(mq - m) / s), t = exp(x - mq) from the stash
+//   LayerNorm     y = (x r - mean r) gamma + beta,  r = 1 / sqrt(M2 / N + eps)
+//   RMSNorm       y = (x r) w,                      r = 1 / sqrt(ss / N + eps)
+template <int OP, typename T>
+struct OutputMap {
+    float c0 = 0.f, c1 = 0.f;
+    __device__ __forceinline__ OutputMap(float st0, float st1, float st2, float mq, int64_t N,
+                                         float eps) {
+        if constexpr (OP == kSoftmax) {
+            if constexpr (sizeof(T) == 4) { c1 = rescale(1.f, mq, st0) / st1; }
+            else { c0 = -st0 * kLog2e; c1 = 1.f / st1; }
+        } else if constexpr (OP == kLayerNorm) {
+            const float r = 1.f / sqrtf(fmaxf(st2 / (float)N, 0.f) + eps);
+            c0 = r;
+            c1 = -st1 * r;
+        } else {
+            c0 = 1.f / sqrtf(st0 / (float)N + eps);
+        }
+    }
+    __device__ __forceinline__ F2 operator()(F2 x, F2 g, F2 b) const {
+        if constexpr (OP == kSoftmax) {
+            if constexpr (sizeof(T) == 4) return mul2(x, f2(c1));
+            const F2 a = fma2(x, f2(kLog2e), f2(c0));
+            return mul2(F2{fast_ex2(a.x), fast_ex2(a.y)}, f2(c1));
+        } else if constexpr (OP == kLayerNorm) {
+            return fma2(fma2(x, f2(c0), f2(c1)), g, b);
+        } else {
+            return mul2(mul2(x, f2(c0)), g);
+        }
+    }
+    // the same arithmetic on one element (element path)
+    __device__ __forceinline__ float one(float x, float g, float b) const {
+        if constexpr (OP == kSoftmax) {
+            if constexpr (sizeof(T) == 4) return x * c1;
+            return fast_ex2(fmaf(x, kLog2e, c0)) * c1;
+        } else if constexpr (OP == kLayerNorm) {
+            return fmaf(fmaf(x, c0, c1), g, b);
+        } else {
+            return (x * c0) * g;
+        }
+    }
+};
+
+// Statistics over staged 16-byte vectors [0, n) at `base`.
+template <int OP, typename T>
+__device__ __forceinline__ void stats_tiles(Stats<OP, T>& st, const unsigned char* base, int n,
+                                            int warp, int nwarps, int lane) {
+    for_tiles<4>(n, warp, nwarps, lane, [&](int v) { st.add(lds16(base + (size_t)v * 16)); });
+}
+
+// Output granule of an operator: 4 elements for bf16 data with fp32
+// parameters (so one 16-byte gamma load and one 16-byte beta load cover it),
+// else one 16-byte vector of data.
+template <int OP, typename T, typename PT>
+struct Granule {
+    static constexpr bool kHalf = OP != kSoftmax && sizeof(T) == 2 && sizeof(PT) == 4;
+    static constexpr int kElems = kHalf ? 4 : 16 / (int)sizeof(T);
+    static constexpr int kBytes = kElems * (int)sizeof(T);
+    static constexpr int kPairs = kElems / 2;
+};
+
+// Load the parameters of one granule (kElems values, <= 16 bytes) as pairs.
+template <typename PT, int NP>
+__device__ __forceinline__ void granule_params(const PT* p, int q, F2* out) {
+    if constexpr (sizeof(PT) == 4) {
+        if constexpr (NP == 2) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(p) + q);
+            out[0] = make_float2(v.x, v.y);
+            out[1] = make_float2(v.z, v.w);
+        } else {  // NP == 4 cannot happen for fp32 parameters (16 bytes max)
+            static_assert(NP == 2, "fp32 parameters: 4 per granule");
+        }
+    } else {
+        if constexpr (NP == 4) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + q);
+            Pairs<bf16>::unpack(v, out);
+        } else {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(p) + q);
+            out[0] = Pairs<bf16>::one(v.x);
+            out[1] = Pairs<bf16>::one(v.y);
+        }
+    }
+}
+
+// Apply h to the staged slice ([0, nvec) 16-byte vectors at `base`) and
+// store it to `yrow`; gp / bp are the slice's parameters (null = absent).
+// Each warp tile loads all its data and parameters before its first store,
+// so parameter fetches overlap instead of queueing behind stores.
+template <int OP, typename T, typename PT>
+__device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const unsigned char* base,
+                                             T* yrow, const PT* gp, const PT* bp, int nvec,
+                                             int warp, int nwarps, int lane) {
+    using G = Granule<OP, T, PT>;
+    constexpr int U = 4, NP = G::kPairs, kTile = 32 * U;
+    const int ngran = nvec * (16 / G::kBytes);
+    const bool has_g = OP != kSoftmax && gp != nullptr;
+    const bool has_b = OP != kSoftmax && bp != nullptr;
+
+    auto tile = [&](int t, bool full) {
+        uint4 raw[U];
+        F2 gv[U][NP], bv[U][NP];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = t + lane + 32 * u;
+            if (full || q < ngran) {
+                if constexpr (G::kBytes == 8) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(base + (size_t)q * 8);
+                    raw[u] = make_uint4(w.x, w.y, 0u, 0u);
+                } else {
+                    raw[u] = lds16(base + (size_t)q * 16);
+                }
+                if constexpr (OP != kSoftmax) {
+                    if (has_g) granule_params<PT, NP>(gp, q, gv[u]);
+                    else for (int i = 0; i < NP; ++i) gv[u][i] = f2(1.f);
+                    if (has_b) granule_params<PT, NP>(bp, q, bv[u]);
+                    else for (int i = 0; i < NP; ++i) bv[u][i] = f2(0.f);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = t + lane + 32 * u;
+            if (full || q < ngran) {
+                F2 p[NP];
+                if constexpr (G::kBytes == 8) {
+                    p[0] = Pairs<bf16>::one(raw[u].x);
+                    p[1] = Pairs<bf16>::one(raw[u].y);
+                } else {
+                    Pairs<T>::unpack(raw[u], p);
+                }
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    if constexpr (OP == kSoftmax) p[i] = h(p[i], p[i], p[i]);
+                    else p[i] = h(p[i], gv[u][i], bv[u][i]);
+                }
+                if constexpr (G::kBytes == 8) {
+                    __stcs(reinterpret_cast<uint2*>(yrow) + q,
+                           make_uint2(Pairs<bf16>::two(p[0]), Pairs<bf16>::two(p[1])));
+                } else {
+                    stg16_stream(reinterpret_cast<uint4*>(yrow) + q, Pairs<T>::pack(p));
+                }
+            }
+        }
+    };
+    int t = warp * kTile;
+    for (; t + kTile <= ngran; t += nwarps * kTile) tile(t, true);
+    if (t < ngran) tile(t, false);
+}
+
+}  // namespace credit

@@ -1,0 +1,44 @@
+"""DSMEM microbenchmark suite (command line).
+
+Measures, on one GPU, the cluster-barrier round trip and the replicated-push
+exchange for every cluster size 2..16, remote and local shared-memory load
+latency (pointer chase), and remote / local 16-byte load and store throughput
+of one CTA, each as the median of 15 launches (CREDIT summary page, "C.
+Positioning": latency, throughput and repeated cluster-synchronisation
+microbenchmarks with the CTAs on different SMs).  Prints one JSON object.
+
+    python -m dsmem_thread_block_gb300.microbench [--device 0] [--runs 15]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+from . import _credit as C
+
+
+def run_suite(device: int = 0, runs: int = 15, sizes=range(2, 17)) -> dict:
+    out = {"device": device, "runs": runs, "barrier": {}, "exchange": {}}
+    for P in sizes:
+        out["barrier"][P] = C.credit_bench_dsmem(device, C.BENCH_BARRIER, P, 2000, runs).as_dict()
+        out["exchange"][P] = C.credit_bench_dsmem(device, C.BENCH_EXCHANGE, P, 2000, runs).as_dict()
+    for name, kind, iters in (("remote_load_latency", C.BENCH_REMOTE_LOAD_LATENCY, 20000),
+                              ("local_load_latency", C.BENCH_LOCAL_LOAD_LATENCY, 20000),
+                              ("remote_store_bw", C.BENCH_REMOTE_STORE_BW, 64),
+                              ("remote_load_bw", C.BENCH_REMOTE_LOAD_BW, 64),
+                              ("local_store_bw", C.BENCH_LOCAL_STORE_BW, 64),
+                              ("local_load_bw", C.BENCH_LOCAL_LOAD_BW, 64)):
+        out[name] = C.credit_bench_dsmem(device, kind, 2, iters, runs).as_dict()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--device", type=int, default=0)
+    ap.add_argument("--runs", type=int, default=15)
+    a = ap.parse_args()
+    print(json.dumps(run_suite(a.device, a.runs)))
+
+
+if __name__ == "__main__":
+    main()

@@ -59,22 +59,31 @@ typedef enum {
 
 typedef enum {
     CREDIT_AUTO = 0,       /* let credit_plan decide */
-    CREDIT_CLUSTER = 1,    /* clustered DSMEM kernel, cluster_size = P (1..16) */
-    CREDIT_TWO_PASS = 2    /* non-clustered two-pass re-read kernel pair */
+    CREDIT_CLUSTER = 1,    /* clustered DSMEM kernel, one row per cluster of
+                              cluster_size = P CTAs (1..16) */
+    CREDIT_TWO_PASS = 2,   /* non-clustered two-pass re-read kernel pair */
+    CREDIT_CLUSTER_PERSISTENT = 3  /* clustered DSMEM kernel, resident clusters
+                              loop over rows; a producer warp streams chunks
+                              into a ring of shared-memory slots */
 } credit_variant_t;
 
 /*
  * A launch plan.  Produced by credit_plan / credit_plan_for; may be passed to
  * the operator calls (NULL there means "plan automatically").
- *   variant          CREDIT_CLUSTER or CREDIT_TWO_PASS (never AUTO once planned)
+ *   variant          CREDIT_CLUSTER, CREDIT_CLUSTER_PERSISTENT or
+ *                    CREDIT_TWO_PASS (never AUTO once planned)
  *   cluster_size     P, CTAs per row (1..16; 1 = one CTA stages the whole row)
  *   threads          threads per CTA
- *   smem_bytes       dynamic shared memory per CTA (the staged slice)
- *   workspace_bytes  device workspace the call needs (TWO_PASS only, else 0)
- *   slice_elems      elements of a row owned by one CTA (CLUSTER) or one
- *                    chunk (TWO_PASS)
  *   waves            predicted waves of resident clusters, ceil(rows / active)
- *   active_clusters  clusters resident at once (cudaOccupancyMaxActiveClusters)
+ *   smem_bytes       dynamic shared memory per CTA (staged slice or ring)
+ *   workspace_bytes  device workspace the call needs (TWO_PASS only, else 0)
+ *   slice_elems      elements of a row owned by one CTA (CLUSTER variants) or
+ *                    one chunk (TWO_PASS)
+ *   active_clusters  clusters resident at once (cudaOccupancyMaxActiveClusters);
+ *                    the persistent grid has this many clusters
+ *   ctas_per_sm      CTAs the plan expects to share one SM
+ *   chunk_elems      elements per bulk copy (one mbarrier each)
+ *   ring_slots       shared-memory chunk slots per CTA (persistent only)
  *   pred_us          predicted time of this plan, microseconds (0 = none)
  *   pred_two_pass_us predicted / measured time of the two-pass baseline
  */
@@ -87,7 +96,9 @@ typedef struct {
     int64_t workspace_bytes;
     int64_t slice_elems;
     int32_t active_clusters;
-    int32_t reserved0;
+    int32_t ctas_per_sm;
+    int32_t chunk_elems;
+    int32_t ring_slots;
     float pred_us;
     float pred_two_pass_us;
 } credit_plan_t;
@@ -106,8 +117,9 @@ credit_status_t credit_plan(credit_op_t op, int64_t rows, int64_t cols,
                             credit_plan_t *out);
 
 /*
- * Build a plan for a forced variant: CREDIT_CLUSTER with the given
- * cluster_size (1..16), or CREDIT_TWO_PASS (cluster_size ignored).
+ * Build a plan for a forced variant: CREDIT_CLUSTER or
+ * CREDIT_CLUSTER_PERSISTENT with the given cluster_size (1..16), or
+ * CREDIT_TWO_PASS (cluster_size ignored).
  * Returns CREDIT_ERR_NO_LEGAL_PLAN if the slice does not fit in shared memory
  * or no cluster of that size can be resident.
  */
@@ -194,6 +206,62 @@ credit_status_t credit_two_pass_noalloc(credit_op_t op, const void *x, void *y,
                                         const void *p1,
                                         credit_dtype_t param_dtype, float eps,
                                         void *stream);
+
+/* ------------------------------------------------------------------------
+ * DSMEM characterisation (CREDIT "C. Positioning": latency, throughput and
+ * repeated cluster-synchronisation microbenchmarks with the CTAs on
+ * different SMs, median of the runs).  Each benchmark CTA claims more than
+ * half of an SM's shared memory, so no two CTAs share an SM; `smids` reports
+ * where they ran.  These calls allocate a few bytes of device memory and
+ * synchronise the device: they are for calibration, not for a hot path.
+ */
+typedef enum {
+    CREDIT_BENCH_BARRIER = 0,             /* cluster barrier round trip, P CTAs */
+    CREDIT_BENCH_EXCHANGE = 1,            /* replicated 16-byte push + barrier, P CTAs */
+    CREDIT_BENCH_REMOTE_LOAD_LATENCY = 2, /* pointer chase in a peer's SMEM */
+    CREDIT_BENCH_LOCAL_LOAD_LATENCY = 3,  /* the same chase in the CTA's own SMEM */
+    CREDIT_BENCH_REMOTE_STORE_BW = 4,     /* one CTA storing 16-byte vectors to a peer */
+    CREDIT_BENCH_REMOTE_LOAD_BW = 5,      /* one CTA loading 16-byte vectors from a peer */
+    CREDIT_BENCH_LOCAL_STORE_BW = 6,      /* the same stores to its own SMEM */
+    CREDIT_BENCH_LOCAL_LOAD_BW = 7        /* the same loads from its own SMEM */
+} credit_bench_kind_t;
+
+typedef struct {
+    int32_t kind;
+    int32_t cluster_size;    /* CTAs launched (2 for the pair kinds) */
+    int32_t runs;
+    int32_t smids[16];       /* SM id of each CTA, rank order (last run) */
+    double median_cycles;    /* per operation (barrier, hop, or 64 KiB pass), SM cycles */
+    double median_ns;        /* the same in nanoseconds (%globaltimer) */
+    double iqr_cycles;       /* interquartile range of the runs, cycles */
+    double bytes_per_cycle;  /* throughput kinds: bytes per SM cycle of one CTA */
+    double gbps;             /* throughput kinds: GB/s of one CTA */
+} credit_bench_result_t;
+
+/*
+ * Run one DSMEM microbenchmark on `device`: `iters` operations per launch,
+ * `runs` timed launches after one warm-up, median reported.  cluster_size
+ * (1..16) applies to the BARRIER and EXCHANGE kinds; the other kinds always
+ * use a pair of CTAs.  Returns CREDIT_ERR_INVALID_ARG for bad arguments.
+ */
+credit_status_t credit_bench_dsmem(int device, int kind, int cluster_size,
+                                   int iters, int runs,
+                                   credit_bench_result_t *out);
+
+/*
+ * Time the work-free control kernel (CREDIT "D. Profitability and Candidate
+ * Selection"): `nclusters` clusters of `cluster_size` CTAs of `threads`
+ * threads and `smem_bytes` dynamic shared memory, each passing
+ * `barriers_per_row` cluster barriers (block barriers when cluster_size is
+ * 1) for `rows_per_cluster` rows.  Median over `runs` launches, in
+ * microseconds (CUDA events).  T_ctrl of a candidate is its control time
+ * minus that of the one-CTA control with the same grid.
+ */
+credit_status_t credit_control_time(int device, int64_t nclusters,
+                                    int cluster_size, int threads,
+                                    int64_t smem_bytes, int rows_per_cluster,
+                                    int barriers_per_row, int runs,
+                                    double *median_us);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *credit_status_string(credit_status_t status);

@@ -22,10 +22,23 @@ pytestmark = pytest.mark.gpu
 TWO = ("two_pass", 0)
 
 
+def _try_plan(w, variant, P, rows=None):
+    try:
+        return make_plan(w, variant, P, rows=rows)
+    except C.CreditError as e:
+        assert e.status == C.ERR_NO_LEGAL_PLAN
+        return None
+
+
 def _plans(w, cluster_sizes, rows=None):
+    """One-row-per-cluster plans for `cluster_sizes` (must be legal), the
+    persistent plans of those sizes that are legal, and the two-pass plan."""
     out = []
     for P in cluster_sizes:
         out.append(make_plan(w, C.CLUSTER, P, rows=rows))
+        p = _try_plan(w, C.CLUSTER_PERSISTENT, P, rows=rows)
+        if p is not None:
+            out.append(p)
     out.append(make_plan(w, C.TWO_PASS, rows=rows))
     return out
 
@@ -36,6 +49,8 @@ def test_softmax_f32_64x4096_all_cluster_sizes():
     inp = w.generate()
     for P in (1, 2, 3, 4, 8, 16):
         got = run(w, inp, make_plan(w, C.CLUSTER, P))
+        check(w, got, inp)
+        got = run(w, inp, make_plan(w, C.CLUSTER_PERSISTENT, P))
         check(w, got, inp)
     got = run(w, inp, make_plan(w, C.TWO_PASS))
     check(w, got, inp)
@@ -75,12 +90,10 @@ def test_bf16_softmax_sweep_shapes(cols):
     inp = w.generate()
     # every power-of-two cluster size that is legal at this width, and two-pass
     for P in (1, 2, 4, 8, 16):
-        try:
-            p = make_plan(w, C.CLUSTER, P)
-        except C.CreditError as e:
-            assert e.status == C.ERR_NO_LEGAL_PLAN
-            continue
-        check(w, run(w, inp, p), inp)
+        for variant in (C.CLUSTER, C.CLUSTER_PERSISTENT):
+            p = _try_plan(w, variant, P)
+            if p is not None:
+                check(w, run(w, inp, p), inp)
     check(w, run(w, inp, make_plan(w, C.TWO_PASS)), inp)
 
 
@@ -109,17 +122,16 @@ EDGE = [
 def test_edge_shapes(w):
     inp = w.generate()
     for P in (1, 2, 3, 4, 7, 16):
-        try:
-            p = make_plan(w, C.CLUSTER, P)
-        except C.CreditError as e:
-            assert e.status == C.ERR_NO_LEGAL_PLAN
-            continue
-        check(w, run(w, inp, p), inp)
+        for variant in (C.CLUSTER, C.CLUSTER_PERSISTENT):
+            p = _try_plan(w, variant, P)
+            if p is not None:  # persistent plans of ragged rows run the element path
+                check(w, run(w, inp, p), inp)
     check(w, run(w, inp, make_plan(w, C.TWO_PASS)), inp)
     check(w, run(w, inp, None), inp)  # automatic plan
 
 
-@pytest.mark.parametrize("variant,P", [(C.CLUSTER, 1), (C.CLUSTER, 4), (C.TWO_PASS, 1)])
+@pytest.mark.parametrize("variant,P", [(C.CLUSTER, 1), (C.CLUSTER, 4), (C.TWO_PASS, 1),
+                                       (C.CLUSTER_PERSISTENT, 1), (C.CLUSTER_PERSISTENT, 4)])
 def test_in_place(variant, P):
     for w in (_custom(wl.SOFTMAX, "f32", 4, 16384, 20, x_std=2.0),
               _custom(wl.LAYERNORM, "bf16", 4, 16384, 21, eps=1e-5, param_dtype="f32"),
@@ -129,7 +141,8 @@ def test_in_place(variant, P):
         check(w, got, inp)
 
 
-@pytest.mark.parametrize("variant,P", [(C.CLUSTER, 1), (C.CLUSTER, 4), (C.TWO_PASS, 1)])
+@pytest.mark.parametrize("variant,P", [(C.CLUSTER, 1), (C.CLUSTER, 4), (C.TWO_PASS, 1),
+                                       (C.CLUSTER_PERSISTENT, 4)])
 def test_misaligned_pointers_take_element_path(variant, P):
     w = _custom(wl.LAYERNORM, "bf16", 3, 8192, 23, eps=1e-5, param_dtype="f32")
     inp = w.generate()
@@ -165,7 +178,7 @@ def test_auto_plan_is_legal_and_clustered_for_wide_rows():
     for w in (wl.LAYERNORM_BF16_1024x262144, wl.SOFTMAX_F32_512x131072_SPIKES,
               wl.RMSNORM_BF16_2048x786432):
         p = make_plan(w)
-        assert p.variant == C.CLUSTER
+        assert p.variant in (C.CLUSTER, C.CLUSTER_PERSISTENT)
         assert p.slice_elems * p.cluster_size >= w.cols
         assert p.smem_bytes <= 232448
 
@@ -215,3 +228,31 @@ def test_illegal_cluster_sizes_are_rejected():
     inp = w.generate()
     dx = to_device(inp["x"])
     assert call(w, dx, torch.empty_like(dx), {}, p) == C.ERR_NO_LEGAL_PLAN
+
+
+@pytest.mark.parametrize("rows", [1, 7, 300])
+def test_persistent_row_counts(rows):
+    # fewer rows than resident clusters, a few rows per cluster, many rows
+    # per cluster (slot and ring reuse over many phases); one and two CTAs
+    # per SM
+    w = _custom(wl.LAYERNORM, "bf16", rows, 32768, 30, x_mean=0.5, x_std=2.0, eps=1e-5,
+                param_dtype="f32")
+    inp = w.generate()
+    ran = 0
+    for P in (1, 2, 4, 8):
+        p = _try_plan(w, C.CLUSTER_PERSISTENT, P)
+        if p is None:
+            continue
+        for cps in (1, 2):
+            p.ctas_per_sm = cps
+            dx = to_device(inp["x"])
+            dy = torch.empty_like(dx)
+            params = {k: to_device(v) for k, v in inp.items() if k != "x"}
+            st = call(w, dx, dy, params, p)
+            if st == C.ERR_NO_LEGAL_PLAN:
+                continue
+            assert st == C.OK
+            torch.cuda.synchronize()
+            check(w, to_host(dy), inp)
+            ran += 1
+    assert ran >= 4
