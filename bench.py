@@ -210,7 +210,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="layernorm_bf16_1024x262144")
-    ap.add_argument("--variant", default="auto", help="auto | cluster:P | persist:P | two_pass")
+    ap.add_argument("--variant", default="auto",
+                    help="auto (cost model + tuning) | static | cluster:P | persist:P | two_pass")
     ap.add_argument("--cps", type=int, default=0, help="persistent CTAs per SM (0 = planner)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=20.0,
@@ -252,6 +253,13 @@ def main():
     params = {k: to_device(v) for k, v in inputs.items() if k != "x"}
 
     if args.variant == "auto":
+        # the cost model screens the legal cluster sizes and a short tuning
+        # step times the best predicted ones; planning and tuning happen
+        # once, before (and outside) the timed region
+        pdt_model = DT[w.param_dtype] if w.param_dtype else -1
+        plan, _ = C.credit_plan_profiled(OPS[w.op], w.rows, w.cols, DT[w.dtype], pdt_model, dev,
+                                         5, 4)
+    elif args.variant == "static":
         plan = C.credit_plan(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev)
     elif args.variant == "two_pass":
         plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.TWO_PASS, 1)

@@ -31,11 +31,12 @@ class Plan(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("slice_elems", ctypes.c_int64), ("active_clusters", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("chunk_elems", ctypes.c_int32),
-                ("ring_slots", ctypes.c_int32), ("pred_us", ctypes.c_float),
+                ("ring_slots", ctypes.c_int32), ("rows_per_cluster", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("pred_us", ctypes.c_float),
                 ("pred_two_pass_us", ctypes.c_float)]
 
     def as_dict(self) -> dict:
-        return {f: getattr(self, f) for f, _ in self._fields_}
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
 
     def __repr__(self):
         return f"Plan({self.as_dict()})"
@@ -55,6 +56,32 @@ class BenchResult(ctypes.Structure):
         return d
 
 
+class Candidate(ctypes.Structure):
+    """Mirror of credit_candidate_t."""
+    _fields_ = [("cluster_size", ctypes.c_int32), ("legal", ctypes.c_int32), ("plan", Plan),
+                ("t_ctrl_us", ctypes.c_double), ("t_comm_us", ctypes.c_double),
+                ("pred_us", ctypes.c_double), ("measured_us", ctypes.c_double),
+                ("persistent_us", ctypes.c_double)]
+
+
+class ModelReport(ctypes.Structure):
+    """Mirror of credit_model_report_t."""
+    _fields_ = [("baseline_variant", ctypes.c_int32), ("model_cluster_size", ctypes.c_int32),
+                ("profitable", ctypes.c_int32), ("chosen_cluster_size", ctypes.c_int32),
+                ("chosen_variant", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("t_base_us", ctypes.c_double), ("b_base_bytes", ctypes.c_double),
+                ("b_credit_bytes", ctypes.c_double), ("t_ctrl_base_us", ctypes.c_double),
+                ("cand", Candidate * 16)]
+
+    def as_dict(self) -> dict:
+        d = {f: getattr(self, f) for f, _ in self._fields_ if f not in ("cand", "reserved")}
+        d["candidates"] = [{"P": c.cluster_size, "t_ctrl_us": c.t_ctrl_us, "t_comm_us": c.t_comm_us,
+                            "pred_us": c.pred_us, "measured_us": c.measured_us,
+                            "persistent_us": c.persistent_us, "plan": c.plan.as_dict()}
+                           for c in self.cand if c.legal]
+        return d
+
+
 BENCH_BARRIER, BENCH_EXCHANGE, BENCH_REMOTE_LOAD_LATENCY, BENCH_LOCAL_LOAD_LATENCY, \
     BENCH_REMOTE_STORE_BW, BENCH_REMOTE_LOAD_BW, BENCH_LOCAL_STORE_BW, \
     BENCH_LOCAL_LOAD_BW = range(8)
@@ -70,6 +97,8 @@ class CreditError(RuntimeError):
 SIGNATURES = {
     "credit_plan": (_i32, [_i32, _i64, _i64, _i32, _i32, ctypes.POINTER(Plan)]),
     "credit_plan_for": (_i32, [_i32, _i64, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(Plan)]),
+    "credit_plan_with": (_i32, [_i32, _i64, _i64, _i32, _i32, ctypes.POINTER(Plan),
+                                ctypes.POINTER(Plan)]),
     "credit_softmax": (_i32, [_vp, _vp, _i64, _i64, _i32, ctypes.POINTER(Plan), _vp, _sz, _vp]),
     "credit_layernorm": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _i32, _f32,
                                 ctypes.POINTER(Plan), _vp, _sz, _vp]),
@@ -80,6 +109,9 @@ SIGNATURES = {
     "credit_bench_dsmem": (_i32, [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(BenchResult)]),
     "credit_control_time": (_i32, [_i32, _i64, _i32, _i32, _i64, _i32, _i32, _i32,
                                    ctypes.POINTER(ctypes.c_double)]),
+    "credit_calibrate": (_i32, [_i32, _i32, ctypes.c_char_p]),
+    "credit_plan_profiled": (_i32, [_i32, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
+                                    ctypes.POINTER(Plan), ctypes.POINTER(ModelReport)]),
     "credit_status_string": (ctypes.c_char_p, [_i32]),
     "credit_get_device_error": (_i32, [_i32]),
     "credit_version": (ctypes.c_char_p, []),
@@ -143,6 +175,18 @@ def credit_plan_for(op: int, rows: int, cols: int, dtype: int, device: int,
     return p
 
 
+def credit_plan_with(op: int, rows: int, cols: int, dtype: int, device: int, variant: int,
+                     cluster_size: int = 1, threads: int = 0, ctas_per_sm: int = 0,
+                     chunk_elems: int = 0, rows_per_cluster: int = 0) -> Plan:
+    req = Plan(variant=variant, cluster_size=cluster_size, threads=threads,
+               ctas_per_sm=ctas_per_sm, chunk_elems=chunk_elems,
+               rows_per_cluster=rows_per_cluster)
+    p = Plan()
+    _check(load().credit_plan_with(op, rows, cols, dtype, device, ctypes.byref(req),
+                                   ctypes.byref(p)), "credit_plan_with")
+    return p
+
+
 def credit_softmax(x: int, y: int, rows: int, cols: int, dtype: int, plan=None,
                    workspace: int = 0, workspace_bytes: int = 0, stream: int = 0) -> int:
     return load().credit_softmax(x, y, rows, cols, dtype, _plan_ptr(plan), workspace or None,
@@ -190,6 +234,19 @@ def credit_control_time(device: int, nclusters: int, cluster_size: int, threads:
                                       rows_per_cluster, barriers_per_row, runs, ctypes.byref(t)),
            "credit_control_time")
     return t.value
+
+
+def credit_calibrate(device: int = 0, runs: int = 7, profile_path: str | None = None) -> None:
+    _check(load().credit_calibrate(device, runs, profile_path.encode() if profile_path else None),
+           "credit_calibrate")
+
+
+def credit_plan_profiled(op: int, rows: int, cols: int, dtype: int, param_dtype: int = -1,
+                         device: int = 0, runs: int = 7, tune: int = 0):
+    p, r = Plan(), ModelReport()
+    _check(load().credit_plan_profiled(op, rows, cols, dtype, param_dtype, device, runs, tune,
+                                       ctypes.byref(p), ctypes.byref(r)), "credit_plan_profiled")
+    return p, r
 
 
 def credit_get_device_error(device: int) -> int:

@@ -154,6 +154,21 @@ struct OpCall {
     cudaStream_t stream;
 };
 
+// Complete / re-derive a plan from the fields a caller may set.
+credit_status_t plan_from_request(int dev, credit_op_t op, int64_t rows, int64_t cols,
+                                  credit_dtype_t dtype, const credit_plan_t& r,
+                                  credit_plan_t* out) {
+    const credit_variant_t v = (credit_variant_t)r.variant;
+    if (v != CREDIT_CLUSTER && v != CREDIT_CLUSTER_PERSISTENT && v != CREDIT_TWO_PASS)
+        return CREDIT_ERR_INVALID_ARG;
+    if (r.threads < 0 || r.ctas_per_sm < 0 || r.chunk_elems < 0 || r.rows_per_cluster < 0)
+        return CREDIT_ERR_INVALID_ARG;
+    const bool pers = v == CREDIT_CLUSTER_PERSISTENT;
+    return make_plan(dev, op, rows, cols, dtype, v, r.cluster_size, r.threads,
+                     pers ? r.ctas_per_sm : 0, out, pers ? r.chunk_elems : 0,
+                     v == CREDIT_CLUSTER ? r.rows_per_cluster : 0);
+}
+
 credit_status_t run(const OpCall& c) {
     if (!c.x || !c.y || c.rows < 1 || c.cols < 1) return CREDIT_ERR_INVALID_ARG;
     if (!dtype_ok(c.dtype)) return CREDIT_ERR_UNSUPPORTED;
@@ -175,10 +190,7 @@ credit_status_t run(const OpCall& c) {
     if (c.plan && c.plan->variant != CREDIT_AUTO) {
         // re-derive the launch shape from (variant, P, threads) so a stale or
         // hand-edited plan can never launch an illegal configuration
-        const bool pers = c.plan->variant == CREDIT_CLUSTER_PERSISTENT;
-        st = make_plan(dev, c.op, c.rows, c.cols, c.dtype, (credit_variant_t)c.plan->variant,
-                       c.plan->cluster_size, c.plan->threads, pers ? c.plan->ctas_per_sm : 0,
-                       &plan, pers ? c.plan->chunk_elems : 0);
+        st = plan_from_request(dev, c.op, c.rows, c.cols, c.dtype, *c.plan, &plan);
     } else {
         st = auto_plan(dev, c.op, c.rows, c.cols, c.dtype, &plan);
     }
@@ -189,13 +201,15 @@ credit_status_t run(const OpCall& c) {
     KernelKey key{(int)c.op, (int)c.dtype, (c.p0 || c.p1) ? (int)c.pdtype : 0, vec};
     unsigned* err = device_error_word();
     if (!err) return CREDIT_ERR_CUDA;
-    if (plan.variant == CREDIT_CLUSTER_PERSISTENT && !vec) {
-        // the ring is filled by bulk copies: misaligned or ragged rows take
+    if (!vec && plan.variant != CREDIT_TWO_PASS &&
+        (plan.variant == CREDIT_CLUSTER_PERSISTENT || plan.rows_per_cluster != 1)) {
+        // bulk copies need 16-byte alignment: misaligned or ragged rows take
         // the one-row-per-cluster kernel's element path instead
         st = make_plan(dev, c.op, c.rows, c.cols, c.dtype, CREDIT_CLUSTER, plan.cluster_size, 0, 0,
-                       &plan);
+                       &plan, 0, 1);
         if (st != CREDIT_OK) return st;
     }
+    key.rows = plan.variant == CREDIT_CLUSTER ? plan.rows_per_cluster : 1;
     if (plan.variant == CREDIT_CLUSTER_PERSISTENT) {
         PersistArgs a;
         a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;
@@ -216,14 +230,16 @@ credit_status_t run(const OpCall& c) {
     if (plan.variant == CREDIT_CLUSTER) {
         ClusterArgs a;
         a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;
+        a.rows = c.rows;
         a.cols = c.cols;
         a.slice = plan.slice_elems;
-        a.chunk_elems = (int32_t)bulk_chunk_elems(plan.slice_elems, (int)es);
+        a.chunk_elems = plan.chunk_elems;
+        a.pitch = (int32_t)row_pitch(plan.slice_elems, (int)es);
         a.eps = c.eps;
         a.err = err;
         const void* fn = cluster_kernel(key);
         if (!kernel_info(dev, fn, true)) return CREDIT_ERR_CUDA;
-        return from_cuda(launch_cluster(key, a, c.rows, plan.cluster_size, plan.threads,
+        return from_cuda(launch_cluster(key, a, plan.cluster_size, plan.threads,
                                         (size_t)plan.smem_bytes, c.stream));
     }
     // two-pass baseline
@@ -257,6 +273,12 @@ credit_status_t credit_plan_for(credit_op_t op, int64_t rows, int64_t cols, cred
         variant != CREDIT_CLUSTER_PERSISTENT)
         return CREDIT_ERR_INVALID_ARG;
     return make_plan(device, op, rows, cols, dtype, variant, cluster_size, 0, 0, out);
+}
+
+credit_status_t credit_plan_with(credit_op_t op, int64_t rows, int64_t cols, credit_dtype_t dtype,
+                                 int device, const credit_plan_t* request, credit_plan_t* out) {
+    if (!out || !request) return CREDIT_ERR_INVALID_ARG;
+    return plan_from_request(device, op, rows, cols, dtype, *request, out);
 }
 
 credit_status_t credit_softmax(const void* x, void* y, int64_t rows, int64_t cols,

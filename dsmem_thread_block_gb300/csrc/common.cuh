@@ -28,7 +28,8 @@ namespace credit {
 enum Op : int { kSoftmax = 0, kLayerNorm = 1, kRMSNorm = 2 };
 
 constexpr int kMaxCluster = 16;   // non-portable cluster size limit
-constexpr int kMaxThreads = 512;
+constexpr int kMaxThreads = 512;         // two-pass kernels
+constexpr int kClusterMaxThreads = 256;  // one-row-per-cluster kernel (three CTAs per SM)
 constexpr int kMaxWarps = kMaxThreads / 32;
 constexpr int kMaxChunks = 16;    // mbarriers per CTA for the staged slice
 constexpr int kSlotStride = 4;    // floats per pushed partial (16 bytes)
@@ -208,6 +209,41 @@ __device__ __forceinline__ void named_sync(int nthreads) {
 //              form: n = sum n_q, mean = sum n_q mean_q / n,
 //              M2 = sum (M2_q + n_q (mean_q - mean)^2)
 //   RMSNorm:   ss = sum ss_q
+template <int OP>
+__device__ __forceinline__ void combine_slots(const float* sl, uint32_t P, float& st0,
+                                              float& st1, float& st2);
+
+// The same fold over partials `stride` floats apart (several rows' partials
+// interleaved per source CTA).
+template <int OP>
+__device__ __forceinline__ void combine_slots_strided(const float* sl, uint32_t P, int stride,
+                                                      float& st0, float& st1, float& st2) {
+    if constexpr (OP == kSoftmax) {
+        float m = -INFINITY;
+        for (uint32_t q = 0; q < P; ++q) m = fmaxf(m, sl[q * stride]);
+        float s = 0.f;
+        for (uint32_t q = 0; q < P; ++q) s += rescale(sl[q * stride + 1], sl[q * stride], m);
+        st0 = m; st1 = s; st2 = 0.f;
+    } else if constexpr (OP == kLayerNorm) {
+        float n = 0.f, nm = 0.f;
+        for (uint32_t q = 0; q < P; ++q) {
+            n += sl[q * stride];
+            nm = fmaf(sl[q * stride], sl[q * stride + 1], nm);
+        }
+        const float mean = n > 0.f ? nm / n : 0.f;
+        float m2 = 0.f;
+        for (uint32_t q = 0; q < P; ++q) {
+            const float d = sl[q * stride + 1] - mean;
+            m2 += fmaf(sl[q * stride] * d, d, sl[q * stride + 2]);
+        }
+        st0 = n; st1 = mean; st2 = m2;
+    } else {
+        float ss = 0.f;
+        for (uint32_t q = 0; q < P; ++q) ss += sl[q * stride];
+        st0 = ss; st1 = st2 = 0.f;
+    }
+}
+
 template <int OP>
 __device__ __forceinline__ void combine_slots(const float* sl, uint32_t P, float& st0,
                                               float& st1, float& st2) {

@@ -1,0 +1,326 @@
+// costmodel.cu -- the profiling-fed profitability model and the per-device
+// DSMEM profile it reads.
+//
+// CREDIT summary page (arXiv 2609.01864v1), "D. Profitability and Candidate
+// Selection": one timing of the selected non-DSMEM CUDA path is the first
+// screen (no peak-bandwidth assumptions); a work-free control kernel with
+// the candidate's grid, cluster size, dynamic-SMEM footprint and K = 2L
+// barriers measures launch, scheduling, occupancy and synchronisation cost
+// (T_ctrl = its excess over the one-CTA control); communication is charged
+// as local replay plus remote-store issue plus the non-overlapped deposit
+// residual; the avoided source time is valued at the baseline's achieved
+// rate ("D. Traffic Validation", cost accounting).  See include/credit.h for
+// the formula as implemented.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "credit.h"
+#include "common.cuh"
+#include "internal.h"
+#include "planner.h"
+
+namespace credit {
+namespace {
+
+struct DsmemProfile {
+    bool valid = false;
+    double barrier_ns[kMaxCluster + 1] = {};
+    double exchange_ns[kMaxCluster + 1] = {};
+};
+
+std::mutex g_cm_mu;
+DsmemProfile g_profile[kMaxDevices];
+std::map<std::tuple<int, int, int, int64_t, int64_t>, credit_plan_t> g_chosen;
+
+int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Scratch {
+    void* p = nullptr;
+    ~Scratch() { if (p) cudaFree(p); }
+    bool alloc(size_t n) {
+        if (n == 0) return true;
+        if (cudaMalloc(&p, n) != cudaSuccess) { cudaGetLastError(); p = nullptr; return false; }
+        return cudaMemset(p, 0, n) == cudaSuccess;
+    }
+};
+
+double median_of(std::vector<double> v) {
+    std::sort(v.begin(), v.end());
+    const size_t n = v.size();
+    return n % 2 ? v[n / 2] : 0.5 * (v[n / 2 - 1] + v[n / 2]);
+}
+
+}  // namespace
+
+bool lookup_profiled_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
+                          credit_dtype_t dtype, credit_plan_t* out) {
+    std::lock_guard<std::mutex> lk(g_cm_mu);
+    auto it = g_chosen.find(std::make_tuple(dev, (int)op, (int)dtype, rows, cols));
+    if (it == g_chosen.end()) return false;
+    *out = it->second;
+    return true;
+}
+
+}  // namespace credit
+
+using namespace credit;
+
+extern "C" credit_status_t credit_calibrate(int device, int runs, const char* profile_path) {
+    if (device < 0 || device >= kMaxDevices || runs < 1) return CREDIT_ERR_INVALID_ARG;
+    DsmemProfile prof;
+    for (int P = 2; P <= kMaxCluster; ++P) {
+        credit_bench_result_t b, e;
+        credit_status_t st = credit_bench_dsmem(device, CREDIT_BENCH_BARRIER, P, 500, runs, &b);
+        if (st != CREDIT_OK) return st;
+        st = credit_bench_dsmem(device, CREDIT_BENCH_EXCHANGE, P, 500, runs, &e);
+        if (st != CREDIT_OK) return st;
+        prof.barrier_ns[P] = b.median_ns;
+        prof.exchange_ns[P] = e.median_ns;
+    }
+    prof.valid = true;
+    {
+        std::lock_guard<std::mutex> lk(g_cm_mu);
+        g_profile[device] = prof;
+    }
+    if (profile_path) {
+        FILE* f = std::fopen(profile_path, "w");
+        if (!f) return CREDIT_ERR_INVALID_ARG;
+        std::fprintf(f, "{\"device\": %d, \"runs\": %d, \"barrier_ns\": {", device, runs);
+        for (int P = 2; P <= kMaxCluster; ++P)
+            std::fprintf(f, "%s\"%d\": %.2f", P > 2 ? ", " : "", P, prof.barrier_ns[P]);
+        std::fprintf(f, "}, \"exchange_ns\": {");
+        for (int P = 2; P <= kMaxCluster; ++P)
+            std::fprintf(f, "%s\"%d\": %.2f", P > 2 ? ", " : "", P, prof.exchange_ns[P]);
+        std::fprintf(f, "}}\n");
+        std::fclose(f);
+    }
+    return CREDIT_OK;
+}
+
+namespace {
+
+// One launch of the operator with an explicit plan on the default stream.
+credit_status_t call_op(credit_op_t op, const void* x, void* y, int64_t rows, int64_t cols,
+                        credit_dtype_t dtype, const void* p0, const void* p1, int pdt,
+                        const credit_plan_t* plan, void* ws, size_t wsb) {
+    const credit_dtype_t pd = pdt < 0 ? CREDIT_F32 : (credit_dtype_t)pdt;
+    switch (op) {
+        case CREDIT_SOFTMAX: return credit_softmax(x, y, rows, cols, dtype, plan, ws, wsb, nullptr);
+        case CREDIT_LAYERNORM:
+            return credit_layernorm(x, y, rows, cols, dtype, p0, p1, pd, 1e-5f, plan, ws, wsb, nullptr);
+        case CREDIT_RMSNORM:
+            return credit_rmsnorm(x, y, rows, cols, dtype, p0, pd, 1e-6f, plan, ws, wsb, nullptr);
+    }
+    return CREDIT_ERR_UNSUPPORTED;
+}
+
+// Median time of `runs` launches (after one warm-up) in microseconds.
+credit_status_t time_op(credit_op_t op, const void* x, void* y, int64_t rows, int64_t cols,
+                        credit_dtype_t dtype, const void* p0, const void* p1, int pdt,
+                        const credit_plan_t* plan, void* ws, size_t wsb, int runs, double* us) {
+    cudaEvent_t e0, e1;
+    if (cudaEventCreate(&e0) != cudaSuccess) return CREDIT_ERR_CUDA;
+    if (cudaEventCreate(&e1) != cudaSuccess) { cudaEventDestroy(e0); return CREDIT_ERR_CUDA; }
+    std::vector<double> t;
+    credit_status_t st = CREDIT_OK;
+    for (int r = 0; r <= runs && st == CREDIT_OK; ++r) {
+        float ms = 0.f;
+        if (cudaEventRecord(e0, nullptr) != cudaSuccess) { st = CREDIT_ERR_CUDA; break; }
+        st = call_op(op, x, y, rows, cols, dtype, p0, p1, pdt, plan, ws, wsb);
+        if (st != CREDIT_OK) break;
+        if (cudaEventRecord(e1, nullptr) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) {
+            st = CREDIT_ERR_CUDA;
+            break;
+        }
+        if (r > 0) t.push_back(1e3 * ms);
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (st == CREDIT_OK) *us = median_of(t);
+    return st;
+}
+
+}  // namespace
+
+extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, int64_t cols,
+                                                credit_dtype_t dtype, int param_dtype, int device,
+                                                int runs, int tune, credit_plan_t* out,
+                                                credit_model_report_t* report) {
+    if (!out || rows < 1 || cols < 1 || runs < 1 || tune < 0 || device < 0 ||
+        device >= kMaxDevices)
+        return CREDIT_ERR_INVALID_ARG;
+    if (dtype != CREDIT_F32 && dtype != CREDIT_BF16) return CREDIT_ERR_UNSUPPORTED;
+    if (param_dtype != -1 && param_dtype != CREDIT_F32 && param_dtype != CREDIT_BF16)
+        return CREDIT_ERR_UNSUPPORTED;
+    DsmemProfile prof;
+    {
+        std::lock_guard<std::mutex> lk(g_cm_mu);
+        prof = g_profile[device];
+    }
+    if (!prof.valid) {
+        const credit_status_t st = credit_calibrate(device, 7, nullptr);
+        if (st != CREDIT_OK) return st;
+        std::lock_guard<std::mutex> lk(g_cm_mu);
+        prof = g_profile[device];
+    }
+    int old = 0;
+    if (cudaGetDevice(&old) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
+    struct Restore { int d; ~Restore() { cudaSetDevice(d); } } restore{old};
+
+    const DevInfo* d = device_info(device);
+    if (!d) return CREDIT_ERR_CUDA;
+    const int es = dtype == CREDIT_F32 ? 4 : 2;
+    const double mat = (double)rows * (double)cols * es;
+
+    // the baseline: local staging when one CTA can hold a row, else re-reads
+    credit_plan_t base;
+    const int64_t row_bytes = cols * es;
+    const int Rb = row_bytes * 4 <= 65536 ? 4 : 1;
+    credit_status_t st =
+        make_plan(device, op, rows, cols, dtype, CREDIT_CLUSTER, 1, 0, 0, &base, 0, Rb);
+    if (st != CREDIT_OK && Rb != 1)
+        st = make_plan(device, op, rows, cols, dtype, CREDIT_CLUSTER, 1, 0, 0, &base, 0, 1);
+    const bool staging = st == CREDIT_OK;
+    if (!staging) {
+        st = make_plan(device, op, rows, cols, dtype, CREDIT_TWO_PASS, 0, 0, 0, &base);
+        if (st != CREDIT_OK) return st;
+    }
+    const double b_base = staging ? 2.0 * mat : 3.0 * mat;
+    const double b_credit = 2.0 * mat;
+
+    // scratch buffers of the shape
+    Scratch x, y, g, b, ws;
+    const size_t pbytes = (size_t)cols * (param_dtype == CREDIT_F32 ? 4 : 2);
+    if (!x.alloc((size_t)mat) || !y.alloc((size_t)mat) ||
+        (param_dtype >= 0 && (!g.alloc(pbytes) || !b.alloc(pbytes))))
+        return CREDIT_ERR_CUDA;
+    if (!staging && !ws.alloc((size_t)base.workspace_bytes)) return CREDIT_ERR_CUDA;
+
+    double t_base = 0.0;
+    st = time_op(op, x.p, y.p, rows, cols, dtype, g.p, b.p, param_dtype, &base, ws.p,
+                 (size_t)base.workspace_bytes, runs, &t_base);
+    if (st != CREDIT_OK) return st;
+    const double r_base = b_base / t_base;  // bytes per microsecond
+
+    // the baseline's control: its grid, footprint and barriers, no work
+    double ctrl_base = 0.0;
+    if (staging) {
+        st = credit_control_time(device, ceil_div64(rows, base.rows_per_cluster), 1, base.threads,
+                                 base.smem_bytes, 1, 2, runs, &ctrl_base);
+    } else {
+        const int64_t nch = ceil_div64(cols, base.slice_elems);
+        double one = 0.0;
+        st = credit_control_time(device, rows * nch, 1, base.threads, 0, 1, 2, runs, &one);
+        ctrl_base = 2.0 * one;  // two launches
+    }
+    if (st != CREDIT_OK) return st;
+
+    credit_model_report_t rep;
+    std::memset(&rep, 0, sizeof(rep));
+    rep.baseline_variant = staging ? CREDIT_CLUSTER : CREDIT_TWO_PASS;
+    rep.t_base_us = t_base;
+    rep.b_base_bytes = b_base;
+    rep.b_credit_bytes = b_credit;
+    rep.t_ctrl_base_us = ctrl_base;
+    rep.cand[0].cluster_size = 1;
+    rep.cand[0].legal = 1;
+    rep.cand[0].plan = base;
+    rep.cand[0].pred_us = t_base;
+
+    double best = t_base;
+    int best_P = 1;
+    credit_plan_t chosen = base;
+    for (int P = 2; P <= kMaxCluster; ++P) {
+        credit_candidate_t& c = rep.cand[P - 1];
+        c.cluster_size = P;
+        credit_plan_t p;
+        if (make_plan(device, op, rows, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1) != CREDIT_OK)
+            continue;
+        if ((int64_t)(P - 1) * p.slice_elems >= cols) continue;  // an idle CTA
+        double ctrl = 0.0;
+        st = credit_control_time(device, rows, P, p.threads, p.smem_bytes, 1, 2, runs, &ctrl);
+        if (st == CREDIT_ERR_NO_LEGAL_PLAN) continue;
+        if (st != CREDIT_OK) return st;
+        c.legal = 1;
+        c.plan = p;
+        c.t_ctrl_us = ctrl - ctrl_base;
+        const double push_ns = std::max(0.0, prof.exchange_ns[P] - prof.barrier_ns[P]);
+        c.t_comm_us = (double)p.waves * push_ns * 1e-3;
+        c.pred_us = t_base - (b_base - b_credit) / r_base + c.t_ctrl_us + c.t_comm_us;
+        c.plan.pred_us = (float)c.pred_us;
+        c.plan.pred_two_pass_us = (float)t_base;
+        if (c.pred_us < best) {
+            best = c.pred_us;
+            best_P = P;
+            chosen = c.plan;
+        }
+    }
+    rep.model_cluster_size = best_P;
+    rep.profitable = best_P > 1;
+    chosen.pred_us = (float)best;
+    chosen.pred_two_pass_us = (float)t_base;
+
+    // final tuning: time the `tune` best-predicted candidates (and the
+    // persistent kernel of the same P) and keep the fastest measured plan
+    if (tune > 0) {
+        std::vector<int> order;
+        for (int P = 2; P <= kMaxCluster; ++P)
+            if (rep.cand[P - 1].legal) order.push_back(P);
+        std::sort(order.begin(), order.end(), [&](int a2, int b2) {
+            return rep.cand[a2 - 1].pred_us < rep.cand[b2 - 1].pred_us;
+        });
+        if ((int)order.size() > tune) order.resize(tune);
+        double best_meas = t_base;
+        credit_plan_t best_plan = base;
+        int best_meas_P = 1;
+        rep.cand[0].measured_us = t_base;
+        for (int P : order) {
+            credit_candidate_t& c = rep.cand[P - 1];
+            st = time_op(op, x.p, y.p, rows, cols, dtype, g.p, b.p, param_dtype, &c.plan, nullptr,
+                         0, runs, &c.measured_us);
+            if (st != CREDIT_OK) return st;
+            if (c.measured_us < best_meas) {
+                best_meas = c.measured_us;
+                best_plan = c.plan;
+                best_meas_P = P;
+            }
+            credit_plan_t pp;
+            if (make_plan(device, op, rows, cols, dtype, CREDIT_CLUSTER_PERSISTENT, P, 0, 0, &pp) ==
+                CREDIT_OK) {
+                st = time_op(op, x.p, y.p, rows, cols, dtype, g.p, b.p, param_dtype, &pp, nullptr,
+                             0, runs, &c.persistent_us);
+                if (st != CREDIT_OK) return st;
+                if (c.persistent_us < best_meas) {
+                    best_meas = c.persistent_us;
+                    best_plan = pp;
+                    best_meas_P = P;
+                }
+            }
+        }
+        chosen = best_plan;
+        chosen.pred_us = (float)best_meas;
+        chosen.pred_two_pass_us = (float)t_base;
+        best_P = best_meas_P;
+    }
+    rep.chosen_cluster_size = best_P;
+    rep.chosen_variant = chosen.variant;
+    {
+        std::lock_guard<std::mutex> lk(g_cm_mu);
+        g_chosen[std::make_tuple(device, (int)op, (int)dtype, rows, cols)] = chosen;
+    }
+    *out = chosen;
+    if (report) *report = rep;
+    return CREDIT_OK;
+}

@@ -13,12 +13,16 @@ struct ClusterArgs {
     void* y;
     const void* p0;       // gamma (LayerNorm) or weight (RMSNorm), may be null
     const void* p1;       // beta (LayerNorm), may be null
+    int64_t rows;         // rows of this launch (the last cluster may hold fewer than R)
     int64_t cols;
     int64_t slice;        // elements owned by one CTA (multiple of the vector width)
     int32_t chunk_elems;  // elements per bulk copy / mbarrier
+    int32_t pitch;        // bytes between the staged slices of a CTA's rows
     float eps;
     unsigned* err;        // device error word
 };
+
+constexpr int kMaxRowsPerCluster = 4;
 
 // Arguments of the two-pass (global re-read) kernel pair.
 struct TwoPassArgs {
@@ -57,10 +61,12 @@ constexpr int kPersistMaxSlots = 32;
 constexpr int kPersistMaxThreads = 544;  // 16 consumer warps + 1 producer warp
 
 // Kernel selector: op 0..2, dtype 0 = fp32 / 1 = bf16, pdtype likewise,
-// vec = aligned 16-byte path.
+// vec = aligned 16-byte path, rows = rows per cluster (1, 2 or 4; the
+// element path has 1).
 struct KernelKey {
     int op, dtype, pdtype;
     bool vec;
+    int rows = 1;
 };
 
 const void* cluster_kernel(KernelKey k);
@@ -68,8 +74,8 @@ const void* persistent_kernel(KernelKey k);
 const void* two_pass_stats_kernel(KernelKey k);
 const void* two_pass_apply_kernel(KernelKey k);
 
-cudaError_t launch_cluster(KernelKey k, const ClusterArgs& a, int64_t rows,
-                           int P, int threads, size_t smem, cudaStream_t s);
+cudaError_t launch_cluster(KernelKey k, const ClusterArgs& a, int P, int threads, size_t smem,
+                           cudaStream_t s);
 cudaError_t launch_persistent(KernelKey k, const PersistArgs& a, int P, int threads,
                               size_t smem, cudaStream_t s);
 cudaError_t launch_two_pass(KernelKey k, const TwoPassArgs& a, int64_t rows,

@@ -26,10 +26,11 @@ bool op_ok(credit_op_t op) {
     return op == CREDIT_SOFTMAX || op == CREDIT_LAYERNORM || op == CREDIT_RMSNORM;
 }
 
-int cluster_threads(int64_t slice_vecs) {
-    // about four 16-byte vectors per thread, warp multiples, 64..512
-    int64_t t = round_up(std::max<int64_t>(1, slice_vecs / 4), 32);
-    return (int)std::min<int64_t>(512, std::max<int64_t>(64, t));
+int cluster_threads(int64_t staged_vecs) {
+    // about sixteen 16-byte vectors per thread (four warp tiles of four), warp
+    // multiples, 64..256 threads: three such CTAs share an SM
+    int64_t t = round_up(std::max<int64_t>(1, staged_vecs / 16), 32);
+    return (int)std::min<int64_t>(256, std::max<int64_t>(64, t));
 }
 
 // Static model used until the device is calibrated: one HBM stream at a
@@ -43,10 +44,14 @@ constexpr double kLaunchUs = 3.0;
 
 }  // namespace
 
-int64_t bulk_chunk_elems(int64_t slice_elems, int elem_bytes) {
+int64_t bulk_chunk_elems(int64_t slice_elems, int elem_bytes, int rows_per_cluster) {
     const int64_t vec = 16 / elem_bytes;
     const int64_t target = 16384 / elem_bytes;
-    return round_up(std::max(target, ceil_div(slice_elems, kMaxChunks)), vec);
+    return round_up(std::max(target, ceil_div(slice_elems, kMaxChunks / rows_per_cluster)), vec);
+}
+
+int64_t row_pitch(int64_t slice_elems, int elem_bytes) {
+    return round_up(slice_elems * elem_bytes, 128);
 }
 
 namespace {
@@ -96,6 +101,7 @@ credit_status_t persistent_plan(int dev, const DevInfo* d, credit_op_t op, int64
     p->ring_slots = (int32_t)S;
     p->active_clusters = (int32_t)G;
     p->ctas_per_sm = cps;
+    p->rows_per_cluster = 1;
     p->waves = (int32_t)std::min<int64_t>(ceil_div(rows, G), INT32_MAX);
     const double bytes = 2.0 * (double)rows * (double)cols * es;
     const double coverage = std::min(1.0, (double)G * P / ((double)d->sms * cps));
@@ -108,12 +114,15 @@ credit_status_t persistent_plan(int dev, const DevInfo* d, credit_op_t op, int64
 
 credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
                           credit_dtype_t dtype, credit_variant_t variant, int P,
-                          int threads, int cps, credit_plan_t* out, int64_t chunk) {
+                          int threads, int cps, credit_plan_t* out, int64_t chunk,
+                          int rows_per_cluster) {
     if (!out || rows < 1 || cols < 1) return CREDIT_ERR_INVALID_ARG;
     if (!op_ok(op)) return CREDIT_ERR_UNSUPPORTED;
     if (dtype != CREDIT_F32 && dtype != CREDIT_BF16) return CREDIT_ERR_UNSUPPORTED;
     if (threads != 0 && (threads < 32 || threads % 32 != 0)) return CREDIT_ERR_INVALID_ARG;
-    if (threads > (variant == CREDIT_CLUSTER_PERSISTENT ? kPersistMaxThreads : kMaxThreads))
+    if (threads > (variant == CREDIT_CLUSTER_PERSISTENT ? kPersistMaxThreads
+                   : variant == CREDIT_CLUSTER             ? kClusterMaxThreads
+                                                           : kMaxThreads))
         return CREDIT_ERR_INVALID_ARG;
     const DevInfo* d = device_info(dev);
     if (!d) return CREDIT_ERR_CUDA;
@@ -127,23 +136,27 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
 
     if (variant == CREDIT_CLUSTER) {
         if (P < 1 || P > kMaxCluster) return CREDIT_ERR_NO_LEGAL_PLAN;
+        const int R = rows_per_cluster ? rows_per_cluster : 1;
+        if (R != 1 && R != 2 && R != 4) return CREDIT_ERR_INVALID_ARG;
         const int64_t slice = round_up(ceil_div(cols, P), vec);
-        const int64_t smem = round_up(slice * es, 16);
-        const void* fn = cluster_kernel(KernelKey{(int)op, (int)dtype, 0, true});
+        const int64_t pitch = row_pitch(slice, es);
+        const int64_t smem = R == 1 ? round_up(slice * es, 16) : R * pitch;
+        const void* fn = cluster_kernel(KernelKey{(int)op, (int)dtype, 0, true, R});
         const KernelInfo* ki = kernel_info(dev, fn, true);
         if (!ki) return CREDIT_ERR_CUDA;
-        if (smem > ki->max_dyn_smem) return CREDIT_ERR_NO_LEGAL_PLAN;
-        const int t = threads ? threads : cluster_threads(slice / vec);
+        if (smem > ki->max_dyn_smem || pitch > INT32_MAX) return CREDIT_ERR_NO_LEGAL_PLAN;
+        const int t = threads ? threads : cluster_threads(R * slice / vec);
         const int active = occupancy_clusters(dev, fn, P, t, (size_t)smem, rows);
         if (active < 1) return CREDIT_ERR_NO_LEGAL_PLAN;
         p.cluster_size = P;
         p.threads = t;
         p.smem_bytes = smem;
         p.slice_elems = slice;
-        p.chunk_elems = (int32_t)bulk_chunk_elems(slice, es);
+        p.chunk_elems = (int32_t)bulk_chunk_elems(slice, es, R);
+        p.rows_per_cluster = R;
         p.active_clusters = active;
         p.ctas_per_sm = std::max(1, (int)((int64_t)active * P / d->sms));
-        p.waves = (int32_t)std::min<int64_t>(ceil_div(rows, active), INT32_MAX);
+        p.waves = (int32_t)std::min<int64_t>(ceil_div(ceil_div(rows, R), active), INT32_MAX);
         const double ctas_per_sm = (double)active * P / d->sms;
         const double eff = ctas_per_sm >= 2.0 ? 0.9 : 0.7;
         p.pred_us = (float)(bytes / (kNominalBytesPerUs * eff) +
@@ -182,6 +195,7 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
         const int active = occupancy_clusters(dev, fn, 1, t, 0, rows);
         if (active < 1) return CREDIT_ERR_NO_LEGAL_PLAN;
         p.cluster_size = 1;
+        p.rows_per_cluster = 1;
         p.threads = t;
         p.slice_elems = chunk;
         p.chunk_elems = (int32_t)chunk;
@@ -200,21 +214,32 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
 credit_status_t auto_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
                           credit_dtype_t dtype, credit_plan_t* out) {
     if (!out || rows < 1 || cols < 1) return CREDIT_ERR_INVALID_ARG;
+    credit_plan_t profiled;
+    if (lookup_profiled_plan(dev, op, rows, cols, dtype, &profiled)) {
+        *out = profiled;
+        return CREDIT_OK;
+    }
     credit_plan_t base;
     credit_status_t st = make_plan(dev, op, rows, cols, dtype, CREDIT_TWO_PASS, 0, 0, 0, &base);
     if (st != CREDIT_OK) return st;
-    credit_plan_t best = base;
-    for (int v = 0; v < 2; ++v) {
-        const credit_variant_t var = v == 0 ? CREDIT_CLUSTER : CREDIT_CLUSTER_PERSISTENT;
-        for (int P = 1; P <= kMaxCluster; ++P) {
-            credit_plan_t c;
-            if (make_plan(dev, op, rows, cols, dtype, var, P, 0, 0, &c) != CREDIT_OK) continue;
-            if (P > 1 && (int64_t)(P - 1) * c.slice_elems >= cols) continue;  // an idle CTA
-            if (c.pred_us < best.pred_us) best = c;
-        }
+    // Static choice (no profile for this shape): the one-row-per-cluster
+    // kernel with the smallest P whose slice stays within 64 KiB (three
+    // 256-thread CTAs per SM), rows of 16 KiB or less batched four to a CTA;
+    // the two-pass kernel only when no cluster size fits.
+    const int es = dtype == CREDIT_F32 ? 4 : 2;
+    for (int P = 1; P <= kMaxCluster; ++P) {
+        const int64_t slice_bytes = ceil_div(cols, P) * es;
+        if (slice_bytes > 65536 && P < kMaxCluster) continue;
+        const int R = (P == 1 && slice_bytes * 4 <= 65536) ? 4 : 1;
+        credit_plan_t c;
+        if (make_plan(dev, op, rows, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &c, 0, R) != CREDIT_OK)
+            continue;
+        c.pred_two_pass_us = base.pred_us;
+        *out = c;
+        return CREDIT_OK;
     }
-    best.pred_two_pass_us = base.pred_us;
-    *out = best;
+    base.pred_two_pass_us = base.pred_us;
+    *out = base;
     return CREDIT_OK;
 }
 

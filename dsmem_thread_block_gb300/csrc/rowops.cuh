@@ -247,6 +247,7 @@ __device__ __forceinline__ void cta_partial(const Stats<OP, T>& st, float* redA,
 template <int OP, typename T>
 struct OutputMap {
     float c0 = 0.f, c1 = 0.f;
+    __device__ __forceinline__ OutputMap() {}
     __device__ __forceinline__ OutputMap(float st0, float st1, float st2, float mq, int64_t N,
                                          float eps) {
         if constexpr (OP == kSoftmax) {
@@ -334,7 +335,7 @@ __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const un
                                              T* yrow, const PT* gp, const PT* bp, int nvec,
                                              int warp, int nwarps, int lane) {
     using G = Granule<OP, T, PT>;
-    constexpr int U = 4, NP = G::kPairs, kTile = 32 * U;
+    constexpr int U = (OP != kSoftmax && G::kPairs == 4) ? 2 : 4, NP = G::kPairs, kTile = 32 * U;
     const int ngran = nvec * (16 / G::kBytes);
     const bool has_g = OP != kSoftmax && gp != nullptr;
     const bool has_b = OP != kSoftmax && bp != nullptr;
@@ -381,6 +382,173 @@ __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const un
                            make_uint2(Pairs<bf16>::two(p[0]), Pairs<bf16>::two(p[1])));
                 } else {
                     stg16_stream(reinterpret_cast<uint4*>(yrow) + q, Pairs<T>::pack(p));
+                }
+            }
+        }
+    };
+    int t = warp * kTile;
+    for (; t + kTile <= ngran; t += nwarps * kTile) tile(t, true);
+    if (t < ngran) tile(t, false);
+}
+
+}  // namespace credit
+
+namespace credit {
+
+// ----------------------------------------------------- multi-row tiles
+// Block-wide sums / maxima of N values per thread (named barrier 1 over the
+// first `nthreads` threads); every participating thread returns the folded
+// values.  `red` holds N floats per warp and must not be read by any thread
+// from an earlier use.
+template <int N, bool kMax>
+__device__ __forceinline__ void block_reduce_n(float (&x)[N], float* red, int nwarps, int nthreads) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const float y = __shfl_xor_sync(0xffffffffu, x[i], o);
+            x[i] = kMax ? fmaxf(x[i], y) : x[i] + y;
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) red[N * warp + i] = x[i];
+    }
+    named_sync(nthreads);
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = kMax ? -INFINITY : 0.f;
+    for (int w = 0; w < nwarps; ++w) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) x[i] = kMax ? fmaxf(x[i], red[N * w + i]) : x[i] + red[N * w + i];
+    }
+}
+
+// The CTA partials of R rows at once (see cta_partial): two block reductions
+// of R or 2R values in total instead of two per row.  stash_sum(i, mq) runs
+// the fp32 softmax stash pass of row i.  redA / redB: 2R floats per warp.
+template <int OP, typename T, int R, typename StashFn>
+__device__ __forceinline__ void cta_partial_rows(const Stats<OP, T> (&st)[R], float* redA,
+                                                 float* redB, int nwarps, int nthreads,
+                                                 StashFn stash_sum, float (&p)[R][3]) {
+    if constexpr (OP == kSoftmax) {
+        float m[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) m[i] = st[i].m;
+        block_reduce_n<R, true>(m, redA, nwarps, nthreads);
+        float s[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            if constexpr (sizeof(T) == 4) s[i] = m[i] == -INFINITY ? 0.f : stash_sum(i, m[i]);
+            else s[i] = rescale(st[i].s.x + st[i].s.y, st[i].m, m[i]);
+        }
+        block_reduce_n<R, false>(s, redB, nwarps, nthreads);
+#pragma unroll
+        for (int i = 0; i < R; ++i) { p[i][0] = m[i]; p[i][1] = s[i]; p[i][2] = 0.f; }
+    } else if constexpr (OP == kLayerNorm) {
+        float a[2 * R], mt[R], m2t[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const float s1 = st[i].s1.x + st[i].s1.y, s2 = st[i].s2.x + st[i].s2.y, nn = st[i].n;
+            mt[i] = nn > 0.f ? s1 / nn - st[i].nK.x : 0.f;
+            m2t[i] = nn > 0.f ? fmaxf(s2 - s1 * (s1 / nn), 0.f) : 0.f;
+            a[2 * i] = nn;
+            a[2 * i + 1] = nn * mt[i];
+        }
+        block_reduce_n<2 * R, false>(a, redA, nwarps, nthreads);
+        float q[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const float mean = a[2 * i] > 0.f ? a[2 * i + 1] / a[2 * i] : 0.f;
+            const float d = mt[i] - mean;
+            q[i] = fmaf(st[i].n * d, d, m2t[i]);
+            p[i][0] = a[2 * i];
+            p[i][1] = mean;
+        }
+        block_reduce_n<R, false>(q, redB, nwarps, nthreads);
+#pragma unroll
+        for (int i = 0; i < R; ++i) p[i][2] = q[i];
+    } else {
+        float q[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) q[i] = st[i].q.x + st[i].q.y;
+        block_reduce_n<R, false>(q, redA, nwarps, nthreads);
+#pragma unroll
+        for (int i = 0; i < R; ++i) { p[i][0] = q[i]; p[i][1] = p[i][2] = 0.f; }
+    }
+}
+
+// Output of R rows that share a column slice: each granule's parameters are
+// loaded once and applied to all live rows (row i staged at base + i * pitch,
+// written to yrow[i]); the first `rows` <= R rows are live.
+template <int OP, typename T, typename PT, int R>
+__device__ __forceinline__ void output_tiles_rows(const OutputMap<OP, T> (&h)[R],
+                                                  const unsigned char* base, int pitch,
+                                                  T* const (&yrow)[R], int rows, const PT* gp,
+                                                  const PT* bp, int nvec, int warp, int nwarps,
+                                                  int lane) {
+    using G = Granule<OP, T, PT>;
+    // granules in flight per thread: 4, halved when a granule carries 8
+    // parameters, divided among the rows
+    constexpr int kBase = (OP != kSoftmax && G::kPairs == 4) ? 2 : 4;
+    constexpr int U = kBase / R > 0 ? kBase / R : 1, NP = G::kPairs, kTile = 32 * U;
+    const int ngran = nvec * (16 / G::kBytes);
+    const bool has_g = OP != kSoftmax && gp != nullptr;
+    const bool has_b = OP != kSoftmax && bp != nullptr;
+
+    auto tile = [&](int t, bool full) {
+        uint4 raw[U][R];
+        F2 gv[U][NP], bv[U][NP];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = t + lane + 32 * u;
+            if (full || q < ngran) {
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    if (i < rows) {
+                        const unsigned char* b = base + (size_t)i * pitch;
+                        if constexpr (G::kBytes == 8) {
+                            const uint2 w = *reinterpret_cast<const uint2*>(b + (size_t)q * 8);
+                            raw[u][i] = make_uint4(w.x, w.y, 0u, 0u);
+                        } else {
+                            raw[u][i] = lds16(b + (size_t)q * 16);
+                        }
+                    }
+                }
+                if constexpr (OP != kSoftmax) {
+                    if (has_g) granule_params<PT, NP>(gp, q, gv[u]);
+                    else for (int j = 0; j < NP; ++j) gv[u][j] = f2(1.f);
+                    if (has_b) granule_params<PT, NP>(bp, q, bv[u]);
+                    else for (int j = 0; j < NP; ++j) bv[u][j] = f2(0.f);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = t + lane + 32 * u;
+            if (full || q < ngran) {
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    if (i < rows) {
+                        F2 pp[NP];
+                        if constexpr (G::kBytes == 8) {
+                            pp[0] = Pairs<bf16>::one(raw[u][i].x);
+                            pp[1] = Pairs<bf16>::one(raw[u][i].y);
+                        } else {
+                            Pairs<T>::unpack(raw[u][i], pp);
+                        }
+#pragma unroll
+                        for (int j = 0; j < NP; ++j) {
+                            if constexpr (OP == kSoftmax) pp[j] = h[i](pp[j], pp[j], pp[j]);
+                            else pp[j] = h[i](pp[j], gv[u][j], bv[u][j]);
+                        }
+                        if constexpr (G::kBytes == 8) {
+                            __stcs(reinterpret_cast<uint2*>(yrow[i]) + q,
+                                   make_uint2(Pairs<bf16>::two(pp[0]), Pairs<bf16>::two(pp[1])));
+                        } else {
+                            stg16_stream(reinterpret_cast<uint4*>(yrow[i]) + q, Pairs<T>::pack(pp));
+                        }
+                    }
                 }
             }
         }

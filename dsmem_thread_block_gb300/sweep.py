@@ -1,0 +1,125 @@
+"""Profitability sweep: the cost model's pick against measurement.
+
+For each width of the bf16 softmax sweep (2^28 elements, 1024..1048576
+columns) the cost model (credit_plan_profiled) predicts the time of every
+legal cluster size and of the non-DSMEM baseline and picks one; then every
+candidate is timed on the seeded input (median of `runs` launches, CUDA
+events).  A point is correct when the pick's measured time is within
+max(2 %, the runs' interquartile spread) of the fastest measured candidate
+(CREDIT summary page, "C. Cost-Model Validation": profitability accuracy
+and crossover prediction).  Prints one JSON object per point and a summary.
+
+    python -m dsmem_thread_block_gb300.sweep [--cols 1024,4096,...] [--runs 15]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import numpy as np
+
+from . import _credit as C
+from . import workloads as wl
+
+
+def _timed(fn, runs: int):
+    import torch
+    ts = []
+    fn()
+    torch.cuda.synchronize()
+    for _ in range(runs):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    ts = np.array(ts)
+    return float(np.median(ts)), float(np.percentile(ts, 75) - np.percentile(ts, 25))
+
+
+def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
+              total_elements: int = wl.SWEEP_ELEMENTS, tune: int = 3) -> dict:
+    import torch
+    w = wl.Workload(f"softmax_bf16_sweep_{cols}", wl.SOFTMAX, "bf16", total_elements // cols,
+                    cols, seed=4)
+    x = torch.from_numpy(w.generate()["x"].view(np.int16)).view(torch.bfloat16).to(device)
+    y = torch.empty_like(x)
+    plan, rep = C.credit_plan_profiled(C.SOFTMAX, w.rows, w.cols, C.BF16, -1, device, model_runs,
+                                       tune)
+    stream = torch.cuda.current_stream().cuda_stream
+    measured = {}
+    for cand in rep.cand:
+        if not cand.legal:
+            continue
+        p = cand.plan
+        ws = torch.empty(max(1, int(p.workspace_bytes)), dtype=torch.uint8, device=x.device)
+
+        def go(p=p, ws=ws):
+            st = C.credit_softmax(x.data_ptr(), y.data_ptr(), w.rows, w.cols, C.BF16, p,
+                                  ws.data_ptr(), int(p.workspace_bytes), stream)
+            if st != C.OK:
+                raise C.CreditError(st, "sweep launch")
+
+        med, iqr = _timed(go, runs)
+        measured[cand.cluster_size] = {"us": med, "iqr_us": iqr, "pred_us": cand.pred_us}
+    # the tuned plan may be a persistent one: time it as chosen
+    ws = torch.empty(max(1, int(plan.workspace_bytes)), dtype=torch.uint8, device=x.device)
+    tuned_us, tuned_iqr = _timed(lambda: C.credit_softmax(
+        x.data_ptr(), y.data_ptr(), w.rows, w.cols, C.BF16, plan, ws.data_ptr(),
+        int(plan.workspace_bytes), stream), runs)
+    best_P = min(measured, key=lambda k: measured[k]["us"])
+    best = min(measured[best_P]["us"], tuned_us)
+    pick = rep.model_cluster_size
+    tol = max(0.02 * best, measured[best_P]["iqr_us"], measured[pick]["iqr_us"])
+    return {
+        "cols": cols, "rows": w.rows,
+        "baseline": "local-staging P=1" if rep.baseline_variant == C.CLUSTER else "two-pass",
+        "t_base_us": rep.t_base_us, "picked_P": pick, "predicted_profitable": bool(rep.profitable),
+        "measured_best_P": best_P, "measured_profitable": best_P != 1,
+        "picked_us": measured[pick]["us"], "best_us": best,
+        "tuned_P": rep.chosen_cluster_size, "tuned_variant": int(plan.variant),
+        "tuned_us": tuned_us, "tuned_correct": tuned_us <= best + max(tol, tuned_iqr),
+        "correct": measured[pick]["us"] <= best + tol,
+        "profitability_correct": bool(rep.profitable) == (best_P != 1),
+        "candidates": {str(k): v for k, v in sorted(measured.items())},
+        "gbps_best": 2 * w.rows * w.cols * 2 / best / 1e3,
+    }
+
+
+def summarize(points: list[dict]) -> dict:
+    n = len(points)
+    widths = [p["cols"] for p in points]
+    pred = [p["cols"] for p in points if p["predicted_profitable"]]
+    meas = [p["cols"] for p in points if p["measured_profitable"]]
+    return {
+        "points": n,
+        "pick_accuracy": sum(p["correct"] for p in points) / n,
+        "tuned_pick_accuracy": sum(p["tuned_correct"] for p in points) / n,
+        "profitability_accuracy": sum(p["profitability_correct"] for p in points) / n,
+        "predicted_crossover_cols": min(pred) if pred else None,
+        "measured_crossover_cols": min(meas) if meas else None,
+        "crossover_interval_error": (None if not pred or not meas else
+                                     abs(widths.index(min(pred)) - widths.index(min(meas)))),
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--cols", default=",".join(str(c) for c in wl.SWEEP_COLS))
+    ap.add_argument("--runs", type=int, default=15)
+    ap.add_argument("--device", type=int, default=0)
+    a = ap.parse_args()
+    import torch
+    torch.cuda.set_device(a.device)
+    C.credit_calibrate(a.device, 7)
+    points = []
+    for c in [int(v) for v in a.cols.split(",")]:
+        pt = run_point(c, a.runs, a.device)
+        points.append(pt)
+        print(json.dumps(pt), flush=True)
+    print(json.dumps({"summary": summarize(points)}), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -84,6 +84,9 @@ typedef enum {
  *   ctas_per_sm      CTAs the plan expects to share one SM
  *   chunk_elems      elements per bulk copy (one mbarrier each)
  *   ring_slots       shared-memory chunk slots per CTA (persistent only)
+ *   rows_per_cluster rows one cluster stages and reduces together (CLUSTER:
+ *                    1, 2 or 4; their partials share one exchange and each
+ *                    parameter load serves all of them)
  *   pred_us          predicted time of this plan, microseconds (0 = none)
  *   pred_two_pass_us predicted / measured time of the two-pass baseline
  */
@@ -99,6 +102,8 @@ typedef struct {
     int32_t ctas_per_sm;
     int32_t chunk_elems;
     int32_t ring_slots;
+    int32_t rows_per_cluster;
+    int32_t reserved;
     float pred_us;
     float pred_two_pass_us;
 } credit_plan_t;
@@ -127,6 +132,21 @@ credit_status_t credit_plan_for(credit_op_t op, int64_t rows, int64_t cols,
                                 credit_dtype_t dtype, int device,
                                 credit_variant_t variant, int cluster_size,
                                 credit_plan_t *out);
+
+/*
+ * Complete a plan from a partial request: `request->variant` (CLUSTER,
+ * CLUSTER_PERSISTENT or TWO_PASS) and, for the clustered variants,
+ * `request->cluster_size` are required; `threads`, `ctas_per_sm`,
+ * `chunk_elems` and `rows_per_cluster` are used when non-zero and chosen
+ * otherwise; every other field is ignored.  The operator calls re-derive a
+ * passed plan the same way, so a plan can never launch an illegal shape.
+ * Returns CREDIT_ERR_INVALID_ARG for malformed requests and
+ * CREDIT_ERR_NO_LEGAL_PLAN when the shape does not fit.
+ */
+credit_status_t credit_plan_with(credit_op_t op, int64_t rows, int64_t cols,
+                                 credit_dtype_t dtype, int device,
+                                 const credit_plan_t *request,
+                                 credit_plan_t *out);
 
 /*
  * Row softmax: y[r, j] = exp(x[r, j] - max_r) / sum_k exp(x[r, k] - max_r).
@@ -262,6 +282,76 @@ credit_status_t credit_control_time(int device, int64_t nclusters,
                                     int64_t smem_bytes, int rows_per_cluster,
                                     int barriers_per_row, int runs,
                                     double *median_us);
+
+/* ------------------------------------------------------------------------
+ * Profitability cost model (CREDIT "D. Profitability and Candidate
+ * Selection").  For one shape it times the non-DSMEM baseline once -- the
+ * one-CTA-per-row local-staging kernel when a row fits one CTA's shared
+ * memory, else the two-pass global re-read pair -- times the work-free
+ * control kernel of every legal clustered candidate and of the baseline, and
+ * predicts
+ *     T_CREDIT(P) = T_base - (B_base - B_credit) / R_base + T_ctrl(P) + T_comm(P)
+ * with R_base = B_base / T_base the baseline's achieved byte rate, T_ctrl(P)
+ * the candidate's control time minus the baseline's, and T_comm(P) the
+ * replicated push's cost beyond the barrier (DSMEM profile) times the
+ * candidate's waves of resident clusters.  The deposit residual
+ * [T_wSMEM - T_input]+ is zero: a 16-byte push per peer is far below the
+ * per-SM input stream.  The candidate with the smallest prediction is kept
+ * if it beats T_base, else the baseline.  As on the pages, the model screens
+ * and a final tuning step may pick another legal size: with tune > 0 the
+ * `tune` best-predicted clustered candidates (one-row-per-cluster, and the
+ * persistent kernel of the same P) are timed and the fastest measured plan,
+ * baseline included, is chosen.
+ */
+typedef struct {
+    int32_t cluster_size;    /* P; 1 = the baseline */
+    int32_t legal;           /* 0: the slice does not fit / no residency */
+    credit_plan_t plan;
+    double t_ctrl_us;        /* control time excess over the baseline's control */
+    double t_comm_us;        /* push cost beyond the barrier, all waves */
+    double pred_us;          /* predicted time */
+    double measured_us;      /* tuning: measured time of `plan` (0 = not timed) */
+    double persistent_us;    /* tuning: measured time of the persistent kernel
+                                of this P (0 = not timed or not legal) */
+} credit_candidate_t;
+
+typedef struct {
+    int32_t baseline_variant;     /* CREDIT_CLUSTER (P = 1 staging) or CREDIT_TWO_PASS */
+    int32_t model_cluster_size;   /* the model's pick (1 = the baseline) */
+    int32_t profitable;           /* 1 if a clustered candidate is predicted faster */
+    int32_t chosen_cluster_size;  /* after tuning (equals the model's pick if tune = 0) */
+    int32_t chosen_variant;       /* variant of the chosen plan */
+    int32_t reserved;
+    double t_base_us;             /* measured baseline time (median) */
+    double b_base_bytes;          /* bytes the baseline moves */
+    double b_credit_bytes;        /* bytes a clustered candidate moves */
+    double t_ctrl_base_us;        /* the baseline's control time */
+    credit_candidate_t cand[16];  /* index P - 1; [0] describes the baseline */
+} credit_model_report_t;
+
+/*
+ * Run the DSMEM microbenchmarks the cost model uses (cluster barrier and
+ * replicated push for P = 2..16, median of `runs`) on `device` and keep the
+ * profile in memory.  If profile_path is not NULL the profile is also written
+ * there as JSON.  Synchronises the device; allocates a few bytes.
+ */
+credit_status_t credit_calibrate(int device, int runs, const char *profile_path);
+
+/*
+ * Apply the cost model to one shape on `device` (calibrating first if
+ * needed).  Allocates scratch x / y / parameter / workspace buffers of the
+ * shape (zero-filled), times the baseline (median of `runs`), runs the
+ * control kernels, fills `report` (may be NULL) and writes the chosen plan to
+ * `out`.  param_dtype is the parameters' dtype, or -1 for none; tune is the
+ * number of best-predicted candidates to time (0 = the model alone).  The choice
+ * is cached: later credit_plan calls for the same (op, rows, cols, dtype,
+ * device) return it.  Synchronises the device.
+ */
+credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows,
+                                     int64_t cols, credit_dtype_t dtype,
+                                     int param_dtype, int device, int runs,
+                                     int tune, credit_plan_t *out,
+                                     credit_model_report_t *report);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *credit_status_string(credit_status_t status);

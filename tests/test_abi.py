@@ -48,9 +48,9 @@ def test_binding_covers_the_abi(lib):
 
 
 def test_plan_struct_layout_matches_header():
-    # int32 x4, int64 x3, int32 x4, float x2 -> 64 bytes, no padding surprises
-    assert ctypes.sizeof(C.Plan) == 64
-    assert C.Plan.smem_bytes.offset == 16 and C.Plan.pred_us.offset == 56
+    # int32 x4, int64 x3, int32 x6, float x2 -> 72 bytes, no padding surprises
+    assert ctypes.sizeof(C.Plan) == 72
+    assert C.Plan.smem_bytes.offset == 16 and C.Plan.pred_us.offset == 64
 
 
 def test_status_strings(lib):

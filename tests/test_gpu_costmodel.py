@@ -1,0 +1,53 @@
+"""The profiling-fed cost model: its report is consistent, its choice is a
+legal plan that the automatic planner then reuses, and on a few widths of
+the bf16 softmax sweep (scaled down) the pick is close to the fastest
+measured candidate."""
+import pytest
+import torch
+
+from dsmem_thread_block_gb300 import _credit as C
+from dsmem_thread_block_gb300 import sweep
+
+pytestmark = pytest.mark.gpu
+
+
+def test_report_is_consistent_and_choice_is_cached():
+    rows, cols = 256, 131072  # 256 KiB bf16 rows: the baseline is the two-pass pair
+    C.credit_calibrate(0, 3)
+    plan, rep = C.credit_plan_profiled(C.SOFTMAX, rows, cols, C.BF16, -1, 0, 3, 0)
+    assert rep.baseline_variant == C.TWO_PASS
+    assert rep.cand[0].legal and rep.cand[0].pred_us == rep.t_base_us > 0
+    legal = [c for c in rep.cand[1:] if c.legal]
+    assert legal, "some cluster size must fit a 256 KiB row"
+    best = min([rep.t_base_us] + [c.pred_us for c in legal])
+    assert abs(plan.pred_us - best) <= 1e-3 * best + 1e-3
+    assert rep.model_cluster_size == rep.chosen_cluster_size  # no tuning requested
+    assert rep.chosen_cluster_size == plan.cluster_size or (
+        rep.chosen_cluster_size == 1 and plan.variant == C.TWO_PASS)
+    auto = C.credit_plan(C.SOFTMAX, rows, cols, C.BF16, 0)
+    assert auto.variant == plan.variant and auto.cluster_size == plan.cluster_size
+
+
+def test_local_staging_baseline_for_narrow_rows():
+    plan, rep = C.credit_plan_profiled(C.LAYERNORM, 4096, 4096, C.BF16, C.F32, 0, 3, 0)
+    assert rep.baseline_variant == C.CLUSTER and rep.cand[0].plan.cluster_size == 1
+    assert rep.b_base_bytes == rep.b_credit_bytes
+
+
+def test_tuning_times_the_top_candidates():
+    plan, rep = C.credit_plan_profiled(C.LAYERNORM, 256, 262144, C.BF16, C.F32, 0, 3, 3)
+    timed = [c for c in rep.cand[1:] if c.legal and c.measured_us > 0]
+    assert 1 <= len(timed) <= 3
+    best = min([rep.t_base_us] + [c.measured_us for c in timed] +
+               [c.persistent_us for c in timed if c.persistent_us > 0])
+    assert abs(plan.pred_us - best) <= 1e-3 * best + 1e-3  # the plan carries its measured time
+
+
+def test_small_sweep_picks_near_best():
+    pts = [sweep.run_point(c, runs=7, total_elements=1 << 24) for c in (4096, 65536, 262144)]
+    for p in pts:
+        # scaled-down shapes run for tens of microseconds: allow timing noise
+        assert p["tuned_us"] <= 1.30 * p["best_us"], p
+    s = sweep.summarize(pts)
+    assert 0.0 <= s["pick_accuracy"] <= 1.0
+    torch.cuda.synchronize()

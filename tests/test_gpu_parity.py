@@ -256,3 +256,41 @@ def test_persistent_row_counts(rows):
             check(w, to_host(dy), inp)
             ran += 1
     assert ran >= 4
+
+
+@pytest.mark.parametrize("R", [2, 4])
+def test_rows_per_cluster(R):
+    # several rows per cluster share one exchange and each parameter load;
+    # row counts that are not a multiple of R leave a partial last cluster
+    cases = [
+        _custom(wl.LAYERNORM, "bf16", 7, 65536, 40, x_mean=0.5, x_std=2.0, eps=1e-5,
+                param_dtype="f32"),
+        _custom(wl.LAYERNORM, "f32", 5, 12288, 41, x_mean=-1.0, x_std=3.0, eps=1e-5,
+                param_dtype="bf16"),
+        _custom(wl.RMSNORM, "bf16", 6, 98304, 42, eps=1e-6, param_dtype="bf16"),
+        _custom(wl.SOFTMAX, "f32", 9, 32768, 43, x_std=4.0, spike_frac=0.01),
+        _custom(wl.SOFTMAX, "bf16", 3, 4096, 44),
+    ]
+    dev = torch.cuda.current_device()
+    for w in cases:
+        inp = w.generate()
+        for P in (1, 2, 4, 8):
+            try:
+                p = C.credit_plan_with(gh_ops(w), w.rows, w.cols, gh_dt(w), dev, C.CLUSTER, P,
+                                       rows_per_cluster=R)
+            except C.CreditError as e:
+                assert e.status == C.ERR_NO_LEGAL_PLAN
+                continue
+            assert p.rows_per_cluster == R
+            check(w, run(w, inp, p), inp)
+            check(w, run(w, inp, p, in_place=True), inp)
+
+
+def gh_ops(w):
+    from gpu_helpers import OPS
+    return OPS[w.op]
+
+
+def gh_dt(w):
+    from gpu_helpers import DT
+    return DT[w.dtype]
