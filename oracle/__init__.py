@@ -1,4 +1,5 @@
-"""Plain fp64 CPU oracle for row softmax, LayerNorm and RMSNorm.
+"""Plain CPU oracle for row softmax, LayerNorm, RMSNorm, int8 quantization and
+weighted standardization (fp64; the quantization codes in IEEE single).
 
 TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
 CPU-baseline / reference legs of ``bench.py`` may import this package.  The
@@ -60,8 +61,10 @@ def _load():
                                              dbl, vp, vp]
             lib.oracle_rmsnorm.argtypes = [vp, i32, i64, i64, vp, i32, dbl,
                                            vp]
-            for f in (lib.oracle_widen, lib.oracle_softmax,
-                      lib.oracle_layernorm, lib.oracle_rmsnorm):
+            lib.oracle_quantize.argtypes = [vp, i32, i64, i64, vp, vp]
+            lib.oracle_weighted_std.argtypes = [vp, i32, i64, i64, vp, i32, dbl, vp]
+            for f in (lib.oracle_widen, lib.oracle_softmax, lib.oracle_layernorm,
+                      lib.oracle_rmsnorm, lib.oracle_quantize, lib.oracle_weighted_std):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -145,6 +148,26 @@ def rmsnorm(x: np.ndarray, weight=None, eps: float = 1e-6) -> np.ndarray:
     _check(_load().oracle_rmsnorm(_ptr(x), _dtype_code(x), x.shape[0],
                                   x.shape[1], _ptr(w), wd, float(eps),
                                   _ptr(y)), "rmsnorm")
+    return y
+
+
+def quantize(x: np.ndarray):
+    """Row-wise symmetric int8 codes and fp32 scales (see oracle.c)."""
+    x = _prep(x)
+    q = np.empty(x.shape, dtype=np.int8)
+    s = np.empty(x.shape[0], dtype=np.float32)
+    _check(_load().oracle_quantize(_ptr(x), _dtype_code(x), x.shape[0], x.shape[1], _ptr(q),
+                                   _ptr(s)), "quantize")
+    return q, s
+
+
+def weighted_std(x: np.ndarray, w: np.ndarray, eps: float = 1e-5) -> np.ndarray:
+    """Row-wise weighted standardization with per-column weights (see oracle.c)."""
+    x = _prep(x)
+    wv, wd = _vec(w, x.shape[1])
+    y = np.empty(x.shape, dtype=np.float64)
+    _check(_load().oracle_weighted_std(_ptr(x), _dtype_code(x), x.shape[0], x.shape[1],
+                                       _ptr(wv), wd, float(eps), _ptr(y)), "weighted_std")
     return y
 
 

@@ -170,3 +170,93 @@ int oracle_rmsnorm(const void *x, int dtype, int64_t rows, int64_t cols,
     }
     return OR_OK;
 }
+
+/*
+ * Row-wise symmetric int8 quantization (CREDIT summary page, "B. Workload-by-
+ * Workload Scaling" and "D. Traffic Validation": the quantization workload,
+ * 9 -> 5 B/element for FP32 input, i.e. a 4-byte read and a 1-byte write).
+ * The pages do not spell the codes out; the reading is the textbook one:
+ *   amax = max_j |x_j|,  scale = amax / 127,
+ *   q_j  = clamp(round_half_even(x_j / scale), -127, 127),
+ * with q = 0 and scale = 0 for an all-zero row.  scale and x_j / scale are
+ * computed in IEEE single precision (the precision of the GPU kernel), so
+ * the integer decision is taken in the same precision on both sides; amax is
+ * exact in any precision.
+ */
+int oracle_quantize(const void *x, int dtype, int64_t rows, int64_t cols,
+                    int8_t *q, float *scales)
+{
+    int64_t r, j;
+    if (!x || !q || !scales || rows < 0 || cols <= 0 || !or_dtype_ok(dtype))
+        return OR_BAD_ARG;
+    for (r = 0; r < rows; ++r) {
+        int64_t base = r * cols;
+        double amax = 0.0;
+        float s;
+        for (j = 0; j < cols; ++j) {
+            double v = fabs(or_load(x, dtype, base + j));
+            if (v > amax)
+                amax = v;
+        }
+        s = (float)amax / 127.0f;
+        scales[r] = s;
+        for (j = 0; j < cols; ++j) {
+            float v = (float)or_load(x, dtype, base + j);
+            float c;
+            if (s == 0.0f) {
+                q[base + j] = 0;
+                continue;
+            }
+            c = rintf(v / s);
+            if (c > 127.0f)
+                c = 127.0f;
+            if (c < -127.0f)
+                c = -127.0f;
+            q[base + j] = (int8_t)c;
+        }
+    }
+    return OR_OK;
+}
+
+/*
+ * Row-wise weighted standardization ("weighted variance" workload of the
+ * CREDIT summary page, section "B. Workload-by-Workload Scaling").  The
+ * pages name the workload but not its output; the reading taken here makes it
+ * the weighted counterpart of LayerNorm's reduce-then-reuse: per-column
+ * weights w_j >= 0 (a second input vector),
+ *   W = sum_j w_j,  mu = sum_j w_j x_j / W,
+ *   var = sum_j w_j (x_j - mu)^2 / W,
+ *   y_j = (x_j - mu) / sqrt(var + eps).
+ * Rows with W == 0 are rejected.
+ */
+int oracle_weighted_std(const void *x, int dtype, int64_t rows, int64_t cols,
+                        const void *w, int wdtype, double eps, double *y)
+{
+    int64_t r, j;
+    if (!x || !w || !y || rows < 0 || cols <= 0 || !or_dtype_ok(dtype) ||
+        !or_dtype_ok(wdtype) || !(eps >= 0.0))
+        return OR_BAD_ARG;
+    for (r = 0; r < rows; ++r) {
+        int64_t base = r * cols;
+        double W = 0.0, sw = 0.0, ssd = 0.0, mu, var, inv;
+        for (j = 0; j < cols; ++j) {
+            double wj = or_load(w, wdtype, j);
+            if (!(wj >= 0.0))
+                return OR_BAD_ARG;
+            W += wj;
+            sw += wj * or_load(x, dtype, base + j);
+        }
+        if (!(W > 0.0))
+            return OR_BAD_ARG;
+        mu = sw / W;
+        for (j = 0; j < cols; ++j) {
+            double d = or_load(x, dtype, base + j) - mu;
+            ssd += or_load(w, wdtype, j) * d * d;
+        }
+        var = ssd / W;
+        inv = 1.0 / sqrt(var + eps);
+        for (j = 0; j < cols; ++j)
+            y[base + j] = (or_load(x, dtype, base + j) - mu) * inv;
+    }
+    return OR_OK;
+}

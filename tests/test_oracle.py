@@ -246,3 +246,70 @@ def test_workload_generators_are_seeded_and_shaped():
     frac = float((s == 30.0).mean())
     assert 0.008 < frac < 0.012
     assert wl.sweep_point(1024).rows * 1024 == 1 << 28
+
+
+# ----------------------------------------------------------------- quantization
+def test_quantize_power_of_two_closed_form(golden):
+    g = golden["quantize_power_of_two"]
+    q, s = oracle.quantize(np.array(g["x"], dtype=np.float32))
+    assert q[0].tolist() == g["q"] and s[0] == _frac(g["scale"])
+
+
+def test_quantize_invariants():
+    rng = np.random.default_rng(51)
+    x = (rng.standard_normal((6, 999)) * 3).astype(np.float32)
+    q, s = oracle.quantize(x)
+    assert (np.abs(q) <= 127).all()
+    # the absmax element maps to +-127, and the codes reconstruct x to half a step
+    i = np.abs(x).argmax(axis=1)
+    assert (np.abs(q[np.arange(6), i]) == 127).all()
+    np.testing.assert_array_less(np.abs(q * s[:, None].astype(np.float64) - x) - 0.5 * s[:, None] * 1.0001, 0)
+    # odd symmetry and exact scaling by powers of two
+    qn, sn = oracle.quantize(-x)
+    assert (qn == -q).all() and (sn == s).all()
+    q4, s4 = oracle.quantize(x * np.float32(4))
+    assert (q4 == q).all() and (s4 == 4 * s).all()
+
+
+def test_quantize_zero_row_and_bf16_input():
+    q, s = oracle.quantize(np.zeros((2, 8), np.float32))
+    assert (q == 0).all() and (s == 0).all()
+    x = wl.to_bf16_bits(np.array([[1.0, -0.5, 0.25, 127.0]], np.float32))
+    q, s = oracle.quantize(x)
+    assert q[0].tolist() == [1, 0, 0, 127] and s[0] == 1.0
+
+
+# ------------------------------------------------------------ weighted variance
+def test_weighted_std_integer_weights_closed_form(golden):
+    g = golden["weighted_std_integer_weights"]
+    eps = 0.125
+    y = oracle.weighted_std(np.array(g["x"], np.float32), np.array(g["w"], np.float32), eps=eps)
+    mu, var = _frac(g["mean"]), _frac(g["var"])
+    np.testing.assert_allclose(y[0], (np.array(g["x"]) - mu) / math.sqrt(var + eps), rtol=1e-14)
+
+
+def test_weighted_std_is_layernorm_of_the_expanded_row():
+    # integer weights: weighted statistics equal those of the repeated multiset
+    rng = np.random.default_rng(52)
+    x = rng.standard_normal((3, 40)).astype(np.float32)
+    w = rng.integers(0, 4, size=40).astype(np.float32)
+    w[0] = 1.0
+    y = oracle.weighted_std(x, w, eps=1e-3)
+    for r in range(3):
+        expanded = np.repeat(x[r].astype(np.float64), w.astype(int))
+        z = oracle.layernorm(expanded.reshape(1, -1), eps=1e-3)[0]
+        # the value at each kept column equals LayerNorm of the expanded row
+        firsts = np.cumsum(np.concatenate([[0], w[:-1].astype(int)]))
+        keep = w > 0
+        np.testing.assert_allclose(y[r, keep], z[firsts[keep]], rtol=1e-12, atol=1e-13)
+
+
+def test_weighted_std_unit_weights_is_layernorm_and_rejects_bad_weights():
+    rng = np.random.default_rng(53)
+    x = rng.standard_normal((4, 77)).astype(np.float32)
+    np.testing.assert_allclose(oracle.weighted_std(x, np.ones(77, np.float32), eps=1e-5),
+                               oracle.layernorm(x, eps=1e-5), rtol=1e-13, atol=1e-13)
+    with pytest.raises(ValueError):
+        oracle.weighted_std(x, np.zeros(77, np.float32))
+    with pytest.raises(ValueError):
+        oracle.weighted_std(x, -np.ones(77, np.float32))
