@@ -155,7 +155,15 @@ def cpu_oracle_rate(w, inputs, rows: int, threads: int):
     sub = dict(inputs)
     sub["x"] = inputs["x"][:rows]
     t0 = time.perf_counter()
-    if w.op == "softmax":
+    if w.op == "quantize":
+        bounds = np.linspace(0, rows, min(threads, rows) + 1, dtype=np.int64)
+        import concurrent.futures as cf
+        with cf.ThreadPoolExecutor(len(bounds) - 1) as ex:
+            list(ex.map(lambda i: oracle.quantize(sub["x"][bounds[i]:bounds[i + 1]]),
+                        range(len(bounds) - 1)))
+    elif w.op == "weighted_std":
+        oracle.run_rows(oracle.weighted_std, sub["x"], sub["weight"], threads=threads, eps=w.eps)
+    elif w.op == "softmax":
         oracle.run_rows(oracle.softmax, sub["x"], threads=threads)
     elif w.op == "layernorm":
         oracle.run_rows(oracle.layernorm, sub["x"], sub.get("gamma"), sub.get("beta"),
@@ -242,14 +250,17 @@ def main():
 
     inputs = w.generate()
     DT = {"f32": C.F32, "bf16": C.BF16}
-    OPS = {"softmax": C.SOFTMAX, "layernorm": C.LAYERNORM, "rmsnorm": C.RMSNORM}
+    OPS = {"softmax": C.SOFTMAX, "layernorm": C.LAYERNORM, "rmsnorm": C.RMSNORM,
+           "quantize": C.QUANTIZE, "weighted_std": C.WEIGHTED_STD}
 
     def to_device(a):
         if a.dtype == np.uint16:
             return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to("cuda")
         return torch.from_numpy(a).to("cuda")
     dx = to_device(inputs["x"])
-    dy = torch.empty_like(dx)
+    quant = w.op == "quantize"
+    dy = torch.empty(dx.shape, dtype=torch.int8, device=dx.device) if quant else torch.empty_like(dx)
+    dscales = torch.empty(w.rows, dtype=torch.float32, device=dx.device) if quant else None
     params = {k: to_device(v) for k, v in inputs.items() if k != "x"}
 
     if args.variant == "auto":
@@ -281,6 +292,13 @@ def main():
     pp = C._plan_ptr(plan)
 
     def launch(xp, yp):
+        if quant:
+            return lib.credit_quantize(xp, yp, dscales.data_ptr(), w.rows, w.cols, DT[w.dtype], pp,
+                                       wptr or None, wbytes, sptr)
+        if w.op == "weighted_std":
+            return lib.credit_weighted_std(xp, yp, w.rows, w.cols, DT[w.dtype],
+                                           params["weight"].data_ptr(), pdt, w.eps, pp,
+                                           wptr or None, wbytes, sptr)
         if w.op == "softmax":
             return lib.credit_softmax(xp, yp, w.rows, w.cols, DT[w.dtype], pp, wptr or None,
                                       wbytes, sptr)
@@ -343,10 +361,11 @@ def main():
     hparams = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v)
                for k, v in params.items()}
     hy = torch.empty(dy.shape, dtype=dy.dtype, pin_memory=True)
+    hs = torch.empty(w.rows, dtype=torch.float32, pin_memory=True) if quant else None
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
     h2d = hx.numel() * hx.element_size() + sum(v.numel() * v.element_size()
                                                for v in hparams.values())
-    d2h = hy.numel() * hy.element_size()
+    d2h = hy.numel() * hy.element_size() + (hs.numel() * 4 if quant else 0)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -359,6 +378,8 @@ def main():
                 params[k].copy_(v, non_blocking=True)
             launch(xp, yp)
             hy.copy_(dy, non_blocking=True)
+            if quant:
+                hs.copy_(dscales, non_blocking=True)
         f1.record(stream)
     torch.cuda.synchronize()
     te = torch.tensor([f0.elapsed_time(f1)], dtype=torch.float64, device="cuda")

@@ -17,10 +17,11 @@ from __future__ import annotations
 from . import _credit as C
 from ._credit import CreditError, Plan  # noqa: F401
 
-__all__ = ["softmax", "layernorm", "rmsnorm", "plan", "CreditError", "Plan",
-           "device_error", "load_library"]
+__all__ = ["softmax", "layernorm", "rmsnorm", "quantize", "weighted_std", "plan", "CreditError",
+           "Plan", "device_error", "load_library"]
 
-_OPS = {"softmax": C.SOFTMAX, "layernorm": C.LAYERNORM, "rmsnorm": C.RMSNORM}
+_OPS = {"softmax": C.SOFTMAX, "layernorm": C.LAYERNORM, "rmsnorm": C.RMSNORM,
+        "quantize": C.QUANTIZE, "weighted_std": C.WEIGHTED_STD}
 _plan_cache: dict = {}
 
 
@@ -140,6 +141,42 @@ def rmsnorm(x, weight=None, eps: float = 1e-6, out=None, plan: Plan | None = Non
                           _ptr(weight), _pdtype(weight), float(eps), p, w, wb, _stream(x))
     if st != C.OK:
         raise CreditError(st, "credit_rmsnorm")
+    return out
+
+
+def quantize(x, out=None, scales=None, plan: Plan | None = None, workspace=None):
+    """Row-wise symmetric int8 quantization over the last dimension; returns
+    (codes int8 shaped like x, fp32 scales, one per row)."""
+    import torch
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("credit: x must be a contiguous CUDA tensor")
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    if scales is None:
+        scales = torch.empty(rows, dtype=torch.float32, device=x.device)
+    p, w, wb = _plan_and_ws("quantize", rows, cols, x, plan, workspace)
+    st = C.credit_quantize(x.data_ptr(), out.data_ptr(), scales.data_ptr(), rows, cols,
+                           _dtype(x.dtype), p, w, wb, _stream(x))
+    if st != C.OK:
+        raise CreditError(st, "credit_quantize")
+    return out, scales
+
+
+def weighted_std(x, weights, eps: float = 1e-5, out=None, plan: Plan | None = None,
+                 workspace=None):
+    """Weighted standardization over the last dimension with per-column
+    weights: (x - mean_w) / sqrt(var_w + eps)."""
+    rows, cols, out = _prep(x, out)
+    if weights is None or weights.numel() != cols:
+        raise ValueError("credit: weights must have cols elements")
+    p, w, wb = _plan_and_ws("weighted_std", rows, cols, x, plan, workspace)
+    st = C.credit_weighted_std(x.data_ptr(), out.data_ptr(), rows, cols, _dtype(x.dtype),
+                               weights.data_ptr(), _pdtype(weights), float(eps), p, w, wb,
+                               _stream(x))
+    if st != C.OK:
+        raise CreditError(st, "credit_weighted_std")
     return out
 
 

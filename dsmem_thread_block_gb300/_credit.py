@@ -17,7 +17,7 @@ from . import build as _build
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_LEGAL_PLAN, ERR_CUDA, \
     ERR_DEVICE_TIMEOUT, ERR_NOT_CALIBRATED = range(7)
 F32, BF16 = 0, 1
-SOFTMAX, LAYERNORM, RMSNORM = 0, 1, 2
+SOFTMAX, LAYERNORM, RMSNORM, QUANTIZE, WEIGHTED_STD = 0, 1, 2, 3, 4
 AUTO, CLUSTER, TWO_PASS, CLUSTER_PERSISTENT = 0, 1, 2, 3
 
 _vp, _i64, _i32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -104,6 +104,10 @@ SIGNATURES = {
                                 ctypes.POINTER(Plan), _vp, _sz, _vp]),
     "credit_rmsnorm": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _i32, _f32,
                               ctypes.POINTER(Plan), _vp, _sz, _vp]),
+    "credit_quantize": (_i32, [_vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(Plan), _vp, _sz,
+                               _vp]),
+    "credit_weighted_std": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _i32, _f32,
+                                   ctypes.POINTER(Plan), _vp, _sz, _vp]),
     "credit_two_pass_noalloc": (_i32, [_i32, _vp, _vp, _i64, _i64, _i32, _vp, _vp, _i32, _f32,
                                        _vp]),
     "credit_bench_dsmem": (_i32, [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(BenchResult)]),
@@ -207,6 +211,20 @@ def credit_rmsnorm(x: int, y: int, rows: int, cols: int, dtype: int, weight: int
     return load().credit_rmsnorm(x, y, rows, cols, dtype, weight or None, param_dtype, eps,
                                  _plan_ptr(plan), workspace or None, workspace_bytes,
                                  stream or None)
+
+
+def credit_quantize(x: int, q: int, scales: int, rows: int, cols: int, dtype: int, plan=None,
+                    workspace: int = 0, workspace_bytes: int = 0, stream: int = 0) -> int:
+    return load().credit_quantize(x, q, scales, rows, cols, dtype, _plan_ptr(plan),
+                                  workspace or None, workspace_bytes, stream or None)
+
+
+def credit_weighted_std(x: int, y: int, rows: int, cols: int, dtype: int, weights: int,
+                        weight_dtype: int, eps: float, plan=None, workspace: int = 0,
+                        workspace_bytes: int = 0, stream: int = 0) -> int:
+    return load().credit_weighted_std(x, y, rows, cols, dtype, weights or None, weight_dtype,
+                                      eps, _plan_ptr(plan), workspace or None, workspace_bytes,
+                                      stream or None)
 
 
 def credit_two_pass_noalloc(op: int, x: int, y: int, rows: int, cols: int, dtype: int,

@@ -152,6 +152,7 @@ struct OpCall {
     void* ws;
     size_t ws_bytes;
     cudaStream_t stream;
+    float* aux = nullptr;  // quantization: per-row scales out
 };
 
 // Complete / re-derive a plan from the fields a caller may set.
@@ -173,15 +174,26 @@ credit_status_t run(const OpCall& c) {
     if (!c.x || !c.y || c.rows < 1 || c.cols < 1) return CREDIT_ERR_INVALID_ARG;
     if (!dtype_ok(c.dtype)) return CREDIT_ERR_UNSUPPORTED;
     if ((c.p0 || c.p1) && !dtype_ok(c.pdtype)) return CREDIT_ERR_UNSUPPORTED;
-    if (c.op != CREDIT_SOFTMAX && !(c.eps >= 0.f)) return CREDIT_ERR_INVALID_ARG;
+    const bool quant = c.op == CREDIT_QUANTIZE;
+    if (!quant && c.op != CREDIT_SOFTMAX && !(c.eps >= 0.f)) return CREDIT_ERR_INVALID_ARG;
+    if (quant && !c.aux) return CREDIT_ERR_INVALID_ARG;
+    if (c.op == CREDIT_WEIGHTED_STD && !c.p0) return CREDIT_ERR_INVALID_ARG;
     if (c.rows > INT64_MAX / c.cols) return CREDIT_ERR_INVALID_ARG;
     const size_t es = esize(c.dtype);
     const int64_t n = c.rows * c.cols;
     if (n > INT64_MAX / (int64_t)es) return CREDIT_ERR_INVALID_ARG;
     // in place is fine (each element is read before it is written, by the
-    // same CTA); any other overlap is rejected
-    const uintptr_t xb = (uintptr_t)c.x, yb = (uintptr_t)c.y, bytes = (uintptr_t)(n * (int64_t)es);
-    if (xb != yb && xb < yb + bytes && yb < xb + bytes) return CREDIT_ERR_INVALID_ARG;
+    // same CTA); any other overlap is rejected -- and quantization, whose
+    // int8 output is narrower than its input, may not overlap at all
+    const uintptr_t xb = (uintptr_t)c.x, yb = (uintptr_t)c.y;
+    const uintptr_t xbytes = (uintptr_t)(n * (int64_t)es);
+    const uintptr_t ybytes = quant ? (uintptr_t)n : xbytes;
+    if ((quant || xb != yb) && xb < yb + ybytes && yb < xb + xbytes) return CREDIT_ERR_INVALID_ARG;
+    if (quant) {
+        const uintptr_t ab = (uintptr_t)c.aux, abytes = (uintptr_t)(c.rows * 4);
+        if ((ab & 3u) || (ab < xb + xbytes && xb < ab + abytes) || (ab < yb + ybytes && yb < ab + abytes))
+            return CREDIT_ERR_INVALID_ARG;
+    }
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return CREDIT_ERR_CUDA; }
@@ -196,8 +208,12 @@ credit_status_t run(const OpCall& c) {
     }
     if (st != CREDIT_OK) return st;
 
+    // the bulk path also needs 16-byte-aligned output rows; the int8 rows of
+    // quantization are cols bytes long
+    const int64_t out_row_bytes = quant ? c.cols : (int64_t)(c.cols * es);
     const bool vec = aligned16(c.x) && aligned16(c.y) && ((int64_t)(c.cols * es) % 16 == 0) &&
-                     (!c.p0 || aligned16(c.p0)) && (!c.p1 || aligned16(c.p1));
+                     out_row_bytes % 16 == 0 && (!c.p0 || aligned16(c.p0)) &&
+                     (!c.p1 || aligned16(c.p1));
     KernelKey key{(int)c.op, (int)c.dtype, (c.p0 || c.p1) ? (int)c.pdtype : 0, vec};
     unsigned* err = device_error_word();
     if (!err) return CREDIT_ERR_CUDA;
@@ -237,6 +253,7 @@ credit_status_t run(const OpCall& c) {
         a.pitch = (int32_t)row_pitch(plan.slice_elems, (int)es);
         a.eps = c.eps;
         a.err = err;
+        a.aux = c.aux;
         const void* fn = cluster_kernel(key);
         if (!kernel_info(dev, fn, true)) return CREDIT_ERR_CUDA;
         return from_cuda(launch_cluster(key, a, plan.cluster_size, plan.threads,
@@ -252,6 +269,7 @@ credit_status_t run(const OpCall& c) {
     a.nch = (int32_t)((c.cols + plan.slice_elems - 1) / plan.slice_elems);
     a.eps = c.eps;
     a.ws = static_cast<float*>(c.ws);
+    a.aux = c.aux;
     return from_cuda(launch_two_pass(key, a, c.rows, plan.threads, c.stream));
 }
 
@@ -303,6 +321,24 @@ credit_status_t credit_rmsnorm(const void* x, void* y, int64_t rows, int64_t col
                                float eps, const credit_plan_t* plan, void* workspace,
                                size_t workspace_bytes, void* stream) {
     OpCall c{CREDIT_RMSNORM, x, y, rows, cols, dtype, weight, nullptr, param_dtype, eps,
+             plan, workspace, workspace_bytes, (cudaStream_t)stream};
+    return run(c);
+}
+
+credit_status_t credit_quantize(const void* x, int8_t* q, float* scales, int64_t rows, int64_t cols,
+                                credit_dtype_t dtype, const credit_plan_t* plan, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    OpCall c{CREDIT_QUANTIZE, x, q, rows, cols, dtype, nullptr, nullptr, CREDIT_F32, 0.f,
+             plan, workspace, workspace_bytes, (cudaStream_t)stream, scales};
+    return run(c);
+}
+
+credit_status_t credit_weighted_std(const void* x, void* y, int64_t rows, int64_t cols,
+                                    credit_dtype_t dtype, const void* weights,
+                                    credit_dtype_t weight_dtype, float eps,
+                                    const credit_plan_t* plan, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    OpCall c{CREDIT_WEIGHTED_STD, x, y, rows, cols, dtype, weights, nullptr, weight_dtype, eps,
              plan, workspace, workspace_bytes, (cudaStream_t)stream};
     return run(c);
 }

@@ -85,6 +85,7 @@ cluster_reduce_reuse(const ClusterArgs a) {
 
     // --------------------------------------------- a3 local partials
     // each chunk is folded into the threads' statistics as soon as it lands
+    const PT* wp = OP == kWStd ? static_cast<const PT*>(a.p0) + start : nullptr;  // weights
     Stats<OP, T> st[R];
 #pragma unroll
     for (int i = 0; i < R; ++i) {
@@ -92,13 +93,20 @@ cluster_reduce_reuse(const ClusterArgs a) {
             for (int c = 0; c < cpr; ++c) {
                 if constexpr (BULK) mbar_wait_bounded(smem_u32(&mbar[i * cpr + c]), 0, a.err);
                 const int v0 = c * vpc;
+                if constexpr (OP == kWStd && !BULK) continue;  // weights may be misaligned
                 stats_tiles(st[i], stage + (size_t)i * a.pitch + (size_t)v0 * 16,
-                            min(nvec, v0 + vpc) - v0, warp, nwarps, lane);
+                            min(nvec, v0 + vpc) - v0, warp, nwarps, lane,
+                            wp ? wp + (int64_t)v0 * VEC : wp);
             }
         }
     }
-    if constexpr (!BULK)
-        for (int i = nvec * VEC + tid; i < n; i += nt) st[0].add1(tail_at(i));
+    if constexpr (!BULK) {
+        if constexpr (OP == kWStd) {
+            for (int i = tid; i < n; i += nt) st[0].add1(tail_at(i), load_param1<PT>(wp, i));
+        } else {
+            for (int i = nvec * VEC + tid; i < n; i += nt) st[0].add1(tail_at(i));
+        }
+    }
     auto stash = [&](int i, float mq) {
         float s = softmax_stash(stage + (size_t)i * a.pitch, nvec, warp, nwarps, lane, mq);
         if constexpr (!BULK) {
@@ -137,22 +145,36 @@ cluster_reduce_reuse(const ClusterArgs a) {
     }
 
     // ------------------------------------------------------- a7 output
-    const PT* g = static_cast<const PT*>(a.p0);
-    const PT* b = static_cast<const PT*>(a.p1);
+    constexpr bool kParams = OP == kLayerNorm || OP == kRMSNorm;
+    const PT* g = kParams ? static_cast<const PT*>(a.p0) : nullptr;
+    const PT* b = kParams ? static_cast<const PT*>(a.p1) : nullptr;
     OutputMap<OP, T> h[R];
 #pragma unroll
     for (int i = 0; i < R; ++i) h[i] = OutputMap<OP, T>(stv[i][0], stv[i][1], stv[i][2], p[i][0], a.cols, a.eps);
-    T* yrow[R];
+    if constexpr (OP == kQuant) {
+        int8_t* qrow[R];
 #pragma unroll
-    for (int i = 0; i < R; ++i) yrow[i] = static_cast<T*>(a.y) + (row0 + i) * a.cols + start;
-    if constexpr (BULK) {
-        output_tiles_rows<OP, T, PT, R>(h, stage, a.pitch, yrow, rows, g ? g + start : nullptr,
-                                        b ? b + start : nullptr, nvec, warp, nwarps, lane);
+        for (int i = 0; i < R; ++i) qrow[i] = static_cast<int8_t*>(a.y) + (row0 + i) * a.cols + start;
+        if (rank == 0 && tid == 0)
+            for (int i = 0; i < rows; ++i) a.aux[row0 + i] = h[i].c0;  // the row scales
+        if constexpr (BULK) {
+            output_quant_rows<T, R>(h, stage, a.pitch, qrow, rows, nvec, warp, nwarps, lane);
+        } else {
+            for (int i = tid; i < n; i += nt) qrow[0][i] = (int8_t)h[0].code(tail_at(i));
+        }
     } else {
-        for (int i = tid; i < n; i += nt) {
-            const float gj = (OP != kSoftmax && g) ? load_param1<PT>(g, start + i) : 1.f;
-            const float bj = (OP != kSoftmax && b) ? load_param1<PT>(b, start + i) : 0.f;
-            yrow[0][i] = E::from_f(h[0].one(tail_at(i), gj, bj));
+        T* yrow[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) yrow[i] = static_cast<T*>(a.y) + (row0 + i) * a.cols + start;
+        if constexpr (BULK) {
+            output_tiles_rows<OP, T, PT, R>(h, stage, a.pitch, yrow, rows, g ? g + start : nullptr,
+                                            b ? b + start : nullptr, nvec, warp, nwarps, lane);
+        } else {
+            for (int i = tid; i < n; i += nt) {
+                const float gj = g ? load_param1<PT>(g, start + i) : 1.f;
+                const float bj = b ? load_param1<PT>(b, start + i) : 0.f;
+                yrow[0][i] = E::from_f(h[0].one(tail_at(i), gj, bj));
+            }
         }
     }
 }
@@ -186,6 +208,9 @@ const void* cluster_kernel(KernelKey k) {
                                            : pick_rows<kSoftmax, bf16, float>(k.vec, k.rows);
         case kLayerNorm: return pick_dtype<kLayerNorm>(k.dtype, k.pdtype, k.vec, k.rows);
         case kRMSNorm: return pick_dtype<kRMSNorm>(k.dtype, k.pdtype, k.vec, k.rows);
+        case kQuant: return k.dtype == 0 ? pick_rows<kQuant, float, float>(k.vec, k.rows)
+                                         : pick_rows<kQuant, bf16, float>(k.vec, k.rows);
+        case kWStd: return pick_dtype<kWStd>(k.dtype, k.pdtype, k.vec, k.rows);
     }
     return nullptr;
 }

@@ -25,7 +25,13 @@
 
 namespace credit {
 
-enum Op : int { kSoftmax = 0, kLayerNorm = 1, kRMSNorm = 2 };
+// Operators.  kQuant: row absmax -> scale -> int8 codes; kWStd: weighted
+// standardization with per-column weights (the weighted counterpart of
+// LayerNorm without the affine step).
+enum Op : int { kSoftmax = 0, kLayerNorm = 1, kRMSNorm = 2, kQuant = 3, kWStd = 4 };
+
+// LayerNorm-like statistics (count or weight, mean, M2).
+constexpr bool norm_like(int op) { return op == kLayerNorm || op == kWStd; }
 
 constexpr int kMaxCluster = 16;   // non-portable cluster size limit
 constexpr int kMaxThreads = 512;         // two-pass kernels
@@ -209,6 +215,8 @@ __device__ __forceinline__ void named_sync(int nthreads) {
 //              form: n = sum n_q, mean = sum n_q mean_q / n,
 //              M2 = sum (M2_q + n_q (mean_q - mean)^2)
 //   RMSNorm:   ss = sum ss_q
+//   quantize:  amax = max amax_q;  weighted standardization: as LayerNorm
+//              with weight sums in place of counts
 template <int OP>
 __device__ __forceinline__ void combine_slots(const float* sl, uint32_t P, float& st0,
                                               float& st1, float& st2);
@@ -218,13 +226,17 @@ __device__ __forceinline__ void combine_slots(const float* sl, uint32_t P, float
 template <int OP>
 __device__ __forceinline__ void combine_slots_strided(const float* sl, uint32_t P, int stride,
                                                       float& st0, float& st1, float& st2) {
-    if constexpr (OP == kSoftmax) {
+    if constexpr (OP == kQuant) {
+        float m = 0.f;
+        for (uint32_t q = 0; q < P; ++q) m = fmaxf(m, sl[q * stride]);
+        st0 = m; st1 = st2 = 0.f;
+    } else if constexpr (OP == kSoftmax) {
         float m = -INFINITY;
         for (uint32_t q = 0; q < P; ++q) m = fmaxf(m, sl[q * stride]);
         float s = 0.f;
         for (uint32_t q = 0; q < P; ++q) s += rescale(sl[q * stride + 1], sl[q * stride], m);
         st0 = m; st1 = s; st2 = 0.f;
-    } else if constexpr (OP == kLayerNorm) {
+    } else if constexpr (norm_like(OP)) {
         float n = 0.f, nm = 0.f;
         for (uint32_t q = 0; q < P; ++q) {
             n += sl[q * stride];
@@ -247,14 +259,18 @@ __device__ __forceinline__ void combine_slots_strided(const float* sl, uint32_t 
 template <int OP>
 __device__ __forceinline__ void combine_slots(const float* sl, uint32_t P, float& st0,
                                               float& st1, float& st2) {
-    if constexpr (OP == kSoftmax) {
+    if constexpr (OP == kQuant) {
+        float m = 0.f;
+        for (uint32_t q = 0; q < P; ++q) m = fmaxf(m, sl[q * kSlotStride]);
+        st0 = m; st1 = st2 = 0.f;
+    } else if constexpr (OP == kSoftmax) {
         float m = -INFINITY;
         for (uint32_t q = 0; q < P; ++q) m = fmaxf(m, sl[q * kSlotStride]);
         float s = 0.f;
         for (uint32_t q = 0; q < P; ++q)
             s += rescale(sl[q * kSlotStride + 1], sl[q * kSlotStride], m);
         st0 = m; st1 = s; st2 = 0.f;
-    } else if constexpr (OP == kLayerNorm) {
+    } else if constexpr (norm_like(OP)) {
         float n = 0.f, nm = 0.f;
         for (uint32_t q = 0; q < P; ++q) {
             n += sl[q * kSlotStride];

@@ -107,12 +107,19 @@ extern "C" credit_status_t credit_calibrate(int device, int runs, const char* pr
 
 namespace {
 
-// One launch of the operator with an explicit plan on the default stream.
+// One launch of the operator with an explicit plan on the default stream
+// (aux: the row scales of quantization).
 credit_status_t call_op(credit_op_t op, const void* x, void* y, int64_t rows, int64_t cols,
                         credit_dtype_t dtype, const void* p0, const void* p1, int pdt,
-                        const credit_plan_t* plan, void* ws, size_t wsb) {
+                        const credit_plan_t* plan, void* ws, size_t wsb, float* aux) {
     const credit_dtype_t pd = pdt < 0 ? CREDIT_F32 : (credit_dtype_t)pdt;
     switch (op) {
+        case CREDIT_QUANTIZE:
+            return credit_quantize(x, static_cast<int8_t*>(y), aux, rows, cols, dtype, plan, ws, wsb,
+                                   nullptr);
+        case CREDIT_WEIGHTED_STD:
+            return credit_weighted_std(x, y, rows, cols, dtype, p0, pd, 1e-5f, plan, ws, wsb,
+                                       nullptr);
         case CREDIT_SOFTMAX: return credit_softmax(x, y, rows, cols, dtype, plan, ws, wsb, nullptr);
         case CREDIT_LAYERNORM:
             return credit_layernorm(x, y, rows, cols, dtype, p0, p1, pd, 1e-5f, plan, ws, wsb, nullptr);
@@ -125,7 +132,8 @@ credit_status_t call_op(credit_op_t op, const void* x, void* y, int64_t rows, in
 // Median time of `runs` launches (after one warm-up) in microseconds.
 credit_status_t time_op(credit_op_t op, const void* x, void* y, int64_t rows, int64_t cols,
                         credit_dtype_t dtype, const void* p0, const void* p1, int pdt,
-                        const credit_plan_t* plan, void* ws, size_t wsb, int runs, double* us) {
+                        const credit_plan_t* plan, void* ws, size_t wsb, int runs, double* us,
+                        float* aux) {
     cudaEvent_t e0, e1;
     if (cudaEventCreate(&e0) != cudaSuccess) return CREDIT_ERR_CUDA;
     if (cudaEventCreate(&e1) != cudaSuccess) { cudaEventDestroy(e0); return CREDIT_ERR_CUDA; }
@@ -134,7 +142,7 @@ credit_status_t time_op(credit_op_t op, const void* x, void* y, int64_t rows, in
     for (int r = 0; r <= runs && st == CREDIT_OK; ++r) {
         float ms = 0.f;
         if (cudaEventRecord(e0, nullptr) != cudaSuccess) { st = CREDIT_ERR_CUDA; break; }
-        st = call_op(op, x, y, rows, cols, dtype, p0, p1, pdt, plan, ws, wsb);
+        st = call_op(op, x, y, rows, cols, dtype, p0, p1, pdt, plan, ws, wsb, aux);
         if (st != CREDIT_OK) break;
         if (cudaEventRecord(e1, nullptr) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
             cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) {
@@ -197,20 +205,25 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         st = make_plan(device, op, rows, cols, dtype, CREDIT_TWO_PASS, 0, 0, 0, &base);
         if (st != CREDIT_OK) return st;
     }
-    const double b_base = staging ? 2.0 * mat : 3.0 * mat;
-    const double b_credit = 2.0 * mat;
+    // bytes: one read of x and one write of the output (int8 codes for
+    // quantization); the re-read baseline reads x twice
+    const double b_write = op == CREDIT_QUANTIZE ? (double)rows * (double)cols : mat;
+    const double b_credit = mat + b_write;
+    const double b_base = staging ? b_credit : b_credit + mat;
 
     // scratch buffers of the shape
-    Scratch x, y, g, b, ws;
+    Scratch x, y, g, b, ws, aux;
     const size_t pbytes = (size_t)cols * (param_dtype == CREDIT_F32 ? 4 : 2);
-    if (!x.alloc((size_t)mat) || !y.alloc((size_t)mat) ||
+    if (op == CREDIT_WEIGHTED_STD && param_dtype < 0) return CREDIT_ERR_INVALID_ARG;
+    if (!x.alloc((size_t)mat) || !y.alloc((size_t)mat) || !aux.alloc((size_t)rows * 4) ||
         (param_dtype >= 0 && (!g.alloc(pbytes) || !b.alloc(pbytes))))
         return CREDIT_ERR_CUDA;
     if (!staging && !ws.alloc((size_t)base.workspace_bytes)) return CREDIT_ERR_CUDA;
 
     double t_base = 0.0;
+    float* auxp = static_cast<float*>(aux.p);
     st = time_op(op, x.p, y.p, rows, cols, dtype, g.p, b.p, param_dtype, &base, ws.p,
-                 (size_t)base.workspace_bytes, runs, &t_base);
+                 (size_t)base.workspace_bytes, runs, &t_base, auxp);
     if (st != CREDIT_OK) return st;
     const double r_base = b_base / t_base;  // bytes per microsecond
 
@@ -289,7 +302,7 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         for (int P : order) {
             credit_candidate_t& c = rep.cand[P - 1];
             st = time_op(op, x.p, y.p, rows, cols, dtype, g.p, b.p, param_dtype, &c.plan, nullptr,
-                         0, runs, &c.measured_us);
+                         0, runs, &c.measured_us, auxp);
             if (st != CREDIT_OK) return st;
             if (c.measured_us < best_meas) {
                 best_meas = c.measured_us;
@@ -300,7 +313,7 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
             if (make_plan(device, op, rows, cols, dtype, CREDIT_CLUSTER_PERSISTENT, P, 0, 0, &pp) ==
                 CREDIT_OK) {
                 st = time_op(op, x.p, y.p, rows, cols, dtype, g.p, b.p, param_dtype, &pp, nullptr,
-                             0, runs, &c.persistent_us);
+                             0, runs, &c.persistent_us, auxp);
                 if (st != CREDIT_OK) return st;
                 if (c.persistent_us < best_meas) {
                     best_meas = c.persistent_us;

@@ -20,6 +20,7 @@ struct ClusterArgs {
     int32_t pitch;        // bytes between the staged slices of a CTA's rows
     float eps;
     unsigned* err;        // device error word
+    float* aux;           // quantization: per-row scales out (else unused)
 };
 
 constexpr int kMaxRowsPerCluster = 4;
@@ -35,6 +36,7 @@ struct TwoPassArgs {
     int32_t nch;          // chunks per row
     float eps;
     float* ws;            // rows * nch * 4 floats
+    float* aux;           // quantization: per-row scales out (else unused)
 };
 
 constexpr int kTwoPassVpt = 4;  // 16-byte vectors per thread per chunk

@@ -23,7 +23,8 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 bool op_ok(credit_op_t op) {
-    return op == CREDIT_SOFTMAX || op == CREDIT_LAYERNORM || op == CREDIT_RMSNORM;
+    return op == CREDIT_SOFTMAX || op == CREDIT_LAYERNORM || op == CREDIT_RMSNORM ||
+           op == CREDIT_QUANTIZE || op == CREDIT_WEIGHTED_STD;
 }
 
 int cluster_threads(int64_t staged_vecs) {
@@ -75,6 +76,7 @@ credit_status_t persistent_plan(int dev, const DevInfo* d, credit_op_t op, int64
     const int64_t chunk_bytes = chunk * es;
     const int64_t cpr = ceil_div(slice, chunk);
     const void* fn = persistent_kernel(KernelKey{(int)op, (int)dtype, 0, true});
+    if (!fn) return CREDIT_ERR_NO_LEGAL_PLAN;  // operator not offered by the persistent kernel
     const KernelInfo* ki = kernel_info(dev, fn, true);
     if (!ki) return CREDIT_ERR_CUDA;
     const int64_t budget = cps == 1

@@ -179,6 +179,45 @@ template <> struct Stats<kSoftmax, float> {
     __device__ __forceinline__ void add1(float f) { m = fmaxf(m, f); }
 };
 
+// quantization: the row's absolute maximum
+template <typename T> struct Stats<kQuant, T> {
+    float a = 0.f;
+    __device__ __forceinline__ void add(uint4 raw) {
+        F2 p[Pairs<T>::kN];
+        Pairs<T>::unpack(raw, p);
+#pragma unroll
+        for (int i = 0; i < Pairs<T>::kN; ++i) a = max3(a, fabsf(p[i].x), fabsf(p[i].y));
+    }
+    __device__ __forceinline__ void add1(float f) { a = fmaxf(a, fabsf(f)); }
+};
+
+// weighted standardization: weighted shifted sums around the thread's first
+// element K: W = sum w, s1 = sum w (x - K), s2 = sum w (x - K)^2
+template <typename T> struct Stats<kWStd, T> {
+    F2 nK = {0.f, 0.f}, sw = {0.f, 0.f}, s1 = {0.f, 0.f}, s2 = {0.f, 0.f};
+    bool started = false;
+    __device__ __forceinline__ void add(uint4 raw, const F2* w) {
+        F2 p[Pairs<T>::kN];
+        Pairs<T>::unpack(raw, p);
+        if (!started) { nK = f2(-p[0].x); started = true; }
+#pragma unroll
+        for (int i = 0; i < Pairs<T>::kN; ++i) {
+            const F2 d = add2(p[i], nK);
+            const F2 wd = mul2(w[i], d);
+            sw = add2(sw, w[i]);
+            s1 = add2(s1, wd);
+            s2 = fma2(wd, d, s2);
+        }
+    }
+    __device__ __forceinline__ void add1(float f, float w) {
+        if (!started) { nK = f2(-f); started = true; }
+        const float d = f + nK.x;
+        sw.x += w;
+        s1.x = fmaf(w, d, s1.x);
+        s2.x = fmaf(w * d, d, s2.x);
+    }
+};
+
 // fp32 softmax stash pass over the staged vectors [0, nvec) at `base`:
 // t = exp(x - mq) written back in place (accurate expf); returns this
 // thread's sum of t.  Vectors are visited in the same warp tiles as the
@@ -250,7 +289,13 @@ struct OutputMap {
     __device__ __forceinline__ OutputMap() {}
     __device__ __forceinline__ OutputMap(float st0, float st1, float st2, float mq, int64_t N,
                                          float eps) {
-        if constexpr (OP == kSoftmax) {
+        if constexpr (OP == kQuant) {
+            c0 = st0 / 127.f;  // the row scale (IEEE division)
+        } else if constexpr (OP == kWStd) {
+            const float r = 1.f / sqrtf(fmaxf(st0 > 0.f ? st2 / st0 : 0.f, 0.f) + eps);
+            c0 = r;
+            c1 = -st1 * r;
+        } else if constexpr (OP == kSoftmax) {
             if constexpr (sizeof(T) == 4) { c1 = rescale(1.f, mq, st0) / st1; }
             else { c0 = -st0 * kLog2e; c1 = 1.f / st1; }
         } else if constexpr (OP == kLayerNorm) {
@@ -261,8 +306,16 @@ struct OutputMap {
             c0 = 1.f / sqrtf(st0 / (float)N + eps);
         }
     }
+    // int8 code of x (quantization): round half to even of x / scale, clamped
+    __device__ __forceinline__ int code(float x) const {
+        if (c0 == 0.f) return 0;
+        const int q = __float2int_rn(__fdiv_rn(x, c0));
+        return max(-127, min(127, q));
+    }
     __device__ __forceinline__ F2 operator()(F2 x, F2 g, F2 b) const {
-        if constexpr (OP == kSoftmax) {
+        if constexpr (OP == kWStd) {
+            return fma2(x, f2(c0), f2(c1));
+        } else if constexpr (OP == kSoftmax) {
             if constexpr (sizeof(T) == 4) return mul2(x, f2(c1));
             const F2 a = fma2(x, f2(kLog2e), f2(c0));
             return mul2(F2{fast_ex2(a.x), fast_ex2(a.y)}, f2(c1));
@@ -274,7 +327,9 @@ struct OutputMap {
     }
     // the same arithmetic on one element (element path)
     __device__ __forceinline__ float one(float x, float g, float b) const {
-        if constexpr (OP == kSoftmax) {
+        if constexpr (OP == kWStd) {
+            return fmaf(x, c0, c1);
+        } else if constexpr (OP == kSoftmax) {
             if constexpr (sizeof(T) == 4) return x * c1;
             return fast_ex2(fmaf(x, kLog2e, c0)) * c1;
         } else if constexpr (OP == kLayerNorm) {
@@ -285,11 +340,22 @@ struct OutputMap {
     }
 };
 
-// Statistics over staged 16-byte vectors [0, n) at `base`.
-template <int OP, typename T>
+// Statistics over staged 16-byte vectors [0, n) at `base`; `wp` are the
+// per-column weights of those vectors (weighted standardization only).
+template <int OP, typename T, typename PT = float>
 __device__ __forceinline__ void stats_tiles(Stats<OP, T>& st, const unsigned char* base, int n,
-                                            int warp, int nwarps, int lane) {
-    for_tiles<4>(n, warp, nwarps, lane, [&](int v) { st.add(lds16(base + (size_t)v * 16)); });
+                                            int warp, int nwarps, int lane,
+                                            const PT* wp = nullptr) {
+    if constexpr (OP == kWStd) {
+        constexpr int NP = Pairs<T>::kN;
+        for_tiles<4>(n, warp, nwarps, lane, [&](int v) {
+            F2 w[NP];
+            load_param_pairs<PT, NP>(wp, (int64_t)v * 2 * NP, w, 1.f);
+            st.add(lds16(base + (size_t)v * 16), w);
+        });
+    } else {
+        for_tiles<4>(n, warp, nwarps, lane, [&](int v) { st.add(lds16(base + (size_t)v * 16)); });
+    }
 }
 
 // Output granule of an operator: 4 elements for bf16 data with fp32
@@ -297,7 +363,8 @@ __device__ __forceinline__ void stats_tiles(Stats<OP, T>& st, const unsigned cha
 // else one 16-byte vector of data.
 template <int OP, typename T, typename PT>
 struct Granule {
-    static constexpr bool kHalf = OP != kSoftmax && sizeof(T) == 2 && sizeof(PT) == 4;
+    static constexpr bool kHalf =
+        (OP == kLayerNorm || OP == kRMSNorm) && sizeof(T) == 2 && sizeof(PT) == 4;
     static constexpr int kElems = kHalf ? 4 : 16 / (int)sizeof(T);
     static constexpr int kBytes = kElems * (int)sizeof(T);
     static constexpr int kPairs = kElems / 2;
@@ -337,8 +404,9 @@ __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const un
     using G = Granule<OP, T, PT>;
     constexpr int U = (OP != kSoftmax && G::kPairs == 4) ? 2 : 4, NP = G::kPairs, kTile = 32 * U;
     const int ngran = nvec * (16 / G::kBytes);
-    const bool has_g = OP != kSoftmax && gp != nullptr;
-    const bool has_b = OP != kSoftmax && bp != nullptr;
+    constexpr bool kParams = OP == kLayerNorm || OP == kRMSNorm;
+    const bool has_g = kParams && gp != nullptr;
+    const bool has_b = kParams && bp != nullptr;
 
     auto tile = [&](int t, bool full) {
         uint4 raw[U];
@@ -353,7 +421,7 @@ __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const un
                 } else {
                     raw[u] = lds16(base + (size_t)q * 16);
                 }
-                if constexpr (OP != kSoftmax) {
+                if constexpr (kParams) {
                     if (has_g) granule_params<PT, NP>(gp, q, gv[u]);
                     else for (int i = 0; i < NP; ++i) gv[u][i] = f2(1.f);
                     if (has_b) granule_params<PT, NP>(bp, q, bv[u]);
@@ -374,8 +442,8 @@ __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const un
                 }
 #pragma unroll
                 for (int i = 0; i < NP; ++i) {
-                    if constexpr (OP == kSoftmax) p[i] = h(p[i], p[i], p[i]);
-                    else p[i] = h(p[i], gv[u][i], bv[u][i]);
+                    if constexpr (kParams) p[i] = h(p[i], gv[u][i], bv[u][i]);
+                    else p[i] = h(p[i], p[i], p[i]);
                 }
                 if constexpr (G::kBytes == 8) {
                     __stcs(reinterpret_cast<uint2*>(yrow) + q,
@@ -431,7 +499,39 @@ template <int OP, typename T, int R, typename StashFn>
 __device__ __forceinline__ void cta_partial_rows(const Stats<OP, T> (&st)[R], float* redA,
                                                  float* redB, int nwarps, int nthreads,
                                                  StashFn stash_sum, float (&p)[R][3]) {
-    if constexpr (OP == kSoftmax) {
+    if constexpr (OP == kQuant) {
+        float a[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) a[i] = st[i].a;
+        block_reduce_n<R, true>(a, redA, nwarps, nthreads);
+#pragma unroll
+        for (int i = 0; i < R; ++i) { p[i][0] = a[i]; p[i][1] = p[i][2] = 0.f; }
+    } else if constexpr (OP == kWStd) {
+        float a[2 * R], mt[R], m2t[R], wt[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const float W = st[i].sw.x + st[i].sw.y;
+            const float s1 = st[i].s1.x + st[i].s1.y, s2 = st[i].s2.x + st[i].s2.y;
+            wt[i] = W;
+            mt[i] = W > 0.f ? s1 / W - st[i].nK.x : 0.f;
+            m2t[i] = W > 0.f ? fmaxf(s2 - s1 * (s1 / W), 0.f) : 0.f;
+            a[2 * i] = W;
+            a[2 * i + 1] = W * mt[i];
+        }
+        block_reduce_n<2 * R, false>(a, redA, nwarps, nthreads);
+        float q[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const float mean = a[2 * i] > 0.f ? a[2 * i + 1] / a[2 * i] : 0.f;
+            const float d = mt[i] - mean;
+            q[i] = fmaf(wt[i] * d, d, m2t[i]);
+            p[i][0] = a[2 * i];
+            p[i][1] = mean;
+        }
+        block_reduce_n<R, false>(q, redB, nwarps, nthreads);
+#pragma unroll
+        for (int i = 0; i < R; ++i) p[i][2] = q[i];
+    } else if constexpr (OP == kSoftmax) {
         float m[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) m[i] = st[i].m;
@@ -493,8 +593,9 @@ __device__ __forceinline__ void output_tiles_rows(const OutputMap<OP, T> (&h)[R]
     constexpr int kBase = (OP != kSoftmax && G::kPairs == 4) ? 2 : 4;
     constexpr int U = kBase / R > 0 ? kBase / R : 1, NP = G::kPairs, kTile = 32 * U;
     const int ngran = nvec * (16 / G::kBytes);
-    const bool has_g = OP != kSoftmax && gp != nullptr;
-    const bool has_b = OP != kSoftmax && bp != nullptr;
+    constexpr bool kParams = OP == kLayerNorm || OP == kRMSNorm;
+    const bool has_g = kParams && gp != nullptr;
+    const bool has_b = kParams && bp != nullptr;
 
     auto tile = [&](int t, bool full) {
         uint4 raw[U][R];
@@ -515,7 +616,7 @@ __device__ __forceinline__ void output_tiles_rows(const OutputMap<OP, T> (&h)[R]
                         }
                     }
                 }
-                if constexpr (OP != kSoftmax) {
+                if constexpr (kParams) {
                     if (has_g) granule_params<PT, NP>(gp, q, gv[u]);
                     else for (int j = 0; j < NP; ++j) gv[u][j] = f2(1.f);
                     if (has_b) granule_params<PT, NP>(bp, q, bv[u]);
@@ -539,8 +640,8 @@ __device__ __forceinline__ void output_tiles_rows(const OutputMap<OP, T> (&h)[R]
                         }
 #pragma unroll
                         for (int j = 0; j < NP; ++j) {
-                            if constexpr (OP == kSoftmax) pp[j] = h[i](pp[j], pp[j], pp[j]);
-                            else pp[j] = h[i](pp[j], gv[u][j], bv[u][j]);
+                            if constexpr (kParams) pp[j] = h[i](pp[j], gv[u][j], bv[u][j]);
+                            else pp[j] = h[i](pp[j], pp[j], pp[j]);
                         }
                         if constexpr (G::kBytes == 8) {
                             __stcs(reinterpret_cast<uint2*>(yrow[i]) + q,
@@ -556,6 +657,41 @@ __device__ __forceinline__ void output_tiles_rows(const OutputMap<OP, T> (&h)[R]
     int t = warp * kTile;
     for (; t + kTile <= ngran; t += nwarps * kTile) tile(t, true);
     if (t < ngran) tile(t, false);
+}
+
+}  // namespace credit
+
+namespace credit {
+
+// Quantization output of R rows: each staged 16-byte vector becomes VEC int8
+// codes (4 bytes for fp32 input, 8 for bf16), stored with one streaming
+// store per vector.
+template <typename T, int R>
+__device__ __forceinline__ void output_quant_rows(const OutputMap<kQuant, T> (&h)[R],
+                                                  const unsigned char* base, int pitch,
+                                                  int8_t* const (&qrow)[R], int rows, int nvec,
+                                                  int warp, int nwarps, int lane) {
+    constexpr int NP = Pairs<T>::kN;
+    for_tiles<4>(nvec, warp, nwarps, lane, [&](int v) {
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            if (i < rows) {
+                F2 p[NP];
+                Pairs<T>::unpack(lds16(base + (size_t)i * pitch + (size_t)v * 16), p);
+                uint32_t w[NP / 2];
+#pragma unroll
+                for (int k = 0; k < NP / 2; ++k) {
+                    const uint32_t b0 = (uint32_t)(h[i].code(p[2 * k].x) & 0xff);
+                    const uint32_t b1 = (uint32_t)(h[i].code(p[2 * k].y) & 0xff);
+                    const uint32_t b2 = (uint32_t)(h[i].code(p[2 * k + 1].x) & 0xff);
+                    const uint32_t b3 = (uint32_t)(h[i].code(p[2 * k + 1].y) & 0xff);
+                    w[k] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                }
+                if constexpr (NP == 2) __stcs(reinterpret_cast<unsigned int*>(qrow[i]) + v, w[0]);
+                else __stcs(reinterpret_cast<uint2*>(qrow[i]) + v, make_uint2(w[0], w[1]));
+            }
+        }
+    });
 }
 
 }  // namespace credit

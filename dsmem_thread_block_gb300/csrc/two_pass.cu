@@ -51,7 +51,7 @@ struct ChunkRegs {
     }
 };
 
-template <int OP, typename T, bool VEC_PATH>
+template <int OP, typename T, typename PT, bool VEC_PATH>
 __global__ void __launch_bounds__(kMaxThreads)
 two_pass_stats(const TwoPassArgs a) {
     __shared__ float red[2][kMaxWarps];
@@ -65,7 +65,36 @@ two_pass_stats(const TwoPassArgs a) {
     constexpr int N = ChunkRegs<T, VEC_PATH>::kN;
 
     float p0 = 0.f, p1 = 0.f, p2 = 0.f;
-    if constexpr (OP == kSoftmax) {
+    if constexpr (OP == kQuant) {
+        float m = 0.f;
+#pragma unroll
+        for (int e = 0; e < N; ++e) m = fmaxf(m, fabsf(r.f[e]));  // masked entries are 0
+        p0 = block_allreduce(m, red[0], MaxOp{}, 0.f);
+    } else if constexpr (OP == kWStd) {
+        // weights of this thread's elements, then an exact two-pass over the chunk
+        float w[N];
+        const PT* wp = static_cast<const PT*>(a.p0) + j0;
+        constexpr int kV = Elem<T>::kVec;
+#pragma unroll
+        for (int k = 0; k < kTwoPassVpt; ++k) {
+            const int64_t e0 = ((int64_t)k * blockDim.x + threadIdx.x) * kV;
+#pragma unroll
+            for (int i = 0; i < kV; ++i)
+                w[k * kV + i] = (e0 + i < n) ? load_param1<PT>(wp, e0 + i) : 0.f;
+        }
+        float sw = 0.f, swx = 0.f;
+#pragma unroll
+        for (int e = 0; e < N; ++e) { sw += w[e]; swx = fmaf(w[e], r.f[e], swx); }
+        sw = block_allreduce(sw, red[0], SumOp{}, 0.f);
+        swx = block_allreduce(swx, red[1], SumOp{}, 0.f);
+        const float mu = sw > 0.f ? swx / sw : 0.f;
+        float m2 = 0.f;
+#pragma unroll
+        for (int e = 0; e < N; ++e) { const float d = r.f[e] - mu; m2 = fmaf(w[e] * d, d, m2); }
+        __syncthreads();  // red[0] is reused below
+        m2 = block_allreduce(m2, red[0], SumOp{}, 0.f);
+        p0 = sw; p1 = mu; p2 = m2;
+    } else if constexpr (OP == kSoftmax) {
         float m = -INFINITY;
 #pragma unroll
         for (int e = 0; e < N; ++e) if (r.ok[e]) m = fmaxf(m, r.f[e]);
@@ -113,7 +142,25 @@ two_pass_apply(const TwoPassArgs a) {
 
     // fold the row's partials in chunk order (identical in every block)
     float c0, c1 = 0.f;
-    if constexpr (OP == kSoftmax) {
+    if constexpr (OP == kQuant) {
+        float m = 0.f;
+        for (int q = 0; q < a.nch; ++q) m = fmaxf(m, w[q].x);
+        c0 = m / 127.f;  // the row scale (IEEE division)
+        if (c == 0 && threadIdx.x == 0) a.aux[row] = c0;
+    } else if constexpr (OP == kWStd) {
+        float W = 0.f, wm = 0.f;
+        for (int q = 0; q < a.nch; ++q) { const float4 v = w[q]; W += v.x; wm = fmaf(v.x, v.y, wm); }
+        const float mean = W > 0.f ? wm / W : 0.f;
+        float m2 = 0.f;
+        for (int q = 0; q < a.nch; ++q) {
+            const float4 v = w[q];
+            const float d = v.y - mean;
+            m2 += fmaf(v.x * d, d, v.z);
+        }
+        const float rr = 1.f / sqrtf(fmaxf(W > 0.f ? m2 / W : 0.f, 0.f) + a.eps);
+        c0 = rr;
+        c1 = -mean * rr;
+    } else if constexpr (OP == kSoftmax) {
         float m = -INFINITY;
         for (int q = 0; q < a.nch; ++q) m = fmaxf(m, w[q].x);
         float s = 0.f;
@@ -136,6 +183,23 @@ two_pass_apply(const TwoPassArgs a) {
     T* ys = static_cast<T*>(a.y) + row * a.cols + j0;
     ChunkRegs<T, VEC_PATH> r;
     r.load(xs, n, threadIdx.x, blockDim.x);
+    if constexpr (OP == kQuant) {
+        int8_t* qs = static_cast<int8_t*>(a.y) + row * a.cols + j0;
+        constexpr int kV = Elem<T>::kVec;
+#pragma unroll
+        for (int k = 0; k < kTwoPassVpt; ++k) {
+            const int64_t e0 = ((int64_t)k * blockDim.x + threadIdx.x) * kV;
+#pragma unroll
+            for (int i = 0; i < kV; ++i) {
+                if (e0 + i < n) {
+                    int qv = 0;
+                    if (c0 != 0.f) qv = max(-127, min(127, __float2int_rn(__fdiv_rn(r.f[k * kV + i], c0))));
+                    qs[e0 + i] = (int8_t)qv;
+                }
+            }
+        }
+        return;
+    }
     const PT* g = static_cast<const PT*>(a.p0);
     const PT* b = static_cast<const PT*>(a.p1);
 #pragma unroll
@@ -146,7 +210,7 @@ two_pass_apply(const TwoPassArgs a) {
         float gv[VEC], bv[VEC];
 #pragma unroll
         for (int i = 0; i < VEC; ++i) { gv[i] = 1.f; bv[i] = 0.f; }
-        if constexpr (OP != kSoftmax) {
+        if constexpr (OP == kLayerNorm || OP == kRMSNorm) {
             if constexpr (VEC_PATH) {
                 if (g) load_params<PT, VEC>(g, j0 + e0, gv);
                 if (b) load_params<PT, VEC>(b, j0 + e0, bv);
@@ -162,7 +226,9 @@ two_pass_apply(const TwoPassArgs a) {
         }
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
-            if constexpr (OP == kSoftmax) {
+            if constexpr (OP == kWStd) {
+                f[i] = fmaf(f[i], c0, c1);
+            } else if constexpr (OP == kSoftmax) {
                 if constexpr (sizeof(T) == 4) f[i] = expf(f[i] - c0) * c1;
                 else f[i] = fast_ex2(fmaf(f[i], kLog2e, -c0)) * c1;
             } else if constexpr (OP == kLayerNorm) {
@@ -181,16 +247,24 @@ two_pass_apply(const TwoPassArgs a) {
 }
 
 // ----------------------------------------------------------- dispatch
-template <int OP, typename T>
+template <int OP, typename T, typename PT>
 static const void* stats_pick(bool vec) {
-    return vec ? (const void*)two_pass_stats<OP, T, true> : (const void*)two_pass_stats<OP, T, false>;
+    return vec ? (const void*)two_pass_stats<OP, T, PT, true>
+               : (const void*)two_pass_stats<OP, T, PT, false>;
+}
+
+template <int OP, typename T>
+static const void* stats_param(int pdtype, bool vec) {
+    return pdtype == 0 ? stats_pick<OP, T, float>(vec) : stats_pick<OP, T, bf16>(vec);
 }
 
 const void* two_pass_stats_kernel(KernelKey k) {
     switch (k.op) {
-        case kSoftmax: return k.dtype == 0 ? stats_pick<kSoftmax, float>(k.vec) : stats_pick<kSoftmax, bf16>(k.vec);
-        case kLayerNorm: return k.dtype == 0 ? stats_pick<kLayerNorm, float>(k.vec) : stats_pick<kLayerNorm, bf16>(k.vec);
-        case kRMSNorm: return k.dtype == 0 ? stats_pick<kRMSNorm, float>(k.vec) : stats_pick<kRMSNorm, bf16>(k.vec);
+        case kSoftmax: return k.dtype == 0 ? stats_pick<kSoftmax, float, float>(k.vec) : stats_pick<kSoftmax, bf16, float>(k.vec);
+        case kLayerNorm: return k.dtype == 0 ? stats_pick<kLayerNorm, float, float>(k.vec) : stats_pick<kLayerNorm, bf16, float>(k.vec);
+        case kRMSNorm: return k.dtype == 0 ? stats_pick<kRMSNorm, float, float>(k.vec) : stats_pick<kRMSNorm, bf16, float>(k.vec);
+        case kQuant: return k.dtype == 0 ? stats_pick<kQuant, float, float>(k.vec) : stats_pick<kQuant, bf16, float>(k.vec);
+        case kWStd: return k.dtype == 0 ? stats_param<kWStd, float>(k.pdtype, k.vec) : stats_param<kWStd, bf16>(k.pdtype, k.vec);
     }
     return nullptr;
 }
@@ -212,6 +286,9 @@ const void* two_pass_apply_kernel(KernelKey k) {
                                            : apply_pick<kSoftmax, bf16, float>(k.vec);
         case kLayerNorm: return apply_dtype<kLayerNorm>(k.dtype, k.pdtype, k.vec);
         case kRMSNorm: return apply_dtype<kRMSNorm>(k.dtype, k.pdtype, k.vec);
+        case kQuant: return k.dtype == 0 ? apply_pick<kQuant, float, float>(k.vec)
+                                         : apply_pick<kQuant, bf16, float>(k.vec);
+        case kWStd: return apply_dtype<kWStd>(k.dtype, k.pdtype, k.vec);
     }
     return nullptr;
 }

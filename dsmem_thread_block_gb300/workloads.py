@@ -19,6 +19,7 @@ import dataclasses
 import numpy as np
 
 SOFTMAX, LAYERNORM, RMSNORM = "softmax", "layernorm", "rmsnorm"
+QUANTIZE, WEIGHTED_STD = "quantize", "weighted_std"
 
 
 def to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -53,6 +54,7 @@ class Workload:
     p_std: float = 0.1
     b_mean: float = 0.0         # beta ~ N(b_mean, b_std)
     b_std: float = 0.1
+    p_uniform: bool = False     # parameters ~ U(0, 1) instead (weights of weighted_std)
 
     @property
     def elem_bytes(self) -> int:
@@ -62,7 +64,10 @@ class Workload:
         return dataclasses.replace(self, rows=rows, name=f"{self.name}[rows={rows}]")
 
     def ideal_bytes(self) -> int:
-        """One read plus one write of the matrix, parameter vectors once."""
+        """One read plus one write of the matrix, parameter vectors once
+        (quantization writes one byte per element plus a scale per row)."""
+        if self.op == QUANTIZE:
+            return self.rows * self.cols * (self.elem_bytes + 1) + 4 * self.rows
         b = 2 * self.rows * self.cols * self.elem_bytes
         if self.param_dtype is not None:
             pb = 4 if self.param_dtype == "f32" else 2
@@ -84,8 +89,11 @@ class Workload:
             x[mask] = np.float32(self.spike_value)
         out = {}
         if self.param_dtype is not None:
-            g = rng.standard_normal(self.cols, dtype=np.float32) * \
-                np.float32(self.p_std) + np.float32(self.p_mean)
+            if self.p_uniform:
+                g = rng.random(self.cols, dtype=np.float32)
+            else:
+                g = rng.standard_normal(self.cols, dtype=np.float32) * \
+                    np.float32(self.p_std) + np.float32(self.p_mean)
             if self.op == LAYERNORM:
                 b = rng.standard_normal(self.cols, dtype=np.float32) * \
                     np.float32(self.b_std) + np.float32(self.b_mean)
@@ -122,5 +130,13 @@ def sweep_point(cols: int) -> Workload:
                     SWEEP_ELEMENTS // cols, cols, seed=4)
 
 
+# the pages' FP32 widths (4K-64K, 4,096 rows) at the widest point
+QUANTIZE_F32_4096x65536 = Workload(
+    "quantize_f32_4096x65536", QUANTIZE, "f32", 4096, 65536, seed=5)
+WEIGHTED_STD_F32_4096x65536 = Workload(
+    "weighted_std_f32_4096x65536", WEIGHTED_STD, "f32", 4096, 65536, seed=6, x_mean=0.5,
+    x_std=2.0, eps=1e-5, param_dtype="f32", p_uniform=True)
+
 ALL = [SOFTMAX_F32_64x4096, LAYERNORM_BF16_1024x262144,
-       SOFTMAX_F32_512x131072_SPIKES, RMSNORM_BF16_2048x786432]
+       SOFTMAX_F32_512x131072_SPIKES, RMSNORM_BF16_2048x786432,
+       QUANTIZE_F32_4096x65536, WEIGHTED_STD_F32_4096x65536]

@@ -54,7 +54,9 @@ typedef enum { CREDIT_F32 = 0, CREDIT_BF16 = 1 } credit_dtype_t;
 typedef enum {
     CREDIT_SOFTMAX = 0,
     CREDIT_LAYERNORM = 1,
-    CREDIT_RMSNORM = 2
+    CREDIT_RMSNORM = 2,
+    CREDIT_QUANTIZE = 3,      /* row absmax -> scale -> int8 codes */
+    CREDIT_WEIGHTED_STD = 4   /* weighted standardization, per-column weights */
 } credit_op_t;
 
 typedef enum {
@@ -352,6 +354,46 @@ credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows,
                                      int param_dtype, int device, int runs,
                                      int tune, credit_plan_t *out,
                                      credit_model_report_t *report);
+
+/*
+ * Row-wise symmetric int8 quantization (CREDIT "B. Workload-by-Workload
+ * Scaling" and "D. Traffic Validation": the quantization workload, a 4-byte
+ * read and a 1-byte write per element for fp32 input).  Per row:
+ *   amax = max |x_j|,  scale = amax / 127 (fp32),
+ *   q_j = clamp(round_half_even(x_j / scale), -127, 127)  (IEEE fp32 division)
+ * and q = 0, scale = 0 for an all-zero row.  The partial a CTA pushes is its
+ * absmax.
+ *   x       device, rows x cols of `dtype` (fp32 or bf16)
+ *   q       device, rows x cols int8 codes; must not overlap x or scales
+ *   scales  device, rows fp32 scales (4-byte aligned)
+ * The bulk path also needs cols to be a multiple of 16.  Persistent plans are
+ * not offered for this operator.  Other arguments as credit_softmax.
+ */
+credit_status_t credit_quantize(const void *x, int8_t *q, float *scales,
+                                int64_t rows, int64_t cols,
+                                credit_dtype_t dtype,
+                                const credit_plan_t *plan, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
+ * Row-wise weighted standardization (the weighted-variance workload of
+ * CREDIT "B. Workload-by-Workload Scaling", read as the weighted counterpart
+ * of LayerNorm): with per-column weights w_j >= 0,
+ *   W = sum w_j,  mean = sum w_j x_j / W,  var = sum w_j (x_j - mean)^2 / W,
+ *   y_j = (x_j - mean) / sqrt(var + eps).
+ * The partial a CTA pushes is (W_q, mean_q, M2_q), merged like LayerNorm's with
+ * weight sums in place of counts.  Rows whose weights sum to 0 produce
+ * unspecified values.
+ *   weights       device vector of cols weights of weight_dtype (not NULL)
+ * Persistent plans are not offered for this operator.  Other arguments as
+ * credit_layernorm.
+ */
+credit_status_t credit_weighted_std(const void *x, void *y, int64_t rows,
+                                    int64_t cols, credit_dtype_t dtype,
+                                    const void *weights,
+                                    credit_dtype_t weight_dtype, float eps,
+                                    const credit_plan_t *plan, void *workspace,
+                                    size_t workspace_bytes, void *stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *credit_status_string(credit_status_t status);

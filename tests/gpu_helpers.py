@@ -25,7 +25,8 @@ from dsmem_thread_block_gb300 import workloads as wl
 
 RTOL = {"f32": 1e-5, "bf16": 2.0 ** -7}
 LN_CANCEL = 1e-5
-OPS = {wl.SOFTMAX: C.SOFTMAX, wl.LAYERNORM: C.LAYERNORM, wl.RMSNORM: C.RMSNORM}
+OPS = {wl.SOFTMAX: C.SOFTMAX, wl.LAYERNORM: C.LAYERNORM, wl.RMSNORM: C.RMSNORM,
+       wl.QUANTIZE: C.QUANTIZE, wl.WEIGHTED_STD: C.WEIGHTED_STD}
 DT = {"f32": C.F32, "bf16": C.BF16}
 
 
@@ -74,17 +75,33 @@ def call(w: wl.Workload, dx: torch.Tensor, dy: torch.Tensor, params: dict, plan,
                                   g.data_ptr() if g is not None else 0,
                                   b.data_ptr() if b is not None else 0, pdt, w.eps, plan,
                                   wptr, wbytes, s)
+    if w.op == wl.QUANTIZE:
+        return C.credit_quantize(dx.data_ptr(), dy.data_ptr(), params["scales"].data_ptr(), rows,
+                                 w.cols, DT[w.dtype], plan, wptr, wbytes, s)
     wt = params.get("weight")
+    if w.op == wl.WEIGHTED_STD:
+        return C.credit_weighted_std(dx.data_ptr(), dy.data_ptr(), rows, w.cols, DT[w.dtype],
+                                     wt.data_ptr(), pdt, w.eps, plan, wptr, wbytes, s)
     return C.credit_rmsnorm(dx.data_ptr(), dy.data_ptr(), rows, w.cols, DT[w.dtype],
                             wt.data_ptr() if wt is not None else 0, pdt, w.eps, plan, wptr,
                             wbytes, s)
 
 
-def run(w: wl.Workload, inputs: dict, plan, in_place=False) -> np.ndarray:
-    """Run the library on host inputs; return the output bytes (numpy)."""
+def run(w: wl.Workload, inputs: dict, plan, in_place=False):
+    """Run the library on host inputs; return the output bytes (numpy) -- for
+    quantization the pair (int8 codes, fp32 scales)."""
     dx = to_device(inputs["x"])
-    dy = dx if in_place else torch.empty_like(dx)
     params = {k: to_device(v) for k, v in inputs.items() if k != "x"}
+    if w.op == wl.QUANTIZE:
+        rows = inputs["x"].shape[0]
+        dq = torch.full(dx.shape, 77, dtype=torch.int8, device=dx.device)
+        params["scales"] = torch.full((rows,), -1.0, dtype=torch.float32, device=dx.device)
+        st = call(w, dx, dq, params, plan, rows=rows)
+        assert st == C.OK, C.status_string(st)
+        torch.cuda.synchronize()
+        assert C.credit_get_device_error(torch.cuda.current_device()) == C.OK
+        return dq.cpu().numpy(), params["scales"].cpu().numpy()
+    dy = dx if in_place else torch.empty_like(dx)
     st = call(w, dx, dy, params, plan, rows=inputs["x"].shape[0])
     assert st == C.OK, C.status_string(st)
     torch.cuda.synchronize()
@@ -101,6 +118,9 @@ def oracle_rows(w: wl.Workload, inputs: dict, rows=None, want_z=False):
         y, z = oracle.layernorm(x, inputs.get("gamma"), inputs.get("beta"), eps=w.eps,
                                 want_z=True)
         return y, z
+    if w.op == wl.WEIGHTED_STD:
+        y = oracle.weighted_std(x, inputs["weight"], eps=w.eps)
+        return y, y
     return oracle.rmsnorm(x, inputs.get("weight"), eps=w.eps), None
 
 
@@ -112,12 +132,14 @@ def check(w: wl.Workload, got: np.ndarray, inputs: dict, rows=None, scale=1.0) -
     err = np.abs(g - want)
     bound = rtol * np.abs(want)
     only_cancel = 0
-    if w.op == wl.LAYERNORM:
+    if w.op in (wl.LAYERNORM, wl.WEIGHTED_STD):
         gam = oracle.widen(inputs["gamma"]) if "gamma" in inputs else 1.0
         bet = oracle.widen(inputs["beta"]) if "beta" in inputs else 0.0
         xw = oracle.widen(inputs["x"] if rows is None else inputs["x"][rows])
-        mu_over_sigma = np.abs(xw.mean(axis=1, keepdims=True)) / np.sqrt(
-            xw.var(axis=1, keepdims=True) + w.eps)
+        wts = oracle.widen(inputs["weight"]) if w.op == wl.WEIGHTED_STD else np.ones(xw.shape[1])
+        mean = (xw * wts).sum(axis=1, keepdims=True) / wts.sum()
+        var = (wts * (xw - mean) ** 2).sum(axis=1, keepdims=True) / wts.sum()
+        mu_over_sigma = np.abs(mean) / np.sqrt(var + w.eps)
         extra = LN_CANCEL * scale * (np.abs(gam) * (np.abs(z) + mu_over_sigma) + np.abs(bet))
         only_cancel = int(((err > bound) & (err <= bound + extra)).sum())
         bound = bound + extra
@@ -129,3 +151,15 @@ def check(w: wl.Workload, got: np.ndarray, inputs: dict, rows=None, scale=1.0) -
             f"{i}: got {g[i]!r} want {want[i]!r} err {err[i]:.3e} bound {bound[i]:.3e}")
     rel = err / np.maximum(np.abs(want), 1e-300)
     return {"max_rel": float(rel.max()), "only_cancel": only_cancel, "n": int(err.size)}
+
+
+def check_quant(got, inputs: dict, rows=None):
+    """Quantization parity is bit-exact: codes and scales."""
+    q, s = got
+    x = inputs["x"] if rows is None else inputs["x"][rows]
+    qo, so = oracle.quantize(x)
+    if rows is not None:
+        q, s = q[rows], s[rows]
+    assert np.array_equal(s.view(np.uint32), so.view(np.uint32)), "scales differ"
+    bad = np.argwhere(q != qo)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[0]}: {q[tuple(bad[0])]} vs {qo[tuple(bad[0])]}"
