@@ -221,6 +221,8 @@ def main():
     ap.add_argument("--variant", default="auto",
                     help="auto (cost model + tuning) | static | cluster:P | persist:P | two_pass")
     ap.add_argument("--cps", type=int, default=0, help="persistent CTAs per SM (0 = planner)")
+    ap.add_argument("--exchange", default="plan", choices=["plan", "barrier", "async"],
+                    help="partial exchange of a one-pass clustered plan (plan = as planned)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the cpu_baseline sample")
@@ -263,13 +265,20 @@ def main():
     dscales = torch.empty(w.rows, dtype=torch.float32, device=dx.device) if quant else None
     params = {k: to_device(v) for k, v in inputs.items() if k != "x"}
 
+    tuning = None
     if args.variant == "auto":
         # the cost model screens the legal cluster sizes and a short tuning
         # step times the best predicted ones; planning and tuning happen
         # once, before (and outside) the timed region
         pdt_model = DT[w.param_dtype] if w.param_dtype else -1
-        plan, _ = C.credit_plan_profiled(OPS[w.op], w.rows, w.cols, DT[w.dtype], pdt_model, dev,
-                                         5, 4)
+        plan, report = C.credit_plan_profiled(OPS[w.op], w.rows, w.cols, DT[w.dtype], pdt_model,
+                                              dev, 15, 5)
+        tuning = {"model_P": report.model_cluster_size, "baseline_us": round(report.t_base_us, 2)}
+        for c in report.cand:
+            if c.legal and c.measured_us > 0 and c.cluster_size > 1:
+                tuning[f"cluster:{c.cluster_size}"] = round(c.measured_us, 2)
+            if c.legal and c.persistent_us > 0:
+                tuning[f"persist:{c.cluster_size}"] = round(c.persistent_us, 2)
     elif args.variant == "static":
         plan = C.credit_plan(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev)
     elif args.variant == "two_pass":
@@ -281,6 +290,8 @@ def main():
     if args.cps:
         plan.ctas_per_sm = args.cps
         plan = C.Plan.from_buffer_copy(plan)
+    if args.exchange != "plan" and plan.variant == C.CLUSTER:
+        plan.exchange = C.EXCHANGE_ASYNC if args.exchange == "async" else C.EXCHANGE_BARRIER
     ws = None
     if plan.workspace_bytes:
         ws = torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=dx.device)
@@ -390,6 +401,8 @@ def main():
     peak, peak_kind = measured_peak()
     variant_key = {C.TWO_PASS: "two_pass", C.CLUSTER: f"cluster:{plan.cluster_size}",
                    C.CLUSTER_PERSISTENT: f"persist:{plan.cluster_size}"}[plan.variant]
+    if plan.variant == C.CLUSTER and plan.exchange == C.EXCHANGE_BARRIER:
+        variant_key += ":barrier"
     launches_per_step = 2 if plan.variant == C.TWO_PASS else 1
     traffic = stored_traffic(w.name, variant_key)
     # the dominant kernel is the only kernel of a clustered step
@@ -417,6 +430,7 @@ def main():
                        "param_dtype": w.param_dtype, "variant": variant_key,
                        "threads": plan.threads, "smem_bytes": int(plan.smem_bytes),
                        "ctas_per_sm": plan.ctas_per_sm, "clusters": plan.active_clusters,
+                       "tuning_us": tuning,
                        "parallelism": f"replicas x{world}",
                        "l2": "input larger than L2 (no flush)",
                        "pct_of_nominal_8TBps": 100 * achieved / 8000.0},

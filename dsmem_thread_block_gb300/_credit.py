@@ -19,6 +19,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_LEGAL_PLAN, ERR_CUDA, \
 F32, BF16 = 0, 1
 SOFTMAX, LAYERNORM, RMSNORM, QUANTIZE, WEIGHTED_STD = 0, 1, 2, 3, 4
 AUTO, CLUSTER, TWO_PASS, CLUSTER_PERSISTENT = 0, 1, 2, 3
+EXCHANGE_DEFAULT, EXCHANGE_BARRIER, EXCHANGE_ASYNC = 0, 1, 2
 
 _vp, _i64, _i32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                               ctypes.c_float, ctypes.c_size_t)
@@ -32,11 +33,11 @@ class Plan(ctypes.Structure):
                 ("slice_elems", ctypes.c_int64), ("active_clusters", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("chunk_elems", ctypes.c_int32),
                 ("ring_slots", ctypes.c_int32), ("rows_per_cluster", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("pred_us", ctypes.c_float),
+                ("exchange", ctypes.c_int32), ("pred_us", ctypes.c_float),
                 ("pred_two_pass_us", ctypes.c_float)]
 
     def as_dict(self) -> dict:
-        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
     def __repr__(self):
         return f"Plan({self.as_dict()})"
@@ -84,7 +85,7 @@ class ModelReport(ctypes.Structure):
 
 BENCH_BARRIER, BENCH_EXCHANGE, BENCH_REMOTE_LOAD_LATENCY, BENCH_LOCAL_LOAD_LATENCY, \
     BENCH_REMOTE_STORE_BW, BENCH_REMOTE_LOAD_BW, BENCH_LOCAL_STORE_BW, \
-    BENCH_LOCAL_LOAD_BW = range(8)
+    BENCH_LOCAL_LOAD_BW, BENCH_ASYNC_EXCHANGE = range(9)
 
 
 class CreditError(RuntimeError):
@@ -118,6 +119,7 @@ SIGNATURES = {
                                     ctypes.POINTER(Plan), ctypes.POINTER(ModelReport)]),
     "credit_status_string": (ctypes.c_char_p, [_i32]),
     "credit_get_device_error": (_i32, [_i32]),
+    "credit_selftest_wait_timeout": (_i32, [_i32, _i64]),
     "credit_version": (ctypes.c_char_p, []),
 }
 
@@ -181,10 +183,11 @@ def credit_plan_for(op: int, rows: int, cols: int, dtype: int, device: int,
 
 def credit_plan_with(op: int, rows: int, cols: int, dtype: int, device: int, variant: int,
                      cluster_size: int = 1, threads: int = 0, ctas_per_sm: int = 0,
-                     chunk_elems: int = 0, rows_per_cluster: int = 0) -> Plan:
+                     chunk_elems: int = 0, rows_per_cluster: int = 0,
+                     exchange: int = EXCHANGE_DEFAULT) -> Plan:
     req = Plan(variant=variant, cluster_size=cluster_size, threads=threads,
                ctas_per_sm=ctas_per_sm, chunk_elems=chunk_elems,
-               rows_per_cluster=rows_per_cluster)
+               rows_per_cluster=rows_per_cluster, exchange=exchange)
     p = Plan()
     _check(load().credit_plan_with(op, rows, cols, dtype, device, ctypes.byref(req),
                                    ctypes.byref(p)), "credit_plan_with")
@@ -269,6 +272,10 @@ def credit_plan_profiled(op: int, rows: int, cols: int, dtype: int, param_dtype:
 
 def credit_get_device_error(device: int) -> int:
     return load().credit_get_device_error(device)
+
+
+def credit_selftest_wait_timeout(device: int = 0, limit_ns: int = 2_000_000) -> int:
+    return load().credit_selftest_wait_timeout(device, limit_ns)
 
 
 def credit_version() -> str:

@@ -17,6 +17,18 @@ namespace credit {
 
 __device__ unsigned g_device_error;
 
+// Self-test of the bounded-wait path: one thread waits on an mbarrier that
+// nothing ever completes, gives up after `limit_ns` and records the timeout
+// in the device error word, exactly as the kernels' waits do.  No copy is in
+// flight, so the CTA exits cleanly.
+__global__ void selftest_wait_kernel(unsigned* err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    mbar_wait_limited(b, 0, err, limit_ns);
+}
+
 namespace {
 
 std::mutex g_mu;
@@ -164,10 +176,17 @@ credit_status_t plan_from_request(int dev, credit_op_t op, int64_t rows, int64_t
         return CREDIT_ERR_INVALID_ARG;
     if (r.threads < 0 || r.ctas_per_sm < 0 || r.chunk_elems < 0 || r.rows_per_cluster < 0)
         return CREDIT_ERR_INVALID_ARG;
+    const bool xok = r.exchange == CREDIT_EXCHANGE_DEFAULT ||
+                     (r.exchange == CREDIT_EXCHANGE_BARRIER && v != CREDIT_TWO_PASS) ||
+                     (r.exchange == CREDIT_EXCHANGE_ASYNC && v == CREDIT_CLUSTER);
+    if (!xok) return CREDIT_ERR_INVALID_ARG;
     const bool pers = v == CREDIT_CLUSTER_PERSISTENT;
-    return make_plan(dev, op, rows, cols, dtype, v, r.cluster_size, r.threads,
-                     pers ? r.ctas_per_sm : 0, out, pers ? r.chunk_elems : 0,
-                     v == CREDIT_CLUSTER ? r.rows_per_cluster : 0);
+    const credit_status_t st =
+        make_plan(dev, op, rows, cols, dtype, v, r.cluster_size, r.threads,
+                  pers ? r.ctas_per_sm : 0, out, pers ? r.chunk_elems : 0,
+                  v == CREDIT_CLUSTER ? r.rows_per_cluster : 0);
+    if (st == CREDIT_OK && r.exchange != CREDIT_EXCHANGE_DEFAULT) out->exchange = r.exchange;
+    return st;
 }
 
 credit_status_t run(const OpCall& c) {
@@ -221,9 +240,11 @@ credit_status_t run(const OpCall& c) {
         (plan.variant == CREDIT_CLUSTER_PERSISTENT || plan.rows_per_cluster != 1)) {
         // bulk copies need 16-byte alignment: misaligned or ragged rows take
         // the one-row-per-cluster kernel's element path instead
+        const int32_t xchg = plan.exchange;
         st = make_plan(dev, c.op, c.rows, c.cols, c.dtype, CREDIT_CLUSTER, plan.cluster_size, 0, 0,
                        &plan, 0, 1);
         if (st != CREDIT_OK) return st;
+        plan.exchange = xchg;
     }
     key.rows = plan.variant == CREDIT_CLUSTER ? plan.rows_per_cluster : 1;
     if (plan.variant == CREDIT_CLUSTER_PERSISTENT) {
@@ -254,6 +275,7 @@ credit_status_t run(const OpCall& c) {
         a.eps = c.eps;
         a.err = err;
         a.aux = c.aux;
+        a.exchange = plan.exchange == CREDIT_EXCHANGE_ASYNC ? 1 : 0;
         const void* fn = cluster_kernel(key);
         if (!kernel_info(dev, fn, true)) return CREDIT_ERR_CUDA;
         return from_cuda(launch_cluster(key, a, plan.cluster_size, plan.threads,
@@ -367,6 +389,17 @@ credit_status_t credit_get_device_error(int device) {
         return CREDIT_ERR_CUDA;
     }
     return (v & kErrTimeout) ? CREDIT_ERR_DEVICE_TIMEOUT : CREDIT_OK;
+}
+
+credit_status_t credit_selftest_wait_timeout(int device, int64_t limit_ns) {
+    if (limit_ns < 1000 || limit_ns > 1000000000) return CREDIT_ERR_INVALID_ARG;
+    DeviceGuard g(device);
+    if (!g.ok) return CREDIT_ERR_INVALID_ARG;
+    unsigned* err = device_error_word();
+    if (!err) return CREDIT_ERR_CUDA;
+    selftest_wait_kernel<<<1, 1>>>(err, (unsigned long long)limit_ns);
+    if (cudaGetLastError() != cudaSuccess) return CREDIT_ERR_CUDA;
+    return credit_get_device_error(device);
 }
 
 const char* credit_version(void) { return "0.1.0"; }

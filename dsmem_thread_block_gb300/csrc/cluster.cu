@@ -11,6 +11,11 @@
 //       mapa + st.shared::cluster ("Replicated Push");
 //   a5  cluster barrier (arrive.release / wait.acquire) makes the pushes
 //       visible ("Synchronization");
+//       -- or, with the st.async exchange, each push is an st.async whose
+//       bytes complete on the receiving CTA's mbarrier, and every CTA waits
+//       for its own P - 1 deposits alone; the cluster barrier moves to the
+//       kernel's end, where it only keeps CTAs alive until every deposit
+//       has landed;
 //   a6  fold the P local slots in rank order: every CTA rebuilds the same
 //       statistics with local reads only ("All-Gather Trade-off");
 //   a7  apply h to the staged slice and write the output slice
@@ -36,9 +41,11 @@ cluster_reduce_reuse(const ClusterArgs a) {
     __shared__ __align__(16) float slots[kMaxCluster * R * kSlotStride];
     __shared__ __align__(16) float red[2][kMaxWarps * 2 * R];
     __shared__ __align__(8) uint64_t mbar[kMaxChunks];
+    __shared__ __align__(8) uint64_t recv_bar;  // st.async exchange: deposits land here
 
     const uint32_t P = cluster_nctarank();
     const uint32_t rank = cluster_ctarank();
+    const bool async_x = a.exchange == 1 && P > 1;
     const int64_t row0 = (blockIdx.x / P) * (int64_t)R;
     const int rows = (int)min((int64_t)R, a.rows - row0);  // live rows of this cluster
     const int64_t start = (int64_t)rank * a.slice;
@@ -48,6 +55,16 @@ cluster_reduce_reuse(const ClusterArgs a) {
     const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
     const int nvec = n / VEC;  // whole 16-byte vectors (all of n on the bulk path)
 
+    if (async_x && threadIdx.x == 0) {
+        // the exchange's mbarrier: two arrivals (this one, which registers the
+        // P - 1 peers' R deposits of 16 bytes each before any peer can pass
+        // the entry barrier below, and the thread that stores this CTA's own
+        // partials locally) plus those bytes
+        const uint32_t rb = smem_u32(&recv_bar);
+        mbar_init(rb, 2);
+        mbar_arrive_expect_tx(rb, (P - 1) * R * 16u);
+        fence_mbar_init();
+    }
     if (P > 1) cluster_arrive_relaxed();
 
     // ---------------------------------------------------------- a2 stage
@@ -126,17 +143,40 @@ cluster_reduce_reuse(const ClusterArgs a) {
 #pragma unroll
     for (int i = 0; i < R; ++i) { stv[i][0] = p[i][0]; stv[i][1] = p[i][1]; stv[i][2] = p[i][2]; }
     if (P > 1) {
-        cluster_wait_acquire();  // every peer has started: its slots exist
-        if (tid < (int)P) {
+        cluster_wait_acquire();  // every peer has started: its slots (and mbarrier) exist
+        if (async_x) {
+            // thread t deposits into peer t (each deposit counts 16 bytes on
+            // that peer's mbarrier); thread `rank` stores locally and arrives
+            if (tid == (int)rank) {
 #pragma unroll
-            for (int i = 0; i < R; ++i) {
-                const uint32_t dst =
-                    mapa_shared(smem_u32(&slots[(rank * R + i) * kSlotStride]), (uint32_t)tid);
-                st_cluster_v4f32(dst, p[i][0], p[i][1], p[i][2], 0.f);
+                for (int i = 0; i < R; ++i) {
+                    float* d = &slots[(rank * R + i) * kSlotStride];
+                    d[0] = p[i][0]; d[1] = p[i][1]; d[2] = p[i][2];
+                }
+                mbar_arrive(smem_u32(&recv_bar));
+            } else if (tid < (int)P) {
+                const uint32_t rbar = mapa_shared(smem_u32(&recv_bar), (uint32_t)tid);
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    const uint32_t dst =
+                        mapa_shared(smem_u32(&slots[(rank * R + i) * kSlotStride]), (uint32_t)tid);
+                    st_async_v4f32(dst, p[i][0], p[i][1], p[i][2], 0.f, rbar);
+                }
             }
+            mbar_wait_bounded(smem_u32(&recv_bar), 0, a.err);  // all P partials are here
+            cluster_arrive_relaxed();  // nothing more lands in this CTA's shared memory
+        } else {
+            if (tid < (int)P) {
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    const uint32_t dst =
+                        mapa_shared(smem_u32(&slots[(rank * R + i) * kSlotStride]), (uint32_t)tid);
+                    st_cluster_v4f32(dst, p[i][0], p[i][1], p[i][2], 0.f);
+                }
+            }
+            cluster_arrive_release();
+            cluster_wait_acquire();
         }
-        cluster_arrive_release();
-        cluster_wait_acquire();
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             combine_slots_strided<OP>(slots + i * kSlotStride, P, R * kSlotStride, stv[i][0],
@@ -177,6 +217,10 @@ cluster_reduce_reuse(const ClusterArgs a) {
             }
         }
     }
+    // st.async exchange: a peer arrives only once all deposits to it have
+    // landed, so when this completes every deposit in the cluster has, and
+    // no CTA leaves while one is in flight
+    if (async_x) cluster_wait_acquire();
 }
 
 // ----------------------------------------------------------- dispatch

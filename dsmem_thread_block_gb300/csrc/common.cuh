@@ -31,7 +31,7 @@ namespace credit {
 enum Op : int { kSoftmax = 0, kLayerNorm = 1, kRMSNorm = 2, kQuant = 3, kWStd = 4 };
 
 // LayerNorm-like statistics (count or weight, mean, M2).
-constexpr bool norm_like(int op) { return op == kLayerNorm || op == kWStd; }
+__host__ __device__ constexpr bool norm_like(int op) { return op == kLayerNorm || op == kWStd; }
 
 constexpr int kMaxCluster = 16;   // non-portable cluster size limit
 constexpr int kMaxThreads = 512;         // two-pass kernels
@@ -181,18 +181,23 @@ __device__ __forceinline__ float block_allreduce(float v, float* buf, F f, float
 // Bounded mbarrier wait: spins on try_wait; after kWaitLimitNs sets the
 // device error word and returns false (the caller carries on so that every
 // cluster barrier is still reached).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  unsigned* err) {
+__device__ __forceinline__ bool mbar_wait_limited(uint32_t bar, uint32_t parity, unsigned* err,
+                                                  uint64_t limit_ns) {
     for (int i = 0; i < 256; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             atomicOr(err, kErrTimeout);
             return false;
         }
     }
     return true;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned* err) {
+    return mbar_wait_limited(bar, parity, err, kWaitLimitNs);
 }
 
 }  // namespace credit

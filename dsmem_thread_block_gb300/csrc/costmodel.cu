@@ -34,6 +34,7 @@ struct DsmemProfile {
     bool valid = false;
     double barrier_ns[kMaxCluster + 1] = {};
     double exchange_ns[kMaxCluster + 1] = {};
+    double async_exchange_ns[kMaxCluster + 1] = {};
 };
 
 std::mutex g_cm_mu;
@@ -77,13 +78,16 @@ extern "C" credit_status_t credit_calibrate(int device, int runs, const char* pr
     if (device < 0 || device >= kMaxDevices || runs < 1) return CREDIT_ERR_INVALID_ARG;
     DsmemProfile prof;
     for (int P = 2; P <= kMaxCluster; ++P) {
-        credit_bench_result_t b, e;
+        credit_bench_result_t b, e, x;
         credit_status_t st = credit_bench_dsmem(device, CREDIT_BENCH_BARRIER, P, 500, runs, &b);
         if (st != CREDIT_OK) return st;
         st = credit_bench_dsmem(device, CREDIT_BENCH_EXCHANGE, P, 500, runs, &e);
         if (st != CREDIT_OK) return st;
+        st = credit_bench_dsmem(device, CREDIT_BENCH_ASYNC_EXCHANGE, P, 500, runs, &x);
+        if (st != CREDIT_OK) return st;
         prof.barrier_ns[P] = b.median_ns;
         prof.exchange_ns[P] = e.median_ns;
+        prof.async_exchange_ns[P] = x.median_ns;
     }
     prof.valid = true;
     {
@@ -99,6 +103,9 @@ extern "C" credit_status_t credit_calibrate(int device, int runs, const char* pr
         std::fprintf(f, "}, \"exchange_ns\": {");
         for (int P = 2; P <= kMaxCluster; ++P)
             std::fprintf(f, "%s\"%d\": %.2f", P > 2 ? ", " : "", P, prof.exchange_ns[P]);
+        std::fprintf(f, "}, \"async_exchange_ns\": {");
+        for (int P = 2; P <= kMaxCluster; ++P)
+            std::fprintf(f, "%s\"%d\": %.2f", P > 2 ? ", " : "", P, prof.async_exchange_ns[P]);
         std::fprintf(f, "}}\n");
         std::fclose(f);
     }
@@ -269,7 +276,12 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         c.legal = 1;
         c.plan = p;
         c.t_ctrl_us = ctrl - ctrl_base;
-        const double push_ns = std::max(0.0, prof.exchange_ns[P] - prof.barrier_ns[P]);
+        // the control kernel already pays the exchange's barrier; the push
+        // costs what the measured exchange adds to it (with st.async
+        // deposits the exchange replaces that barrier on the critical path)
+        const double xchg_ns = p.exchange == CREDIT_EXCHANGE_ASYNC ? prof.async_exchange_ns[P]
+                                                                   : prof.exchange_ns[P];
+        const double push_ns = std::max(0.0, xchg_ns - prof.barrier_ns[P]);
         c.t_comm_us = (double)p.waves * push_ns * 1e-3;
         c.pred_us = t_base - (b_base - b_credit) / r_base + c.t_ctrl_us + c.t_comm_us;
         c.plan.pred_us = (float)c.pred_us;

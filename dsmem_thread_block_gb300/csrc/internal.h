@@ -21,6 +21,7 @@ struct ClusterArgs {
     float eps;
     unsigned* err;        // device error word
     float* aux;           // quantization: per-row scales out (else unused)
+    int32_t exchange;     // 0: push + cluster barrier; 1: st.async deposits + mbarrier
 };
 
 constexpr int kMaxRowsPerCluster = 4;

@@ -33,7 +33,10 @@ struct BenchOut {
     long long ns;
     unsigned smid[kMaxCluster];
     unsigned sink;
+    unsigned err;         // a bounded wait gave up
 };
+
+constexpr uint64_t kBenchWaitNs = 100000000ull;  // 0.1 s per exchange wait
 
 constexpr int kChaseEntries = 4096;      // u32 ring in shared memory
 constexpr int kBwBytes = 64 * 1024;      // remote buffer for the throughput kinds
@@ -68,6 +71,50 @@ __global__ void bench_barrier(BenchOut* out, int iters, int exchange) {
         out->sink = (unsigned)slots[0];
     }
     cluster_sync_all();
+}
+
+// kind ASYNC_EXCHANGE: iters x (st.async of a 16-byte partial into every
+// peer, counted on the peer's mbarrier, then a wait on the CTA's own
+// mbarrier for its P - 1 deposits) -- the exchange without a cluster barrier.
+// Two mbarriers and two slot arrays alternate by iteration: a peer can be at
+// most one exchange ahead (its next wait needs this CTA's next deposit), so
+// a deposit never lands in the phase or the slots of the exchange before.
+__global__ void bench_async_exchange(BenchOut* out, int iters) {
+    __shared__ __align__(16) float slots[2][kMaxCluster * 4];
+    __shared__ __align__(8) uint64_t bar[2];
+    const uint32_t P = cluster_nctarank(), rank = cluster_ctarank();
+    const uint32_t bytes = (P - 1) * 16u;
+    if (threadIdx.x == 0) {
+        out->smid[rank] = smid();
+        mbar_init(smem_u32(&bar[0]), 1);
+        mbar_init(smem_u32(&bar[1]), 1);
+        fence_mbar_init();
+    }
+    cluster_sync_all();
+    const long long c0 = clock64();
+    const uint64_t t0 = globaltimer_ns();
+    // warp 0 alone exchanges; the warp-wide vote after each wait keeps its
+    // lanes within one phase of each other (no lane can miss a phase of the
+    // mbarrier it waits on) and makes a give-up uniform across the warp
+    for (int i = 0; threadIdx.x < 32 && i < iters; ++i) {
+        const int b = i & 1;
+        const uint32_t lb = smem_u32(&bar[b]);
+        if (threadIdx.x == 0) mbar_arrive_expect_tx(lb, bytes);
+        if (threadIdx.x < P && threadIdx.x != rank) {
+            const uint32_t dst = mapa_shared(smem_u32(&slots[b][rank * 4]), threadIdx.x);
+            st_async_v4f32(dst, (float)i, 1.f, 2.f, 3.f, mapa_shared(lb, threadIdx.x));
+        }
+        const bool ok = mbar_wait_limited(lb, (uint32_t)(i >> 1) & 1u, &out->err, kBenchWaitNs);
+        if (!__all_sync(0xffffffffu, ok)) break;
+    }
+    const long long c1 = clock64();
+    const uint64_t t1 = globaltimer_ns();
+    if (rank == 0 && threadIdx.x == 0) {
+        out->cycles = c1 - c0;
+        out->ns = (long long)(t1 - t0);
+        out->sink = (unsigned)slots[0][4 * (P - 1)];
+    }
+    cluster_sync_all();  // every deposit has landed before any CTA exits
 }
 
 // kind LOAD_LATENCY: rank 0 chases a pointer ring that lives in rank 1's
@@ -196,7 +243,8 @@ extern "C" credit_status_t credit_bench_dsmem(int device, int kind, int cluster_
     const bool pair = kind == CREDIT_BENCH_REMOTE_LOAD_LATENCY || kind == CREDIT_BENCH_LOCAL_LOAD_LATENCY ||
                       kind == CREDIT_BENCH_REMOTE_STORE_BW || kind == CREDIT_BENCH_REMOTE_LOAD_BW ||
                       kind == CREDIT_BENCH_LOCAL_STORE_BW || kind == CREDIT_BENCH_LOCAL_LOAD_BW;
-    if (!pair && kind != CREDIT_BENCH_BARRIER && kind != CREDIT_BENCH_EXCHANGE)
+    if (!pair && kind != CREDIT_BENCH_BARRIER && kind != CREDIT_BENCH_EXCHANGE &&
+        kind != CREDIT_BENCH_ASYNC_EXCHANGE)
         return CREDIT_ERR_INVALID_ARG;
     const int P = pair ? 2 : cluster_size;
     const DevInfo* d = device_info(device);
@@ -221,6 +269,9 @@ extern "C" credit_status_t credit_bench_dsmem(int device, int kind, int cluster_
     if (kind == CREDIT_BENCH_BARRIER || kind == CREDIT_BENCH_EXCHANGE) {
         fn = (const void*)bench_barrier;
         threads = 128;
+    } else if (kind == CREDIT_BENCH_ASYNC_EXCHANGE) {
+        fn = (const void*)bench_async_exchange;
+        threads = 128;
     } else if (kind == CREDIT_BENCH_REMOTE_LOAD_LATENCY || kind == CREDIT_BENCH_LOCAL_LOAD_LATENCY) {
         fn = (const void*)bench_chase;
         threads = 128;
@@ -235,14 +286,20 @@ extern "C" credit_status_t credit_bench_dsmem(int device, int kind, int cluster_
         void* args_barrier[] = {&dout, &iters, &exchange};
         void* args_chase[] = {&dout, &iters, &remote};
         void* args_bw[] = {&dout, &iters, &remote, &store};
+        void* args_async[] = {&dout, &iters};
         void** args = fn == (const void*)bench_barrier ? args_barrier
-                      : fn == (const void*)bench_chase ? args_chase : args_bw;
+                      : fn == (const void*)bench_chase ? args_chase
+                      : fn == (const void*)bench_async_exchange ? args_async : args_bw;
         if (cudaMemset(dout, 0, sizeof(BenchOut)) != cudaSuccess ||
             launch_cluster_kernel(fn, P, P, threads, smem, args, 0) != cudaSuccess ||
             cudaDeviceSynchronize() != cudaSuccess ||
             cudaMemcpy(&h, dout, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
             cudaGetLastError();
             status = CREDIT_ERR_CUDA;
+            break;
+        }
+        if (h.err) {
+            status = CREDIT_ERR_DEVICE_TIMEOUT;
             break;
         }
         if (r == 0) continue;

@@ -73,6 +73,15 @@ __device__ __forceinline__ void st_cluster_v4f32(uint32_t addr, float a, float b
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
                  :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
+// 16-byte asynchronous store into a peer's shared memory whose completion is
+// counted as 16 transaction bytes on the peer's mbarrier `remote_bar` (both
+// addresses mapped into the cluster window with mapa).
+__device__ __forceinline__ void st_async_v4f32(uint32_t remote_addr, float a, float b, float c,
+                                               float d, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+        :: "r"(remote_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar) : "memory");
+}
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr)

@@ -1,7 +1,8 @@
 """DSMEM microbenchmark suite (command line).
 
-Measures, on one GPU, the cluster-barrier round trip and the replicated-push
-exchange for every cluster size 2..16, remote and local shared-memory load
+Measures, on one GPU, the cluster-barrier round trip, the replicated-push
+exchange and the st.async exchange (deposits counted on each receiver's
+mbarrier, no cluster barrier) for every cluster size 2..16, remote and local shared-memory load
 latency (pointer chase), and remote / local 16-byte load and store throughput
 of one CTA, each as the median of 15 launches (CREDIT summary page, "C.
 Positioning": latency, throughput and repeated cluster-synchronisation
@@ -18,10 +19,12 @@ from . import _credit as C
 
 
 def run_suite(device: int = 0, runs: int = 15, sizes=range(2, 17)) -> dict:
-    out = {"device": device, "runs": runs, "barrier": {}, "exchange": {}}
+    out = {"device": device, "runs": runs, "barrier": {}, "exchange": {}, "async_exchange": {}}
     for P in sizes:
         out["barrier"][P] = C.credit_bench_dsmem(device, C.BENCH_BARRIER, P, 2000, runs).as_dict()
         out["exchange"][P] = C.credit_bench_dsmem(device, C.BENCH_EXCHANGE, P, 2000, runs).as_dict()
+        out["async_exchange"][P] = C.credit_bench_dsmem(device, C.BENCH_ASYNC_EXCHANGE, P, 2000,
+                                                        runs).as_dict()
     for name, kind, iters in (("remote_load_latency", C.BENCH_REMOTE_LOAD_LATENCY, 20000),
                               ("local_load_latency", C.BENCH_LOCAL_LOAD_LATENCY, 20000),
                               ("remote_store_bw", C.BENCH_REMOTE_STORE_BW, 64),

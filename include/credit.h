@@ -70,6 +70,25 @@ typedef enum {
 } credit_variant_t;
 
 /*
+ * How the clustered kernels hand their partials to the peers
+ * (credit_plan_t.exchange):
+ *   DEFAULT  in a request: let the planner choose; in a planned TWO_PASS
+ *            plan: there is no exchange
+ *   BARRIER  remote 16-byte stores into every peer's slot array, then a
+ *            release/acquire cluster barrier (CREDIT "C. Cluster Reduction
+ *            and Reuse Protocol", Replicated Push + Synchronization)
+ *   ASYNC    st.async 16-byte deposits whose bytes complete on the receiving
+ *            CTA's mbarrier; each CTA waits for its own P - 1 deposits, and
+ *            the cluster barrier moves to kernel exit (one-pass CLUSTER
+ *            plans only; the planner's choice for them)
+ */
+typedef enum {
+    CREDIT_EXCHANGE_DEFAULT = 0,
+    CREDIT_EXCHANGE_BARRIER = 1,
+    CREDIT_EXCHANGE_ASYNC = 2
+} credit_exchange_t;
+
+/*
  * A launch plan.  Produced by credit_plan / credit_plan_for; may be passed to
  * the operator calls (NULL there means "plan automatically").
  *   variant          CREDIT_CLUSTER, CREDIT_CLUSTER_PERSISTENT or
@@ -89,6 +108,9 @@ typedef enum {
  *   rows_per_cluster rows one cluster stages and reduces together (CLUSTER:
  *                    1, 2 or 4; their partials share one exchange and each
  *                    parameter load serves all of them)
+ *   exchange         credit_exchange_t: ASYNC for planned CLUSTER plans,
+ *                    BARRIER for CLUSTER_PERSISTENT, DEFAULT for TWO_PASS; a
+ *                    request may ask for BARRIER on a CLUSTER plan
  *   pred_us          predicted time of this plan, microseconds (0 = none)
  *   pred_two_pass_us predicted / measured time of the two-pass baseline
  */
@@ -105,7 +127,7 @@ typedef struct {
     int32_t chunk_elems;
     int32_t ring_slots;
     int32_t rows_per_cluster;
-    int32_t reserved;
+    int32_t exchange;
     float pred_us;
     float pred_two_pass_us;
 } credit_plan_t;
@@ -245,7 +267,9 @@ typedef enum {
     CREDIT_BENCH_REMOTE_STORE_BW = 4,     /* one CTA storing 16-byte vectors to a peer */
     CREDIT_BENCH_REMOTE_LOAD_BW = 5,      /* one CTA loading 16-byte vectors from a peer */
     CREDIT_BENCH_LOCAL_STORE_BW = 6,      /* the same stores to its own SMEM */
-    CREDIT_BENCH_LOCAL_LOAD_BW = 7        /* the same loads from its own SMEM */
+    CREDIT_BENCH_LOCAL_LOAD_BW = 7,       /* the same loads from its own SMEM */
+    CREDIT_BENCH_ASYNC_EXCHANGE = 8       /* st.async 16-byte push to every peer +
+                                             wait on the own mbarrier, P CTAs */
 } credit_bench_kind_t;
 
 typedef struct {
@@ -263,8 +287,9 @@ typedef struct {
 /*
  * Run one DSMEM microbenchmark on `device`: `iters` operations per launch,
  * `runs` timed launches after one warm-up, median reported.  cluster_size
- * (1..16) applies to the BARRIER and EXCHANGE kinds; the other kinds always
- * use a pair of CTAs.  Returns CREDIT_ERR_INVALID_ARG for bad arguments.
+ * (1..16) applies to the BARRIER, EXCHANGE and ASYNC_EXCHANGE kinds; the
+ * other kinds always use a pair of CTAs.  Returns CREDIT_ERR_INVALID_ARG for
+ * bad arguments and CREDIT_ERR_DEVICE_TIMEOUT if an exchange wait gave up.
  */
 credit_status_t credit_bench_dsmem(int device, int kind, int cluster_size,
                                    int iters, int runs,
@@ -295,8 +320,9 @@ credit_status_t credit_control_time(int device, int64_t nclusters,
  *     T_CREDIT(P) = T_base - (B_base - B_credit) / R_base + T_ctrl(P) + T_comm(P)
  * with R_base = B_base / T_base the baseline's achieved byte rate, T_ctrl(P)
  * the candidate's control time minus the baseline's, and T_comm(P) the
- * replicated push's cost beyond the barrier (DSMEM profile) times the
- * candidate's waves of resident clusters.  The deposit residual
+ * measured exchange's cost beyond one cluster barrier (DSMEM profile: the
+ * st.async exchange for ASYNC plans, clamped at zero, push + barrier for
+ * BARRIER plans) times the candidate's waves of resident clusters.  The deposit residual
  * [T_wSMEM - T_input]+ is zero: a 16-byte push per peer is far below the
  * per-SM input stream.  The candidate with the smallest prediction is kept
  * if it beats T_base, else the baseline.  As on the pages, the model screens
@@ -404,6 +430,15 @@ const char *credit_status_string(credit_status_t status);
  * else CREDIT_OK.  Synchronises the device.
  */
 credit_status_t credit_get_device_error(int device);
+
+/*
+ * Exercise the bounded-wait path on `device`: a one-thread kernel waits on an
+ * mbarrier that nothing completes, gives up after limit_ns (1 us .. 1 s) and
+ * sets the device error word, which is then read and cleared.  Returns
+ * CREDIT_ERR_DEVICE_TIMEOUT when the path works.  The kernel ends by itself
+ * (no copy in flight, no cluster barrier), so the context stays usable.
+ */
+credit_status_t credit_selftest_wait_timeout(int device, int64_t limit_ns);
 
 /* Library version as "major.minor.patch" (static storage). */
 const char *credit_version(void);

@@ -51,6 +51,7 @@ def test_plan_struct_layout_matches_header():
     # int32 x4, int64 x3, int32 x6, float x2 -> 72 bytes, no padding surprises
     assert ctypes.sizeof(C.Plan) == 72
     assert C.Plan.smem_bytes.offset == 16 and C.Plan.pred_us.offset == 64
+    assert C.Plan.exchange.offset == 60
 
 
 def test_status_strings(lib):
@@ -71,6 +72,14 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     assert C.credit_rmsnorm(4096, 4100, 1, 64, C.F32, 0, C.F32, 1e-6) == C.ERR_INVALID_ARG
     assert lib.credit_plan(C.SOFTMAX, 4, 4, C.F32, 0, None) == C.ERR_INVALID_ARG
     assert lib.credit_plan_for(C.SOFTMAX, 4, 4, C.F32, 0, 9, 1, None) == C.ERR_INVALID_ARG
+    # the st.async exchange exists only for the one-pass clustered kernel
+    out = C.Plan()
+    for variant, exchange in ((C.TWO_PASS, C.EXCHANGE_ASYNC), (C.TWO_PASS, C.EXCHANGE_BARRIER),
+                              (C.CLUSTER_PERSISTENT, C.EXCHANGE_ASYNC), (C.CLUSTER, 3),
+                              (C.CLUSTER, -1)):
+        req = C.Plan(variant=variant, cluster_size=2, exchange=exchange)
+        assert lib.credit_plan_with(C.SOFTMAX, 4, 4, C.F32, 0, ctypes.byref(req),
+                                    ctypes.byref(out)) == C.ERR_INVALID_ARG
 
 
 def test_library_fails_loudly_when_missing(monkeypatch, tmp_path):

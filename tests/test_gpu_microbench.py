@@ -29,6 +29,17 @@ def test_barrier_and_exchange_costs(P):
     assert e.median_cycles >= 0.8 * b.median_cycles  # the push adds to the barrier
 
 
+@pytest.mark.parametrize("P", [2, 4, 8, 16])
+def test_async_exchange_runs_on_distinct_sms(P):
+    # st.async deposits + a wait on the own mbarrier: no cluster barrier per
+    # exchange, so one exchange should cost no more than push + barrier
+    a = C.credit_bench_dsmem(0, C.BENCH_ASYNC_EXCHANGE, P, 500, 5)
+    e = C.credit_bench_dsmem(0, C.BENCH_EXCHANGE, P, 500, 5)
+    assert len(set(a.smids[:P])) == P
+    assert 0 < a.median_cycles < 1e5
+    assert a.median_cycles <= 1.5 * e.median_cycles
+
+
 def test_barrier_cost_grows_with_cluster_size():
     c2 = C.credit_bench_dsmem(0, C.BENCH_BARRIER, 2, 1000, 7).median_cycles
     c16 = C.credit_bench_dsmem(0, C.BENCH_BARRIER, 16, 1000, 7).median_cycles

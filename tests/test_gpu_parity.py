@@ -15,7 +15,7 @@ import torch
 from dsmem_thread_block_gb300 import _credit as C
 from dsmem_thread_block_gb300 import workloads as wl
 
-from gpu_helpers import check, make_plan, oracle_rows, run, to_device, to_host, call
+from gpu_helpers import call, check, check_quant, make_plan, oracle_rows, run, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -284,6 +284,71 @@ def test_rows_per_cluster(R):
             assert p.rows_per_cluster == R
             check(w, run(w, inp, p), inp)
             check(w, run(w, inp, p, in_place=True), inp)
+
+
+@pytest.mark.parametrize("exchange", ["barrier", "async"])
+@pytest.mark.parametrize("R", [1, 2, 4])
+def test_exchange_modes(R, exchange):
+    # st.async deposits counted on each receiver's mbarrier, or remote stores
+    # plus the release/acquire cluster barrier: same statistics, same outputs
+    xc = C.EXCHANGE_ASYNC if exchange == "async" else C.EXCHANGE_BARRIER
+    cases = [
+        _custom(wl.LAYERNORM, "bf16", 9, 131072, 50, x_mean=0.5, x_std=2.0, eps=1e-5,
+                param_dtype="f32"),
+        _custom(wl.RMSNORM, "f32", 5, 65536, 51, eps=1e-6, param_dtype="f32"),
+        _custom(wl.SOFTMAX, "f32", 7, 65536, 52, x_std=4.0, spike_frac=0.01),
+        _custom(wl.SOFTMAX, "bf16", 6, 262144, 53),
+        _custom(wl.WEIGHTED_STD, "f32", 5, 32768, 54, x_mean=0.5, x_std=2.0, eps=1e-5,
+                param_dtype="f32", p_uniform=True),
+    ]
+    dev = torch.cuda.current_device()
+    ran = 0
+    for w in cases:
+        inp = w.generate()
+        for P in (2, 3, 4, 8, 16):
+            try:
+                p = C.credit_plan_with(gh_ops(w), w.rows, w.cols, gh_dt(w), dev, C.CLUSTER, P,
+                                       rows_per_cluster=R, exchange=xc)
+            except C.CreditError as e:
+                assert e.status == C.ERR_NO_LEGAL_PLAN
+                continue
+            assert p.exchange == xc and p.cluster_size == P
+            check(w, run(w, inp, p), inp)
+            ran += 1
+    assert ran >= 10
+    assert C.credit_get_device_error(dev) == C.OK
+
+
+def test_planned_exchange():
+    dev = torch.cuda.current_device()
+    w = _custom(wl.SOFTMAX, "f32", 4, 65536, 57)
+    assert make_plan(w, C.CLUSTER, 4).exchange == C.EXCHANGE_ASYNC
+    assert make_plan(w, C.TWO_PASS, 1).exchange == C.EXCHANGE_DEFAULT
+    p = _try_plan(w, C.CLUSTER_PERSISTENT, 4)
+    if p is not None:
+        assert p.exchange == C.EXCHANGE_BARRIER
+    assert C.credit_plan_with(C.SOFTMAX, 4, 65536, C.F32, dev, C.CLUSTER, 4,
+                              exchange=C.EXCHANGE_BARRIER).exchange == C.EXCHANGE_BARRIER
+
+
+def test_async_exchange_quantize_and_ragged():
+    # int8 codes stay bit-exact; a ragged, misaligned row takes the element
+    # path with the same exchange
+    dev = torch.cuda.current_device()
+    q = _custom(wl.QUANTIZE, "f32", 6, 65536, 55, x_std=3.0)
+    inp = q.generate()
+    for P in (2, 4, 16):
+        p = C.credit_plan_with(gh_ops(q), q.rows, q.cols, gh_dt(q), dev, C.CLUSTER, P,
+                               exchange=C.EXCHANGE_ASYNC)
+        check_quant(run(q, inp, p), inp)
+    w = _custom(wl.LAYERNORM, "bf16", 5, 40001, 56, x_mean=-0.25, x_std=1.5, eps=1e-5,
+                param_dtype="bf16")
+    inp = w.generate()
+    for P in (3, 5):
+        p = C.credit_plan_with(gh_ops(w), w.rows, w.cols, gh_dt(w), dev, C.CLUSTER, P,
+                               exchange=C.EXCHANGE_ASYNC)
+        check(w, run(w, inp, p), inp)
+    assert C.credit_get_device_error(dev) == C.OK
 
 
 def gh_ops(w):
