@@ -267,12 +267,13 @@ def main():
 
     tuning = None
     if args.variant == "auto":
-        # the cost model screens the legal cluster sizes and a short tuning
-        # step times the best predicted ones; planning and tuning happen
-        # once, before (and outside) the timed region
+        # the cost model screens profitability (its prediction is nearly
+        # flat across cluster sizes: it is no ranking tool), and the tuning
+        # step times every legal candidate; planning and tuning happen once,
+        # before (and outside) the timed region
         pdt_model = DT[w.param_dtype] if w.param_dtype else -1
         plan, report = C.credit_plan_profiled(OPS[w.op], w.rows, w.cols, DT[w.dtype], pdt_model,
-                                              dev, 15, 5)
+                                              dev, 15, 16)
         tuning = {"model_P": report.model_cluster_size, "baseline_us": round(report.t_base_us, 2)}
         for c in report.cand:
             if c.legal and c.measured_us > 0 and c.cluster_size > 1:

@@ -31,6 +31,8 @@
 
 namespace credit {
 
+constexpr int kPipeU = 2;  // granules per lane in a pipelined output tile
+
 template <int OP, typename T, typename PT, bool BULK, int R>
 __global__ void __launch_bounds__(kClusterMaxThreads, 3)
 cluster_reduce_reuse(const ClusterArgs a) {
@@ -206,7 +208,18 @@ cluster_reduce_reuse(const ClusterArgs a) {
         T* yrow[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) yrow[i] = static_cast<T*>(a.y) + (row0 + i) * a.cols + start;
-        if constexpr (BULK) {
+        // RMSNorm with bf16 data and bf16 weights gains from the pipelined
+        // pass (measured); the other operator / type combinations do not
+        constexpr bool kPipe = BULK && R == 1 && OP == kRMSNorm && Granule<OP, T, PT>::kPairs == 4;
+        if constexpr (kPipe) {
+            if (g) {
+                output_tiles_pipelined<OP, T, PT, kPipeU>(h[0], stage, yrow[0], g + start, nullptr,
+                                                          nvec, warp, nwarps, lane);
+            } else {
+                output_tiles_rows<OP, T, PT, R>(h, stage, a.pitch, yrow, rows, nullptr, nullptr,
+                                                nvec, warp, nwarps, lane);
+            }
+        } else if constexpr (BULK) {
             output_tiles_rows<OP, T, PT, R>(h, stage, a.pitch, yrow, rows, g ? g + start : nullptr,
                                             b ? b + start : nullptr, nvec, warp, nwarps, lane);
         } else {

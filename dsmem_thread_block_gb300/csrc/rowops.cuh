@@ -578,6 +578,93 @@ __device__ __forceinline__ void cta_partial_rows(const Stats<OP, T> (&st)[R], fl
     }
 }
 
+// Output of one row with parameters, software-pipelined: a warp's next tile
+// of parameters is requested before the current tile is computed and stored,
+// so their L2 latency overlaps the work instead of stalling each tile (the
+// parameter vectors are re-read by every row, from L2).  Two register sets
+// alternate; tiles are U granules per lane.
+template <int OP, typename T, typename PT, int U>
+__device__ __forceinline__ void output_tiles_pipelined(const OutputMap<OP, T>& h,
+                                                       const unsigned char* base, T* yrow,
+                                                       const PT* gp, const PT* bp, int nvec,
+                                                       int warp, int nwarps, int lane) {
+    using G = Granule<OP, T, PT>;
+    constexpr int NP = G::kPairs, kTile = 32 * U;
+    const int ngran = nvec * (16 / G::kBytes);
+    const int stride = nwarps * kTile;
+    const bool has_g = gp != nullptr, has_b = bp != nullptr;
+
+    auto load = [&](int t, F2 (&gv)[U][NP], F2 (&bv)[U][NP]) {
+        const bool full = t + kTile <= ngran;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = t + lane + 32 * u;
+            if (full || q < ngran) {
+                if (has_g) granule_params<PT, NP>(gp, q, gv[u]);
+                if (has_b) granule_params<PT, NP>(bp, q, bv[u]);
+            }
+        }
+    };
+    auto apply = [&](int t, const F2 (&gv)[U][NP], const F2 (&bv)[U][NP]) {
+        const bool full = t + kTile <= ngran;
+        uint4 raw[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = t + lane + 32 * u;
+            if (full || q < ngran) {
+                if constexpr (G::kBytes == 8) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(base + (size_t)q * 8);
+                    raw[u] = make_uint4(w.x, w.y, 0u, 0u);
+                } else {
+                    raw[u] = lds16(base + (size_t)q * 16);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = t + lane + 32 * u;
+            if (full || q < ngran) {
+                F2 p[NP];
+                if constexpr (G::kBytes == 8) {
+                    p[0] = Pairs<bf16>::one(raw[u].x);
+                    p[1] = Pairs<bf16>::one(raw[u].y);
+                } else {
+                    Pairs<T>::unpack(raw[u], p);
+                }
+#pragma unroll
+                for (int i = 0; i < NP; ++i) p[i] = h(p[i], gv[u][i], bv[u][i]);
+                if constexpr (G::kBytes == 8) {
+                    __stcs(reinterpret_cast<uint2*>(yrow) + q,
+                           make_uint2(Pairs<bf16>::two(p[0]), Pairs<bf16>::two(p[1])));
+                } else {
+                    stg16_stream(reinterpret_cast<uint4*>(yrow) + q, Pairs<T>::pack(p));
+                }
+            }
+        }
+    };
+    F2 ga[U][NP], ba[U][NP], gb[U][NP], bb[U][NP];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            ga[u][i] = gb[u][i] = f2(1.f);
+            ba[u][i] = bb[u][i] = f2(0.f);
+        }
+    }
+    int t = warp * kTile;
+    if (t < ngran) load(t, ga, ba);
+    while (t < ngran) {
+        const int t1 = t + stride;
+        if (t1 < ngran) load(t1, gb, bb);
+        apply(t, ga, ba);
+        if (t1 >= ngran) break;
+        const int t2 = t1 + stride;
+        if (t2 < ngran) load(t2, ga, ba);
+        apply(t1, gb, bb);
+        t = t2;
+    }
+}
+
 // Output of R rows that share a column slice: each granule's parameters are
 // loaded once and applied to all live rows (row i staged at base + i * pitch,
 // written to yrow[i]); the first `rows` <= R rows are live.

@@ -319,6 +319,24 @@ def test_exchange_modes(R, exchange):
     assert C.credit_get_device_error(dev) == C.OK
 
 
+def test_rmsnorm_bf16_weights_pipelined_output():
+    # bf16 data with bf16 weights takes the software-pipelined output pass:
+    # slices whose granule count leaves partial warp tiles and odd tile
+    # counts per warp
+    dev = torch.cuda.current_device()
+    for cols in (98312, 24584, 8200):
+        w = _custom(wl.RMSNORM, "bf16", 3, cols, 58, eps=1e-6, param_dtype="bf16")
+        inp = w.generate()
+        for P in (1, 2, 3, 5, 7, 16):
+            try:
+                p = C.credit_plan_with(gh_ops(w), w.rows, w.cols, gh_dt(w), dev, C.CLUSTER, P)
+            except C.CreditError as e:
+                assert e.status == C.ERR_NO_LEGAL_PLAN
+                continue
+            check(w, run(w, inp, p), inp)
+    assert C.credit_get_device_error(dev) == C.OK
+
+
 def test_planned_exchange():
     dev = torch.cuda.current_device()
     w = _custom(wl.SOFTMAX, "f32", 4, 65536, 57)
