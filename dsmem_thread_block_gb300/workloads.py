@@ -19,7 +19,7 @@ import dataclasses
 import numpy as np
 
 SOFTMAX, LAYERNORM, RMSNORM = "softmax", "layernorm", "rmsnorm"
-QUANTIZE, WEIGHTED_STD = "quantize", "weighted_std"
+QUANTIZE, WEIGHTED_STD, PEARSON = "quantize", "weighted_std", "pearson"
 
 
 def to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -55,6 +55,7 @@ class Workload:
     b_mean: float = 0.0         # beta ~ N(b_mean, b_std)
     b_std: float = 0.1
     p_uniform: bool = False     # parameters ~ U(0, 1) instead (weights of weighted_std)
+    u_corr: float = 0.6         # Pearson: u = u_corr * x + sqrt(1 - u_corr^2) * N(0, 1)
 
     @property
     def elem_bytes(self) -> int:
@@ -68,6 +69,8 @@ class Workload:
         (quantization writes one byte per element plus a scale per row)."""
         if self.op == QUANTIZE:
             return self.rows * self.cols * (self.elem_bytes + 1) + 4 * self.rows
+        if self.op == PEARSON:  # x and u read, y written, one r per row
+            return 3 * self.rows * self.cols * self.elem_bytes + 4 * self.rows
         b = 2 * self.rows * self.cols * self.elem_bytes
         if self.param_dtype is not None:
             pb = 4 if self.param_dtype == "f32" else 2
@@ -76,7 +79,7 @@ class Workload:
         return b
 
     def generate(self) -> dict:
-        """Draw x (and gamma/beta or weight) in a fixed order from `seed`."""
+        """Draw x (then u, or gamma/beta or weight) in a fixed order from `seed`."""
         rng = np.random.default_rng(self.seed)
         n = self.rows * self.cols
         x = rng.standard_normal(n, dtype=np.float32)
@@ -88,6 +91,11 @@ class Workload:
             mask = rng.random(n, dtype=np.float32) < self.spike_frac
             x[mask] = np.float32(self.spike_value)
         out = {}
+        if self.op == PEARSON:
+            e = rng.standard_normal(n, dtype=np.float32)
+            u = np.float32(self.u_corr) * x + np.float32(np.sqrt(1.0 - self.u_corr ** 2)) * e
+            u = u.reshape(self.rows, self.cols)
+            out["u"] = u if self.dtype == "f32" else to_bf16_bits(u)
         if self.param_dtype is not None:
             if self.p_uniform:
                 g = rng.random(self.cols, dtype=np.float32)
@@ -137,6 +145,10 @@ WEIGHTED_STD_F32_4096x65536 = Workload(
     "weighted_std_f32_4096x65536", WEIGHTED_STD, "f32", 4096, 65536, seed=6, x_mean=0.5,
     x_std=2.0, eps=1e-5, param_dtype="f32", p_uniform=True)
 
+PEARSON_F32_4096x65536 = Workload(
+    "pearson_f32_4096x65536", PEARSON, "f32", 4096, 65536, seed=7, x_mean=0.5, x_std=2.0,
+    eps=1e-5)
+
 ALL = [SOFTMAX_F32_64x4096, LAYERNORM_BF16_1024x262144,
        SOFTMAX_F32_512x131072_SPIKES, RMSNORM_BF16_2048x786432,
-       QUANTIZE_F32_4096x65536, WEIGHTED_STD_F32_4096x65536]
+       QUANTIZE_F32_4096x65536, WEIGHTED_STD_F32_4096x65536, PEARSON_F32_4096x65536]

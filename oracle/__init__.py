@@ -1,5 +1,6 @@
-"""Plain CPU oracle for row softmax, LayerNorm, RMSNorm, int8 quantization and
-weighted standardization (fp64; the quantization codes in IEEE single).
+"""Plain CPU oracle for row softmax, LayerNorm, RMSNorm, int8 quantization,
+weighted standardization and Pearson correlation (fp64; the quantization
+codes in IEEE single).
 
 TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
 CPU-baseline / reference legs of ``bench.py`` may import this package.  The
@@ -63,8 +64,10 @@ def _load():
                                            vp]
             lib.oracle_quantize.argtypes = [vp, i32, i64, i64, vp, vp]
             lib.oracle_weighted_std.argtypes = [vp, i32, i64, i64, vp, i32, dbl, vp]
+            lib.oracle_pearson.argtypes = [vp, vp, i32, i64, i64, dbl, vp, vp]
             for f in (lib.oracle_widen, lib.oracle_softmax, lib.oracle_layernorm,
-                      lib.oracle_rmsnorm, lib.oracle_quantize, lib.oracle_weighted_std):
+                      lib.oracle_rmsnorm, lib.oracle_quantize, lib.oracle_weighted_std,
+                      lib.oracle_pearson):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -169,6 +172,20 @@ def weighted_std(x: np.ndarray, w: np.ndarray, eps: float = 1e-5) -> np.ndarray:
     _check(_load().oracle_weighted_std(_ptr(x), _dtype_code(x), x.shape[0], x.shape[1],
                                        _ptr(wv), wd, float(eps), _ptr(y)), "weighted_std")
     return y
+
+
+def pearson(x: np.ndarray, u: np.ndarray, eps: float = 0.0):
+    """Row-wise standardized co-deviations and correlations (see oracle.c):
+    returns (y fp64 shaped like x, r fp64 one per row)."""
+    x = _prep(x)
+    u = _prep(u)
+    if u.shape != x.shape or _dtype_code(u) != _dtype_code(x):
+        raise ValueError("oracle: x and u must share shape and dtype")
+    y = np.empty(x.shape, dtype=np.float64)
+    r = np.empty(x.shape[0], dtype=np.float64)
+    _check(_load().oracle_pearson(_ptr(x), _ptr(u), _dtype_code(x), x.shape[0], x.shape[1],
+                                  float(eps), _ptr(y), _ptr(r)), "pearson")
+    return y, r
 
 
 def run_rows(fn, x: np.ndarray, *args, threads: int = 1, **kw) -> np.ndarray:

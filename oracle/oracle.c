@@ -1,6 +1,7 @@
 /*
  * oracle.c -- plain, slow, fp64 CPU oracle for the wide-row reduce-then-reuse
- * operators (row softmax, LayerNorm, RMSNorm).
+ * operators (row softmax, LayerNorm, RMSNorm, int8 quantization, weighted
+ * standardization, Pearson correlation).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
  * call this file: it is used by the tests, by the package smoke check and by
@@ -257,6 +258,57 @@ int oracle_weighted_std(const void *x, int dtype, int64_t rows, int64_t cols,
         inv = 1.0 / sqrt(var + eps);
         for (j = 0; j < cols; ++j)
             y[base + j] = (or_load(x, dtype, base + j) - mu) * inv;
+    }
+    return OR_OK;
+}
+
+/*
+ * Row-wise Pearson correlation of two matrices x and u of the same shape
+ * (the Pearson workload of the CREDIT summary page, section "B. Workload-by-
+ * Workload Scaling").  The pages name the workload only; the reading taken
+ * here keeps the reduce-then-reuse shape: the statistics are the row means,
+ * biased variances and covariance,
+ *   mx = sum_j x_j / N,  mu = sum_j u_j / N,
+ *   vx = sum_j (x_j - mx)^2 / N,  vu = sum_j (u_j - mu)^2 / N,
+ *   cxu = sum_j (x_j - mx)(u_j - mu) / N,
+ * and h writes every column's standardized co-deviation
+ *   y_j = (x_j - mx)(u_j - mu) / sqrt((vx + eps)(vu + eps)),
+ * whose row mean is the correlation r = cxu / sqrt((vx + eps)(vu + eps))
+ * (Pearson's r when eps = 0), written to r[row].  Two passes per statistic,
+ * every sum in fp64 in column order.  A row whose denominator is zero
+ * (eps = 0 and a constant x or u) is rejected.
+ */
+int oracle_pearson(const void *x, const void *u, int dtype, int64_t rows, int64_t cols,
+                   double eps, double *y, double *r)
+{
+    int64_t i, j;
+    if (!x || !u || !y || !r || rows < 0 || cols <= 0 || !or_dtype_ok(dtype) || !(eps >= 0.0))
+        return OR_BAD_ARG;
+    for (i = 0; i < rows; ++i) {
+        int64_t base = i * cols;
+        double sx = 0.0, su = 0.0, mx, mu, sxx = 0.0, suu = 0.0, sxu = 0.0, den;
+        for (j = 0; j < cols; ++j) {
+            sx += or_load(x, dtype, base + j);
+            su += or_load(u, dtype, base + j);
+        }
+        mx = sx / (double)cols;
+        mu = su / (double)cols;
+        for (j = 0; j < cols; ++j) {
+            double dx = or_load(x, dtype, base + j) - mx;
+            double du = or_load(u, dtype, base + j) - mu;
+            sxx += dx * dx;
+            suu += du * du;
+            sxu += dx * du;
+        }
+        den = sqrt((sxx / (double)cols + eps) * (suu / (double)cols + eps));
+        if (!(den > 0.0))
+            return OR_BAD_ARG;
+        for (j = 0; j < cols; ++j) {
+            double dx = or_load(x, dtype, base + j) - mx;
+            double du = or_load(u, dtype, base + j) - mu;
+            y[base + j] = dx * du / den;
+        }
+        r[i] = (sxu / (double)cols) / den;
     }
     return OR_OK;
 }

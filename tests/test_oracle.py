@@ -246,6 +246,11 @@ def test_workload_generators_are_seeded_and_shaped():
     frac = float((s == 30.0).mean())
     assert 0.008 < frac < 0.012
     assert wl.sweep_point(1024).rows * 1024 == 1 << 28
+    pr = wl.PEARSON_F32_4096x65536.with_rows(2).generate()
+    assert pr["u"].shape == pr["x"].shape == (2, 65536)
+    _, r = oracle.pearson(pr["x"], pr["u"])
+    # u = 0.6 x + 0.8 e with std(x) = 2: r = 1.2 / sqrt(1.44 + 0.64) ~ 0.832
+    assert np.all(np.abs(r - 1.2 / math.sqrt(2.08)) < 0.01)
 
 
 # ----------------------------------------------------------------- quantization
@@ -313,3 +318,71 @@ def test_weighted_std_unit_weights_is_layernorm_and_rejects_bad_weights():
         oracle.weighted_std(x, np.zeros(77, np.float32))
     with pytest.raises(ValueError):
         oracle.weighted_std(x, -np.ones(77, np.float32))
+
+
+# ------------------------------------------------------------------- Pearson
+def test_pearson_small_integers_closed_form(golden):
+    g = golden["pearson_small_integers"]
+    y, r = oracle.pearson(np.array([g["x"]], np.float32), np.array([g["u"]], np.float32))
+    den = math.sqrt(_frac(g["var_product"]))
+    np.testing.assert_allclose(y[0], [_frac(p) / den for p in g["products"]], rtol=1e-14,
+                               atol=1e-15)
+    assert r[0] > 0 and abs(r[0] ** 2 - _frac(g["r_squared"])) < 1e-14
+
+
+def test_pearson_matches_numpy_corrcoef_and_mean_of_outputs():
+    # eps = 0: r is the textbook correlation coefficient (numpy's routine),
+    # and the row mean of the outputs is r
+    rng = np.random.default_rng(61)
+    x = rng.standard_normal((5, 300)).astype(np.float32)
+    u = (0.7 * x + rng.standard_normal((5, 300))).astype(np.float32)
+    y, r = oracle.pearson(x, u)
+    for i in range(5):
+        ref = np.corrcoef(x[i].astype(np.float64), u[i].astype(np.float64))[0, 1]
+        assert abs(r[i] - ref) < 1e-12
+        assert abs(y[i].mean() - r[i]) < 1e-12
+    assert np.all(np.abs(r) <= 1.0)
+
+
+def test_pearson_linear_relations_and_symmetry():
+    rng = np.random.default_rng(62)
+    x = rng.standard_normal((3, 64))
+    # u = a x + b: r = +-1 and the outputs are the squared z-scores (times the sign)
+    for a, sign in ((4.0, 1.0), (-0.5, -1.0)):
+        y, r = oracle.pearson(x, a * x + 3.0)
+        np.testing.assert_allclose(r, sign, atol=1e-12)
+        z = (x - x.mean(axis=1, keepdims=True)) / x.std(axis=1, keepdims=True)
+        np.testing.assert_allclose(y, sign * z * z, rtol=1e-10, atol=1e-12)
+    # swapping the operands changes nothing
+    u = rng.standard_normal((3, 64))
+    y1, r1 = oracle.pearson(x, u)
+    y2, r2 = oracle.pearson(u, x)
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(r1, r2)
+
+
+def test_pearson_eps_closed_form_and_bad_rows():
+    # x = u = (1, -1): means 0, variances 1, so y_j = 1 / (1 + eps) = r
+    eps = 0.25
+    y, r = oracle.pearson(np.array([[1, -1]], np.float32), np.array([[1, -1]], np.float32),
+                          eps=eps)
+    np.testing.assert_allclose(y[0], [0.8, 0.8], rtol=1e-15)
+    np.testing.assert_allclose(r, [0.8], rtol=1e-15)
+    # a constant operand with eps = 0 has no correlation; with eps > 0 it gives 0
+    c = np.full((1, 8), 3.0, np.float32)
+    v = np.arange(8, dtype=np.float32).reshape(1, 8)
+    with pytest.raises(ValueError):
+        oracle.pearson(c, v)
+    y, r = oracle.pearson(c, v, eps=1e-3)
+    assert np.all(y == 0.0) and r[0] == 0.0
+
+
+def test_pearson_bf16_inputs_widen_exactly():
+    rng = np.random.default_rng(63)
+    x32 = rng.standard_normal((2, 50)).astype(np.float32)
+    u32 = rng.standard_normal((2, 50)).astype(np.float32)
+    xb, ub = wl.to_bf16_bits(x32), wl.to_bf16_bits(u32)
+    y1, r1 = oracle.pearson(xb, ub, eps=1e-5)
+    y2, r2 = oracle.pearson(wl.bf16_bits_to_f32(xb), wl.bf16_bits_to_f32(ub), eps=1e-5)
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(r1, r2)
