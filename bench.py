@@ -161,6 +161,14 @@ def cpu_oracle_rate(w, inputs, rows: int, threads: int):
         with cf.ThreadPoolExecutor(len(bounds) - 1) as ex:
             list(ex.map(lambda i: oracle.quantize(sub["x"][bounds[i]:bounds[i + 1]]),
                         range(len(bounds) - 1)))
+    elif w.op == "pearson":
+        bounds = np.linspace(0, rows, min(threads, rows) + 1, dtype=np.int64)
+        import concurrent.futures as cf
+        u = inputs["u"][:rows]
+        with cf.ThreadPoolExecutor(len(bounds) - 1) as ex:
+            list(ex.map(lambda i: oracle.pearson(sub["x"][bounds[i]:bounds[i + 1]],
+                                                 u[bounds[i]:bounds[i + 1]], eps=w.eps),
+                        range(len(bounds) - 1)))
     elif w.op == "weighted_std":
         oracle.run_rows(oracle.weighted_std, sub["x"], sub["weight"], threads=threads, eps=w.eps)
     elif w.op == "softmax":
@@ -253,7 +261,7 @@ def main():
     inputs = w.generate()
     DT = {"f32": C.F32, "bf16": C.BF16}
     OPS = {"softmax": C.SOFTMAX, "layernorm": C.LAYERNORM, "rmsnorm": C.RMSNORM,
-           "quantize": C.QUANTIZE, "weighted_std": C.WEIGHTED_STD}
+           "quantize": C.QUANTIZE, "weighted_std": C.WEIGHTED_STD, "pearson": C.PEARSON}
 
     def to_device(a):
         if a.dtype == np.uint16:
@@ -261,8 +269,9 @@ def main():
         return torch.from_numpy(a).to("cuda")
     dx = to_device(inputs["x"])
     quant = w.op == "quantize"
+    row_out = quant or w.op == "pearson"  # a per-row fp32 result: scales or r
     dy = torch.empty(dx.shape, dtype=torch.int8, device=dx.device) if quant else torch.empty_like(dx)
-    dscales = torch.empty(w.rows, dtype=torch.float32, device=dx.device) if quant else None
+    dscales = torch.empty(w.rows, dtype=torch.float32, device=dx.device) if row_out else None
     params = {k: to_device(v) for k, v in inputs.items() if k != "x"}
 
     tuning = None
@@ -307,6 +316,9 @@ def main():
         if quant:
             return lib.credit_quantize(xp, yp, dscales.data_ptr(), w.rows, w.cols, DT[w.dtype], pp,
                                        wptr or None, wbytes, sptr)
+        if w.op == "pearson":
+            return lib.credit_pearson(xp, params["u"].data_ptr(), yp, dscales.data_ptr(), w.rows,
+                                      w.cols, DT[w.dtype], w.eps, pp, wptr or None, wbytes, sptr)
         if w.op == "weighted_std":
             return lib.credit_weighted_std(xp, yp, w.rows, w.cols, DT[w.dtype],
                                            params["weight"].data_ptr(), pdt, w.eps, pp,
@@ -373,11 +385,11 @@ def main():
     hparams = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v)
                for k, v in params.items()}
     hy = torch.empty(dy.shape, dtype=dy.dtype, pin_memory=True)
-    hs = torch.empty(w.rows, dtype=torch.float32, pin_memory=True) if quant else None
+    hs = torch.empty(w.rows, dtype=torch.float32, pin_memory=True) if row_out else None
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
     h2d = hx.numel() * hx.element_size() + sum(v.numel() * v.element_size()
                                                for v in hparams.values())
-    d2h = hy.numel() * hy.element_size() + (hs.numel() * 4 if quant else 0)
+    d2h = hy.numel() * hy.element_size() + (hs.numel() * 4 if row_out else 0)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -390,7 +402,7 @@ def main():
                 params[k].copy_(v, non_blocking=True)
             launch(xp, yp)
             hy.copy_(dy, non_blocking=True)
-            if quant:
+            if row_out:
                 hs.copy_(dscales, non_blocking=True)
         f1.record(stream)
     torch.cuda.synchronize()

@@ -1,6 +1,7 @@
 """GB300-native CREDIT reduce-reuse library.
 
-Clustered DSMEM row softmax, LayerNorm and RMSNorm behind a C ABI
+Clustered DSMEM row softmax, LayerNorm, RMSNorm, int8 quantization, weighted
+standardization and Pearson correlation behind a C ABI
 (``libcredit.so``, declared in ``include/credit.h``), with this thin torch
 binding on top.  The binding only marshals arguments (device pointers, sizes,
 the current CUDA stream, a workspace from torch's allocator); every step of
@@ -17,11 +18,11 @@ from __future__ import annotations
 from . import _credit as C
 from ._credit import CreditError, Plan  # noqa: F401
 
-__all__ = ["softmax", "layernorm", "rmsnorm", "quantize", "weighted_std", "plan", "CreditError",
-           "Plan", "device_error", "load_library"]
+__all__ = ["softmax", "layernorm", "rmsnorm", "quantize", "weighted_std", "pearson", "plan",
+           "CreditError", "Plan", "device_error", "load_library"]
 
 _OPS = {"softmax": C.SOFTMAX, "layernorm": C.LAYERNORM, "rmsnorm": C.RMSNORM,
-        "quantize": C.QUANTIZE, "weighted_std": C.WEIGHTED_STD}
+        "quantize": C.QUANTIZE, "weighted_std": C.WEIGHTED_STD, "pearson": C.PEARSON}
 _plan_cache: dict = {}
 
 
@@ -178,6 +179,24 @@ def weighted_std(x, weights, eps: float = 1e-5, out=None, plan: Plan | None = No
     if st != C.OK:
         raise CreditError(st, "credit_weighted_std")
     return out
+
+
+def pearson(x, u, eps: float = 0.0, out=None, r=None, plan: Plan | None = None, workspace=None):
+    """Row-wise Pearson correlation of x and u over the last dimension;
+    returns (standardized co-deviations shaped like x, fp32 r per row)."""
+    import torch
+    rows, cols, out = _prep(x, out)
+    if u is None or u.shape != x.shape or u.dtype != x.dtype or not u.is_cuda or \
+            not u.is_contiguous():
+        raise ValueError("credit: u must be a contiguous CUDA tensor shaped like x")
+    if r is None:
+        r = torch.empty(rows, dtype=torch.float32, device=x.device)
+    p, w, wb = _plan_and_ws("pearson", rows, cols, x, plan, workspace)
+    st = C.credit_pearson(x.data_ptr(), u.data_ptr(), out.data_ptr(), r.data_ptr(), rows, cols,
+                          _dtype(x.dtype), float(eps), p, w, wb, _stream(x))
+    if st != C.OK:
+        raise CreditError(st, "credit_pearson")
+    return out, r
 
 
 def device_error(device: int = 0) -> int:

@@ -17,7 +17,7 @@ from . import build as _build
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_LEGAL_PLAN, ERR_CUDA, \
     ERR_DEVICE_TIMEOUT, ERR_NOT_CALIBRATED = range(7)
 F32, BF16 = 0, 1
-SOFTMAX, LAYERNORM, RMSNORM, QUANTIZE, WEIGHTED_STD = 0, 1, 2, 3, 4
+SOFTMAX, LAYERNORM, RMSNORM, QUANTIZE, WEIGHTED_STD, PEARSON = 0, 1, 2, 3, 4, 5
 AUTO, CLUSTER, TWO_PASS, CLUSTER_PERSISTENT = 0, 1, 2, 3
 EXCHANGE_DEFAULT, EXCHANGE_BARRIER, EXCHANGE_ASYNC = 0, 1, 2
 
@@ -109,6 +109,8 @@ SIGNATURES = {
                                _vp]),
     "credit_weighted_std": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _i32, _f32,
                                    ctypes.POINTER(Plan), _vp, _sz, _vp]),
+    "credit_pearson": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _f32, ctypes.POINTER(Plan),
+                              _vp, _sz, _vp]),
     "credit_two_pass_noalloc": (_i32, [_i32, _vp, _vp, _i64, _i64, _i32, _vp, _vp, _i32, _f32,
                                        _vp]),
     "credit_bench_dsmem": (_i32, [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(BenchResult)]),
@@ -228,6 +230,14 @@ def credit_weighted_std(x: int, y: int, rows: int, cols: int, dtype: int, weight
     return load().credit_weighted_std(x, y, rows, cols, dtype, weights or None, weight_dtype,
                                       eps, _plan_ptr(plan), workspace or None, workspace_bytes,
                                       stream or None)
+
+
+def credit_pearson(x: int, u: int, y: int, r: int, rows: int, cols: int, dtype: int,
+                   eps: float, plan=None, workspace: int = 0, workspace_bytes: int = 0,
+                   stream: int = 0) -> int:
+    return load().credit_pearson(x or None, u or None, y or None, r or None, rows, cols, dtype,
+                                 eps, _plan_ptr(plan), workspace or None, workspace_bytes,
+                                 stream or None)
 
 
 def credit_two_pass_noalloc(op: int, x: int, y: int, rows: int, cols: int, dtype: int,

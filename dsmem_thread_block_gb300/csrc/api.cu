@@ -195,8 +195,9 @@ credit_status_t run(const OpCall& c) {
     if ((c.p0 || c.p1) && !dtype_ok(c.pdtype)) return CREDIT_ERR_UNSUPPORTED;
     const bool quant = c.op == CREDIT_QUANTIZE;
     if (!quant && c.op != CREDIT_SOFTMAX && !(c.eps >= 0.f)) return CREDIT_ERR_INVALID_ARG;
-    if (quant && !c.aux) return CREDIT_ERR_INVALID_ARG;
-    if (c.op == CREDIT_WEIGHTED_STD && !c.p0) return CREDIT_ERR_INVALID_ARG;
+    const bool pearson = c.op == CREDIT_PEARSON;
+    if ((quant || pearson) && !c.aux) return CREDIT_ERR_INVALID_ARG;
+    if ((c.op == CREDIT_WEIGHTED_STD || pearson) && !c.p0) return CREDIT_ERR_INVALID_ARG;
     if (c.rows > INT64_MAX / c.cols) return CREDIT_ERR_INVALID_ARG;
     const size_t es = esize(c.dtype);
     const int64_t n = c.rows * c.cols;
@@ -208,10 +209,15 @@ credit_status_t run(const OpCall& c) {
     const uintptr_t xbytes = (uintptr_t)(n * (int64_t)es);
     const uintptr_t ybytes = quant ? (uintptr_t)n : xbytes;
     if ((quant || xb != yb) && xb < yb + ybytes && yb < xb + xbytes) return CREDIT_ERR_INVALID_ARG;
-    if (quant) {
+    // Pearson's second operand u has the shape of x: y may equal it (in
+    // place) but may not partially overlap it
+    const uintptr_t ub = pearson ? (uintptr_t)c.p0 : 0;
+    if (pearson && ub != yb && ub < yb + ybytes && yb < ub + xbytes) return CREDIT_ERR_INVALID_ARG;
+    if (quant || pearson) {
         const uintptr_t ab = (uintptr_t)c.aux, abytes = (uintptr_t)(c.rows * 4);
         if ((ab & 3u) || (ab < xb + xbytes && xb < ab + abytes) || (ab < yb + ybytes && yb < ab + abytes))
             return CREDIT_ERR_INVALID_ARG;
+        if (pearson && ab < ub + xbytes && ub < ab + abytes) return CREDIT_ERR_INVALID_ARG;
     }
 
     int dev = 0;
@@ -362,6 +368,15 @@ credit_status_t credit_weighted_std(const void* x, void* y, int64_t rows, int64_
                                     size_t workspace_bytes, void* stream) {
     OpCall c{CREDIT_WEIGHTED_STD, x, y, rows, cols, dtype, weights, nullptr, weight_dtype, eps,
              plan, workspace, workspace_bytes, (cudaStream_t)stream};
+    return run(c);
+}
+
+credit_status_t credit_pearson(const void* x, const void* u, void* y, float* r, int64_t rows,
+                               int64_t cols, credit_dtype_t dtype, float eps,
+                               const credit_plan_t* plan, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+    OpCall c{CREDIT_PEARSON, x, y, rows, cols, dtype, u, nullptr, dtype, eps,
+             plan, workspace, workspace_bytes, (cudaStream_t)stream, r};
     return run(c);
 }
 

@@ -268,6 +268,7 @@ const void* cluster_kernel(KernelKey k) {
         case kQuant: return k.dtype == 0 ? pick_rows<kQuant, float, float>(k.vec, k.rows)
                                          : pick_rows<kQuant, bf16, float>(k.vec, k.rows);
         case kWStd: return pick_dtype<kWStd>(k.dtype, k.pdtype, k.vec, k.rows);
+        case kPearson: return k.rows == 1 ? pearson_cluster_kernel(k.dtype, k.vec) : nullptr;
     }
     return nullptr;
 }
@@ -277,13 +278,16 @@ cudaError_t launch_cluster(KernelKey k, const ClusterArgs& a, int P, int threads
     const void* fn = cluster_kernel(k);
     if (!fn) return cudaErrorInvalidDeviceFunction;
     const size_t esz = k.dtype == 0 ? 4 : 2;
+    const size_t yesz = k.op == kQuant ? 1 : esz;  // int8 codes
     // gridDim.x is limited to 2^31 - 1: launch in batches of whole clusters
     const int64_t max_rows = (int64_t)(0x7fffffff / P) * k.rows;
     for (int64_t r0 = 0; r0 < a.rows; r0 += max_rows) {
         const int64_t nr = a.rows - r0 < max_rows ? a.rows - r0 : max_rows;
         ClusterArgs b = a;
         b.x = static_cast<const char*>(a.x) + r0 * a.cols * (int64_t)esz;
-        b.y = static_cast<char*>(a.y) + r0 * a.cols * (int64_t)esz;
+        b.y = static_cast<char*>(a.y) + r0 * a.cols * (int64_t)yesz;
+        if (a.aux) b.aux = a.aux + r0;
+        if (k.op == kPearson) b.p0 = static_cast<const char*>(a.p0) + r0 * a.cols * (int64_t)esz;
         b.rows = nr;
         const int64_t nclusters = (nr + k.rows - 1) / k.rows;
         cudaLaunchConfig_t cfg = {};

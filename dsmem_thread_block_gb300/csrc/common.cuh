@@ -28,7 +28,7 @@ namespace credit {
 // Operators.  kQuant: row absmax -> scale -> int8 codes; kWStd: weighted
 // standardization with per-column weights (the weighted counterpart of
 // LayerNorm without the affine step).
-enum Op : int { kSoftmax = 0, kLayerNorm = 1, kRMSNorm = 2, kQuant = 3, kWStd = 4 };
+enum Op : int { kSoftmax = 0, kLayerNorm = 1, kRMSNorm = 2, kQuant = 3, kWStd = 4, kPearson = 5 };
 
 // LayerNorm-like statistics (count or weight, mean, M2).
 __host__ __device__ constexpr bool norm_like(int op) { return op == kLayerNorm || op == kWStd; }

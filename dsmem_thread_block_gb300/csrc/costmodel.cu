@@ -127,6 +127,8 @@ credit_status_t call_op(credit_op_t op, const void* x, void* y, int64_t rows, in
         case CREDIT_WEIGHTED_STD:
             return credit_weighted_std(x, y, rows, cols, dtype, p0, pd, 1e-5f, plan, ws, wsb,
                                        nullptr);
+        case CREDIT_PEARSON:
+            return credit_pearson(x, p0, y, aux, rows, cols, dtype, 1e-5f, plan, ws, wsb, nullptr);
         case CREDIT_SOFTMAX: return credit_softmax(x, y, rows, cols, dtype, plan, ws, wsb, nullptr);
         case CREDIT_LAYERNORM:
             return credit_layernorm(x, y, rows, cols, dtype, p0, p1, pd, 1e-5f, plan, ws, wsb, nullptr);
@@ -212,18 +214,22 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         st = make_plan(device, op, rows, cols, dtype, CREDIT_TWO_PASS, 0, 0, 0, &base);
         if (st != CREDIT_OK) return st;
     }
-    // bytes: one read of x and one write of the output (int8 codes for
-    // quantization); the re-read baseline reads x twice
+    // bytes: one read of x (and of u for Pearson) and one write of the
+    // output (int8 codes for quantization); the re-read baseline reads the
+    // inputs twice
+    const bool pearson = op == CREDIT_PEARSON;
+    const double b_read = pearson ? 2.0 * mat : mat;
     const double b_write = op == CREDIT_QUANTIZE ? (double)rows * (double)cols : mat;
-    const double b_credit = mat + b_write;
-    const double b_base = staging ? b_credit : b_credit + mat;
+    const double b_credit = b_read + b_write;
+    const double b_base = staging ? b_credit : b_credit + b_read;
 
     // scratch buffers of the shape
     Scratch x, y, g, b, ws, aux;
     const size_t pbytes = (size_t)cols * (param_dtype == CREDIT_F32 ? 4 : 2);
     if (op == CREDIT_WEIGHTED_STD && param_dtype < 0) return CREDIT_ERR_INVALID_ARG;
     if (!x.alloc((size_t)mat) || !y.alloc((size_t)mat) || !aux.alloc((size_t)rows * 4) ||
-        (param_dtype >= 0 && (!g.alloc(pbytes) || !b.alloc(pbytes))))
+        (pearson && !g.alloc((size_t)mat)) ||  // the second operand u
+        (!pearson && param_dtype >= 0 && (!g.alloc(pbytes) || !b.alloc(pbytes))))
         return CREDIT_ERR_CUDA;
     if (!staging && !ws.alloc((size_t)base.workspace_bytes)) return CREDIT_ERR_CUDA;
 

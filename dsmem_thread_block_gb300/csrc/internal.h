@@ -11,7 +11,7 @@ namespace credit {
 struct ClusterArgs {
     const void* x;
     void* y;
-    const void* p0;       // gamma (LayerNorm) or weight (RMSNorm), may be null
+    const void* p0;       // gamma (LayerNorm), weight (RMSNorm, weighted std) or u (Pearson)
     const void* p1;       // beta (LayerNorm), may be null
     int64_t rows;         // rows of this launch (the last cluster may hold fewer than R)
     int64_t cols;
@@ -20,7 +20,7 @@ struct ClusterArgs {
     int32_t pitch;        // bytes between the staged slices of a CTA's rows
     float eps;
     unsigned* err;        // device error word
-    float* aux;           // quantization: per-row scales out (else unused)
+    float* aux;           // per-row scales (quantization) or r (Pearson) out
     int32_t exchange;     // 0: push + cluster barrier; 1: st.async deposits + mbarrier
 };
 
@@ -36,8 +36,8 @@ struct TwoPassArgs {
     int32_t chunk;        // elements per block (threads * kTwoPassVpt * vector)
     int32_t nch;          // chunks per row
     float eps;
-    float* ws;            // rows * nch * 4 floats
-    float* aux;           // quantization: per-row scales out (else unused)
+    float* ws;            // rows * nch * 4 floats (8 for Pearson)
+    float* aux;           // per-row scales (quantization) or r (Pearson) out
 };
 
 constexpr int kTwoPassVpt = 4;  // 16-byte vectors per thread per chunk
@@ -73,6 +73,10 @@ struct KernelKey {
 };
 
 const void* cluster_kernel(KernelKey k);
+// Pearson correlation (two staged operands): dtype 0 = fp32 / 1 = bf16
+const void* pearson_cluster_kernel(int dtype, bool vec);
+const void* pearson_stats_kernel(int dtype, bool vec);
+const void* pearson_apply_kernel(int dtype, bool vec);
 const void* persistent_kernel(KernelKey k);
 const void* two_pass_stats_kernel(KernelKey k);
 const void* two_pass_apply_kernel(KernelKey k);

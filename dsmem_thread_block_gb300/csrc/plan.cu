@@ -24,7 +24,7 @@ int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 bool op_ok(credit_op_t op) {
     return op == CREDIT_SOFTMAX || op == CREDIT_LAYERNORM || op == CREDIT_RMSNORM ||
-           op == CREDIT_QUANTIZE || op == CREDIT_WEIGHTED_STD;
+           op == CREDIT_QUANTIZE || op == CREDIT_WEIGHTED_STD || op == CREDIT_PEARSON;
 }
 
 int cluster_threads(int64_t staged_vecs) {
@@ -106,7 +106,7 @@ credit_status_t persistent_plan(int dev, const DevInfo* d, credit_op_t op, int64
     p->rows_per_cluster = 1;
     p->exchange = CREDIT_EXCHANGE_BARRIER;
     p->waves = (int32_t)std::min<int64_t>(ceil_div(rows, G), INT32_MAX);
-    const double bytes = 2.0 * (double)rows * (double)cols * es;
+    const double bytes = (op == CREDIT_PEARSON ? 3.0 : 2.0) * (double)rows * (double)cols * es;
     const double coverage = std::min(1.0, (double)G * P / ((double)d->sms * cps));
     const double pipe = nr >= 2 ? 0.95 : 0.8;
     p->pred_us = (float)(bytes / (kNominalBytesPerUs * coverage * pipe) + kLaunchUs);
@@ -140,27 +140,31 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
     p.exchange = variant == CREDIT_CLUSTER ? CREDIT_EXCHANGE_ASYNC
                  : variant == CREDIT_CLUSTER_PERSISTENT ? CREDIT_EXCHANGE_BARRIER
                                                         : CREDIT_EXCHANGE_DEFAULT;
-    const double bytes = 2.0 * (double)rows * (double)cols * es;
+    const double bytes = (op == CREDIT_PEARSON ? 3.0 : 2.0) * (double)rows * (double)cols * es;
 
     if (variant == CREDIT_CLUSTER) {
         if (P < 1 || P > kMaxCluster) return CREDIT_ERR_NO_LEGAL_PLAN;
         const int R = rows_per_cluster ? rows_per_cluster : 1;
         if (R != 1 && R != 2 && R != 4) return CREDIT_ERR_INVALID_ARG;
+        // Pearson stages two operands (x, then u one pitch further) of one row
+        const bool two_ops = op == CREDIT_PEARSON;
+        if (two_ops && R != 1) return CREDIT_ERR_INVALID_ARG;
+        const int staged = two_ops ? 2 : R;  // slices held per CTA
         const int64_t slice = round_up(ceil_div(cols, P), vec);
         const int64_t pitch = row_pitch(slice, es);
-        const int64_t smem = R == 1 ? round_up(slice * es, 16) : R * pitch;
+        const int64_t smem = staged == 1 ? round_up(slice * es, 16) : staged * pitch;
         const void* fn = cluster_kernel(KernelKey{(int)op, (int)dtype, 0, true, R});
         const KernelInfo* ki = kernel_info(dev, fn, true);
         if (!ki) return CREDIT_ERR_CUDA;
         if (smem > ki->max_dyn_smem || pitch > INT32_MAX) return CREDIT_ERR_NO_LEGAL_PLAN;
-        const int t = threads ? threads : cluster_threads(R * slice / vec);
+        const int t = threads ? threads : cluster_threads(staged * slice / vec);
         const int active = occupancy_clusters(dev, fn, P, t, (size_t)smem, rows);
         if (active < 1) return CREDIT_ERR_NO_LEGAL_PLAN;
         p.cluster_size = P;
         p.threads = t;
         p.smem_bytes = smem;
         p.slice_elems = slice;
-        p.chunk_elems = (int32_t)bulk_chunk_elems(slice, es, R);
+        p.chunk_elems = (int32_t)bulk_chunk_elems(slice, es, staged);
         p.rows_per_cluster = R;
         p.active_clusters = active;
         p.ctas_per_sm = std::max(1, (int)((int64_t)active * P / d->sms));
@@ -207,7 +211,7 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
         p.threads = t;
         p.slice_elems = chunk;
         p.chunk_elems = (int32_t)chunk;
-        p.workspace_bytes = rows * nch * 4 * (int64_t)sizeof(float);
+        p.workspace_bytes = rows * nch * (op == CREDIT_PEARSON ? 8 : 4) * (int64_t)sizeof(float);
         p.active_clusters = active;
         p.waves = (int32_t)std::min<int64_t>(ceil_div(rows * nch, active), INT32_MAX);
         p.pred_us = (float)(1.5 * bytes / (kNominalBytesPerUs * 0.9) + 2 * kLaunchUs);
@@ -235,10 +239,11 @@ credit_status_t auto_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
     // 256-thread CTAs per SM), rows of 16 KiB or less batched four to a CTA;
     // the two-pass kernel only when no cluster size fits.
     const int es = dtype == CREDIT_F32 ? 4 : 2;
+    const int nops = op == CREDIT_PEARSON ? 2 : 1;  // staged operands per row
     for (int P = 1; P <= kMaxCluster; ++P) {
-        const int64_t slice_bytes = ceil_div(cols, P) * es;
+        const int64_t slice_bytes = ceil_div(cols, P) * es * nops;
         if (slice_bytes > 65536 && P < kMaxCluster) continue;
-        const int R = (P == 1 && slice_bytes * 4 <= 65536) ? 4 : 1;
+        const int R = (P == 1 && nops == 1 && slice_bytes * 4 <= 65536) ? 4 : 1;
         credit_plan_t c;
         if (make_plan(dev, op, rows, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &c, 0, R) != CREDIT_OK)
             continue;

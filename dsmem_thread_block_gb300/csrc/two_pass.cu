@@ -265,6 +265,7 @@ const void* two_pass_stats_kernel(KernelKey k) {
         case kRMSNorm: return k.dtype == 0 ? stats_pick<kRMSNorm, float, float>(k.vec) : stats_pick<kRMSNorm, bf16, float>(k.vec);
         case kQuant: return k.dtype == 0 ? stats_pick<kQuant, float, float>(k.vec) : stats_pick<kQuant, bf16, float>(k.vec);
         case kWStd: return k.dtype == 0 ? stats_param<kWStd, float>(k.pdtype, k.vec) : stats_param<kWStd, bf16>(k.pdtype, k.vec);
+        case kPearson: return pearson_stats_kernel(k.dtype, k.vec);
     }
     return nullptr;
 }
@@ -289,6 +290,7 @@ const void* two_pass_apply_kernel(KernelKey k) {
         case kQuant: return k.dtype == 0 ? apply_pick<kQuant, float, float>(k.vec)
                                          : apply_pick<kQuant, bf16, float>(k.vec);
         case kWStd: return apply_dtype<kWStd>(k.dtype, k.pdtype, k.vec);
+        case kPearson: return pearson_apply_kernel(k.dtype, k.vec);
     }
     return nullptr;
 }
@@ -299,13 +301,16 @@ cudaError_t launch_two_pass(KernelKey k, const TwoPassArgs& a, int64_t rows, int
     const void* fa = two_pass_apply_kernel(k);
     if (!fs || !fa) return cudaErrorInvalidDeviceFunction;
     const size_t esz = k.dtype == 0 ? 4 : 2;
+    const size_t yesz = k.op == kQuant ? 1 : esz;  // int8 codes
     const int64_t max_rows = 65535;  // gridDim.y limit
     for (int64_t r0 = 0; r0 < rows; r0 += max_rows) {
         const int64_t nr = rows - r0 < max_rows ? rows - r0 : max_rows;
         TwoPassArgs b = a;
         b.x = static_cast<const char*>(a.x) + r0 * a.cols * (int64_t)esz;
-        b.y = static_cast<char*>(a.y) + r0 * a.cols * (int64_t)esz;
-        b.ws = a.ws + r0 * a.nch * 4;
+        b.y = static_cast<char*>(a.y) + r0 * a.cols * (int64_t)yesz;
+        b.ws = a.ws + r0 * a.nch * (k.op == kPearson ? 8 : 4);
+        if (a.aux) b.aux = a.aux + r0;
+        if (k.op == kPearson) b.p0 = static_cast<const char*>(a.p0) + r0 * a.cols * (int64_t)esz;
         void* args[] = {&b};
         const dim3 grid((unsigned)a.nch, (unsigned)nr, 1);
         cudaError_t e = cudaLaunchKernel(fs, grid, dim3((unsigned)threads), args, 0, s);

@@ -56,7 +56,8 @@ typedef enum {
     CREDIT_LAYERNORM = 1,
     CREDIT_RMSNORM = 2,
     CREDIT_QUANTIZE = 3,      /* row absmax -> scale -> int8 codes */
-    CREDIT_WEIGHTED_STD = 4   /* weighted standardization, per-column weights */
+    CREDIT_WEIGHTED_STD = 4,  /* weighted standardization, per-column weights */
+    CREDIT_PEARSON = 5        /* row correlation of two matrices, co-deviations out */
 } credit_op_t;
 
 typedef enum {
@@ -420,6 +421,34 @@ credit_status_t credit_weighted_std(const void *x, void *y, int64_t rows,
                                     credit_dtype_t weight_dtype, float eps,
                                     const credit_plan_t *plan, void *workspace,
                                     size_t workspace_bytes, void *stream);
+
+/*
+ * Row-wise Pearson correlation of two matrices x and u of the same shape
+ * (the Pearson workload of CREDIT "B. Workload-by-Workload Scaling"; the
+ * pages name it only, and this reading keeps the reduce-then-reuse shape):
+ *   mx, mu    row means;  vx, vu  biased variances;  cxu  covariance,
+ *   y_j = (x_j - mx)(u_j - mu) / (sqrt(vx + eps) sqrt(vu + eps)),
+ *   r   = cxu / (sqrt(vx + eps) sqrt(vu + eps))      (Pearson's r at eps = 0),
+ * so the row mean of y is r.  Each CTA stages its slice of both operands
+ * (so P is twice that of a one-operand row) and pushes (n, mx, mu) and
+ * (Mxx, Muu, Cxu) -- two 16-byte slots -- to every peer; co-moments merge
+ * in the parallel-axis form of Chan et al.
+ *   x, u      device inputs, rows x cols, dtype (u not NULL)
+ *   y         device output like x; may equal x or u (in place), may not
+ *             partially overlap either
+ *   r         device output, rows fp32 correlations, 4-byte aligned, not
+ *             overlapping x, u or y
+ *   eps       >= 0; a row with a constant operand and eps = 0 gives
+ *             unspecified values
+ * Persistent plans and rows_per_cluster > 1 are not offered for this
+ * operator; TWO_PASS needs rows * ceil(cols / chunk) * 32 bytes of
+ * workspace (plan.workspace_bytes).  Other arguments as credit_softmax.
+ */
+credit_status_t credit_pearson(const void *x, const void *u, void *y, float *r,
+                               int64_t rows, int64_t cols, credit_dtype_t dtype,
+                               float eps, const credit_plan_t *plan,
+                               void *workspace, size_t workspace_bytes,
+                               void *stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *credit_status_string(credit_status_t status);

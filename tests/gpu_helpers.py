@@ -13,6 +13,12 @@ y = z * gamma + beta can cancel to a tiny |o|.  Its bound is therefore
 with sigma = sqrt(var + eps) of the row (1e-5 is ~170 fp32 ulps: room for
 the summation error of the statistics), and the tests report how many
 elements pass only through that term.
+Pearson's y = zx zu (z the deviations over sqrt(var + eps)) carries that
+error in both factors.  A short row's fp32 mean is off by about 2^-24 times
+the row's typical magnitude rather than |mean| (a mean near zero of values
+near +-2 still errs by ~2^-24 * 2), so the term uses the row's rms:
+  |g - o| <= rtol * |o| + 1e-5 * (|zu| (|zx| + rms_x / sx) + |zx| (|zu| + rms_u / su))
+and its fp32 correlation r is held to |g - o| <= 1e-5 (r lies in [-1, 1]).
 """
 from __future__ import annotations
 
@@ -26,7 +32,7 @@ from dsmem_thread_block_gb300 import workloads as wl
 RTOL = {"f32": 1e-5, "bf16": 2.0 ** -7}
 LN_CANCEL = 1e-5
 OPS = {wl.SOFTMAX: C.SOFTMAX, wl.LAYERNORM: C.LAYERNORM, wl.RMSNORM: C.RMSNORM,
-       wl.QUANTIZE: C.QUANTIZE, wl.WEIGHTED_STD: C.WEIGHTED_STD}
+       wl.QUANTIZE: C.QUANTIZE, wl.WEIGHTED_STD: C.WEIGHTED_STD, wl.PEARSON: C.PEARSON}
 DT = {"f32": C.F32, "bf16": C.BF16}
 
 
@@ -78,6 +84,10 @@ def call(w: wl.Workload, dx: torch.Tensor, dy: torch.Tensor, params: dict, plan,
     if w.op == wl.QUANTIZE:
         return C.credit_quantize(dx.data_ptr(), dy.data_ptr(), params["scales"].data_ptr(), rows,
                                  w.cols, DT[w.dtype], plan, wptr, wbytes, s)
+    if w.op == wl.PEARSON:
+        return C.credit_pearson(dx.data_ptr(), params["u"].data_ptr(), dy.data_ptr(),
+                                params["r"].data_ptr(), rows, w.cols, DT[w.dtype], w.eps, plan,
+                                wptr, wbytes, s)
     wt = params.get("weight")
     if w.op == wl.WEIGHTED_STD:
         return C.credit_weighted_std(dx.data_ptr(), dy.data_ptr(), rows, w.cols, DT[w.dtype],
@@ -101,6 +111,17 @@ def run(w: wl.Workload, inputs: dict, plan, in_place=False):
         torch.cuda.synchronize()
         assert C.credit_get_device_error(torch.cuda.current_device()) == C.OK
         return dq.cpu().numpy(), params["scales"].cpu().numpy()
+    if w.op == wl.PEARSON:
+        rows = inputs["x"].shape[0]
+        params["r"] = torch.full((rows,), 7.0, dtype=torch.float32, device=dx.device)
+        dy = {False: None, True: dx, "x": dx, "u": params["u"]}[in_place]
+        if dy is None:
+            dy = torch.empty_like(dx)
+        st = call(w, dx, dy, params, plan, rows=rows)
+        assert st == C.OK, C.status_string(st)
+        torch.cuda.synchronize()
+        assert C.credit_get_device_error(torch.cuda.current_device()) == C.OK
+        return to_host(dy), params["r"].cpu().numpy()
     dy = dx if in_place else torch.empty_like(dx)
     st = call(w, dx, dy, params, plan, rows=inputs["x"].shape[0])
     assert st == C.OK, C.status_string(st)
@@ -163,3 +184,37 @@ def check_quant(got, inputs: dict, rows=None):
     assert np.array_equal(s.view(np.uint32), so.view(np.uint32)), "scales differ"
     bad = np.argwhere(q != qo)
     assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[0]}: {q[tuple(bad[0])]} vs {qo[tuple(bad[0])]}"
+
+
+PEARSON_CANCEL = 1e-5
+R_ATOL = 1e-5
+
+
+def check_pearson(w: wl.Workload, got, inputs: dict, rows=None, scale=1.0) -> dict:
+    """Compare GPU (y, r) with the oracle's; assert the stated tolerances."""
+    y, r = got
+    x = inputs["x"] if rows is None else inputs["x"][rows]
+    u = inputs["u"] if rows is None else inputs["u"][rows]
+    want, rw = oracle.pearson(x, u, eps=w.eps)
+    g = oracle.widen(y if rows is None else y[rows])
+    rg = (r if rows is None else r[rows]).astype(np.float64)
+    xw, uw = oracle.widen(x), oracle.widen(u)
+    mx, mu = xw.mean(axis=1, keepdims=True), uw.mean(axis=1, keepdims=True)
+    sx = np.sqrt(((xw - mx) ** 2).mean(axis=1, keepdims=True) + w.eps)
+    su = np.sqrt(((uw - mu) ** 2).mean(axis=1, keepdims=True) + w.eps)
+    zx, zu = (xw - mx) / sx, (uw - mu) / su
+    err = np.abs(g - want)
+    rms_x = np.sqrt((xw ** 2).mean(axis=1, keepdims=True))
+    rms_u = np.sqrt((uw ** 2).mean(axis=1, keepdims=True))
+    bound = RTOL[w.dtype] * scale * np.abs(want) + PEARSON_CANCEL * scale * (
+        np.abs(zu) * (np.abs(zx) + rms_x / sx) + np.abs(zx) * (np.abs(zu) + rms_u / su))
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(
+            f"{w.name}: {int(bad.sum())} of {err.size} outputs out of tolerance; worst at {i}: "
+            f"got {g[i]!r} want {want[i]!r} err {err[i]:.3e} bound {bound[i]:.3e}")
+    rerr = np.abs(rg - rw)
+    assert (rerr <= R_ATOL * scale).all(), \
+        f"{w.name}: r differs by {rerr.max():.3e} at row {int(np.argmax(rerr))}"
+    return {"max_r_err": float(rerr.max()), "n": int(err.size)}

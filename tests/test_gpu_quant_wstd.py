@@ -53,6 +53,15 @@ def test_quantize_zero_rows_and_constant_rows():
         check_quant((q, s), inp)
 
 
+def test_quantize_more_rows_than_one_launch_grid():
+    # the two-pass grid holds 65535 rows: later batches offset the int8 codes
+    # by one byte per element and the scales by one per row
+    w = wl.Workload("quantize_f32_70000x16", wl.QUANTIZE, "f32", 70000, 16, seed=64)
+    inp = w.generate()
+    check_quant(run(w, inp, make_plan(w, C.TWO_PASS)), inp)
+    check_quant(run(w, inp, make_plan(w, C.CLUSTER, 1)), inp)
+
+
 def test_quantize_rejects_overlap():
     x = torch.zeros(4, 4096, device="cuda")
     s = torch.zeros(4, device="cuda")
