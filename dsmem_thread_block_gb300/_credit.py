@@ -120,6 +120,8 @@ SIGNATURES = {
     "credit_plan_profiled": (_i32, [_i32, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
                                     ctypes.POINTER(Plan), ctypes.POINTER(ModelReport)]),
     "credit_status_string": (ctypes.c_char_p, [_i32]),
+    "credit_stage_copy_rate": (_i32, [_i32, _i32, _i32, ctypes.POINTER(ctypes.c_double),
+                                      ctypes.POINTER(ctypes.c_int32)]),
     "credit_get_device_error": (_i32, [_i32]),
     "credit_selftest_wait_timeout": (_i32, [_i32, _i64]),
     "credit_version": (ctypes.c_char_p, []),
@@ -278,6 +280,14 @@ def credit_plan_profiled(op: int, rows: int, cols: int, dtype: int, param_dtype:
     _check(load().credit_plan_profiled(op, rows, cols, dtype, param_dtype, device, runs, tune,
                                        ctypes.byref(p), ctypes.byref(r)), "credit_plan_profiled")
     return p, r
+
+
+def credit_stage_copy_rate(device: int, ctas_per_sm: int, runs: int = 7):
+    """(GB/s, resident CTAs per SM) of the staged-copy primitive."""
+    g, k = ctypes.c_double(), ctypes.c_int32()
+    _check(load().credit_stage_copy_rate(device, ctas_per_sm, runs, ctypes.byref(g),
+                                         ctypes.byref(k)), "credit_stage_copy_rate")
+    return g.value, k.value
 
 
 def credit_get_device_error(device: int) -> int:

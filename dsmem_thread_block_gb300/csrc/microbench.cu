@@ -200,6 +200,57 @@ __global__ void control_kernel(int rows_per_cluster, int barriers) {
             else __syncthreads();
 }
 
+// The staged-copy primitive: every CTA moves one footprint of bytes HBM ->
+// shared memory (non-multicast bulk copies, one mbarrier per 16 KiB chunk),
+// reads it back once chunk by chunk as it lands (a fold standing in for the
+// statistics pass), meets at a block barrier (the partial), then reads it a
+// second time and stores it to HBM (streaming 16-byte stores): the data
+// movement and shared-memory passes of a one-pass reduce-reuse CTA without
+// its arithmetic or exchange.  The footprint sets how many CTAs share an SM,
+// so its rate at k CTAs per SM is the measured streaming rate of that
+// residency.
+constexpr int kStageChunk = 16384;
+__global__ void __launch_bounds__(256) stage_copy_kernel(const unsigned char* src,
+                                                         unsigned char* dst, int footprint,
+                                                         unsigned* err) {
+    extern __shared__ __align__(128) unsigned char buf[];
+    __shared__ __align__(8) uint64_t bar[kMaxChunks];
+    const int nch = footprint / kStageChunk;
+    const int64_t base = (int64_t)blockIdx.x * footprint;
+    if (threadIdx.x == 0) {
+        for (int c = 0; c < nch; ++c) mbar_init(smem_u32(&bar[c]), 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        const uint64_t pol = l2_policy_evict_first();
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t b = smem_u32(&bar[c]);
+            mbar_arrive_expect_tx(b, (uint32_t)kStageChunk);
+            bulk_g2s(smem_u32(buf) + (uint32_t)(c * kStageChunk), src + base + (int64_t)c * kStageChunk,
+                     (uint32_t)kStageChunk, b, pol);
+        }
+    }
+    __syncthreads();
+    uint32_t fold = 0;
+    for (int c = 0; c < nch; ++c) {
+        mbar_wait_bounded(smem_u32(&bar[c]), 0, err);
+        const unsigned char* s = buf + c * kStageChunk;
+        for (int v = threadIdx.x; v < kStageChunk / 16; v += blockDim.x) {
+            const uint4 q = lds16(s + v * 16);
+            fold += q.x ^ q.y ^ q.z ^ q.w;
+        }
+    }
+    // keeps the fold live (footprint is never negative, which the compiler
+    // cannot know)
+    if (footprint < 0) err[1] = fold;
+    __syncthreads();
+    for (int c = 0; c < nch; ++c) {
+        const unsigned char* s = buf + c * kStageChunk;
+        unsigned char* d = dst + base + (int64_t)c * kStageChunk;
+        for (int v = threadIdx.x; v < kStageChunk / 16; v += blockDim.x)
+            stg16_stream(d + (int64_t)v * 16, lds16(s + v * 16));
+    }
+}
+
 cudaError_t launch_cluster_kernel(const void* fn, int P, int ctas, int threads, size_t smem,
                                   void** args, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -366,4 +417,73 @@ extern "C" credit_status_t credit_control_time(int device, int64_t nclusters, in
     cudaSetDevice(old);
     if (status == CREDIT_OK) *median_us = median(t);
     return status;
+}
+
+extern "C" credit_status_t credit_stage_copy_rate(int device, int ctas_per_sm, int runs,
+                                                  double* gbps, int* resident) {
+    if (!gbps || ctas_per_sm < 1 || ctas_per_sm > 8 || runs < 1 || runs > 1000)
+        return CREDIT_ERR_INVALID_ARG;
+    const DevInfo* d = device_info(device);
+    if (!d) return CREDIT_ERR_CUDA;
+    const KernelInfo* ki = kernel_info(device, (const void*)stage_copy_kernel, false);
+    if (!ki) return CREDIT_ERR_CUDA;
+    // the largest whole number of 16 KiB chunks that lets ctas_per_sm CTAs
+    // share an SM's shared memory
+    const int64_t per_cta = (int64_t)d->smem_per_sm / ctas_per_sm - ki->static_smem - d->reserved_smem;
+    int64_t fp = std::min<int64_t>(per_cta, ki->max_dyn_smem) / kStageChunk * kStageChunk;
+    fp = std::min<int64_t>(fp, (int64_t)kMaxChunks * kStageChunk);
+    if (fp < kStageChunk) return CREDIT_ERR_NO_LEGAL_PLAN;
+    int old = 0;
+    if (cudaGetDevice(&old) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
+    struct Restore { int d; ~Restore() { cudaSetDevice(d); } } restore{old};
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, stage_copy_kernel, 256, (size_t)fp) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
+    if (resident) *resident = occ;
+    const int64_t ctas = std::max<int64_t>((int64_t)4 * occ * d->sms, ((int64_t)512 << 20) / fp);
+    const int64_t bytes = ctas * fp;
+    unsigned* err = device_error_word();
+    if (!err) return CREDIT_ERR_CUDA;
+    void* src = nullptr;
+    void* dst = nullptr;
+    if (cudaMalloc(&src, (size_t)bytes) != cudaSuccess || cudaMalloc(&dst, (size_t)bytes) != cudaSuccess ||
+        cudaMemset(src, 0, (size_t)bytes) != cudaSuccess) {
+        cudaGetLastError();
+        if (src) cudaFree(src);
+        if (dst) cudaFree(dst);
+        return CREDIT_ERR_CUDA;
+    }
+    credit_status_t status = CREDIT_OK;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    std::vector<double> t;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) status = CREDIT_ERR_CUDA;
+    int fpi = (int)fp;
+    const unsigned char* s = static_cast<const unsigned char*>(src);
+    unsigned char* dd = static_cast<unsigned char*>(dst);
+    for (int r = 0; status == CREDIT_OK && r < runs + 1; ++r) {  // run 0 warms up
+        float ms = 0.f;
+        if (cudaEventRecord(e0, 0) != cudaSuccess) { status = CREDIT_ERR_CUDA; break; }
+        stage_copy_kernel<<<(unsigned)ctas, 256, (size_t)fp>>>(s, dd, fpi, err);
+        if (cudaGetLastError() != cudaSuccess || cudaEventRecord(e1, 0) != cudaSuccess ||
+            cudaEventSynchronize(e1) != cudaSuccess || cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) {
+            cudaGetLastError();
+            status = CREDIT_ERR_CUDA;
+            break;
+        }
+        if (r > 0) t.push_back(1e3 * ms);
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaFree(src);
+    cudaFree(dst);
+    if (status != CREDIT_OK) return status;
+    if (credit_get_device_error(device) != CREDIT_OK) return CREDIT_ERR_DEVICE_TIMEOUT;
+    *gbps = 2.0 * (double)bytes / median(t) / 1e3;  // bytes / us / 1e3 = GB/s
+    return CREDIT_OK;
 }

@@ -2,7 +2,8 @@
 
 Measures, on one GPU, the cluster-barrier round trip, the replicated-push
 exchange and the st.async exchange (deposits counted on each receiver's
-mbarrier, no cluster barrier) for every cluster size 2..16, remote and local shared-memory load
+mbarrier, no cluster barrier) for every cluster size 2..16, the staged-copy
+rate (HBM -> shared memory -> HBM, bulk copies) at 1..8 CTAs per SM, remote and local shared-memory load
 latency (pointer chase), and remote / local 16-byte load and store throughput
 of one CTA, each as the median of 15 launches (CREDIT summary page, "C.
 Positioning": latency, throughput and repeated cluster-synchronisation
@@ -32,6 +33,10 @@ def run_suite(device: int = 0, runs: int = 15, sizes=range(2, 17)) -> dict:
                               ("local_store_bw", C.BENCH_LOCAL_STORE_BW, 64),
                               ("local_load_bw", C.BENCH_LOCAL_LOAD_BW, 64)):
         out[name] = C.credit_bench_dsmem(device, kind, 2, iters, runs).as_dict()
+    out["stage_copy"] = {}
+    for k in (1, 2, 3, 4, 6, 8):
+        g, res = C.credit_stage_copy_rate(device, k, min(runs, 7))
+        out["stage_copy"][k] = {"gbps": g, "resident": res}
     return out
 
 

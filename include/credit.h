@@ -359,12 +359,29 @@ typedef struct {
 } credit_model_report_t;
 
 /*
- * Run the DSMEM microbenchmarks the cost model uses (cluster barrier and
- * replicated push for P = 2..16, median of `runs`) on `device` and keep the
- * profile in memory.  If profile_path is not NULL the profile is also written
- * there as JSON.  Synchronises the device; allocates a few bytes.
+ * Run the DSMEM microbenchmarks the cost model uses (cluster barrier,
+ * replicated push and st.async exchange for P = 2..16, median of `runs`) on
+ * `device` and keep the profile in memory.  If profile_path is not NULL the
+ * profile is also written there as JSON.  Synchronises the device; allocates
+ * a few bytes.
  */
 credit_status_t credit_calibrate(int device, int runs, const char *profile_path);
+
+/*
+ * The staged-copy primitive: every CTA moves one footprint of bytes from HBM
+ * into its shared memory (non-multicast bulk copies, an mbarrier per 16 KiB),
+ * folds it once as the chunks land, meets at a block barrier, and reads it
+ * again to store it back to HBM with streaming stores -- a one-pass
+ * reduce-reuse CTA's data movement and shared-memory passes without its
+ * arithmetic or exchange.  The footprint is the largest multiple of
+ * 16 KiB that lets `ctas_per_sm` (1..8) CTAs share an SM, the grid moves at
+ * least 512 MiB, and *gbps is (bytes read + written) / median time of `runs`
+ * launches (CUDA events).  *resident (may be NULL) receives the CTAs per SM
+ * the occupancy calculator reports for that footprint.  Allocates and frees
+ * the buffers; synchronises the device.
+ */
+credit_status_t credit_stage_copy_rate(int device, int ctas_per_sm, int runs,
+                                       double *gbps, int *resident);
 
 /*
  * Apply the cost model to one shape on `device` (calibrating first if

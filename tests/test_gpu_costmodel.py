@@ -51,3 +51,19 @@ def test_small_sweep_picks_near_best():
     s = sweep.summarize(pts)
     assert 0.0 <= s["pick_accuracy"] <= 1.0
     torch.cuda.synchronize()
+
+
+def test_stage_copy_rate_residency_and_bounds():
+    # the staged-copy primitive: the footprint sets the residency asked for;
+    # bulk-copy staging streams near the copy roofline at any residency (the
+    # measured spread from one to eight CTAs per SM is a few percent)
+    rates = {}
+    for k in (1, 3, 8):
+        g, res = C.credit_stage_copy_rate(0, k, 3)
+        assert res == k, (k, res)
+        assert 3000.0 < g < 9000.0
+        rates[k] = g
+    assert min(rates.values()) > 0.8 * max(rates.values())
+    with pytest.raises(C.CreditError):
+        C.credit_stage_copy_rate(0, 9, 3)
+    torch.cuda.synchronize()
