@@ -313,9 +313,9 @@ credit_status_t credit_control_time(int device, int64_t nclusters,
 
 /* ------------------------------------------------------------------------
  * Profitability cost model (CREDIT "D. Profitability and Candidate
- * Selection").  For one shape it times the non-DSMEM baseline once -- the
- * one-CTA-per-row local-staging kernel when a row fits one CTA's shared
- * memory, else the two-pass global re-read pair -- times the work-free
+ * Selection").  For one shape it times the non-DSMEM baseline -- the faster
+ * of the one-CTA-per-row local-staging kernel (when a row fits one CTA's
+ * shared memory) and the two-pass global re-read pair -- times the work-free
  * control kernel of every legal clustered candidate and of the baseline, and
  * predicts
  *     T_CREDIT(P) = T_base - (B_base - B_credit) / R_base + T_ctrl(P) + T_comm(P)
