@@ -53,6 +53,35 @@ struct Scratch {
     }
 };
 
+// Timing inputs: values spread uniformly over [lo, hi) from an integer hash
+// of the index (Wellons' "lowbias32" mixer), so the kernels are timed on
+// varied data -- constant zeros would skip work (an all-zero quantization row
+// divides nothing; a constant softmax row never rescales).
+__device__ __forceinline__ uint32_t mix32(uint32_t x) {
+    x ^= x >> 16;
+    x *= 0x7feb352du;
+    x ^= x >> 15;
+    x *= 0x846ca68bu;
+    x ^= x >> 16;
+    return x;
+}
+
+__global__ void fill_kernel(void* p, int64_t n, int bf16, float lo, float hi, uint32_t seed) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const uint32_t h = mix32((uint32_t)i ^ mix32((uint32_t)(i >> 32) ^ seed));
+        const float v = lo + (hi - lo) * (float)(h >> 8) * (1.0f / 16777216.0f);
+        if (bf16) static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+        else static_cast<float*>(p)[i] = v;
+    }
+}
+
+bool fill(void* p, int64_t n, credit_dtype_t dt, float lo, float hi, uint32_t seed) {
+    if (!p || n == 0) return true;
+    fill_kernel<<<1024, 256>>>(p, n, dt == CREDIT_BF16 ? 1 : 0, lo, hi, seed);
+    return cudaGetLastError() == cudaSuccess;
+}
+
 double median_of(std::vector<double> v) {
     std::sort(v.begin(), v.end());
     const size_t n = v.size();
@@ -232,6 +261,16 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         (!pearson && param_dtype >= 0 && (!g.alloc(pbytes) || !b.alloc(pbytes))))
         return CREDIT_ERR_CUDA;
     if (!ws.alloc((size_t)reread.workspace_bytes)) return CREDIT_ERR_CUDA;
+    const int64_t nmat = rows * cols;
+    const credit_dtype_t pdt = param_dtype == CREDIT_BF16 ? CREDIT_BF16 : CREDIT_F32;
+    if (!fill(x.p, nmat, dtype, -2.f, 2.f, 1u) ||
+        (pearson && !fill(g.p, nmat, dtype, -2.f, 2.f, 2u)) ||
+        (!pearson && param_dtype >= 0 &&
+         (!fill(g.p, cols, pdt, 0.5f, 1.5f, 3u) || !fill(b.p, cols, pdt, -0.5f, 0.5f, 4u))) ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
 
     double t_base = 0.0;
     float* auxp = static_cast<float*>(aux.p);
