@@ -178,6 +178,93 @@ __device__ __forceinline__ float block_allreduce(float v, float* buf, F f, float
     return r;
 }
 
+// ---------------------------------------------------------- int8 codes
+// Quantization code of x for the row scale s: round-half-even of the IEEE
+// single quotient fl(x / s), clamped to +-127 -- without a division per
+// element.  q = x * fl(1 / s) differs from fl(x / s) by at most 3 * 2^-24 |x/s|
+// (< 2^-14 for |x / s| <= 128), so rint(q) is the code unless q lies within
+// 2^-14 of a half-integer b.  There the exact residual x - b s, computed by
+// one fused multiply-add (exact, since x and b s agree to within s 2^-13 and
+// b carries 9 significant bits), places fl(x / s) against b: above or below
+// by more than half the float spacing on that side of b, or equal to b
+// (ties to even) -- the exact-remainder technique for correctly rounded
+// quotients (Markstein; Boldo and Muller on the exactness of FMA
+// remainders).  Scales outside [2^-90, 2^100], where those products could
+// leave the normal range, use the division.
+__device__ __forceinline__ float quant_inv(float s) {
+    return (s >= 0x1p-90f && s <= 0x1p+100f) ? 1.f / s : 0.f;  // 0: divide per element
+}
+
+static __device__ __noinline__ float quant_near_half(float x, float s, float k, float d) {
+    const float b = k + (d > 0.f ? 0.5f : -0.5f);  // the half-integer next to q (exact)
+    const float rho = fmaf(-b, s, x);               // x - b s, exact
+    const float away = b > 0.f ? rho : -rho;        // > 0: |x / s| beyond |b|
+    const float ab = fabsf(b);
+    float h_away, h_toward;                         // half the float spacing beside b
+    if (ab == 0.5f) {
+        h_away = 0x1p-25f;
+        h_toward = 0x1p-26f;
+    } else {
+        h_away = h_toward = __int_as_float(__float_as_int(ab) & 0x7f800000) * 0x1p-24f;
+    }
+    const float out = b > 0.f ? 0.5f : -0.5f;
+    if (away > s * h_away) return b + out;           // fl(x / s) beyond b
+    if (away < -(s * h_toward)) return b - out;      // fl(x / s) short of b
+    return rintf(b);                                 // fl(x / s) == b: ties to even
+}
+
+// The codes of N values at once, packed four to a 32-bit word (byte e of
+// word e / 4): the reciprocal path for all of them and a single branch to the
+// exact resolution when any quotient lies near a half-integer.
+template <int N>
+__device__ __forceinline__ void quant_codes(const float (&x)[N], float s, float inv,
+                                            uint32_t (&w)[N / 4]) {
+    constexpr float kNear = 0.5f - 0x1p-14f;
+    float c[N];
+    if (inv != 0.f) {
+        float d[N];
+        bool near = false;
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            const float q = x[e] * inv;
+            c[e] = rintf(q);
+            d[e] = q - c[e];
+            near |= fabsf(d[e]) >= kNear;
+        }
+        if (near) {
+#pragma unroll
+            for (int e = 0; e < N; ++e)
+                if (fabsf(d[e]) >= kNear) c[e] = quant_near_half(x[e], s, c[e], d[e]);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < N; ++e) c[e] = s == 0.f ? 0.f : rintf(__fdiv_rn(x[e], s));
+    }
+    int v[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = max(-127, min(127, __float2int_rn(c[e])));
+#pragma unroll
+    for (int k = 0; k < N / 4; ++k) {
+        const uint32_t lo = __byte_perm((uint32_t)v[4 * k], (uint32_t)v[4 * k + 1], 0x0040);
+        const uint32_t hi = __byte_perm((uint32_t)v[4 * k + 2], (uint32_t)v[4 * k + 3], 0x0040);
+        w[k] = __byte_perm(lo, hi, 0x5410);
+    }
+}
+
+__device__ __forceinline__ int quant_code(float x, float s, float inv) {
+    if (s == 0.f) return 0;
+    float c;
+    if (inv == 0.f) {
+        c = rintf(__fdiv_rn(x, s));
+    } else {
+        const float q = x * inv;
+        c = rintf(q);
+        const float d = q - c;
+        if (fabsf(d) >= 0.5f - 0x1p-14f) c = quant_near_half(x, s, c, d);
+    }
+    return max(-127, min(127, __float2int_rn(c)));
+}
+
 // Bounded mbarrier wait: spins on try_wait; after kWaitLimitNs sets the
 // device error word and returns false (the caller carries on so that every
 // cluster barrier is still reached).

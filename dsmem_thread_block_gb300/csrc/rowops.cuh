@@ -291,6 +291,7 @@ struct OutputMap {
                                          float eps) {
         if constexpr (OP == kQuant) {
             c0 = st0 / 127.f;  // the row scale (IEEE division)
+            c1 = quant_inv(c0);
         } else if constexpr (OP == kWStd) {
             const float r = 1.f / sqrtf(fmaxf(st0 > 0.f ? st2 / st0 : 0.f, 0.f) + eps);
             c0 = r;
@@ -307,11 +308,7 @@ struct OutputMap {
         }
     }
     // int8 code of x (quantization): round half to even of x / scale, clamped
-    __device__ __forceinline__ int code(float x) const {
-        if (c0 == 0.f) return 0;
-        const int q = __float2int_rn(__fdiv_rn(x, c0));
-        return max(-127, min(127, q));
-    }
+    __device__ __forceinline__ int code(float x) const { return quant_code(x, c0, c1); }
     __device__ __forceinline__ F2 operator()(F2 x, F2 g, F2 b) const {
         if constexpr (OP == kWStd) {
             return fma2(x, f2(c0), f2(c1));
@@ -765,15 +762,11 @@ __device__ __forceinline__ void output_quant_rows(const OutputMap<kQuant, T> (&h
             if (i < rows) {
                 F2 p[NP];
                 Pairs<T>::unpack(lds16(base + (size_t)i * pitch + (size_t)v * 16), p);
-                uint32_t w[NP / 2];
+                float xf[2 * NP];
 #pragma unroll
-                for (int k = 0; k < NP / 2; ++k) {
-                    const uint32_t b0 = (uint32_t)(h[i].code(p[2 * k].x) & 0xff);
-                    const uint32_t b1 = (uint32_t)(h[i].code(p[2 * k].y) & 0xff);
-                    const uint32_t b2 = (uint32_t)(h[i].code(p[2 * k + 1].x) & 0xff);
-                    const uint32_t b3 = (uint32_t)(h[i].code(p[2 * k + 1].y) & 0xff);
-                    w[k] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-                }
+                for (int k = 0; k < NP; ++k) { xf[2 * k] = p[k].x; xf[2 * k + 1] = p[k].y; }
+                uint32_t w[NP / 2];
+                quant_codes<2 * NP>(xf, h[i].c0, h[i].c1, w);
                 if constexpr (NP == 2) __stcs(reinterpret_cast<unsigned int*>(qrow[i]) + v, w[0]);
                 else __stcs(reinterpret_cast<uint2*>(qrow[i]) + v, make_uint2(w[0], w[1]));
             }

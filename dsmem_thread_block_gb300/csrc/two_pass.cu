@@ -185,17 +185,26 @@ two_pass_apply(const TwoPassArgs a) {
     r.load(xs, n, threadIdx.x, blockDim.x);
     if constexpr (OP == kQuant) {
         int8_t* qs = static_cast<int8_t*>(a.y) + row * a.cols + j0;
+        const float inv = quant_inv(c0);
         constexpr int kV = Elem<T>::kVec;
 #pragma unroll
         for (int k = 0; k < kTwoPassVpt; ++k) {
             const int64_t e0 = ((int64_t)k * blockDim.x + threadIdx.x) * kV;
+            if constexpr (VEC_PATH) {
+                // whole vectors: kV codes packed into 4 or 8 bytes
+                if (e0 < n) {
+                    float xf[kV];
 #pragma unroll
-            for (int i = 0; i < kV; ++i) {
-                if (e0 + i < n) {
-                    int qv = 0;
-                    if (c0 != 0.f) qv = max(-127, min(127, __float2int_rn(__fdiv_rn(r.f[k * kV + i], c0))));
-                    qs[e0 + i] = (int8_t)qv;
+                    for (int i = 0; i < kV; ++i) xf[i] = r.f[k * kV + i];
+                    uint32_t w[kV / 4];
+                    quant_codes<kV>(xf, c0, inv, w);
+                    if constexpr (kV == 4) __stcs(reinterpret_cast<unsigned int*>(qs + e0), w[0]);
+                    else __stcs(reinterpret_cast<uint2*>(qs + e0), make_uint2(w[0], w[1]));
                 }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kV; ++i)
+                    if (e0 + i < n) qs[e0 + i] = (int8_t)quant_code(r.f[k * kV + i], c0, inv);
             }
         }
         return;

@@ -53,6 +53,41 @@ def test_quantize_zero_rows_and_constant_rows():
         check_quant((q, s), inp)
 
 
+def _near_half_row(amax, cols, rng):
+    """A row whose maximum is `amax` and whose other entries sit on and next
+    to the products b * s for half-integers b (s = amax / 127 in IEEE
+    single): the values where rounding x / s to an integer is decided by the
+    last bit of the quotient."""
+    f32 = np.float32
+    s = f32(f32(amax) / f32(127.0))
+    vals = [f32(amax)]
+    for b in np.arange(-126, 127) + 0.5:
+        v = f32(f32(b) * s)
+        vals.append(v)
+        up = dn = v
+        for _ in range(3):
+            up = np.nextafter(up, f32(np.inf))
+            dn = np.nextafter(dn, f32(-np.inf))
+            vals += [up, dn]
+    row = np.array(vals, np.float32)
+    row = row[np.abs(row) <= f32(amax)]
+    out = rng.uniform(-amax, amax, cols).astype(np.float32)
+    out[:len(row)] = row[:cols]
+    return out
+
+
+def test_quantize_codes_decided_by_the_last_quotient_bit():
+    # every near-half-integer quotient must round exactly as the IEEE
+    # division does (including ties to even at s = 1), on both kernel arms
+    rng = np.random.default_rng(65)
+    amaxes = [1.0, 3.7, 127.0, 1e-20, 2.5e30, 0.01, 1e-30, 6.1e-34]
+    x = np.stack([_near_half_row(a, 2048, rng) for a in amaxes])
+    w = wl.Workload("quantize_f32_8x2048_near_half", wl.QUANTIZE, "f32", len(amaxes), 2048, seed=66)
+    inp = {"x": x}
+    for p in _plans(w):
+        check_quant(run(w, inp, p), inp)
+
+
 def test_quantize_more_rows_than_one_launch_grid():
     # the two-pass grid holds 65535 rows: later batches offset the int8 codes
     # by one byte per element and the scales by one per row
