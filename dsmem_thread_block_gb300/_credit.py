@@ -65,6 +65,14 @@ class Candidate(ctypes.Structure):
                 ("persistent_us", ctypes.c_double)]
 
 
+class HostCall(ctypes.Structure):
+    """Mirror of credit_host_call_t."""
+    _fields_ = [("op", ctypes.c_int32), ("dtype", ctypes.c_int32), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("x", ctypes.c_void_p), ("u", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("row_out", ctypes.c_void_p), ("p0", ctypes.c_void_p),
+                ("p1", ctypes.c_void_p), ("param_dtype", ctypes.c_int32), ("eps", ctypes.c_float)]
+
+
 class ModelReport(ctypes.Structure):
     """Mirror of credit_model_report_t."""
     _fields_ = [("baseline_variant", ctypes.c_int32), ("model_cluster_size", ctypes.c_int32),
@@ -122,6 +130,10 @@ SIGNATURES = {
     "credit_status_string": (ctypes.c_char_p, [_i32]),
     "credit_stage_copy_rate": (_i32, [_i32, _i32, _i32, ctypes.POINTER(ctypes.c_double),
                                       ctypes.POINTER(ctypes.c_int32)]),
+    "credit_host_buffer_bytes": (_i32, [ctypes.POINTER(HostCall), ctypes.POINTER(Plan), _i64,
+                                        ctypes.POINTER(ctypes.c_size_t)]),
+    "credit_run_host": (_i32, [ctypes.POINTER(HostCall), ctypes.POINTER(Plan), _vp, _sz, _i64,
+                               _vp]),
     "credit_get_device_error": (_i32, [_i32]),
     "credit_selftest_wait_timeout": (_i32, [_i32, _i64]),
     "credit_version": (ctypes.c_char_p, []),
@@ -288,6 +300,27 @@ def credit_stage_copy_rate(device: int, ctas_per_sm: int, runs: int = 7):
     _check(load().credit_stage_copy_rate(device, ctas_per_sm, runs, ctypes.byref(g),
                                          ctypes.byref(k)), "credit_stage_copy_rate")
     return g.value, k.value
+
+
+def host_call(op: int, dtype: int, rows: int, cols: int, x: int, y: int, u: int = 0,
+              row_out: int = 0, p0: int = 0, p1: int = 0, param_dtype: int = F32,
+              eps: float = 0.0) -> HostCall:
+    return HostCall(op=op, dtype=dtype, rows=rows, cols=cols, x=x or None, u=u or None,
+                    y=y or None, row_out=row_out or None, p0=p0 or None, p1=p1 or None,
+                    param_dtype=param_dtype, eps=eps)
+
+
+def credit_host_buffer_bytes(call: HostCall, plan=None, rows_per_chunk: int = 1) -> int:
+    n = ctypes.c_size_t()
+    _check(load().credit_host_buffer_bytes(ctypes.byref(call), _plan_ptr(plan), rows_per_chunk,
+                                           ctypes.byref(n)), "credit_host_buffer_bytes")
+    return n.value
+
+
+def credit_run_host(call: HostCall, plan, device_buffer: int, device_buffer_bytes: int,
+                    rows_per_chunk: int, stream: int = 0) -> int:
+    return load().credit_run_host(ctypes.byref(call), _plan_ptr(plan), device_buffer or None,
+                                  device_buffer_bytes, rows_per_chunk, stream or None)
 
 
 def credit_get_device_error(device: int) -> int:

@@ -312,6 +312,53 @@ credit_status_t credit_control_time(int device, int64_t nclusters,
                                     double *median_us);
 
 /* ------------------------------------------------------------------------
+ * Host buffers.  An operator call whose x (and u), y and per-row results live
+ * in host memory, pipelined over chunks of rows: library-owned streams carry
+ * the host-to-device copies, the kernels and the device-to-host copies, and
+ * two device slots alternate between chunks, so the copies in both
+ * directions overlap each other and the kernels.  Host buffers should be
+ * pinned (cudaHostAlloc) for the copies to overlap; pageable memory works but
+ * serialises.  Parameter vectors (p0, p1) are device pointers (they are
+ * reused by every chunk).  The call is ordered on `stream` like the other
+ * calls: it starts after the stream's earlier work, the stream continues
+ * after the last output copy, and nothing waits on the host; the host buffers
+ * must stay valid until then.  Concurrent calls on one device share its
+ * pipeline streams and run one after the other.
+ */
+typedef struct {
+    credit_op_t op;
+    credit_dtype_t dtype;        /* of x, u and y (y is int8 for quantization) */
+    int64_t rows, cols;
+    const void *x;               /* host, rows x cols */
+    const void *u;               /* host, Pearson's second operand, else NULL */
+    void *y;                     /* host, rows x cols */
+    float *row_out;              /* host, per-row scales (quantization) or r
+                                    (Pearson), rows floats, else NULL */
+    const void *p0, *p1;         /* device gamma/beta, weight or weights, may be NULL */
+    credit_dtype_t param_dtype;
+    float eps;
+} credit_host_call_t;
+
+/* Device bytes credit_run_host needs for `rows_per_chunk`-row chunks (two
+ * slots of inputs and outputs, plus the two-pass workspace if `plan` is a
+ * TWO_PASS plan).  No CUDA call. */
+credit_status_t credit_host_buffer_bytes(const credit_host_call_t *call,
+                                         const credit_plan_t *plan,
+                                         int64_t rows_per_chunk, size_t *bytes);
+
+/* Run `call` over chunks of rows_per_chunk rows (the last may be shorter)
+ * with `plan` (not NULL; e.g. credit_plan or credit_plan_profiled for the
+ * chunk's shape -- each chunk re-derives it for its row count), using the
+ * caller's 256-byte-aligned device_buffer of at least
+ * credit_host_buffer_bytes bytes.  Returns CREDIT_ERR_INVALID_ARG for missing
+ * pointers or a short buffer; otherwise the status of the first failing
+ * chunk, if any. */
+credit_status_t credit_run_host(const credit_host_call_t *call,
+                                const credit_plan_t *plan, void *device_buffer,
+                                size_t device_buffer_bytes,
+                                int64_t rows_per_chunk, void *stream);
+
+/* ------------------------------------------------------------------------
  * Profitability cost model (CREDIT "D. Profitability and Candidate
  * Selection").  For one shape it times the non-DSMEM baseline -- the faster
  * of the one-CTA-per-row local-staging kernel (when a row fits one CTA's

@@ -87,3 +87,23 @@ def test_library_fails_loudly_when_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(C, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         C.load()
+
+
+def test_host_buffer_layout_needs_no_gpu(lib):
+    # two slots of (x, y) rounded to 256 bytes; Pearson adds u and r, and
+    # quantization's output is int8 plus a scale per row
+    ln = C.host_call(C.LAYERNORM, C.BF16, 1000, 4096, x=16, y=32)
+    assert C.credit_host_buffer_bytes(ln, None, 128) == 2 * (2 * 128 * 4096 * 2)
+    pe = C.host_call(C.PEARSON, C.F32, 1000, 100, x=16, y=32, u=48, row_out=64)
+    slot = 3 * (((10 * 100 * 4) + 255) // 256 * 256) + ((10 * 4 + 255) // 256 * 256)
+    assert C.credit_host_buffer_bytes(pe, None, 10) == 2 * slot
+    q = C.host_call(C.QUANTIZE, C.F32, 8, 4096, x=16, y=32, row_out=64)
+    assert C.credit_host_buffer_bytes(q, None, 8) == 2 * (8 * 4096 * 4 + 8 * 4096 + 256)
+    # argument checks before any CUDA call
+    plan = C.Plan(variant=C.CLUSTER, cluster_size=1)
+    assert C.credit_run_host(ln, None, 4096, 1 << 30, 128) == C.ERR_INVALID_ARG   # no plan
+    assert C.credit_run_host(ln, plan, 4096, 1024, 128) == C.ERR_INVALID_ARG      # short buffer
+    assert C.credit_run_host(ln, plan, 4096 + 16, 1 << 30, 128) == C.ERR_INVALID_ARG  # unaligned
+    assert C.credit_run_host(ln, plan, 4096, 1 << 30, 0) == C.ERR_INVALID_ARG     # no chunk
+    assert C.credit_run_host(C.host_call(C.PEARSON, C.F32, 4, 8, x=16, y=32, row_out=64), plan,
+                             4096, 1 << 30, 4) == C.ERR_INVALID_ARG                # no u
