@@ -218,6 +218,24 @@ def run_reference(args, w, rank: int):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ ranks
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's `x` (every rank calls this)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(bytes_per_rank_step: float, ms_per_step_max: float, world: int) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's step time
+    (replicas: each rank runs the full workload on its own GPU)."""
+    return bytes_per_rank_step * world / (ms_per_step_max * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -373,13 +391,10 @@ def main():
     clocks = sampler.summary(t_host0, t_host1)
     assert C.credit_get_device_error(dev) == C.OK
 
-    t = torch.tensor([ms_total], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms_total, world, "cuda")
     ms_step = ms_max / args.steps
     bytes_step = w.ideal_bytes()
-    value = bytes_step * world / (ms_step * 1e-3) / 1e9
+    value = job_rate(bytes_step, ms_step, world)
 
     # ---- end to end: pinned host buffers through credit_run_host, which
     # pipelines H2D copies, kernels and D2H copies over row chunks; the
@@ -423,10 +438,8 @@ def main():
                 raise C.CreditError(st, "credit_run_host")
         f1.record(stream)
     torch.cuda.synchronize()
-    te = torch.tensor([f0.elapsed_time(f1)], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = bytes_step * world / (float(te.item()) / e2e_steps * 1e-3) / 1e9
+    te = max_over_ranks(f0.elapsed_time(f1), world, "cuda")
+    e2e_value = job_rate(bytes_step, te / e2e_steps, world)
 
     peak, peak_kind = measured_peak()
     variant_key = {C.TWO_PASS: "two_pass", C.CLUSTER: f"cluster:{plan.cluster_size}",
