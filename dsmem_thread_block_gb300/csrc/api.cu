@@ -177,8 +177,8 @@ credit_status_t plan_from_request(int dev, credit_op_t op, int64_t rows, int64_t
     if (r.threads < 0 || r.ctas_per_sm < 0 || r.chunk_elems < 0 || r.rows_per_cluster < 0)
         return CREDIT_ERR_INVALID_ARG;
     const bool xok = r.exchange == CREDIT_EXCHANGE_DEFAULT ||
-                     (r.exchange == CREDIT_EXCHANGE_BARRIER && v != CREDIT_TWO_PASS) ||
-                     (r.exchange == CREDIT_EXCHANGE_ASYNC && v == CREDIT_CLUSTER);
+                     ((r.exchange == CREDIT_EXCHANGE_BARRIER || r.exchange == CREDIT_EXCHANGE_ASYNC) &&
+                      v != CREDIT_TWO_PASS);
     if (!xok) return CREDIT_ERR_INVALID_ARG;
     const bool pers = v == CREDIT_CLUSTER_PERSISTENT;
     const credit_status_t st =
@@ -264,6 +264,7 @@ credit_status_t run(const OpCall& c) {
         a.nclusters = plan.active_clusters;
         a.eps = c.eps;
         a.err = err;
+        a.exchange = plan.exchange == CREDIT_EXCHANGE_ASYNC ? 1 : 0;
         const void* fn = persistent_kernel(key);
         if (!kernel_info(dev, fn, true)) return CREDIT_ERR_CUDA;
         return from_cuda(launch_persistent(key, a, plan.cluster_size, plan.threads,

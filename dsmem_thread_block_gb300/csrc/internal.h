@@ -58,6 +58,7 @@ struct PersistArgs {
     int32_t nclusters;    // clusters in the grid
     float eps;
     unsigned* err;
+    int32_t exchange;     // 0: push + cluster barrier per row; 1: st.async deposits + mbarrier
 };
 
 constexpr int kPersistMaxSlots = 32;

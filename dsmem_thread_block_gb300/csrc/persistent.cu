@@ -41,6 +41,7 @@ cluster_persistent(const PersistArgs a) {
     __shared__ __align__(16) float red[2][2][(kPersistMaxThreads / 32) * 2];  // [row parity][stage]
     __shared__ __align__(8) uint64_t full_bar[kPersistMaxSlots];
     __shared__ __align__(8) uint64_t empty_bar[kPersistMaxSlots];
+    __shared__ __align__(8) uint64_t recv_bar[2];  // st.async exchange, by row parity
 
     const uint32_t P = cluster_nctarank();
     const uint32_t rank = cluster_ctarank();
@@ -60,6 +61,8 @@ cluster_persistent(const PersistArgs a) {
     const uint32_t slot_bytes = (uint32_t)a.chunk * (uint32_t)sizeof(T);
     const int64_t nrows = cid < a.rows ? (a.rows - 1 - cid) / a.nclusters + 1 : 0;
     const bool clustered = P > 1;
+    const bool async_x = clustered && a.exchange == 1;
+    const uint32_t xbytes = (P - 1) * 16u;  // the peers' deposits of one row
     // Row k of this CTA lives in row slot k mod NR: slots
     // [rs * cpr_full, rs * cpr_full + cpr), contiguous in shared memory; the
     // slot's use count is k div NR.  Both are tracked incrementally.
@@ -68,6 +71,14 @@ cluster_persistent(const PersistArgs a) {
         for (int s = 0; s < NR * cpr_full; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), (uint32_t)ncw);
+        }
+        if (async_x) {
+            // two arrivals per row: the expected bytes (posted here for rows
+            // 0 and 1, after each wait for row k + 2) and the local partial
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(smem_u32(&recv_bar[b]), 2);
+                if (b < nrows) mbar_arrive_expect_tx(smem_u32(&recv_bar[b]), xbytes);
+            }
         }
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -95,12 +106,16 @@ cluster_persistent(const PersistArgs a) {
             }
             if (++rs == NR) { rs = 0; ++use; }
             __syncwarp();
-            if (clustered) {
+            if (clustered && !async_x) {
                 cluster_wait_acquire();   // entry phase (k == 0) or row k-1
                 cluster_arrive_relaxed(); // row k
             }
         }
-        if (clustered) cluster_wait_acquire();  // last row (or the entry phase)
+        if (async_x) {
+            cluster_wait_acquire();       // the entry phase
+            cluster_arrive_relaxed();     // the exit phase
+        }
+        if (clustered) cluster_wait_acquire();  // last row (or the entry / exit phase)
         return;
     }
 
@@ -129,12 +144,29 @@ cluster_persistent(const PersistArgs a) {
         if (clustered) {
             if (k == 0) cluster_wait_acquire();  // every peer is running
             float* sl = slots[k & 1];
-            if (tid < (int)P) {
-                const uint32_t dst = mapa_shared(smem_u32(&sl[rank * kSlotStride]), (uint32_t)tid);
-                st_cluster_v4f32(dst, p0, p1, p2, 0.f);
+            if (async_x) {
+                // thread t deposits into peer t; thread `rank` stores locally
+                const uint32_t rb = smem_u32(&recv_bar[k & 1]);
+                if (tid == (int)rank) {
+                    float* d = &sl[rank * kSlotStride];
+                    d[0] = p0; d[1] = p1; d[2] = p2;
+                    mbar_arrive(rb);
+                } else if (tid < (int)P) {
+                    const uint32_t dst = mapa_shared(smem_u32(&sl[rank * kSlotStride]), (uint32_t)tid);
+                    st_async_v4f32(dst, p0, p1, p2, 0.f, mapa_shared(rb, (uint32_t)tid));
+                }
+                mbar_wait_bounded(rb, (uint32_t)(k >> 1) & 1u, a.err);
+                // this slot array's next row (k + 2) expects its deposits;
+                // no peer can deposit them before this CTA's row k + 1 partial
+                if (tid == 0 && k + 2 < nrows) mbar_arrive_expect_tx(rb, xbytes);
+            } else {
+                if (tid < (int)P) {
+                    const uint32_t dst = mapa_shared(smem_u32(&sl[rank * kSlotStride]), (uint32_t)tid);
+                    st_cluster_v4f32(dst, p0, p1, p2, 0.f);
+                }
+                cluster_arrive_release();
+                cluster_wait_acquire();
             }
-            cluster_arrive_release();
-            cluster_wait_acquire();
             combine_slots<OP>(sl, P, st0, st1, st2);
         }
 
@@ -152,6 +184,12 @@ cluster_persistent(const PersistArgs a) {
         if (++rs == NR) { rs = 0; ++use; }
     }
     if (clustered && nrows == 0) cluster_wait_acquire();  // entry phase
+    if (async_x) {
+        // every deposit addressed to this CTA has landed; stay until the
+        // whole cluster can say the same
+        cluster_arrive_relaxed();
+        cluster_wait_acquire();
+    }
 }
 
 // ----------------------------------------------------------- dispatch

@@ -80,8 +80,9 @@ typedef enum {
  *            and Reuse Protocol", Replicated Push + Synchronization)
  *   ASYNC    st.async 16-byte deposits whose bytes complete on the receiving
  *            CTA's mbarrier; each CTA waits for its own P - 1 deposits, and
- *            the cluster barrier moves to kernel exit (one-pass CLUSTER
- *            plans only; the planner's choice for them)
+ *            the cluster barrier moves to kernel exit (the planner's choice
+ *            for both clustered variants; the persistent kernel alternates
+ *            two mbarriers by row parity)
  */
 typedef enum {
     CREDIT_EXCHANGE_DEFAULT = 0,
@@ -109,9 +110,9 @@ typedef enum {
  *   rows_per_cluster rows one cluster stages and reduces together (CLUSTER:
  *                    1, 2 or 4; their partials share one exchange and each
  *                    parameter load serves all of them)
- *   exchange         credit_exchange_t: ASYNC for planned CLUSTER plans,
- *                    BARRIER for CLUSTER_PERSISTENT, DEFAULT for TWO_PASS; a
- *                    request may ask for BARRIER on a CLUSTER plan
+ *   exchange         credit_exchange_t: ASYNC for planned clustered plans,
+ *                    DEFAULT for TWO_PASS; a request may ask for BARRIER on
+ *                    either clustered variant
  *   pred_us          predicted time of this plan, microseconds (0 = none)
  *   pred_two_pass_us predicted / measured time of the two-pass baseline
  */

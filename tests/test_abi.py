@@ -72,11 +72,10 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     assert C.credit_rmsnorm(4096, 4100, 1, 64, C.F32, 0, C.F32, 1e-6) == C.ERR_INVALID_ARG
     assert lib.credit_plan(C.SOFTMAX, 4, 4, C.F32, 0, None) == C.ERR_INVALID_ARG
     assert lib.credit_plan_for(C.SOFTMAX, 4, 4, C.F32, 0, 9, 1, None) == C.ERR_INVALID_ARG
-    # the st.async exchange exists only for the one-pass clustered kernel
+    # exchanges exist only for the clustered kernels
     out = C.Plan()
     for variant, exchange in ((C.TWO_PASS, C.EXCHANGE_ASYNC), (C.TWO_PASS, C.EXCHANGE_BARRIER),
-                              (C.CLUSTER_PERSISTENT, C.EXCHANGE_ASYNC), (C.CLUSTER, 3),
-                              (C.CLUSTER, -1)):
+                              (C.CLUSTER_PERSISTENT, 3), (C.CLUSTER, 3), (C.CLUSTER, -1)):
         req = C.Plan(variant=variant, cluster_size=2, exchange=exchange)
         assert lib.credit_plan_with(C.SOFTMAX, 4, 4, C.F32, 0, ctypes.byref(req),
                                     ctypes.byref(out)) == C.ERR_INVALID_ARG

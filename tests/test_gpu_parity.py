@@ -8,6 +8,8 @@ and the edge cases: ragged widths (element-wise staging path), slices that are
 empty, a single row, in-place calls, misaligned pointers, absent parameters,
 bf16 parameters and constant rows.
 """
+import itertools
+
 import numpy as np
 import pytest
 import torch
@@ -233,17 +235,19 @@ def test_illegal_cluster_sizes_are_rejected():
 @pytest.mark.parametrize("rows", [1, 7, 300])
 def test_persistent_row_counts(rows):
     # fewer rows than resident clusters, a few rows per cluster, many rows
-    # per cluster (slot and ring reuse over many phases); one and two CTAs
-    # per SM
+    # per cluster (slot, ring and mbarrier-phase reuse over many rows); one
+    # and two CTAs per SM; both exchanges
     w = _custom(wl.LAYERNORM, "bf16", rows, 32768, 30, x_mean=0.5, x_std=2.0, eps=1e-5,
                 param_dtype="f32")
     inp = w.generate()
     ran = 0
-    for P in (1, 2, 4, 8):
+    for P, cps, xc in itertools.product((1, 2, 4, 8), (1, 2),
+                                        (C.EXCHANGE_BARRIER, C.EXCHANGE_ASYNC)):
         p = _try_plan(w, C.CLUSTER_PERSISTENT, P)
         if p is None:
             continue
-        for cps in (1, 2):
+        p.exchange = xc
+        if True:
             p.ctas_per_sm = cps
             dx = to_device(inp["x"])
             dy = torch.empty_like(dx)
@@ -255,7 +259,35 @@ def test_persistent_row_counts(rows):
             torch.cuda.synchronize()
             check(w, to_host(dy), inp)
             ran += 1
-    assert ran >= 4
+    assert ran >= 8
+
+
+def test_persistent_async_exchange_all_ops():
+    # the st.async exchange in the persistent ring for every operator it
+    # runs, at cluster sizes whose slices leave a ragged last CTA
+    dev = torch.cuda.current_device()
+    cases = [
+        _custom(wl.SOFTMAX, "f32", 37, 65536, 90, x_std=4.0, spike_frac=0.01),
+        _custom(wl.SOFTMAX, "bf16", 41, 131072, 91),
+        _custom(wl.RMSNORM, "bf16", 33, 196608, 92, eps=1e-6, param_dtype="bf16"),
+        _custom(wl.LAYERNORM, "f32", 29, 49152, 93, x_mean=-1.0, x_std=3.0, eps=1e-5,
+                param_dtype="f32"),
+    ]
+    ran = 0
+    for w in cases:
+        inp = w.generate()
+        for P in (2, 3, 5, 9):
+            try:
+                p = C.credit_plan_with(gh_ops(w), w.rows, w.cols, gh_dt(w), dev,
+                                       C.CLUSTER_PERSISTENT, P, exchange=C.EXCHANGE_ASYNC)
+            except C.CreditError as e:
+                assert e.status == C.ERR_NO_LEGAL_PLAN
+                continue
+            assert p.exchange == C.EXCHANGE_ASYNC
+            check(w, run(w, inp, p), inp)
+            ran += 1
+    assert ran >= 8
+    assert C.credit_get_device_error(dev) == C.OK
 
 
 @pytest.mark.parametrize("R", [2, 4])
@@ -344,7 +376,7 @@ def test_planned_exchange():
     assert make_plan(w, C.TWO_PASS, 1).exchange == C.EXCHANGE_DEFAULT
     p = _try_plan(w, C.CLUSTER_PERSISTENT, 4)
     if p is not None:
-        assert p.exchange == C.EXCHANGE_BARRIER
+        assert p.exchange == C.EXCHANGE_ASYNC
     assert C.credit_plan_with(C.SOFTMAX, 4, 65536, C.F32, dev, C.CLUSTER, 4,
                               exchange=C.EXCHANGE_BARRIER).exchange == C.EXCHANGE_BARRIER
 
