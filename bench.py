@@ -424,6 +424,11 @@ def main():
     rpc = max(1, -(-w.rows // args.e2e_chunks))
     hbytes = C.credit_host_buffer_bytes(call, plan, rpc)
     hbuf = torch.empty(hbytes, dtype=torch.uint8, device=dx.device)
+    with torch.cuda.stream(stream):  # untimed: creates the pipeline streams, touches the buffers
+        for _ in range(2):
+            st = C.credit_run_host(call, plan, hbuf.data_ptr(), hbytes, rpc, sptr)
+            if st != C.OK:
+                raise C.CreditError(st, "credit_run_host")
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
