@@ -41,16 +41,22 @@ def _dtype(t):
 
 
 def plan(op: str, rows: int, cols: int, dtype, device: int | None = None,
-         variant: str | None = None, cluster_size: int = 1) -> Plan:
+         variant: str | None = None, cluster_size: int = 1, rows_per_cluster: int = 0,
+         exchange: str | None = None) -> Plan:
     """Plan a call: automatically (variant None) or for a forced variant
-    ("cluster" with `cluster_size`, or "two_pass")."""
+    ("cluster" with `cluster_size` and optionally `rows_per_cluster`,
+    "persistent" with `cluster_size`, or "two_pass"); `exchange` ("async" or
+    "barrier") picks how a clustered plan exchanges its partials."""
     import torch
     dev = torch.cuda.current_device() if device is None else int(device)
     code = _OPS[op]
     if variant is None:
         return C.credit_plan(code, rows, cols, _dtype(dtype), dev)
-    v = {"cluster": C.CLUSTER, "two_pass": C.TWO_PASS}[variant]
-    return C.credit_plan_for(code, rows, cols, _dtype(dtype), dev, v, cluster_size)
+    v = {"cluster": C.CLUSTER, "persistent": C.CLUSTER_PERSISTENT, "two_pass": C.TWO_PASS}[variant]
+    x = {None: C.EXCHANGE_DEFAULT, "async": C.EXCHANGE_ASYNC,
+         "barrier": C.EXCHANGE_BARRIER}[exchange]
+    return C.credit_plan_with(code, rows, cols, _dtype(dtype), dev, v, cluster_size,
+                              rows_per_cluster=rows_per_cluster, exchange=x)
 
 
 def _prep(x, out):
