@@ -22,9 +22,9 @@
 //       ("Output Generation").
 // A relaxed cluster arrive at kernel entry, waited on just before the push,
 // guarantees every peer is running before its shared memory is written.
-// After barrier a5 no CTA touches a peer's shared memory, so CTAs may exit
-// without the second barrier (the page's second barrier protects slot reuse,
-// which a one-row-per-cluster launch never does).
+// With the barrier exchange no CTA touches a peer's shared memory after a5,
+// so CTAs may exit without the second barrier (the page's second barrier
+// protects slot reuse, which a one-row-per-cluster launch never does).
 #include "common.cuh"
 #include "internal.h"
 #include "rowops.cuh"

@@ -1,25 +1,29 @@
 /*
  * credit.h -- C ABI of libcredit: CREDIT's DSMEM reduction-reuse
  * transformation for wide-row reduce-then-reuse operators (row softmax,
- * LayerNorm, RMSNorm) on GB300 (sm_103a).
+ * LayerNorm, RMSNorm, int8 quantization, weighted standardization, Pearson
+ * correlation) on GB300 (sm_103a).
  *
  * Operation (CREDIT summary page, arXiv 2609.01864v1, "B. Reduction-Reuse
  * Transformation" and "C. Cluster Reduction and Reuse Protocol"): each row is
  * split into P contiguous slices owned by the P CTAs of one thread-block
  * cluster.  Every CTA stages its slice in shared memory once, reduces it to a
  * compact partial statistic, pushes that partial into a slot that each peer
- * CTA owns (distributed shared memory), waits on a cluster barrier, combines
- * the P slots with local reads only, and writes its output slice straight
- * from shared memory.  The row is read from HBM once and written once.
+ * CTA owns (distributed shared memory) -- by default as st.async deposits
+ * that complete on the receiver's mbarrier, or with remote stores and a
+ * cluster barrier -- combines the P slots with local reads only, and writes
+ * its output slice straight from shared memory.  The row is read from HBM
+ * once and written once.
  * The non-clustered two-pass kernel (partials to a global workspace, then a
  * second kernel that re-reads the row) ships alongside as the in-library
  * baseline ("A. Experimental Setup and Baselines": a non-DSMEM CUDA baseline
  * that either stages locally or re-reads global memory).
  *
  * Conventions for every entry point:
- *  - Pointers named x, y, gamma, beta, weight, workspace are DEVICE pointers
- *    on the current CUDA device; the caller owns them.  Nothing on the call
- *    path allocates memory.
+ *  - Pointers named x, u, y, q, scales, r, gamma, beta, weight(s), workspace
+ *    are DEVICE pointers on the current CUDA device; the caller owns them.
+ *    Nothing on the call path allocates memory.  (credit_run_host takes host
+ *    buffers; the calibration and microbenchmark calls allocate scratch.)
  *  - Matrices are row-major with row stride == cols (contiguous rows).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls are asynchronous on that stream and never synchronise
