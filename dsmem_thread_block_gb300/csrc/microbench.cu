@@ -213,8 +213,9 @@ constexpr int kStageChunk = 16384;
 __global__ void __launch_bounds__(256) stage_copy_kernel(const unsigned char* src,
                                                          unsigned char* dst, int footprint,
                                                          unsigned* err) {
-    extern __shared__ __align__(128) unsigned char buf[];
+    extern __shared__ __align__(128) unsigned char stage_buf[];
     __shared__ __align__(8) uint64_t bar[kMaxChunks];
+    unsigned char* buf = stage_buf;
     const int nch = footprint / kStageChunk;
     const int64_t base = (int64_t)blockIdx.x * footprint;
     if (threadIdx.x == 0) {
