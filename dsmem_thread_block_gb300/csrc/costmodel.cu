@@ -228,7 +228,10 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
     const DevInfo* d = device_info(device);
     if (!d) return CREDIT_ERR_CUDA;
     const int es = dtype == CREDIT_F32 ? 4 : 2;
-    const double mat = (double)rows * (double)cols * es;
+    // the model times the shape's first `rt` rows: all of them up to 1 GiB of
+    // input, so that scratch stays small next to a large resident workload
+    const int64_t rt = std::max<int64_t>(1, std::min<int64_t>(rows, ((int64_t)1 << 30) / (cols * es)));
+    const double mat = (double)rt * (double)cols * es;
 
     // the baseline: the faster of local staging (when one CTA can hold a
     // row) and the two-pass re-read pair
@@ -236,12 +239,12 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
     const int64_t row_bytes = cols * es;
     const int Rb = row_bytes * 4 <= 65536 ? 4 : 1;
     credit_status_t st =
-        make_plan(device, op, rows, cols, dtype, CREDIT_CLUSTER, 1, 0, 0, &base, 0, Rb);
+        make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, 1, 0, 0, &base, 0, Rb);
     if (st != CREDIT_OK && Rb != 1)
-        st = make_plan(device, op, rows, cols, dtype, CREDIT_CLUSTER, 1, 0, 0, &base, 0, 1);
+        st = make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, 1, 0, 0, &base, 0, 1);
     bool staging = st == CREDIT_OK;
     credit_plan_t reread;
-    st = make_plan(device, op, rows, cols, dtype, CREDIT_TWO_PASS, 0, 0, 0, &reread);
+    st = make_plan(device, op, rt, cols, dtype, CREDIT_TWO_PASS, 0, 0, 0, &reread);
     if (st != CREDIT_OK) return st;
     if (!staging) base = reread;
     // bytes: one read of x (and of u for Pearson) and one write of the
@@ -249,19 +252,19 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
     // inputs twice
     const bool pearson = op == CREDIT_PEARSON;
     const double b_read = pearson ? 2.0 * mat : mat;
-    const double b_write = op == CREDIT_QUANTIZE ? (double)rows * (double)cols : mat;
+    const double b_write = op == CREDIT_QUANTIZE ? (double)rt * (double)cols : mat;
     const double b_credit = b_read + b_write;
 
     // scratch buffers of the shape
     Scratch x, y, g, b, ws, aux;
     const size_t pbytes = (size_t)cols * (param_dtype == CREDIT_F32 ? 4 : 2);
     if (op == CREDIT_WEIGHTED_STD && param_dtype < 0) return CREDIT_ERR_INVALID_ARG;
-    if (!x.alloc((size_t)mat) || !y.alloc((size_t)mat) || !aux.alloc((size_t)rows * 4) ||
+    if (!x.alloc((size_t)mat) || !y.alloc((size_t)mat) || !aux.alloc((size_t)rt * 4) ||
         (pearson && !g.alloc((size_t)mat)) ||  // the second operand u
         (!pearson && param_dtype >= 0 && (!g.alloc(pbytes) || !b.alloc(pbytes))))
         return CREDIT_ERR_CUDA;
     if (!ws.alloc((size_t)reread.workspace_bytes)) return CREDIT_ERR_CUDA;
-    const int64_t nmat = rows * cols;
+    const int64_t nmat = rt * cols;
     const credit_dtype_t pdt = param_dtype == CREDIT_BF16 ? CREDIT_BF16 : CREDIT_F32;
     if (!fill(x.p, nmat, dtype, -2.f, 2.f, 1u) ||
         (pearson && !fill(g.p, nmat, dtype, -2.f, 2.f, 2u)) ||
@@ -274,12 +277,12 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
 
     double t_base = 0.0;
     float* auxp = static_cast<float*>(aux.p);
-    st = time_op(op, x.p, y.p, rows, cols, dtype, g.p, b.p, param_dtype, &base, ws.p,
+    st = time_op(op, x.p, y.p, rt, cols, dtype, g.p, b.p, param_dtype, &base, ws.p,
                  (size_t)base.workspace_bytes, runs, &t_base, auxp);
     if (st != CREDIT_OK) return st;
     if (staging) {
         double t_rr = 0.0;
-        st = time_op(op, x.p, y.p, rows, cols, dtype, g.p, b.p, param_dtype, &reread, ws.p,
+        st = time_op(op, x.p, y.p, rt, cols, dtype, g.p, b.p, param_dtype, &reread, ws.p,
                      (size_t)reread.workspace_bytes, runs, &t_rr, auxp);
         if (st != CREDIT_OK) return st;
         if (t_rr < t_base) {
@@ -294,12 +297,12 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
     // the baseline's control: its grid, footprint and barriers, no work
     double ctrl_base = 0.0;
     if (staging) {
-        st = credit_control_time(device, ceil_div64(rows, base.rows_per_cluster), 1, base.threads,
+        st = credit_control_time(device, ceil_div64(rt, base.rows_per_cluster), 1, base.threads,
                                  base.smem_bytes, 1, 2, runs, &ctrl_base);
     } else {
         const int64_t nch = ceil_div64(cols, base.slice_elems);
         double one = 0.0;
-        st = credit_control_time(device, rows * nch, 1, base.threads, 0, 1, 2, runs, &one);
+        st = credit_control_time(device, rt * nch, 1, base.threads, 0, 1, 2, runs, &one);
         ctrl_base = 2.0 * one;  // two launches
     }
     if (st != CREDIT_OK) return st;
@@ -323,11 +326,11 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         credit_candidate_t& c = rep.cand[P - 1];
         c.cluster_size = P;
         credit_plan_t p;
-        if (make_plan(device, op, rows, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1) != CREDIT_OK)
+        if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1) != CREDIT_OK)
             continue;
         if ((int64_t)(P - 1) * p.slice_elems >= cols) continue;  // an idle CTA
         double ctrl = 0.0;
-        st = credit_control_time(device, rows, P, p.threads, p.smem_bytes, 1, 2, runs, &ctrl);
+        st = credit_control_time(device, rt, P, p.threads, p.smem_bytes, 1, 2, runs, &ctrl);
         if (st == CREDIT_ERR_NO_LEGAL_PLAN) continue;
         if (st != CREDIT_OK) return st;
         c.legal = 1;
@@ -370,7 +373,7 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         rep.cand[0].measured_us = t_base;
         for (int P : order) {
             credit_candidate_t& c = rep.cand[P - 1];
-            st = time_op(op, x.p, y.p, rows, cols, dtype, g.p, b.p, param_dtype, &c.plan, nullptr,
+            st = time_op(op, x.p, y.p, rt, cols, dtype, g.p, b.p, param_dtype, &c.plan, nullptr,
                          0, runs, &c.measured_us, auxp);
             if (st != CREDIT_OK) return st;
             if (c.measured_us < best_meas) {
@@ -379,9 +382,9 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
                 best_meas_P = P;
             }
             credit_plan_t pp;
-            if (make_plan(device, op, rows, cols, dtype, CREDIT_CLUSTER_PERSISTENT, P, 0, 0, &pp) ==
+            if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER_PERSISTENT, P, 0, 0, &pp) ==
                 CREDIT_OK) {
-                st = time_op(op, x.p, y.p, rows, cols, dtype, g.p, b.p, param_dtype, &pp, nullptr,
+                st = time_op(op, x.p, y.p, rt, cols, dtype, g.p, b.p, param_dtype, &pp, nullptr,
                              0, runs, &c.persistent_us, auxp);
                 if (st != CREDIT_OK) return st;
                 if (c.persistent_us < best_meas) {
@@ -398,6 +401,21 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
     }
     rep.chosen_cluster_size = best_P;
     rep.chosen_variant = chosen.variant;
+    if (rt != rows) {
+        // the chosen configuration, planned for every row of the shape
+        credit_plan_t full;
+        const credit_variant_t v = (credit_variant_t)chosen.variant;
+        const bool pers = v == CREDIT_CLUSTER_PERSISTENT;
+        if (make_plan(device, op, rows, cols, dtype, v, chosen.cluster_size, chosen.threads,
+                      pers ? chosen.ctas_per_sm : 0, &full, pers ? chosen.chunk_elems : 0,
+                      v == CREDIT_CLUSTER ? chosen.rows_per_cluster : 0) == CREDIT_OK) {
+            const double scale = (double)rows / (double)rt;
+            full.exchange = chosen.exchange;
+            full.pred_us = (float)(chosen.pred_us * scale);
+            full.pred_two_pass_us = (float)(chosen.pred_two_pass_us * scale);
+            chosen = full;
+        }
+    }
     {
         std::lock_guard<std::mutex> lk(g_cm_mu);
         g_chosen[std::make_tuple(device, (int)op, (int)dtype, rows, cols)] = chosen;

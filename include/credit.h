@@ -437,10 +437,11 @@ credit_status_t credit_stage_copy_rate(int device, int ctas_per_sm, int runs,
 
 /*
  * Apply the cost model to one shape on `device` (calibrating first if
- * needed).  Allocates scratch x / y / parameter / workspace buffers of the
- * shape (zero-filled), times the baseline (median of `runs`), runs the
- * control kernels, fills `report` (may be NULL) and writes the chosen plan to
- * `out`.  param_dtype is the parameters' dtype, or -1 for none; tune is the
+ * needed).  Allocates scratch x / y / parameter / workspace buffers for the
+ * shape's first rows -- all of them up to 1 GiB of input, fewer beyond --
+ * filled with hashed values, times the baseline (median of `runs`), runs the
+ * control kernels, fills `report` (may be NULL; its times are those of the
+ * timed rows) and writes the chosen plan, planned for every row, to `out`.  param_dtype is the parameters' dtype, or -1 for none; tune is the
  * number of best-predicted candidates to time (0 = the model alone).  The choice
  * is cached: later credit_plan calls for the same (op, rows, cols, dtype,
  * device) return it.  Synchronises the device.

@@ -67,3 +67,18 @@ def test_stage_copy_rate_residency_and_bounds():
     with pytest.raises(C.CreditError):
         C.credit_stage_copy_rate(0, 9, 3)
     torch.cuda.synchronize()
+
+
+def test_large_shape_is_timed_on_its_first_rows():
+    # 8 GiB of bf16 input: the model times the first 1 GiB of rows and plans
+    # the chosen configuration for every row
+    rows, cols = 8192, 524288
+    plan, rep = C.credit_plan_profiled(C.RMSNORM, rows, cols, C.BF16, C.BF16, 0, 3, 2)
+    assert rep.t_base_us > 0
+    if plan.variant == C.CLUSTER:
+        assert plan.waves == -(-rows // (plan.active_clusters * plan.rows_per_cluster))
+    elif plan.variant == C.CLUSTER_PERSISTENT:
+        assert plan.waves == -(-rows // plan.active_clusters)
+    auto = C.credit_plan(C.RMSNORM, rows, cols, C.BF16, 0)
+    assert auto.variant == plan.variant and auto.cluster_size == plan.cluster_size
+    torch.cuda.synchronize()
