@@ -62,7 +62,10 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
                 raise C.CreditError(st, "sweep launch")
 
         med, iqr = _timed(go, runs)
-        measured[cand.cluster_size] = {"us": med, "iqr_us": iqr, "pred_us": cand.pred_us}
+        measured[cand.cluster_size] = {"us": med, "iqr_us": iqr, "pred_us": cand.pred_us,
+                                       "t_ctrl_us": cand.t_ctrl_us, "t_comm_us": cand.t_comm_us,
+                                       "active_clusters": p.active_clusters, "waves": p.waves,
+                                       "threads": p.threads, "smem_bytes": p.smem_bytes}
     # the tuned plan may be a persistent one: time it as chosen
     ws = torch.empty(max(1, int(plan.workspace_bytes)), dtype=torch.uint8, device=x.device)
     tuned_us, tuned_iqr = _timed(lambda: C.credit_softmax(
