@@ -138,6 +138,9 @@ cluster_persistent(const PersistArgs a) {
         auto stash = [&](float mq) { return softmax_stash(base, nvec, warp, ncw, lane, mq); };
         float p0, p1, p2;
         cta_partial<OP, T>(stt, red[k & 1][0], red[k & 1][1], ncw, nct, stash, p0, p1, p2);
+        // the fp32 softmax stash wrote the slots: order those generic-proxy
+        // writes before the bulk copies that will refill them
+        if constexpr (OP == kSoftmax && sizeof(T) == 4) fence_proxy_async_smem();
 
         // a4 + a5 + a6: replicated push, cluster barrier, local combine
         float st0 = p0, st1 = p1, st2 = p2;
@@ -170,17 +173,25 @@ cluster_persistent(const PersistArgs a) {
             combine_slots<OP>(sl, P, st0, st1, st2);
         }
 
-        // a7: apply h to the staged slice, then release the row's slots
+        // a7: apply h to the staged slice; each chunk slot goes back to the
+        // producer as soon as this warp's tiles have moved past it, so the
+        // next row's copies stream in while this row is still being written
         const OutputMap<OP, T> h(st0, st1, st2, p0, a.cols, a.eps);
         T* yrow = static_cast<T*>(a.y) + row * a.cols + start;
+        int released = 0;  // chunks of this row this warp has handed back
+        auto release = [&](int next_vec) {
+            const int done = min(cpr, next_vec / vpc);
+            if (done > released) {
+                __syncwarp();
+                if (lane == 0)
+                    for (int c = released; c < done; ++c)
+                        mbar_arrive(smem_u32(&empty_bar[rs * cpr_full + c]));
+                released = done;
+            }
+        };
         output_tiles<OP, T, PT>(h, base, yrow, gp ? gp + start : nullptr, bp ? bp + start : nullptr,
-                                nvec, warp, ncw, lane);
-        // the fp32 softmax stash wrote the slots: order those generic-proxy
-        // writes before the bulk copies that will refill them
-        if constexpr (OP == kSoftmax && sizeof(T) == 4) fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0)
-            for (int c = 0; c < cpr; ++c) mbar_arrive(smem_u32(&empty_bar[rs * cpr_full + c]));
+                                nvec, warp, ncw, lane, release);
+        release(cpr * vpc);  // chunks past the slice's vectors (none when the slice fills them)
         if (++rs == NR) { rs = 0; ++use; }
     }
     if (clustered && nrows == 0) cluster_wait_acquire();  // entry phase

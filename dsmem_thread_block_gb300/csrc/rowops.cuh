@@ -390,14 +390,23 @@ __device__ __forceinline__ void granule_params(const PT* p, int q, F2* out) {
     }
 }
 
+// No-op progress hook of output_tiles.
+struct NoRelease {
+    __device__ __forceinline__ void operator()(int) const {}
+};
+
 // Apply h to the staged slice ([0, nvec) 16-byte vectors at `base`) and
 // store it to `yrow`; gp / bp are the slice's parameters (null = absent).
 // Each warp tile loads all its data and parameters before its first store,
-// so parameter fetches overlap instead of queueing behind stores.
-template <int OP, typename T, typename PT>
+// so parameter fetches overlap instead of queueing behind stores.  After
+// each tile `release(v)` is told the first staged vector the warp may still
+// read (the start of its next tile; nvec at the end), so a caller can hand
+// back the shared memory the warp has finished with.
+template <int OP, typename T, typename PT, typename Release = NoRelease>
 __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const unsigned char* base,
                                              T* yrow, const PT* gp, const PT* bp, int nvec,
-                                             int warp, int nwarps, int lane) {
+                                             int warp, int nwarps, int lane,
+                                             Release release = Release()) {
     using G = Granule<OP, T, PT>;
     constexpr int U = (OP != kSoftmax && G::kPairs == 4) ? 2 : 4, NP = G::kPairs, kTile = 32 * U;
     const int ngran = nvec * (16 / G::kBytes);
@@ -451,9 +460,14 @@ __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const un
             }
         }
     };
+    constexpr int kGranPerVec = 16 / G::kBytes;
     int t = warp * kTile;
-    for (; t + kTile <= ngran; t += nwarps * kTile) tile(t, true);
+    for (; t + kTile <= ngran; t += nwarps * kTile) {
+        tile(t, true);
+        release(min(nvec, (t + nwarps * kTile) / kGranPerVec));
+    }
     if (t < ngran) tile(t, false);
+    release(nvec);
 }
 
 }  // namespace credit
