@@ -253,6 +253,13 @@ credit_status_t run(const OpCall& c) {
         plan.exchange = xchg;
     }
     key.rows = plan.variant == CREDIT_CLUSTER ? plan.rows_per_cluster : 1;
+    if (plan.variant == CREDIT_CLUSTER && key.rows == 1 && vec) {
+        // slices too large for three CTAs per SM take the instantiation that
+        // spends the spare registers on deeper parameter prefetch (where one
+        // exists; cluster_kernel falls back to the regular one otherwise)
+        const DevInfo* di = device_info(dev);
+        key.deep = di && plan.smem_bytes > (int64_t)di->smem_per_sm / 3 - 4096;
+    }
     if (plan.variant == CREDIT_CLUSTER_PERSISTENT) {
         PersistArgs a;
         a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;

@@ -31,11 +31,13 @@
 
 namespace credit {
 
-constexpr int kPipeU = 2;  // granules per lane in a pipelined output tile
-
-template <int OP, typename T, typename PT, bool BULK, int R>
-__global__ void __launch_bounds__(kClusterMaxThreads, 3)
+// DEEP: the instantiation for slices that leave room for at most two CTAs
+// per SM -- it may use twice the registers, which its pipelined output pass
+// spends on twice as many parameter loads in flight per lane.
+template <int OP, typename T, typename PT, bool BULK, int R, bool DEEP = false>
+__global__ void __launch_bounds__(kClusterMaxThreads, DEEP ? 2 : 3)
 cluster_reduce_reuse(const ClusterArgs a) {
+    constexpr int kPipeU = DEEP ? 4 : 2;  // granules per lane in a pipelined output tile
     static_assert(BULK || R == 1, "the element path stages one row per cluster");
     using E = Elem<T>;
     constexpr int VEC = E::kVec;
@@ -238,8 +240,13 @@ cluster_reduce_reuse(const ClusterArgs a) {
 
 // ----------------------------------------------------------- dispatch
 template <int OP, typename T, typename PT>
-static const void* pick_rows(bool vec, int rows) {
+static const void* pick_rows(bool vec, int rows, bool deep = false) {
     if (!vec) return rows == 1 ? (const void*)cluster_reduce_reuse<OP, T, PT, false, 1> : nullptr;
+    // the deep instantiation exists where the output pass is pipelined
+    constexpr bool kHasDeep = OP == kRMSNorm && Granule<OP, T, PT>::kPairs == 4;
+    if constexpr (kHasDeep) {
+        if (deep && rows == 1) return (const void*)cluster_reduce_reuse<OP, T, PT, true, 1, true>;
+    }
     switch (rows) {
         case 1: return (const void*)cluster_reduce_reuse<OP, T, PT, true, 1>;
         case 2: return (const void*)cluster_reduce_reuse<OP, T, PT, true, 2>;
@@ -249,14 +256,15 @@ static const void* pick_rows(bool vec, int rows) {
 }
 
 template <int OP, typename T>
-static const void* pick_param(int pdtype, bool vec, int rows) {
-    return pdtype == 0 ? pick_rows<OP, T, float>(vec, rows) : pick_rows<OP, T, bf16>(vec, rows);
+static const void* pick_param(int pdtype, bool vec, int rows, bool deep) {
+    return pdtype == 0 ? pick_rows<OP, T, float>(vec, rows, deep)
+                       : pick_rows<OP, T, bf16>(vec, rows, deep);
 }
 
 template <int OP>
-static const void* pick_dtype(int dtype, int pdtype, bool vec, int rows) {
-    return dtype == 0 ? pick_param<OP, float>(pdtype, vec, rows)
-                      : pick_param<OP, bf16>(pdtype, vec, rows);
+static const void* pick_dtype(int dtype, int pdtype, bool vec, int rows, bool deep = false) {
+    return dtype == 0 ? pick_param<OP, float>(pdtype, vec, rows, deep)
+                      : pick_param<OP, bf16>(pdtype, vec, rows, deep);
 }
 
 const void* cluster_kernel(KernelKey k) {
@@ -264,7 +272,7 @@ const void* cluster_kernel(KernelKey k) {
         case kSoftmax: return k.dtype == 0 ? pick_rows<kSoftmax, float, float>(k.vec, k.rows)
                                            : pick_rows<kSoftmax, bf16, float>(k.vec, k.rows);
         case kLayerNorm: return pick_dtype<kLayerNorm>(k.dtype, k.pdtype, k.vec, k.rows);
-        case kRMSNorm: return pick_dtype<kRMSNorm>(k.dtype, k.pdtype, k.vec, k.rows);
+        case kRMSNorm: return pick_dtype<kRMSNorm>(k.dtype, k.pdtype, k.vec, k.rows, k.deep);
         case kQuant: return k.dtype == 0 ? pick_rows<kQuant, float, float>(k.vec, k.rows)
                                          : pick_rows<kQuant, bf16, float>(k.vec, k.rows);
         case kWStd: return pick_dtype<kWStd>(k.dtype, k.pdtype, k.vec, k.rows);

@@ -71,6 +71,7 @@ struct KernelKey {
     int op, dtype, pdtype;
     bool vec;
     int rows = 1;
+    bool deep = false;  // clustered kernel for slices that leave room for <= 2 CTAs per SM
 };
 
 const void* cluster_kernel(KernelKey k);

@@ -369,6 +369,27 @@ def test_rmsnorm_bf16_weights_pipelined_output():
     assert C.credit_get_device_error(dev) == C.OK
 
 
+def test_rmsnorm_bf16_weights_large_slices_deep_kernel():
+    # slices too large for three CTAs per SM take the instantiation with the
+    # deeper weight prefetch: whole, ragged and partial warp tiles
+    dev = torch.cuda.current_device()
+    for cols, sizes in ((786432, (8, 12, 16)), (600000, (4, 7, 9)), (300008, (3, 4))):
+        w = _custom(wl.RMSNORM, "bf16", 3, cols, 59, eps=1e-6, param_dtype="bf16")
+        inp = w.generate()
+        ran = 0
+        for P in sizes:
+            try:
+                p = C.credit_plan_with(gh_ops(w), w.rows, w.cols, gh_dt(w), dev, C.CLUSTER, P)
+            except C.CreditError as e:
+                assert e.status == C.ERR_NO_LEGAL_PLAN
+                continue
+            assert p.smem_bytes > 64 * 1024  # the deep instantiation's range
+            check(w, run(w, inp, p), inp)
+            ran += 1
+        assert ran >= 1
+    assert C.credit_get_device_error(dev) == C.OK
+
+
 def test_planned_exchange():
     dev = torch.cuda.current_device()
     w = _custom(wl.SOFTMAX, "f32", 4, 65536, 57)
