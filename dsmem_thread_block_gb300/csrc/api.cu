@@ -189,6 +189,64 @@ credit_status_t plan_from_request(int dev, credit_op_t op, int64_t rows, int64_t
     return st;
 }
 
+// Derived launch plans, keyed by the shape and the request's fields: a call
+// re-derives its plan (legality, occupancy queries) only the first time it
+// sees a (device, op, shape, dtype, request) combination.  The automatic plan
+// of a shape is cached too, after the profiled choice (which a later
+// calibration may change) has been looked up.
+struct PlanKey {
+    int dev, op, dtype, variant, cluster_size, threads, cps, chunk, rpc, exchange;
+    int64_t rows, cols;
+    bool operator==(const PlanKey& o) const {
+        return std::memcmp(this, &o, sizeof(PlanKey)) == 0;
+    }
+};
+struct PlanKeyHash {
+    size_t operator()(const PlanKey& k) const {
+        uint64_t h = 1469598103934665603ull;
+        const unsigned char* p = reinterpret_cast<const unsigned char*>(&k);
+        for (size_t i = 0; i < sizeof(PlanKey); ++i) h = (h ^ p[i]) * 1099511628211ull;
+        return (size_t)h;
+    }
+};
+std::mutex g_plan_mu;
+std::unordered_map<PlanKey, credit_plan_t, PlanKeyHash> g_plans;
+
+credit_status_t cached_plan(int dev, const OpCall& c, credit_plan_t* out) {
+    credit_plan_t profiled;
+    const bool automatic = !(c.plan && c.plan->variant != CREDIT_AUTO);
+    if (automatic && lookup_profiled_plan(dev, c.op, c.rows, c.cols, c.dtype, &profiled)) {
+        *out = profiled;
+        return CREDIT_OK;
+    }
+    PlanKey k;
+    std::memset(&k, 0, sizeof(k));  // no padding bytes left undefined for the hash
+    k.dev = dev; k.op = (int)c.op; k.dtype = (int)c.dtype; k.rows = c.rows; k.cols = c.cols;
+    if (!automatic) {
+        const credit_plan_t& r = *c.plan;
+        k.variant = r.variant; k.cluster_size = r.cluster_size; k.threads = r.threads;
+        k.cps = r.ctas_per_sm; k.chunk = r.chunk_elems; k.rpc = r.rows_per_cluster;
+        k.exchange = r.exchange;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        auto it = g_plans.find(k);
+        if (it != g_plans.end()) {
+            *out = it->second;
+            return CREDIT_OK;
+        }
+    }
+    const credit_status_t st =
+        automatic ? auto_plan(dev, c.op, c.rows, c.cols, c.dtype, out)
+                  : plan_from_request(dev, c.op, c.rows, c.cols, c.dtype, *c.plan, out);
+    if (st == CREDIT_OK) {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        if (g_plans.size() >= 4096) g_plans.clear();  // bounded: shapes come and go
+        g_plans.emplace(k, *out);
+    }
+    return st;
+}
+
 credit_status_t run(const OpCall& c) {
     if (!c.x || !c.y || c.rows < 1 || c.cols < 1) return CREDIT_ERR_INVALID_ARG;
     if (!dtype_ok(c.dtype)) return CREDIT_ERR_UNSUPPORTED;
@@ -224,13 +282,10 @@ credit_status_t run(const OpCall& c) {
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return CREDIT_ERR_CUDA; }
     credit_plan_t plan;
     credit_status_t st;
-    if (c.plan && c.plan->variant != CREDIT_AUTO) {
-        // re-derive the launch shape from (variant, P, threads) so a stale or
-        // hand-edited plan can never launch an illegal configuration
-        st = plan_from_request(dev, c.op, c.rows, c.cols, c.dtype, *c.plan, &plan);
-    } else {
-        st = auto_plan(dev, c.op, c.rows, c.cols, c.dtype, &plan);
-    }
+    // a requested plan's launch shape is re-derived from (variant, P,
+    // threads, ...) so a stale or hand-edited plan can never launch an
+    // illegal configuration; the derivation is cached per shape and request
+    st = cached_plan(dev, c, &plan);
     if (st != CREDIT_OK) return st;
 
     // the bulk path also needs 16-byte-aligned output rows; the int8 rows of
