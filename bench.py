@@ -255,11 +255,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="run the workload's first ROWS rows (0 = all; for profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     wl, table = _workloads()
     w = table[args.workload]
+    if args.rows:
+        w = w.with_rows(args.rows)  # a smaller case of the same shape (profiling)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -430,3 +430,17 @@ def gh_ops(w):
 def gh_dt(w):
     from gpu_helpers import DT
     return DT[w.dtype]
+
+
+def test_rows_wider_than_any_cluster_fall_back_to_two_pass():
+    # 64 MB fp32 rows: no cluster of up to 16 CTAs can stage one, so the
+    # automatic plan is the two-pass kernel pair, which still matches
+    w = _custom(wl.SOFTMAX, "f32", 2, 1 << 24, 96, x_std=3.0)
+    dev = torch.cuda.current_device()
+    with pytest.raises(C.CreditError) as e:
+        C.credit_plan_for(C.SOFTMAX, w.rows, w.cols, C.F32, dev, C.CLUSTER, 16)
+    assert e.value.status == C.ERR_NO_LEGAL_PLAN
+    p = make_plan(w)
+    assert p.variant == C.TWO_PASS
+    inp = w.generate()
+    check(w, run(w, inp, p), inp)
