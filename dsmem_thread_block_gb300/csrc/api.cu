@@ -480,6 +480,6 @@ credit_status_t credit_selftest_wait_timeout(int device, int64_t limit_ns) {
     return credit_get_device_error(device);
 }
 
-const char* credit_version(void) { return "0.1.0"; }
+const char* credit_version(void) { return "0.2.0"; }
 
 }  // extern "C"

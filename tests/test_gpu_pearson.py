@@ -127,3 +127,24 @@ def test_pearson_full_size_sampled_rows():
     means = y.astype(np.float64).mean(axis=1)
     assert np.abs(means - r).max() < 1e-4
     assert np.all(np.abs(r - 1.2 / np.sqrt(2.08)) < 0.02)
+
+
+@pytest.mark.parametrize("variant,P", [(C.CLUSTER, 1), (C.CLUSTER, 4), (C.TWO_PASS, 1)])
+def test_pearson_misaligned_operands(variant, P):
+    # x, u and y one element past a 16-byte boundary: the element path
+    w = _w("f32", 3, 8192, 78)
+    inp = w.generate()
+    dev = torch.cuda.current_device()
+
+    def shifted(a):
+        t = torch.from_numpy(np.concatenate([np.zeros(1, np.float32), a.reshape(-1)])).cuda()
+        return t[1:]
+    dx, du = shifted(inp["x"]), shifted(inp["u"])
+    dy = torch.empty(dx.numel() + 1, device="cuda")[1:]
+    r = torch.empty(w.rows, device="cuda")
+    p = C.credit_plan_for(C.PEARSON, w.rows, w.cols, C.F32, dev, variant, P)
+    ws = torch.empty(max(1, int(p.workspace_bytes)), dtype=torch.uint8, device="cuda")
+    assert C.credit_pearson(dx.data_ptr(), du.data_ptr(), dy.data_ptr(), r.data_ptr(), w.rows,
+                            w.cols, C.F32, w.eps, p, ws.data_ptr(), int(p.workspace_bytes)) == C.OK
+    torch.cuda.synchronize()
+    check_pearson(w, (dy.cpu().numpy().reshape(w.rows, w.cols), r.cpu().numpy()), inp)

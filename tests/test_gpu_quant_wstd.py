@@ -147,3 +147,20 @@ def test_full_size_sampled_rows(w):
         sub = dict(inp)
         sub["x"] = inp["x"][rows]
         check(w, got[rows], sub)
+
+
+@pytest.mark.parametrize("variant,P", [(C.CLUSTER, 1), (C.CLUSTER, 4), (C.TWO_PASS, 1)])
+def test_quantize_misaligned_codes(variant, P):
+    # int8 codes starting one byte past a 16-byte boundary: the element path
+    w = wl.Workload("quantize_f32_3x8192", wl.QUANTIZE, "f32", 3, 8192, seed=67)
+    inp = w.generate()
+    dev = torch.cuda.current_device()
+    dx = to_device(inp["x"])
+    dq = torch.empty(dx.numel() + 1, dtype=torch.int8, device="cuda")[1:]
+    s = torch.empty(w.rows, device="cuda")
+    p = C.credit_plan_for(C.QUANTIZE, w.rows, w.cols, C.F32, dev, variant, P)
+    ws = torch.empty(max(1, int(p.workspace_bytes)), dtype=torch.uint8, device="cuda")
+    assert C.credit_quantize(dx.data_ptr(), dq.data_ptr(), s.data_ptr(), w.rows, w.cols, C.F32, p,
+                             ws.data_ptr(), int(p.workspace_bytes)) == C.OK
+    torch.cuda.synchronize()
+    check_quant((dq.cpu().numpy().reshape(w.rows, w.cols), s.cpu().numpy()), inp)
