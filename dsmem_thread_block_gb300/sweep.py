@@ -1,15 +1,16 @@
 """Profitability sweep: the cost model's pick against measurement.
 
-For each width of the bf16 softmax sweep (2^28 elements, 1024..1048576
-columns) the cost model (credit_plan_profiled) predicts the time of every
-legal cluster size and of the non-DSMEM baseline and picks one; then every
-candidate is timed on the seeded input (median of `runs` launches, CUDA
-events).  A point is correct when the pick's measured time is within
+For each width of a sweep (2^28 elements, 1024..1048576 columns; bf16
+softmax by default, or another operator and dtype) the cost model
+(credit_plan_profiled) predicts the time of every legal cluster size and of
+the non-DSMEM baseline and picks one; then every candidate is timed on the
+seeded input (median of `runs` launches, CUDA events).  A point is correct when the pick's measured time is within
 max(2 %, the runs' interquartile spread) of the fastest measured candidate
 (CREDIT summary page, "C. Cost-Model Validation": profitability accuracy
 and crossover prediction).  Prints one JSON object per point and a summary.
 
     python -m dsmem_thread_block_gb300.sweep [--cols 1024,4096,...] [--runs 15]
+        [--op layernorm --dtype bf16 --param-dtype f32]
 """
 from __future__ import annotations
 
@@ -38,16 +39,48 @@ def _timed(fn, runs: int):
     return float(np.median(ts)), float(np.percentile(ts, 75) - np.percentile(ts, 25))
 
 
-def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
-              total_elements: int = wl.SWEEP_ELEMENTS, tune: int = 3) -> dict:
+_OPS = {wl.SOFTMAX: C.SOFTMAX, wl.LAYERNORM: C.LAYERNORM, wl.RMSNORM: C.RMSNORM}
+_DT = {"f32": C.F32, "bf16": C.BF16}
+
+
+def _device(a, device):
     import torch
-    w = wl.Workload(f"softmax_bf16_sweep_{cols}", wl.SOFTMAX, "bf16", total_elements // cols,
-                    cols, seed=4)
-    x = torch.from_numpy(w.generate()["x"].view(np.int16)).view(torch.bfloat16).to(device)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(a).to(device)
+
+
+def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
+              total_elements: int = wl.SWEEP_ELEMENTS, tune: int = 3, op: str = wl.SOFTMAX,
+              dtype: str = "bf16", param_dtype: str | None = None) -> dict:
+    import torch
+    w = wl.Workload(f"{op}_{dtype}_sweep_{cols}", op, dtype, total_elements // cols, cols,
+                    seed=4, x_mean=0.0 if op == wl.SOFTMAX else 0.5, eps=1e-5,
+                    param_dtype=param_dtype)
+    inp = w.generate()
+    x = _device(inp["x"], device)
     y = torch.empty_like(x)
-    plan, rep = C.credit_plan_profiled(C.SOFTMAX, w.rows, w.cols, C.BF16, -1, device, model_runs,
-                                       tune)
+    prm = {k: _device(v, device) for k, v in inp.items() if k != "x"}
+    g, b = prm.get("gamma", prm.get("weight")), prm.get("beta")
+    pdt = _DT[param_dtype] if param_dtype else -1
+    plan, rep = C.credit_plan_profiled(_OPS[op], w.rows, w.cols, _DT[dtype], pdt, device,
+                                       model_runs, tune)
     stream = torch.cuda.current_stream().cuda_stream
+
+    def launch(p, ws):
+        if op == wl.SOFTMAX:
+            return C.credit_softmax(x.data_ptr(), y.data_ptr(), w.rows, w.cols, _DT[dtype], p,
+                                    ws.data_ptr(), int(p.workspace_bytes), stream)
+        if op == wl.LAYERNORM:
+            return C.credit_layernorm(x.data_ptr(), y.data_ptr(), w.rows, w.cols, _DT[dtype],
+                                      g.data_ptr() if g is not None else 0,
+                                      b.data_ptr() if b is not None else 0,
+                                      pdt if pdt >= 0 else C.F32, w.eps, p, ws.data_ptr(),
+                                      int(p.workspace_bytes), stream)
+        return C.credit_rmsnorm(x.data_ptr(), y.data_ptr(), w.rows, w.cols, _DT[dtype],
+                                g.data_ptr() if g is not None else 0, pdt if pdt >= 0 else C.F32,
+                                w.eps, p, ws.data_ptr(), int(p.workspace_bytes), stream)
+
     measured = {}
     for cand in rep.cand:
         if not cand.legal:
@@ -56,8 +89,7 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
         ws = torch.empty(max(1, int(p.workspace_bytes)), dtype=torch.uint8, device=x.device)
 
         def go(p=p, ws=ws):
-            st = C.credit_softmax(x.data_ptr(), y.data_ptr(), w.rows, w.cols, C.BF16, p,
-                                  ws.data_ptr(), int(p.workspace_bytes), stream)
+            st = launch(p, ws)
             if st != C.OK:
                 raise C.CreditError(st, "sweep launch")
 
@@ -68,9 +100,7 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
                                        "threads": p.threads, "smem_bytes": p.smem_bytes}
     # the tuned plan may be a persistent one: time it as chosen
     ws = torch.empty(max(1, int(plan.workspace_bytes)), dtype=torch.uint8, device=x.device)
-    tuned_us, tuned_iqr = _timed(lambda: C.credit_softmax(
-        x.data_ptr(), y.data_ptr(), w.rows, w.cols, C.BF16, plan, ws.data_ptr(),
-        int(plan.workspace_bytes), stream), runs)
+    tuned_us, tuned_iqr = _timed(lambda: launch(plan, ws), runs)
     best_P = min(measured, key=lambda k: measured[k]["us"])
     best = min(measured[best_P]["us"], tuned_us)
     clustered = [v["us"] for k, v in measured.items() if k != 1]
@@ -90,7 +120,7 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
         "profitability_correct": bool(rep.profitable) == (best_P != 1),
         "parity_gap": gap,
         "candidates": {str(k): v for k, v in sorted(measured.items())},
-        "gbps_best": 2 * w.rows * w.cols * 2 / best / 1e3,
+        "gbps_best": w.ideal_bytes() / best / 1e3,
     }
 
 
@@ -121,13 +151,16 @@ def main():
     ap.add_argument("--cols", default=",".join(str(c) for c in wl.SWEEP_COLS))
     ap.add_argument("--runs", type=int, default=15)
     ap.add_argument("--device", type=int, default=0)
+    ap.add_argument("--op", default=wl.SOFTMAX, choices=sorted(_OPS))
+    ap.add_argument("--dtype", default="bf16", choices=sorted(_DT))
+    ap.add_argument("--param-dtype", default=None, choices=sorted(_DT))
     a = ap.parse_args()
     import torch
     torch.cuda.set_device(a.device)
     C.credit_calibrate(a.device, 7)
     points = []
     for c in [int(v) for v in a.cols.split(",")]:
-        pt = run_point(c, a.runs, a.device)
+        pt = run_point(c, a.runs, a.device, op=a.op, dtype=a.dtype, param_dtype=a.param_dtype)
         points.append(pt)
         print(json.dumps(pt), flush=True)
     print(json.dumps({"summary": summarize(points)}), flush=True)
