@@ -245,7 +245,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="layernorm_bf16_1024x262144")
     ap.add_argument("--variant", default="auto",
-                    help="auto (cost model + tuning) | static | cluster:P | persist:P | two_pass")
+                    help="auto (cost model + tuning) | static | cluster:P | persist:P | pipe:P | two_pass")
     ap.add_argument("--cps", type=int, default=0, help="persistent CTAs per SM (0 = planner)")
     ap.add_argument("--exchange", default="plan", choices=["plan", "barrier", "async"],
                     help="partial exchange of a one-pass clustered plan (plan = as planned)")
@@ -313,13 +313,16 @@ def main():
                 tuning[f"cluster:{c.cluster_size}"] = round(c.measured_us, 2)
             if c.legal and c.persistent_us > 0:
                 tuning[f"persist:{c.cluster_size}"] = round(c.persistent_us, 2)
+            if c.legal and c.pipelined_us > 0:
+                tuning[f"pipe:{c.cluster_size}"] = round(c.pipelined_us, 2)
     elif args.variant == "static":
         plan = C.credit_plan(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev)
     elif args.variant == "two_pass":
         plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.TWO_PASS, 1)
     else:
         kind, P = args.variant.split(":")
-        var = C.CLUSTER if kind == "cluster" else C.CLUSTER_PERSISTENT
+        var = {"cluster": C.CLUSTER, "persist": C.CLUSTER_PERSISTENT,
+               "pipe": C.CLUSTER_PIPELINED}[kind]
         plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, var, int(P))
     if args.cps:
         plan.ctas_per_sm = args.cps
@@ -452,7 +455,8 @@ def main():
 
     peak, peak_kind = measured_peak()
     variant_key = {C.TWO_PASS: "two_pass", C.CLUSTER: f"cluster:{plan.cluster_size}",
-                   C.CLUSTER_PERSISTENT: f"persist:{plan.cluster_size}"}[plan.variant]
+                   C.CLUSTER_PERSISTENT: f"persist:{plan.cluster_size}",
+                   C.CLUSTER_PIPELINED: f"pipe:{plan.cluster_size}"}[plan.variant]
     if plan.variant == C.CLUSTER and plan.exchange == C.EXCHANGE_BARRIER:
         variant_key += ":barrier"
     launches_per_step = 2 if plan.variant == C.TWO_PASS else 1

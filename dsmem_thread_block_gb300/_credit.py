@@ -18,7 +18,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_LEGAL_PLAN, ERR_CUDA, \
     ERR_DEVICE_TIMEOUT, ERR_NOT_CALIBRATED = range(7)
 F32, BF16 = 0, 1
 SOFTMAX, LAYERNORM, RMSNORM, QUANTIZE, WEIGHTED_STD, PEARSON = 0, 1, 2, 3, 4, 5
-AUTO, CLUSTER, TWO_PASS, CLUSTER_PERSISTENT = 0, 1, 2, 3
+AUTO, CLUSTER, TWO_PASS, CLUSTER_PERSISTENT, CLUSTER_PIPELINED = 0, 1, 2, 3, 4
 EXCHANGE_DEFAULT, EXCHANGE_BARRIER, EXCHANGE_ASYNC = 0, 1, 2
 
 _vp, _i64, _i32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -62,7 +62,8 @@ class Candidate(ctypes.Structure):
     _fields_ = [("cluster_size", ctypes.c_int32), ("legal", ctypes.c_int32), ("plan", Plan),
                 ("t_ctrl_us", ctypes.c_double), ("t_comm_us", ctypes.c_double),
                 ("pred_us", ctypes.c_double), ("measured_us", ctypes.c_double),
-                ("persistent_us", ctypes.c_double)]
+                ("persistent_us", ctypes.c_double),
+                ("pipelined_us", ctypes.c_double)]
 
 
 class HostCall(ctypes.Structure):
@@ -86,7 +87,8 @@ class ModelReport(ctypes.Structure):
         d = {f: getattr(self, f) for f, _ in self._fields_ if f not in ("cand", "reserved")}
         d["candidates"] = [{"P": c.cluster_size, "t_ctrl_us": c.t_ctrl_us, "t_comm_us": c.t_comm_us,
                             "pred_us": c.pred_us, "measured_us": c.measured_us,
-                            "persistent_us": c.persistent_us, "plan": c.plan.as_dict()}
+                            "persistent_us": c.persistent_us, "pipelined_us": c.pipelined_us,
+                            "plan": c.plan.as_dict()}
                            for c in self.cand if c.legal]
         return d
 

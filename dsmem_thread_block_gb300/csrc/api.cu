@@ -172,7 +172,8 @@ credit_status_t plan_from_request(int dev, credit_op_t op, int64_t rows, int64_t
                                   credit_dtype_t dtype, const credit_plan_t& r,
                                   credit_plan_t* out) {
     const credit_variant_t v = (credit_variant_t)r.variant;
-    if (v != CREDIT_CLUSTER && v != CREDIT_CLUSTER_PERSISTENT && v != CREDIT_TWO_PASS)
+    if (v != CREDIT_CLUSTER && v != CREDIT_CLUSTER_PERSISTENT && v != CREDIT_CLUSTER_PIPELINED &&
+        v != CREDIT_TWO_PASS)
         return CREDIT_ERR_INVALID_ARG;
     if (r.threads < 0 || r.ctas_per_sm < 0 || r.chunk_elems < 0 || r.rows_per_cluster < 0)
         return CREDIT_ERR_INVALID_ARG;
@@ -180,7 +181,10 @@ credit_status_t plan_from_request(int dev, credit_op_t op, int64_t rows, int64_t
                      ((r.exchange == CREDIT_EXCHANGE_BARRIER || r.exchange == CREDIT_EXCHANGE_ASYNC) &&
                       v != CREDIT_TWO_PASS);
     if (!xok) return CREDIT_ERR_INVALID_ARG;
-    const bool pers = v == CREDIT_CLUSTER_PERSISTENT;
+    // the warp-specialised kernel exchanges with st.async deposits only
+    if (v == CREDIT_CLUSTER_PIPELINED && r.exchange == CREDIT_EXCHANGE_BARRIER)
+        return CREDIT_ERR_INVALID_ARG;
+    const bool pers = v == CREDIT_CLUSTER_PERSISTENT || v == CREDIT_CLUSTER_PIPELINED;
     const credit_status_t st =
         make_plan(dev, op, rows, cols, dtype, v, r.cluster_size, r.threads,
                   pers ? r.ctas_per_sm : 0, out, pers ? r.chunk_elems : 0,
@@ -298,7 +302,8 @@ credit_status_t run(const OpCall& c) {
     unsigned* err = device_error_word();
     if (!err) return CREDIT_ERR_CUDA;
     if (!vec && plan.variant != CREDIT_TWO_PASS &&
-        (plan.variant == CREDIT_CLUSTER_PERSISTENT || plan.rows_per_cluster != 1)) {
+        (plan.variant == CREDIT_CLUSTER_PERSISTENT || plan.variant == CREDIT_CLUSTER_PIPELINED ||
+         plan.rows_per_cluster != 1)) {
         // bulk copies need 16-byte alignment: misaligned or ragged rows take
         // the one-row-per-cluster kernel's element path instead
         const int32_t xchg = plan.exchange;
@@ -315,7 +320,8 @@ credit_status_t run(const OpCall& c) {
         const DevInfo* di = device_info(dev);
         key.deep = di && plan.smem_bytes > (int64_t)di->smem_per_sm / 3 - 4096;
     }
-    if (plan.variant == CREDIT_CLUSTER_PERSISTENT) {
+    if (plan.variant == CREDIT_CLUSTER_PERSISTENT || plan.variant == CREDIT_CLUSTER_PIPELINED) {
+        const bool piped = plan.variant == CREDIT_CLUSTER_PIPELINED;
         PersistArgs a;
         a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;
         a.rows = c.rows;
@@ -326,8 +332,9 @@ credit_status_t run(const OpCall& c) {
         a.nclusters = plan.active_clusters;
         a.eps = c.eps;
         a.err = err;
-        a.exchange = plan.exchange == CREDIT_EXCHANGE_ASYNC ? 1 : 0;
-        const void* fn = persistent_kernel(key);
+        a.exchange = (piped || plan.exchange == CREDIT_EXCHANGE_ASYNC) ? 1 : 0;
+        a.reducers = piped ? pipelined_reducers(key.op, key.dtype, plan.threads / 32 - 1) : 0;
+        const void* fn = piped ? pipelined_kernel(key) : persistent_kernel(key);
         if (!kernel_info(dev, fn, true)) return CREDIT_ERR_CUDA;
         return from_cuda(launch_persistent(key, a, plan.cluster_size, plan.threads,
                                            (size_t)plan.smem_bytes, c.stream));
@@ -379,7 +386,7 @@ credit_status_t credit_plan_for(credit_op_t op, int64_t rows, int64_t cols, cred
                                 credit_plan_t* out) {
     if (!out) return CREDIT_ERR_INVALID_ARG;
     if (variant != CREDIT_CLUSTER && variant != CREDIT_TWO_PASS &&
-        variant != CREDIT_CLUSTER_PERSISTENT)
+        variant != CREDIT_CLUSTER_PERSISTENT && variant != CREDIT_CLUSTER_PIPELINED)
         return CREDIT_ERR_INVALID_ARG;
     return make_plan(device, op, rows, cols, dtype, variant, cluster_size, 0, 0, out);
 }
@@ -480,6 +487,6 @@ credit_status_t credit_selftest_wait_timeout(int device, int64_t limit_ns) {
     return credit_get_device_error(device);
 }
 
-const char* credit_version(void) { return "0.2.0"; }
+const char* credit_version(void) { return "0.3.0"; }
 
 }  // extern "C"

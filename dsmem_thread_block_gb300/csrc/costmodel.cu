@@ -358,7 +358,8 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
     chosen.pred_two_pass_us = (float)t_base;
 
     // final tuning: time the `tune` best-predicted candidates (and the
-    // persistent kernel of the same P) and keep the fastest measured plan
+    // persistent and pipelined kernels of the same P) and keep the fastest
+    // measured plan
     if (tune > 0) {
         std::vector<int> order;
         for (int P = 2; P <= kMaxCluster; ++P)
@@ -381,14 +382,15 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
                 best_plan = c.plan;
                 best_meas_P = P;
             }
-            credit_plan_t pp;
-            if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER_PERSISTENT, P, 0, 0, &pp) ==
-                CREDIT_OK) {
+            for (credit_variant_t rv : {CREDIT_CLUSTER_PERSISTENT, CREDIT_CLUSTER_PIPELINED}) {
+                credit_plan_t pp;
+                if (make_plan(device, op, rt, cols, dtype, rv, P, 0, 0, &pp) != CREDIT_OK) continue;
+                double* us = rv == CREDIT_CLUSTER_PERSISTENT ? &c.persistent_us : &c.pipelined_us;
                 st = time_op(op, x.p, y.p, rt, cols, dtype, g.p, b.p, param_dtype, &pp, nullptr,
-                             0, runs, &c.persistent_us, auxp);
+                             0, runs, us, auxp);
                 if (st != CREDIT_OK) return st;
-                if (c.persistent_us < best_meas) {
-                    best_meas = c.persistent_us;
+                if (*us < best_meas) {
+                    best_meas = *us;
                     best_plan = pp;
                     best_meas_P = P;
                 }
@@ -405,7 +407,7 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         // the chosen configuration, planned for every row of the shape
         credit_plan_t full;
         const credit_variant_t v = (credit_variant_t)chosen.variant;
-        const bool pers = v == CREDIT_CLUSTER_PERSISTENT;
+        const bool pers = v == CREDIT_CLUSTER_PERSISTENT || v == CREDIT_CLUSTER_PIPELINED;
         if (make_plan(device, op, rows, cols, dtype, v, chosen.cluster_size, chosen.threads,
                       pers ? chosen.ctas_per_sm : 0, &full, pers ? chosen.chunk_elems : 0,
                       v == CREDIT_CLUSTER ? chosen.rows_per_cluster : 0) == CREDIT_OK) {

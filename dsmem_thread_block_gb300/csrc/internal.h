@@ -59,6 +59,7 @@ struct PersistArgs {
     float eps;
     unsigned* err;
     int32_t exchange;     // 0: push + cluster barrier per row; 1: st.async deposits + mbarrier
+    int32_t reducers;     // 0: one consumer role; > 0: reducer warps of the warp-specialised kernel
 };
 
 constexpr int kPersistMaxSlots = 32;
@@ -80,6 +81,9 @@ const void* pearson_cluster_kernel(int dtype, bool vec);
 const void* pearson_stats_kernel(int dtype, bool vec);
 const void* pearson_apply_kernel(int dtype, bool vec);
 const void* persistent_kernel(KernelKey k);
+const void* pipelined_kernel(KernelKey k);  // warp-specialised persistent form
+// Reducer warps of the warp-specialised kernel for `consumer_warps` consumer warps.
+int pipelined_reducers(int op, int dtype, int consumer_warps);
 const void* two_pass_stats_kernel(KernelKey k);
 const void* two_pass_apply_kernel(KernelKey k);
 

@@ -203,11 +203,247 @@ cluster_persistent(const PersistArgs a) {
     }
 }
 
+// The warp-specialised form of the same pipeline.  The consumer warps are
+// split by role so that a row's reduction overlaps the previous row's output:
+//   - reducer warps [0, nred) fold each chunk of row k as it lands, merge the
+//     CTA partial (named barrier among themselves), exchange it with st.async
+//     deposits, combine the P slots and hand the row's statistics to the
+//     storers through a double-buffered hand-off (one "full" mbarrier per
+//     buffer, arrived by one reducer thread; one "empty" mbarrier, arrived by
+//     every storer warp once it has read the statistics);
+//   - storer warps [nred, ncw) wait for row k's statistics, apply h to the
+//     staged slice, write it and hand each chunk slot back to the producer as
+//     their tiles pass it;
+//   - the producer warp streams the rows into the ring as in the kernel above.
+// While the storers write row k the reducers are already folding row k + 1
+// (its chunks land in the slots the storers have released, or in the next row
+// slot when the ring holds two or more rows).  The exchange is always the
+// st.async one: only the reducers take part in it, and the cluster barrier is
+// met twice (entry and exit) by every warp.
+template <int OP, typename T, typename PT>
+__global__ void __launch_bounds__(kPersistMaxThreads, 1)
+cluster_pipelined(const PersistArgs a) {
+    using E = Elem<T>;
+    constexpr int VEC = E::kVec;
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(16) float slots[2][kMaxCluster * kSlotStride];
+    __shared__ __align__(16) float red[2][2][(kPersistMaxThreads / 32) * 2];  // [row parity][stage]
+    __shared__ __align__(16) float hand[2][4];  // row statistics for the storers, by row parity
+    __shared__ __align__(8) uint64_t full_bar[kPersistMaxSlots];
+    __shared__ __align__(8) uint64_t empty_bar[kPersistMaxSlots];
+    __shared__ __align__(8) uint64_t recv_bar[2];     // st.async deposits, by row parity
+    __shared__ __align__(8) uint64_t hand_full[2];    // reducers -> storers
+    __shared__ __align__(8) uint64_t hand_empty[2];   // storers -> reducers
+
+    const uint32_t P = cluster_nctarank();
+    const uint32_t rank = cluster_ctarank();
+    const int64_t cid = blockIdx.x / P;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int ncw = (int)(blockDim.x >> 5) - 1;  // reducer + storer warps; the last warp produces
+    const int nred = a.reducers;                 // 1 <= nred < ncw (checked by the host)
+    const int nsto = ncw - nred;
+    const int64_t start = (int64_t)rank * a.slice;
+    const int n = (int)max((int64_t)0, min(a.cols - start, (int64_t)a.slice));
+    const int nvec = n / VEC;
+    const int vpc = a.chunk / VEC;
+    const int cpr_full = (a.slice + a.chunk - 1) / a.chunk;
+    const int cpr = (n + a.chunk - 1) / a.chunk;
+    const int NR = a.nslots / cpr_full;
+    const uint32_t ring_s = smem_u32(ring);
+    const uint32_t slot_bytes = (uint32_t)a.chunk * (uint32_t)sizeof(T);
+    const int64_t nrows = cid < a.rows ? (a.rows - 1 - cid) / a.nclusters + 1 : 0;
+    const bool clustered = P > 1;
+    const uint32_t xbytes = (P - 1) * 16u;
+    // Every wait is bounded; a thread whose wait gave up (the device error
+    // word records it) skips its later waits, so a launch that went wrong
+    // ends after one time limit per thread instead of one per wait.
+    bool live = true;
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (live) live = mbar_wait_bounded(smem_u32(bar), parity, a.err);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < NR * cpr_full; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), (uint32_t)nsto);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&hand_full[b]), 1);
+            mbar_init(smem_u32(&hand_empty[b]), (uint32_t)nsto);
+            if (clustered) {
+                mbar_init(smem_u32(&recv_bar[b]), 2);
+                if (b < nrows) mbar_arrive_expect_tx(smem_u32(&recv_bar[b]), xbytes);
+            }
+        }
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (clustered) cluster_arrive_relaxed();
+
+    // ------------------------------------------------------------ producer
+    if (warp == ncw) {
+        const uint64_t pol = l2_policy_evict_first();
+        int rs = 0;
+        uint32_t use = 0;
+        for (int64_t k = 0; k < nrows; ++k) {
+            if (lane == 0) {
+                const T* src = static_cast<const T*>(a.x) + (cid + k * a.nclusters) * a.cols + start;
+                for (int c = 0; c < cpr; ++c) {
+                    const int slot = rs * cpr_full + c;
+                    if (use > 0) wait(&empty_bar[slot], (use - 1) & 1u);
+                    const int e0 = c * a.chunk;
+                    const uint32_t bytes = (uint32_t)(min(a.chunk, n - e0) * (int)sizeof(T));
+                    const uint32_t fb = smem_u32(&full_bar[slot]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    bulk_g2s(ring_s + (uint32_t)slot * slot_bytes, src + e0, bytes, fb, pol);
+                }
+            }
+            if (++rs == NR) { rs = 0; ++use; }
+            __syncwarp();
+        }
+        if (clustered) {
+            cluster_wait_acquire();    // entry
+            cluster_arrive_relaxed();  // exit
+            cluster_wait_acquire();
+        }
+        return;
+    }
+
+    if (warp < nred) {
+        // --------------------------------------------------------- reducers
+        const int nrt = nred * 32;
+        int rs = 0;
+        uint32_t use = 0;
+        for (int64_t k = 0; k < nrows; ++k) {
+            unsigned char* base = ring + (size_t)rs * cpr_full * slot_bytes;
+            Stats<OP, T> stt;
+            for (int c = 0; c < cpr; ++c) {
+                wait(&full_bar[rs * cpr_full + c], use & 1u);
+                const int v0 = c * vpc;
+                stats_tiles(stt, base + (size_t)v0 * 16, min(nvec, v0 + vpc) - v0, warp, nred, lane);
+            }
+            auto stash = [&](float mq) { return softmax_stash(base, nvec, warp, nred, lane, mq); };
+            float p0, p1, p2;
+            cta_partial<OP, T>(stt, red[k & 1][0], red[k & 1][1], nred, nrt, stash, p0, p1, p2);
+            // the fp32 softmax stash wrote the slots: order those generic-proxy
+            // writes before the bulk copies that will refill them
+            if constexpr (OP == kSoftmax && sizeof(T) == 4) fence_proxy_async_smem();
+
+            float st0 = p0, st1 = p1, st2 = p2;
+            if (clustered) {
+                if (k == 0) cluster_wait_acquire();  // every peer is running
+                float* sl = slots[k & 1];
+                const uint32_t rb = smem_u32(&recv_bar[k & 1]);
+                if (tid == (int)rank) {
+                    float* d = &sl[rank * kSlotStride];
+                    d[0] = p0; d[1] = p1; d[2] = p2;
+                    mbar_arrive(rb);
+                } else if (tid < (int)P) {
+                    const uint32_t dst = mapa_shared(smem_u32(&sl[rank * kSlotStride]), (uint32_t)tid);
+                    st_async_v4f32(dst, p0, p1, p2, 0.f, mapa_shared(rb, (uint32_t)tid));
+                }
+                wait(&recv_bar[k & 1], (uint32_t)(k >> 1) & 1u);
+                // no peer deposits row k + 2 before this CTA's row k + 1
+                // partial, which follows this row's combine below
+                if (tid == 0 && k + 2 < nrows) mbar_arrive_expect_tx(rb, xbytes);
+                combine_slots<OP>(sl, P, st0, st1, st2);
+            }
+            if (tid == 0) {
+                // the hand-off buffer of row k was last read for row k - 2
+                if (k >= 2)
+                    wait(&hand_empty[k & 1], (uint32_t)((k >> 1) - 1) & 1u);
+                float* h = hand[k & 1];
+                h[0] = st0; h[1] = st1; h[2] = st2; h[3] = p0;
+                mbar_arrive(smem_u32(&hand_full[k & 1]));
+            }
+            if (++rs == NR) { rs = 0; ++use; }
+        }
+        if (clustered && nrows == 0) cluster_wait_acquire();  // entry
+    } else {
+        // ----------------------------------------------------------- storers
+        const int sw = warp - nred;
+        const PT* gp = static_cast<const PT*>(a.p0);
+        const PT* bp = static_cast<const PT*>(a.p1);
+        if (clustered) cluster_wait_acquire();  // entry
+        int rs = 0;
+        uint32_t use = 0;
+        for (int64_t k = 0; k < nrows; ++k) {
+            const int64_t row = cid + k * a.nclusters;
+            unsigned char* base = ring + (size_t)rs * cpr_full * slot_bytes;
+            wait(&hand_full[k & 1], (uint32_t)(k >> 1) & 1u);
+            const float* h4 = hand[k & 1];
+            const float st0 = h4[0], st1 = h4[1], st2 = h4[2], mq = h4[3];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&hand_empty[k & 1]));
+            // the slice's copies have completed (the reducers waited for them
+            // before the hand-off); observe their phases here as well
+            for (int c = 0; c < cpr; ++c)
+                wait(&full_bar[rs * cpr_full + c], use & 1u);
+            const OutputMap<OP, T> hm(st0, st1, st2, mq, a.cols, a.eps);
+            T* yrow = static_cast<T*>(a.y) + row * a.cols + start;
+            int released = 0;
+            auto release = [&](int next_vec) {
+                const int done = min(cpr, next_vec / vpc);
+                if (done > released) {
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int c = released; c < done; ++c)
+                            mbar_arrive(smem_u32(&empty_bar[rs * cpr_full + c]));
+                    released = done;
+                }
+            };
+            output_tiles<OP, T, PT>(hm, base, yrow, gp ? gp + start : nullptr,
+                                    bp ? bp + start : nullptr, nvec, sw, nsto, lane, release);
+            release(cpr * vpc);
+            if (++rs == NR) { rs = 0; ++use; }
+        }
+    }
+    if (clustered) {
+        // every deposit addressed to this CTA has landed (the reducers waited
+        // for each row's); stay until the whole cluster can say the same
+        cluster_arrive_relaxed();
+        cluster_wait_acquire();
+    }
+}
+
 // ----------------------------------------------------------- dispatch
 template <int OP, typename T>
 static const void* pers_param(int pdtype) {
     return pdtype == 0 ? (const void*)cluster_persistent<OP, T, float>
                        : (const void*)cluster_persistent<OP, T, bf16>;
+}
+
+template <int OP, typename T>
+static const void* pipe_param(int pdtype) {
+    return pdtype == 0 ? (const void*)cluster_pipelined<OP, T, float>
+                       : (const void*)cluster_pipelined<OP, T, bf16>;
+}
+
+const void* pipelined_kernel(KernelKey k) {
+    if (!k.vec) return nullptr;
+    switch (k.op) {
+        case kSoftmax: return k.dtype == 0 ? (const void*)cluster_pipelined<kSoftmax, float, float>
+                                           : (const void*)cluster_pipelined<kSoftmax, bf16, float>;
+        case kLayerNorm: return k.dtype == 0 ? pipe_param<kLayerNorm, float>(k.pdtype)
+                                             : pipe_param<kLayerNorm, bf16>(k.pdtype);
+        case kRMSNorm: return k.dtype == 0 ? pipe_param<kRMSNorm, float>(k.pdtype)
+                                           : pipe_param<kRMSNorm, bf16>(k.pdtype);
+    }
+    return nullptr;
+}
+
+// Reducer / storer split of the warp-specialised kernel, from the relative
+// per-element work of the two roles: softmax recomputes the exponential in
+// both (bf16) or stashes it in the reduction (fp32); the norms' output pass
+// carries the parameter loads, RMSNorm's reduction is one FMA per element.
+int pipelined_reducers(int op, int dtype, int consumer_warps) {
+    int r = consumer_warps / 2;
+    if (op == kSoftmax && dtype == 0) r = (consumer_warps * 5) / 8;
+    if (op == kLayerNorm) r = (consumer_warps * 3) / 8;
+    if (op == kRMSNorm) r = consumer_warps / 4;
+    return max(1, min(consumer_warps - 1, r));
 }
 
 const void* persistent_kernel(KernelKey k) {
@@ -225,7 +461,7 @@ const void* persistent_kernel(KernelKey k) {
 
 cudaError_t launch_persistent(KernelKey k, const PersistArgs& a, int P, int threads,
                               size_t smem, cudaStream_t s) {
-    const void* fn = persistent_kernel(k);
+    const void* fn = a.reducers > 0 ? pipelined_kernel(k) : persistent_kernel(k);
     if (!fn) return cudaErrorInvalidDeviceFunction;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.nclusters * P), 1, 1);

@@ -60,7 +60,8 @@ namespace {
 // Persistent plan for a given (P, CTAs per SM).
 credit_status_t persistent_plan(int dev, const DevInfo* d, credit_op_t op, int64_t rows,
                                 int64_t cols, credit_dtype_t dtype, int P, int threads,
-                                int cps, int64_t chunk_override, credit_plan_t* p) {
+                                int cps, int64_t chunk_override, bool pipelined,
+                                credit_plan_t* p) {
     const int es = dtype == CREDIT_F32 ? 4 : 2;
     const int64_t vec = 16 / es;
     const int64_t slice = round_up(ceil_div(cols, P), vec);
@@ -75,7 +76,8 @@ credit_status_t persistent_plan(int dev, const DevInfo* d, credit_op_t op, int64
     const int64_t chunk = chunk_vecs * vec;
     const int64_t chunk_bytes = chunk * es;
     const int64_t cpr = ceil_div(slice, chunk);
-    const void* fn = persistent_kernel(KernelKey{(int)op, (int)dtype, 0, true});
+    const KernelKey key{(int)op, (int)dtype, 0, true};
+    const void* fn = pipelined ? pipelined_kernel(key) : persistent_kernel(key);
     if (!fn) return CREDIT_ERR_NO_LEGAL_PLAN;  // operator not offered by the persistent kernel
     const KernelInfo* ki = kernel_info(dev, fn, true);
     if (!ki) return CREDIT_ERR_CUDA;
@@ -89,12 +91,14 @@ credit_status_t persistent_plan(int dev, const DevInfo* d, credit_op_t op, int64
     if (nr < 1) return CREDIT_ERR_NO_LEGAL_PLAN;  // a whole slice must fit the ring
     const int64_t S = nr * cpr;
     const int t = threads ? threads : (cps == 1 ? kPersistMaxThreads : 288);
-    if (t < 64 || t > kPersistMaxThreads) return CREDIT_ERR_INVALID_ARG;
+    // one producer warp plus at least one consumer warp (one reducer and one
+    // storer warp in the warp-specialised form)
+    if (t < (pipelined ? 96 : 64) || t > kPersistMaxThreads) return CREDIT_ERR_INVALID_ARG;
     const int64_t smem = S * chunk_bytes;
     const int active = occupancy_clusters(dev, fn, P, t, (size_t)smem, rows);
     if (active < 1) return CREDIT_ERR_NO_LEGAL_PLAN;
     const int64_t G = std::min<int64_t>(active, rows);
-    p->variant = CREDIT_CLUSTER_PERSISTENT;
+    p->variant = pipelined ? CREDIT_CLUSTER_PIPELINED : CREDIT_CLUSTER_PERSISTENT;
     p->cluster_size = P;
     p->threads = t;
     p->smem_bytes = smem;
@@ -123,7 +127,8 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
     if (!op_ok(op)) return CREDIT_ERR_UNSUPPORTED;
     if (dtype != CREDIT_F32 && dtype != CREDIT_BF16) return CREDIT_ERR_UNSUPPORTED;
     if (threads != 0 && (threads < 32 || threads % 32 != 0)) return CREDIT_ERR_INVALID_ARG;
-    if (threads > (variant == CREDIT_CLUSTER_PERSISTENT ? kPersistMaxThreads
+    const bool ring = variant == CREDIT_CLUSTER_PERSISTENT || variant == CREDIT_CLUSTER_PIPELINED;
+    if (threads > (ring ? kPersistMaxThreads
                    : variant == CREDIT_CLUSTER             ? kClusterMaxThreads
                                                            : kMaxThreads))
         return CREDIT_ERR_INVALID_ARG;
@@ -171,7 +176,7 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
         const double eff = ctas_per_sm >= 2.0 ? 0.9 : 0.7;
         p.pred_us = (float)(bytes / (kNominalBytesPerUs * eff) +
                             p.waves * (P > 1 ? kWaveUsCluster : kWaveUsSingle));
-    } else if (variant == CREDIT_CLUSTER_PERSISTENT) {
+    } else if (ring) {
         if (P < 1 || P > kMaxCluster) return CREDIT_ERR_NO_LEGAL_PLAN;
         if (cps != 0 && cps != 1 && cps != 2) return CREDIT_ERR_INVALID_ARG;
         credit_status_t best = CREDIT_ERR_NO_LEGAL_PLAN;
@@ -180,7 +185,8 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
             credit_plan_t q;
             std::memset(&q, 0, sizeof(q));
             const credit_status_t st =
-                persistent_plan(dev, d, op, rows, cols, dtype, P, threads, c, chunk, &q);
+                persistent_plan(dev, d, op, rows, cols, dtype, P, threads, c, chunk,
+                                variant == CREDIT_CLUSTER_PIPELINED, &q);
             if (st == CREDIT_ERR_CUDA || st == CREDIT_ERR_INVALID_ARG) return st;
             if (st == CREDIT_OK && (best != CREDIT_OK || q.pred_us < p.pred_us)) {
                 p = q;

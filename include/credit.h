@@ -69,9 +69,14 @@ typedef enum {
     CREDIT_CLUSTER = 1,    /* clustered DSMEM kernel, one row per cluster of
                               cluster_size = P CTAs (1..16) */
     CREDIT_TWO_PASS = 2,   /* non-clustered two-pass re-read kernel pair */
-    CREDIT_CLUSTER_PERSISTENT = 3  /* clustered DSMEM kernel, resident clusters
+    CREDIT_CLUSTER_PERSISTENT = 3, /* clustered DSMEM kernel, resident clusters
                               loop over rows; a producer warp streams chunks
                               into a ring of shared-memory slots */
+    CREDIT_CLUSTER_PIPELINED = 4   /* the persistent kernel with warp-specialised
+                              consumers: reducer warps fold, exchange and
+                              combine row k + 1 while storer warps write row
+                              k (softmax, LayerNorm, RMSNorm; ASYNC exchange
+                              only) */
 } credit_variant_t;
 
 /*
@@ -97,8 +102,9 @@ typedef enum {
 /*
  * A launch plan.  Produced by credit_plan / credit_plan_for; may be passed to
  * the operator calls (NULL there means "plan automatically").
- *   variant          CREDIT_CLUSTER, CREDIT_CLUSTER_PERSISTENT or
- *                    CREDIT_TWO_PASS (never AUTO once planned)
+ *   variant          CREDIT_CLUSTER, CREDIT_CLUSTER_PERSISTENT,
+ *                    CREDIT_CLUSTER_PIPELINED or CREDIT_TWO_PASS (never AUTO
+ *                    once planned)
  *   cluster_size     P, CTAs per row (1..16; 1 = one CTA stages the whole row)
  *   threads          threads per CTA
  *   waves            predicted waves of resident clusters, ceil(rows / active)
@@ -110,7 +116,8 @@ typedef enum {
  *                    the persistent grid has this many clusters
  *   ctas_per_sm      CTAs the plan expects to share one SM
  *   chunk_elems      elements per bulk copy (one mbarrier each)
- *   ring_slots       shared-memory chunk slots per CTA (persistent only)
+ *   ring_slots       shared-memory chunk slots per CTA (persistent and
+ *                    pipelined only)
  *   rows_per_cluster rows one cluster stages and reduces together (CLUSTER:
  *                    1, 2 or 4; their partials share one exchange and each
  *                    parameter load serves all of them)
@@ -152,8 +159,8 @@ credit_status_t credit_plan(credit_op_t op, int64_t rows, int64_t cols,
                             credit_plan_t *out);
 
 /*
- * Build a plan for a forced variant: CREDIT_CLUSTER or
- * CREDIT_CLUSTER_PERSISTENT with the given cluster_size (1..16), or
+ * Build a plan for a forced variant: CREDIT_CLUSTER, CREDIT_CLUSTER_PERSISTENT
+ * or CREDIT_CLUSTER_PIPELINED with the given cluster_size (1..16), or
  * CREDIT_TWO_PASS (cluster_size ignored).
  * Returns CREDIT_ERR_NO_LEGAL_PLAN if the slice does not fit in shared memory
  * or no cluster of that size can be resident.
@@ -165,7 +172,8 @@ credit_status_t credit_plan_for(credit_op_t op, int64_t rows, int64_t cols,
 
 /*
  * Complete a plan from a partial request: `request->variant` (CLUSTER,
- * CLUSTER_PERSISTENT or TWO_PASS) and, for the clustered variants,
+ * CLUSTER_PERSISTENT, CLUSTER_PIPELINED or TWO_PASS) and, for the clustered
+ * variants,
  * `request->cluster_size` are required; `threads`, `ctas_per_sm`,
  * `chunk_elems` and `rows_per_cluster` are used when non-zero and chosen
  * otherwise; every other field is ignored.  The operator calls re-derive a
@@ -381,8 +389,8 @@ credit_status_t credit_run_host(const credit_host_call_t *call,
  * if it beats T_base, else the baseline.  As on the pages, the model screens
  * and a final tuning step may pick another legal size: with tune > 0 the
  * `tune` best-predicted clustered candidates (one-row-per-cluster, and the
- * persistent kernel of the same P) are timed and the fastest measured plan,
- * baseline included, is chosen.
+ * persistent and pipelined kernels of the same P) are timed and the fastest
+ * measured plan, baseline included, is chosen.
  */
 typedef struct {
     int32_t cluster_size;    /* P; 1 = the baseline */
@@ -394,6 +402,9 @@ typedef struct {
     double measured_us;      /* tuning: measured time of `plan` (0 = not timed) */
     double persistent_us;    /* tuning: measured time of the persistent kernel
                                 of this P (0 = not timed or not legal) */
+    double pipelined_us;     /* tuning: measured time of the warp-specialised
+                                persistent kernel of this P (0 = not timed or
+                                not legal) */
 } credit_candidate_t;
 
 typedef struct {

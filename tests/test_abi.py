@@ -54,11 +54,40 @@ def test_plan_struct_layout_matches_header():
     assert C.Plan.exchange.offset == 60
 
 
+def test_struct_mirrors_match_the_header(tmp_path):
+    # sizes and field offsets of the plan, candidate and report structs as
+    # the C compiler lays them out from include/credit.h, against the ctypes
+    # mirrors the binding passes to the library
+    src = tmp_path / "layout.c"
+    src.write_text("""
+#include <stddef.h>
+#include <stdio.h>
+#include "credit.h"
+int main(void) {
+    printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(credit_plan_t), sizeof(credit_candidate_t),
+           sizeof(credit_model_report_t), offsetof(credit_candidate_t, persistent_us),
+           offsetof(credit_candidate_t, pipelined_us), offsetof(credit_model_report_t, cand),
+           sizeof(credit_host_call_t));
+    return 0;
+}
+""")
+    exe = tmp_path / "layout"
+    cuda_inc = "/usr/local/cuda/include"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o",
+                    str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert got == [ctypes.sizeof(C.Plan), ctypes.sizeof(C.Candidate),
+                   ctypes.sizeof(C.ModelReport), C.Candidate.persistent_us.offset,
+                   C.Candidate.pipelined_us.offset, C.ModelReport.cand.offset,
+                   ctypes.sizeof(C.HostCall)]
+
+
 def test_status_strings(lib):
     for s in range(7):
         assert C.status_string(s)
     assert C.status_string(C.ERR_NO_LEGAL_PLAN).startswith("no legal plan")
-    assert C.credit_version().count(".") == 2
+    assert C.credit_version() == "0.3.0"
 
 
 def test_host_side_argument_checks_need_no_gpu(lib):

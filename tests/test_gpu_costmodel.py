@@ -77,7 +77,7 @@ def test_large_shape_is_timed_on_its_first_rows():
     assert rep.t_base_us > 0
     if plan.variant == C.CLUSTER:
         assert plan.waves == -(-rows // (plan.active_clusters * plan.rows_per_cluster))
-    elif plan.variant == C.CLUSTER_PERSISTENT:
+    elif plan.variant in (C.CLUSTER_PERSISTENT, C.CLUSTER_PIPELINED):
         assert plan.waves == -(-rows // plan.active_clusters)
     auto = C.credit_plan(C.RMSNORM, rows, cols, C.BF16, 0)
     assert auto.variant == plan.variant and auto.cluster_size == plan.cluster_size
