@@ -334,6 +334,10 @@ credit_status_t run(const OpCall& c) {
         a.err = err;
         a.exchange = (piped || plan.exchange == CREDIT_EXCHANGE_ASYNC) ? 1 : 0;
         a.reducers = piped ? pipelined_reducers(key.op, key.dtype, plan.threads / 32 - 1) : 0;
+        // the parameter room follows the ring (warp-specialised plans only)
+        const int64_t ring_bytes = (int64_t)plan.ring_slots * plan.chunk_elems * (int64_t)es;
+        a.param_off = piped && plan.smem_bytes > ring_bytes ? (int32_t)ring_bytes : 0;
+        a.param_room = a.param_off ? (int32_t)(plan.smem_bytes - ring_bytes) : 0;
         const void* fn = piped ? pipelined_kernel(key) : persistent_kernel(key);
         if (!kernel_info(dev, fn, true)) return CREDIT_ERR_CUDA;
         return from_cuda(launch_persistent(key, a, plan.cluster_size, plan.threads,

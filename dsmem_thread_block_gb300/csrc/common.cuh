@@ -295,6 +295,11 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
 
+// Named barrier `id` among `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_sync_id(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
 // Barrier among the first `nthreads` threads of the CTA (named barrier 1).
 __device__ __forceinline__ void named_sync(int nthreads) {
     asm volatile("bar.sync 1, %0;" :: "r"(nthreads) : "memory");

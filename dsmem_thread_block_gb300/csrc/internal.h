@@ -60,6 +60,9 @@ struct PersistArgs {
     unsigned* err;
     int32_t exchange;     // 0: push + cluster barrier per row; 1: st.async deposits + mbarrier
     int32_t reducers;     // 0: one consumer role; > 0: reducer warps of the warp-specialised kernel
+    int32_t param_off;    // warp-specialised kernel: byte offset of the parameter room in
+                          // dynamic shared memory (0 = none)
+    int32_t param_room;   // bytes of that room
 };
 
 constexpr int kPersistMaxSlots = 32;

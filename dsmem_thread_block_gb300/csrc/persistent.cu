@@ -215,6 +215,10 @@ cluster_persistent(const PersistArgs a) {
 //     staged slice, write it and hand each chunk slot back to the producer as
 //     their tiles pass it;
 //   - the producer warp streams the rows into the ring as in the kernel above.
+// A CTA owns the same column slice of every row it handles, so when the plan
+// leaves room for them the storers copy the slice's parameters (gamma / beta,
+// weight) into shared memory once per launch and read them from there for
+// every row, instead of streaming them from L2 row after row.
 // While the storers write row k the reducers are already folding row k + 1
 // (its chunks land in the slots the storers have released, or in the next row
 // slot when the ring holds two or more rows).  The exchange is always the
@@ -366,6 +370,35 @@ cluster_pipelined(const PersistArgs a) {
         const int sw = warp - nred;
         const PT* gp = static_cast<const PT*>(a.p0);
         const PT* bp = static_cast<const PT*>(a.p1);
+        constexpr bool kParams = OP == kLayerNorm || OP == kRMSNorm;
+        const int pbytes = (n * (int)sizeof(PT) + 15) & ~15;  // one parameter's slice, padded
+        const int need = kParams ? (gp ? pbytes : 0) + (bp ? pbytes : 0) : 0;
+        const bool pstage = need > 0 && a.param_off > 0 && need <= a.param_room;
+        const PT* gs = nullptr;
+        const PT* bs = nullptr;
+        if (pstage) {
+            // the storers copy the slice's parameters into the room once
+            unsigned char* room = ring + a.param_off;
+            const int stid = tid - nred * 32, nst = nsto * 32;
+            auto copy_slice = [&](const PT* src, unsigned char* dst) {
+                const PT* s0 = src + start;
+                int done = 0;
+                if ((reinterpret_cast<uintptr_t>(s0) & 15) == 0) {
+                    const int nv = n * (int)sizeof(PT) / 16;
+                    for (int i = stid; i < nv; i += nst)
+                        reinterpret_cast<uint4*>(dst)[i] = __ldg(reinterpret_cast<const uint4*>(s0) + i);
+                    done = nv * 16 / (int)sizeof(PT);
+                }
+                for (int i = done + stid; i < n; i += nst) reinterpret_cast<PT*>(dst)[i] = s0[i];
+            };
+            if (gp) { copy_slice(gp, room); gs = reinterpret_cast<const PT*>(room); }
+            if (bp) {
+                unsigned char* d = room + (gp ? pbytes : 0);
+                copy_slice(bp, d);
+                bs = reinterpret_cast<const PT*>(d);
+            }
+            named_sync_id(2, nst);  // the storers only
+        }
         if (clustered) cluster_wait_acquire();  // entry
         int rs = 0;
         uint32_t use = 0;
@@ -394,8 +427,13 @@ cluster_pipelined(const PersistArgs a) {
                     released = done;
                 }
             };
-            output_tiles<OP, T, PT>(hm, base, yrow, gp ? gp + start : nullptr,
-                                    bp ? bp + start : nullptr, nvec, sw, nsto, lane, release);
+            if (pstage) {
+                output_tiles<OP, T, PT, decltype(release), true>(hm, base, yrow, gs, bs, nvec, sw,
+                                                                 nsto, lane, release);
+            } else {
+                output_tiles<OP, T, PT>(hm, base, yrow, gp ? gp + start : nullptr,
+                                        bp ? bp + start : nullptr, nvec, sw, nsto, lane, release);
+            }
             release(cpr * vpc);
             if (++rs == NR) { rs = 0; ++use; }
         }

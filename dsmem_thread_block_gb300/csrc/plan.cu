@@ -84,7 +84,23 @@ credit_status_t persistent_plan(int dev, const DevInfo* d, credit_op_t op, int64
     const int64_t budget = cps == 1
         ? ki->max_dyn_smem
         : (int64_t)d->smem_per_sm / cps - ki->static_smem - d->reserved_smem;
-    const int64_t fit = std::min<int64_t>(kPersistMaxSlots, budget / chunk_bytes);
+    // the warp-specialised kernel keeps the slice's parameters in shared
+    // memory when a room for them (fp32-sized, else sized like the data
+    // elements) fits beside two row slots of the ring, one CTA per SM (with
+    // one row slot the next row's reduction waits for this row's output,
+    // which costs more than the parameter stream saves)
+    int64_t room = 0;
+    if (pipelined && cps == 1 && (op == CREDIT_LAYERNORM || op == CREDIT_RMSNORM)) {
+        const int np = op == CREDIT_LAYERNORM ? 2 : 1;
+        for (int pes : {4, es}) {
+            const int64_t r = np * round_up(slice * pes, 16);
+            if (2 * cpr * chunk_bytes + r <= budget) {
+                room = r;
+                break;
+            }
+        }
+    }
+    const int64_t fit = std::min<int64_t>(kPersistMaxSlots, (budget - room) / chunk_bytes);
     // the ring holds whole row slices (contiguous in shared memory): at least
     // one, up to three
     const int64_t nr = std::min<int64_t>(3, fit / cpr);
@@ -94,7 +110,7 @@ credit_status_t persistent_plan(int dev, const DevInfo* d, credit_op_t op, int64
     // one producer warp plus at least one consumer warp (one reducer and one
     // storer warp in the warp-specialised form)
     if (t < (pipelined ? 96 : 64) || t > kPersistMaxThreads) return CREDIT_ERR_INVALID_ARG;
-    const int64_t smem = S * chunk_bytes;
+    const int64_t smem = S * chunk_bytes + room;  // the ring, then the parameter room
     const int active = occupancy_clusters(dev, fn, P, t, (size_t)smem, rows);
     if (active < 1) return CREDIT_ERR_NO_LEGAL_PLAN;
     const int64_t G = std::min<int64_t>(active, rows);

@@ -367,12 +367,18 @@ struct Granule {
     static constexpr int kPairs = kElems / 2;
 };
 
-// Load the parameters of one granule (kElems values, <= 16 bytes) as pairs.
-template <typename PT, int NP>
+// Load the parameters of one granule (kElems values, <= 16 bytes) as pairs;
+// SMEM: `p` points into shared memory (a slice staged once by the caller),
+// else into global memory (read-only path).
+template <typename T> __device__ __forceinline__ T param_ld(const T* p, bool smem) {
+    return smem ? *p : __ldg(p);
+}
+
+template <typename PT, int NP, bool SMEM = false>
 __device__ __forceinline__ void granule_params(const PT* p, int q, F2* out) {
     if constexpr (sizeof(PT) == 4) {
         if constexpr (NP == 2) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(p) + q);
+            const float4 v = param_ld(reinterpret_cast<const float4*>(p) + q, SMEM);
             out[0] = make_float2(v.x, v.y);
             out[1] = make_float2(v.z, v.w);
         } else {  // NP == 4 cannot happen for fp32 parameters (16 bytes max)
@@ -380,10 +386,10 @@ __device__ __forceinline__ void granule_params(const PT* p, int q, F2* out) {
         }
     } else {
         if constexpr (NP == 4) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + q);
+            const uint4 v = param_ld(reinterpret_cast<const uint4*>(p) + q, SMEM);
             Pairs<bf16>::unpack(v, out);
         } else {
-            const uint2 v = __ldg(reinterpret_cast<const uint2*>(p) + q);
+            const uint2 v = param_ld(reinterpret_cast<const uint2*>(p) + q, SMEM);
             out[0] = Pairs<bf16>::one(v.x);
             out[1] = Pairs<bf16>::one(v.y);
         }
@@ -401,8 +407,9 @@ struct NoRelease {
 // so parameter fetches overlap instead of queueing behind stores.  After
 // each tile `release(v)` is told the first staged vector the warp may still
 // read (the start of its next tile; nvec at the end), so a caller can hand
-// back the shared memory the warp has finished with.
-template <int OP, typename T, typename PT, typename Release = NoRelease>
+// back the shared memory the warp has finished with.  SMEM: gp / bp point to
+// a copy of the slice's parameters in shared memory.
+template <int OP, typename T, typename PT, typename Release = NoRelease, bool SMEM = false>
 __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const unsigned char* base,
                                              T* yrow, const PT* gp, const PT* bp, int nvec,
                                              int warp, int nwarps, int lane,
@@ -428,9 +435,9 @@ __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const un
                     raw[u] = lds16(base + (size_t)q * 16);
                 }
                 if constexpr (kParams) {
-                    if (has_g) granule_params<PT, NP>(gp, q, gv[u]);
+                    if (has_g) granule_params<PT, NP, SMEM>(gp, q, gv[u]);
                     else for (int i = 0; i < NP; ++i) gv[u][i] = f2(1.f);
-                    if (has_b) granule_params<PT, NP>(bp, q, bv[u]);
+                    if (has_b) granule_params<PT, NP, SMEM>(bp, q, bv[u]);
                     else for (int i = 0; i < NP; ++i) bv[u][i] = f2(0.f);
                 }
             }

@@ -136,3 +136,27 @@ def test_pipelined_in_place():
     w = _w(wl.RMSNORM, "bf16", 12, 131072, 212, eps=1e-6, param_dtype="bf16")
     inp = w.generate()
     check(w, run(w, inp, _plan(w, 4), in_place=True), inp)
+
+
+def test_pipelined_staged_parameters():
+    # the storers copy each CTA's parameter slice into shared memory once:
+    # slices whose parameter bytes start 8 bytes past a 16-byte boundary
+    # (fp32 data, bf16 parameters, slice = 4 mod 8) take the element copy;
+    # gamma without beta; many rows per cluster reuse the staged copy
+    dev = torch.cuda.current_device()
+    w = _w(wl.LAYERNORM, "f32", 64, 8200, 213, x_mean=-1.0, x_std=3.0, eps=1e-5,
+           param_dtype="bf16")
+    inp = w.generate()
+    g_only = {k: v for k, v in inp.items() if k != "beta"}
+    ran = 0
+    for P in (2, 3, 6):
+        p = _plan(w, P)
+        if p is None:
+            continue
+        ring = p.ring_slots * p.chunk_elems * 4
+        assert p.smem_bytes > ring  # a parameter room follows the ring
+        check(w, run(w, inp, p), inp)
+        check(w, run(w, g_only, p), g_only)
+        ran += 1
+    assert ran >= 2
+    assert C.credit_get_device_error(dev) == C.OK
