@@ -15,7 +15,8 @@ import threading
 from . import build as _build
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_LEGAL_PLAN, ERR_CUDA, \
-    ERR_DEVICE_TIMEOUT, ERR_NOT_CALIBRATED = range(7)
+    ERR_DEVICE_TIMEOUT, ERR_NOT_CALIBRATED, ERR_DEVICE_BOUNDS = range(8)
+TRACE_CTAS = 8192  # CREDIT_TRACE_CTAS
 F32, BF16 = 0, 1
 SOFTMAX, LAYERNORM, RMSNORM, QUANTIZE, WEIGHTED_STD, PEARSON = 0, 1, 2, 3, 4, 5
 AUTO, CLUSTER, TWO_PASS, CLUSTER_PERSISTENT, CLUSTER_PIPELINED = 0, 1, 2, 3, 4
@@ -138,6 +139,9 @@ SIGNATURES = {
                                _vp]),
     "credit_get_device_error": (_i32, [_i32]),
     "credit_selftest_wait_timeout": (_i32, [_i32, _i64]),
+    "credit_debug_build": (_i32, []),
+    "credit_selftest_bounds": (_i32, [_i32]),
+    "credit_debug_trace": (_i32, [_vp, _i64]),
     "credit_version": (ctypes.c_char_p, []),
 }
 
@@ -147,6 +151,14 @@ _lib = None
 
 def library_path() -> str:
     return _build.LIB
+
+
+def _open(path: str) -> ctypes.CDLL:
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype, f.argtypes = res, args
+    return lib
 
 
 def load(build_if_missing: bool = False) -> ctypes.CDLL:
@@ -161,12 +173,31 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                         f"libcredit.so is not built ({path}); run "
                         "`python -c 'import __graft_entry__ as g; g.build()'`")
                 _build.build()
-            lib = ctypes.CDLL(path)
-            for name, (res, args) in SIGNATURES.items():
-                f = getattr(lib, name)
-                f.restype, f.argtypes = res, args
-            _lib = lib
+            _lib = _open(path)
     return _lib
+
+
+class use_checked_build:
+    """Context manager: route every call of this module to the checked
+    build (libcredit_checked.so: index checks and the phase trace) and back
+    to the regular library on exit."""
+
+    def __enter__(self):
+        global _lib
+        path = _build.CHECKED_LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"the checked build is missing ({path}); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        with _lock:
+            self._saved = _lib
+            _lib = _open(path)
+        return _lib
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self._saved
+        return False
 
 
 def status_string(status: int) -> str:
@@ -331,6 +362,23 @@ def credit_get_device_error(device: int) -> int:
 
 def credit_selftest_wait_timeout(device: int = 0, limit_ns: int = 2_000_000) -> int:
     return load().credit_selftest_wait_timeout(device, limit_ns)
+
+
+def credit_debug_build() -> int:
+    return load().credit_debug_build()
+
+
+def credit_selftest_bounds(device: int = 0) -> int:
+    return load().credit_selftest_bounds(device)
+
+
+def credit_debug_trace(ctas: int):
+    """The checked build's phase trace of the first `ctas` CTAs: an int64
+    array [ctas, 8] (seven %globaltimer stamps in ns, then the SM id)."""
+    import numpy as np
+    out = np.zeros((ctas, 8), dtype=np.uint64)
+    _check(load().credit_debug_trace(out.ctypes.data, ctas), "credit_debug_trace")
+    return out.astype(np.int64)
 
 
 def credit_version() -> str:

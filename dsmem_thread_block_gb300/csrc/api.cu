@@ -29,6 +29,14 @@ __global__ void selftest_wait_kernel(unsigned* err, unsigned long long limit_ns)
     mbar_wait_limited(b, 0, err, limit_ns);
 }
 
+// A failed index check of the checked build, recorded by the same helper the
+// kernels use; nothing outside any buffer is touched.
+__global__ void selftest_bounds_kernel(unsigned* err) {
+    __shared__ float probe[4];
+    const int i = 4 + (int)threadIdx.x;  // one past the end
+    if (in_bounds(i < 4, err)) probe[i] = 0.f;
+}
+
 namespace {
 
 std::mutex g_mu;
@@ -463,6 +471,7 @@ const char* credit_status_string(credit_status_t s) {
         case CREDIT_ERR_CUDA: return "CUDA runtime error";
         case CREDIT_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
         case CREDIT_ERR_NOT_CALIBRATED: return "device not calibrated";
+        case CREDIT_ERR_DEVICE_BOUNDS: return "a device index check failed (checked build)";
     }
     return "unknown status";
 }
@@ -477,7 +486,31 @@ credit_status_t credit_get_device_error(int device) {
         cudaGetLastError();
         return CREDIT_ERR_CUDA;
     }
-    return (v & kErrTimeout) ? CREDIT_ERR_DEVICE_TIMEOUT : CREDIT_OK;
+    if (v & kErrTimeout) return CREDIT_ERR_DEVICE_TIMEOUT;
+    return (v & kErrBounds) ? CREDIT_ERR_DEVICE_BOUNDS : CREDIT_OK;
+}
+
+int credit_debug_build(void) {
+#ifdef CREDIT_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+credit_status_t credit_selftest_bounds(int device) {
+#ifdef CREDIT_DEBUG
+    DeviceGuard g(device);
+    if (!g.ok) return CREDIT_ERR_INVALID_ARG;
+    unsigned* err = device_error_word();
+    if (!err) return CREDIT_ERR_CUDA;
+    selftest_bounds_kernel<<<1, 1>>>(err);
+    if (cudaGetLastError() != cudaSuccess) return CREDIT_ERR_CUDA;
+    return credit_get_device_error(device);
+#else
+    (void)device;
+    return CREDIT_ERR_UNSUPPORTED;
+#endif
 }
 
 credit_status_t credit_selftest_wait_timeout(int device, int64_t limit_ns) {
@@ -491,6 +524,6 @@ credit_status_t credit_selftest_wait_timeout(int device, int64_t limit_ns) {
     return credit_get_device_error(device);
 }
 
-const char* credit_version(void) { return "0.3.0"; }
+const char* credit_version(void) { return "0.4.0"; }
 
 }  // extern "C"

@@ -25,11 +25,28 @@
 // With the barrier exchange no CTA touches a peer's shared memory after a5,
 // so CTAs may exit without the second barrier (the page's second barrier
 // protects slot reuse, which a one-row-per-cluster launch never does).
+#include "credit.h"
 #include "common.cuh"
 #include "internal.h"
 #include "rowops.cuh"
 
 namespace credit {
+
+// Phase trace of the checked build: thread 0 of each CTA below kTraceCtas
+// stamps %globaltimer at seven points of its life, and its SM id.
+constexpr int kTraceCtas = CREDIT_TRACE_CTAS;
+#ifdef CREDIT_DEBUG
+__device__ unsigned long long g_trace[kTraceCtas][8];
+#define CREDIT_TRACE(i)                                                        \
+    do {                                                                       \
+        if (threadIdx.x == 0 && blockIdx.x < (unsigned)kTraceCtas)             \
+            g_trace[blockIdx.x][(i)] = (i) == 7 ? smid() : globaltimer_ns();   \
+    } while (0)
+#else
+#define CREDIT_TRACE(i) \
+    do {                \
+    } while (0)
+#endif
 
 // DEEP: the instantiation for slices that leave room for at most two CTAs
 // per SM -- it may use twice the registers, which its pipelined output pass
@@ -53,11 +70,21 @@ cluster_reduce_reuse(const ClusterArgs a) {
     const int64_t row0 = (blockIdx.x / P) * (int64_t)R;
     const int rows = (int)min((int64_t)R, a.rows - row0);  // live rows of this cluster
     const int64_t start = (int64_t)rank * a.slice;
-    const int n = (int)max((int64_t)0, min(a.cols - start, a.slice));
+    const int n_slice = (int)max((int64_t)0, min(a.cols - start, a.slice));
+    // checked build: the live rows' staged slices and their chunk mbarriers
+    // must fit the launch
+    const int n = layout_fits(BULK ? (uint64_t)(rows - 1) * a.pitch + (uint64_t)n_slice * sizeof(T)
+                                   : (uint64_t)n_slice * sizeof(T),
+                              BULK ? (int64_t)rows * ((n_slice + a.chunk_elems - 1) / a.chunk_elems)
+                                   : 0,
+                              kMaxChunks, a.err)
+                      ? n_slice : 0;
     const T* xs = static_cast<const T*>(a.x) + row0 * a.cols + start;
     const int tid = threadIdx.x, nt = blockDim.x;
     const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
     const int nvec = n / VEC;  // whole 16-byte vectors (all of n on the bulk path)
+    CREDIT_TRACE(0);
+    CREDIT_TRACE(7);
 
     if (async_x && threadIdx.x == 0) {
         // the exchange's mbarrier: two arrivals (this one, which registers the
@@ -97,6 +124,7 @@ cluster_reduce_reuse(const ClusterArgs a) {
             }
         }
         __syncthreads();
+        CREDIT_TRACE(1);
     } else {
         T* st = reinterpret_cast<T*>(stage);
         for (int i = tid; i < n; i += nt) st[i] = xs[i];
@@ -128,6 +156,7 @@ cluster_reduce_reuse(const ClusterArgs a) {
             for (int i = nvec * VEC + tid; i < n; i += nt) st[0].add1(tail_at(i));
         }
     }
+    CREDIT_TRACE(2);
     auto stash = [&](int i, float mq) {
         float s = softmax_stash(stage + (size_t)i * a.pitch, nvec, warp, nwarps, lane, mq);
         if constexpr (!BULK) {
@@ -141,6 +170,7 @@ cluster_reduce_reuse(const ClusterArgs a) {
     };
     float p[R][3];
     cta_partial_rows<OP, T, R>(st, red[0], red[1], nwarps, nt, stash, p);
+    CREDIT_TRACE(3);
 
     // --------------------------------------- a4 push, a5 barrier, a6 combine
     float stv[R][3];  // combined statistics, identical in every CTA of the cluster
@@ -188,6 +218,7 @@ cluster_reduce_reuse(const ClusterArgs a) {
         }
     }
 
+    CREDIT_TRACE(4);
     // ------------------------------------------------------- a7 output
     constexpr bool kParams = OP == kLayerNorm || OP == kRMSNorm;
     const PT* g = kParams ? static_cast<const PT*>(a.p0) : nullptr;
@@ -232,10 +263,12 @@ cluster_reduce_reuse(const ClusterArgs a) {
             }
         }
     }
+    CREDIT_TRACE(5);
     // st.async exchange: a peer arrives only once all deposits to it have
     // landed, so when this completes every deposit in the cluster has, and
     // no CTA leaves while one is in flight
     if (async_x) cluster_wait_acquire();
+    CREDIT_TRACE(6);
 }
 
 // ----------------------------------------------------------- dispatch
@@ -318,3 +351,19 @@ cudaError_t launch_cluster(KernelKey k, const ClusterArgs& a, int P, int threads
 }
 
 }  // namespace credit
+
+extern "C" credit_status_t credit_debug_trace(void* host, int64_t ctas) {
+#ifdef CREDIT_DEBUG
+    if (!host || ctas < 1 || ctas > credit::kTraceCtas) return CREDIT_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(host, credit::g_trace, (size_t)ctas * 64) != cudaSuccess) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
+    return CREDIT_OK;
+#else
+    (void)host;
+    (void)ctas;
+    return CREDIT_ERR_UNSUPPORTED;
+#endif
+}

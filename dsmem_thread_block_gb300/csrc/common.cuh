@@ -42,6 +42,7 @@ constexpr int kSlotStride = 4;    // floats per pushed partial (16 bytes)
 
 // Device error word bits.
 constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrBounds = 2u;  // checked build: an index check failed
 
 // Bounded waits give up after this long (a second or so).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -285,6 +286,46 @@ __device__ __forceinline__ bool mbar_wait_limited(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   unsigned* err) {
     return mbar_wait_limited(bar, parity, err, kWaitLimitNs);
+}
+
+// ------------------------------------------------------------- checked build
+// Index checks of the checked build (-DCREDIT_DEBUG): a failed check records
+// kErrBounds in the device error word and the caller skips the access.  In
+// the regular build every check is a compile-time true.
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned* err) {
+#ifdef CREDIT_DEBUG
+    if (!ok) atomicOr(err, kErrBounds);
+    return ok;
+#else
+    (void)ok;
+    (void)err;
+    return true;
+#endif
+}
+
+// Dynamic shared memory of the running launch, bytes.
+__device__ __forceinline__ uint32_t dyn_smem_bytes() {
+    uint32_t r;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+    return r;
+}
+
+// Does a CTA's staged layout fit its launch?  `end` is one past the highest
+// byte it stages into dynamic shared memory, `chunks` the chunk mbarriers (or
+// ring slots) it needs of `max_chunks`.  A CTA whose layout does not fit
+// stages nothing (its slice counts as empty) but still takes part in every
+// exchange and cluster barrier, so its peers are not left waiting forever.
+__device__ __forceinline__ bool layout_fits(uint64_t end, int64_t chunks, int max_chunks,
+                                            unsigned* err) {
+#ifdef CREDIT_DEBUG
+    return in_bounds(end <= dyn_smem_bytes() && chunks <= max_chunks, err);
+#else
+    (void)end;
+    (void)chunks;
+    (void)max_chunks;
+    (void)err;
+    return true;
+#endif
 }
 
 }  // namespace credit

@@ -153,7 +153,12 @@ cluster_pearson(const ClusterArgs a) {
     const bool async_x = a.exchange == 1 && P > 1;
     const int64_t row = blockIdx.x / P;
     const int64_t start = (int64_t)rank * a.slice;
-    const int n = (int)max((int64_t)0, min(a.cols - start, a.slice));
+    const int n_slice = (int)max((int64_t)0, min(a.cols - start, a.slice));
+    // checked build: both staged operands and their chunk mbarriers must fit
+    const int n = layout_fits((uint64_t)a.pitch + (uint64_t)n_slice * sizeof(T),
+                              BULK ? 2 * (int64_t)((n_slice + a.chunk_elems - 1) / a.chunk_elems) : 0,
+                              kMaxChunks, a.err)
+                      ? n_slice : 0;
     const T* xs = static_cast<const T*>(a.x) + row * a.cols + start;
     const T* us = static_cast<const T*>(a.p0) + row * a.cols + start;
     unsigned char* ustage = stage + a.pitch;

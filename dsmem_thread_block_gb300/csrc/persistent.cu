@@ -51,12 +51,15 @@ cluster_persistent(const PersistArgs a) {
     const int ncw = (int)(blockDim.x >> 5) - 1;  // consumer warps; the last warp produces
     const int nct = ncw * 32;
     const int64_t start = (int64_t)rank * a.slice;
-    const int n = (int)max((int64_t)0, min(a.cols - start, (int64_t)a.slice));
+    const int cpr_full = (a.slice + a.chunk - 1) / a.chunk;  // slots per row slot
+    const int NR = a.nslots / cpr_full;                 // rows the ring holds
+    // checked build: the ring's slots and bytes must fit the launch
+    const bool fits = layout_fits((uint64_t)a.nslots * a.chunk * sizeof(T), (int64_t)NR * cpr_full,
+                                  kPersistMaxSlots, a.err);
+    const int n = fits ? (int)max((int64_t)0, min(a.cols - start, (int64_t)a.slice)) : 0;
     const int nvec = n / VEC;
     const int vpc = a.chunk / VEC;                      // vectors per slot
-    const int cpr_full = (a.slice + a.chunk - 1) / a.chunk;  // slots per row slot
     const int cpr = (n + a.chunk - 1) / a.chunk;        // chunks this CTA stages per row
-    const int NR = a.nslots / cpr_full;                 // rows the ring holds
     const uint32_t ring_s = smem_u32(ring);             // shared-window address for the bulk copies
     const uint32_t slot_bytes = (uint32_t)a.chunk * (uint32_t)sizeof(T);
     const int64_t nrows = cid < a.rows ? (a.rows - 1 - cid) / a.nclusters + 1 : 0;
@@ -68,7 +71,7 @@ cluster_persistent(const PersistArgs a) {
     // slot's use count is k div NR.  Both are tracked incrementally.
 
     if (tid == 0) {
-        for (int s = 0; s < NR * cpr_full; ++s) {
+        for (int s = 0; s < (fits ? NR * cpr_full : 0); ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), (uint32_t)ncw);
         }
@@ -248,12 +251,17 @@ cluster_pipelined(const PersistArgs a) {
     const int nred = a.reducers;                 // 1 <= nred < ncw (checked by the host)
     const int nsto = ncw - nred;
     const int64_t start = (int64_t)rank * a.slice;
-    const int n = (int)max((int64_t)0, min(a.cols - start, (int64_t)a.slice));
+    const int cpr_full = (a.slice + a.chunk - 1) / a.chunk;
+    const int NR = a.nslots / cpr_full;
+    // checked build: the ring and the parameter room must fit the launch
+    const bool fits = layout_fits((uint64_t)a.nslots * a.chunk * sizeof(T), (int64_t)NR * cpr_full,
+                                  kPersistMaxSlots, a.err) &&
+                      (a.param_off == 0 ||
+                       layout_fits((uint64_t)a.param_off + (uint64_t)a.param_room, 0, 0, a.err));
+    const int n = fits ? (int)max((int64_t)0, min(a.cols - start, (int64_t)a.slice)) : 0;
     const int nvec = n / VEC;
     const int vpc = a.chunk / VEC;
-    const int cpr_full = (a.slice + a.chunk - 1) / a.chunk;
     const int cpr = (n + a.chunk - 1) / a.chunk;
-    const int NR = a.nslots / cpr_full;
     const uint32_t ring_s = smem_u32(ring);
     const uint32_t slot_bytes = (uint32_t)a.chunk * (uint32_t)sizeof(T);
     const int64_t nrows = cid < a.rows ? (a.rows - 1 - cid) / a.nclusters + 1 : 0;
@@ -268,7 +276,7 @@ cluster_pipelined(const PersistArgs a) {
     };
 
     if (tid == 0) {
-        for (int s = 0; s < NR * cpr_full; ++s) {
+        for (int s = 0; s < (fits ? NR * cpr_full : 0); ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), (uint32_t)nsto);
         }

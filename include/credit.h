@@ -50,7 +50,8 @@ typedef enum {
     CREDIT_ERR_NO_LEGAL_PLAN = 3,   /* forced plan breaks the SMEM legality rule */
     CREDIT_ERR_CUDA = 4,            /* a CUDA runtime call failed */
     CREDIT_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device-side wait gave up */
-    CREDIT_ERR_NOT_CALIBRATED = 6   /* the cost model has no profile yet */
+    CREDIT_ERR_NOT_CALIBRATED = 6,  /* the cost model has no profile yet */
+    CREDIT_ERR_DEVICE_BOUNDS = 7    /* checked build: a device index check failed */
 } credit_status_t;
 
 typedef enum { CREDIT_F32 = 0, CREDIT_BF16 = 1 } credit_dtype_t;
@@ -536,8 +537,9 @@ const char *credit_status_string(credit_status_t status);
 
 /*
  * Read and clear the device error word of `device`.  Bounded device waits
- * that give up set it; the result is CREDIT_ERR_DEVICE_TIMEOUT in that case,
- * else CREDIT_OK.  Synchronises the device.
+ * that give up set it (CREDIT_ERR_DEVICE_TIMEOUT), and so do the index checks
+ * of the checked build (CREDIT_ERR_DEVICE_BOUNDS; a timeout is reported
+ * first when both happened); CREDIT_OK otherwise.  Synchronises the device.
  */
 credit_status_t credit_get_device_error(int device);
 
@@ -549,6 +551,41 @@ credit_status_t credit_get_device_error(int device);
  * (no copy in flight, no cluster barrier), so the context stays usable.
  */
 credit_status_t credit_selftest_wait_timeout(int device, int64_t limit_ns);
+
+/*
+ * The checked build (libcredit_checked.so, compiled with -DCREDIT_DEBUG) runs
+ * the same kernels with index checks on the staged-slice, ring-slot, chunk
+ * mbarrier and exchange-slot accesses: a failed check records
+ * CREDIT_ERR_DEVICE_BOUNDS in the device error word and skips the access
+ * instead of touching memory outside the buffer.  It also records a phase
+ * trace of the one-row-per-cluster kernel (below).  The regular build has
+ * neither.
+ *
+ * credit_debug_build: 1 for the checked build, 0 otherwise.
+ */
+int credit_debug_build(void);
+
+/*
+ * Exercise the index-check path on `device`: a one-thread kernel records a
+ * failed check (no memory outside any buffer is touched) and the device error
+ * word is read and cleared.  Returns CREDIT_ERR_DEVICE_BOUNDS in the checked
+ * build, CREDIT_ERR_UNSUPPORTED in the regular one.
+ */
+credit_status_t credit_selftest_bounds(int device);
+
+/*
+ * Phase trace of the last launches of the one-row-per-cluster kernel on the
+ * current device (checked build only).  Each CTA with blockIdx.x <
+ * CREDIT_TRACE_CTAS records, from thread 0, 8 unsigned 64-bit words: the
+ * %globaltimer (ns) at kernel entry, after its bulk copies are issued, after
+ * its statistics are folded, after the CTA partial, after the exchange and
+ * combine, after its output, at exit, and its SM id.  Stamps of a CTA index
+ * are overwritten by every launch that reaches it.  Copies `ctas` * 64 bytes
+ * (ctas <= CREDIT_TRACE_CTAS) into `host`; CREDIT_ERR_UNSUPPORTED in the
+ * regular build.  Synchronises the device.
+ */
+#define CREDIT_TRACE_CTAS 8192
+credit_status_t credit_debug_trace(void *host, int64_t ctas);
 
 /* Library version as "major.minor.patch" (static storage). */
 const char *credit_version(void);

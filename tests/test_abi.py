@@ -84,10 +84,10 @@ int main(void) {
 
 
 def test_status_strings(lib):
-    for s in range(7):
-        assert C.status_string(s)
+    for s in range(8):
+        assert C.status_string(s) != "unknown status"
     assert C.status_string(C.ERR_NO_LEGAL_PLAN).startswith("no legal plan")
-    assert C.credit_version() == "0.3.0"
+    assert C.credit_version() == "0.4.0"
 
 
 def test_host_side_argument_checks_need_no_gpu(lib):
@@ -135,3 +135,22 @@ def test_host_buffer_layout_needs_no_gpu(lib):
     assert C.credit_run_host(ln, plan, 4096, 1 << 30, 0) == C.ERR_INVALID_ARG     # no chunk
     assert C.credit_run_host(C.host_call(C.PEARSON, C.F32, 4, 8, x=16, y=32, row_out=64), plan,
                              4096, 1 << 30, 4) == C.ERR_INVALID_ARG                # no u
+
+
+def test_checked_build_exports_the_same_abi_and_reports_itself(lib):
+    # the checked build (-DCREDIT_DEBUG) carries every declared symbol; the
+    # debug entry points answer without a GPU: which build this is, and
+    # UNSUPPORTED / INVALID_ARG before any CUDA call
+    path = B.build(checked=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (credit_[a-z0-9_]+)\b", out))
+    assert not [n for n in declared_functions() if n not in exported]
+    chk = C._open(path)
+    assert chk.credit_debug_build() == 1
+    assert lib.credit_debug_build() == 0
+    assert lib.credit_selftest_bounds(0) == C.ERR_UNSUPPORTED
+    assert lib.credit_debug_trace(None, 1) == C.ERR_UNSUPPORTED
+    assert chk.credit_debug_trace(None, 1) == C.ERR_INVALID_ARG
+    assert chk.credit_debug_trace(None, C.TRACE_CTAS + 1) == C.ERR_INVALID_ARG
+    assert C.status_string(C.ERR_DEVICE_BOUNDS).startswith("a device index check failed")
