@@ -245,7 +245,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="layernorm_bf16_1024x262144")
     ap.add_argument("--variant", default="auto",
-                    help="auto (cost model + tuning) | static | cluster:P | persist:P | pipe:P | two_pass")
+                    help="auto (cost model + tuning) | static | cluster:P | persist:P | pipe:P | warp_rows | two_pass")
     ap.add_argument("--cps", type=int, default=0, help="persistent CTAs per SM (0 = planner)")
     ap.add_argument("--exchange", default="plan", choices=["plan", "barrier", "async"],
                     help="partial exchange of a one-pass clustered plan (plan = as planned)")
@@ -319,6 +319,8 @@ def main():
         plan = C.credit_plan(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev)
     elif args.variant == "two_pass":
         plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.TWO_PASS, 1)
+    elif args.variant == "warp_rows":
+        plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.WARP_ROWS, 1)
     else:
         kind, P = args.variant.split(":")
         var = {"cluster": C.CLUSTER, "persist": C.CLUSTER_PERSISTENT,
@@ -456,7 +458,8 @@ def main():
     peak, peak_kind = measured_peak()
     variant_key = {C.TWO_PASS: "two_pass", C.CLUSTER: f"cluster:{plan.cluster_size}",
                    C.CLUSTER_PERSISTENT: f"persist:{plan.cluster_size}",
-                   C.CLUSTER_PIPELINED: f"pipe:{plan.cluster_size}"}[plan.variant]
+                   C.CLUSTER_PIPELINED: f"pipe:{plan.cluster_size}",
+                   C.WARP_ROWS: "warp_rows"}[plan.variant]
     if plan.variant == C.CLUSTER and plan.exchange == C.EXCHANGE_BARRIER:
         variant_key += ":barrier"
     launches_per_step = 2 if plan.variant == C.TWO_PASS else 1

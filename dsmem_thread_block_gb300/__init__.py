@@ -45,7 +45,8 @@ def plan(op: str, rows: int, cols: int, dtype, device: int | None = None,
          exchange: str | None = None) -> Plan:
     """Plan a call: automatically (variant None) or for a forced variant
     ("cluster" with `cluster_size` and optionally `rows_per_cluster`,
-    "persistent" or "pipelined" with `cluster_size`, or "two_pass"); `exchange` ("async" or
+    "persistent" or "pipelined" with `cluster_size`, "warp_rows" or "two_pass");
+    `exchange` ("async" or
     "barrier") picks how a clustered plan exchanges its partials."""
     import torch
     dev = torch.cuda.current_device() if device is None else int(device)
@@ -53,7 +54,8 @@ def plan(op: str, rows: int, cols: int, dtype, device: int | None = None,
     if variant is None:
         return C.credit_plan(code, rows, cols, _dtype(dtype), dev)
     v = {"cluster": C.CLUSTER, "persistent": C.CLUSTER_PERSISTENT,
-         "pipelined": C.CLUSTER_PIPELINED, "two_pass": C.TWO_PASS}[variant]
+         "pipelined": C.CLUSTER_PIPELINED, "warp_rows": C.WARP_ROWS,
+         "two_pass": C.TWO_PASS}[variant]
     x = {None: C.EXCHANGE_DEFAULT, "async": C.EXCHANGE_ASYNC,
          "barrier": C.EXCHANGE_BARRIER}[exchange]
     return C.credit_plan_with(code, rows, cols, _dtype(dtype), dev, v, cluster_size,

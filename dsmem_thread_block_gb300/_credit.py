@@ -19,7 +19,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NO_LEGAL_PLAN, ERR_CUDA, \
 TRACE_CTAS = 8192  # CREDIT_TRACE_CTAS
 F32, BF16 = 0, 1
 SOFTMAX, LAYERNORM, RMSNORM, QUANTIZE, WEIGHTED_STD, PEARSON = 0, 1, 2, 3, 4, 5
-AUTO, CLUSTER, TWO_PASS, CLUSTER_PERSISTENT, CLUSTER_PIPELINED = 0, 1, 2, 3, 4
+AUTO, CLUSTER, TWO_PASS, CLUSTER_PERSISTENT, CLUSTER_PIPELINED, WARP_ROWS = 0, 1, 2, 3, 4, 5
 EXCHANGE_DEFAULT, EXCHANGE_BARRIER, EXCHANGE_ASYNC = 0, 1, 2
 
 _vp, _i64, _i32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,

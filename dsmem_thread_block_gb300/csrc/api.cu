@@ -181,13 +181,13 @@ credit_status_t plan_from_request(int dev, credit_op_t op, int64_t rows, int64_t
                                   credit_plan_t* out) {
     const credit_variant_t v = (credit_variant_t)r.variant;
     if (v != CREDIT_CLUSTER && v != CREDIT_CLUSTER_PERSISTENT && v != CREDIT_CLUSTER_PIPELINED &&
-        v != CREDIT_TWO_PASS)
+        v != CREDIT_WARP_ROWS && v != CREDIT_TWO_PASS)
         return CREDIT_ERR_INVALID_ARG;
     if (r.threads < 0 || r.ctas_per_sm < 0 || r.chunk_elems < 0 || r.rows_per_cluster < 0)
         return CREDIT_ERR_INVALID_ARG;
     const bool xok = r.exchange == CREDIT_EXCHANGE_DEFAULT ||
                      ((r.exchange == CREDIT_EXCHANGE_BARRIER || r.exchange == CREDIT_EXCHANGE_ASYNC) &&
-                      v != CREDIT_TWO_PASS);
+                      v != CREDIT_TWO_PASS && v != CREDIT_WARP_ROWS);
     if (!xok) return CREDIT_ERR_INVALID_ARG;
     // the warp-specialised kernel exchanges with st.async deposits only
     if (v == CREDIT_CLUSTER_PIPELINED && r.exchange == CREDIT_EXCHANGE_BARRIER)
@@ -311,7 +311,7 @@ credit_status_t run(const OpCall& c) {
     if (!err) return CREDIT_ERR_CUDA;
     if (!vec && plan.variant != CREDIT_TWO_PASS &&
         (plan.variant == CREDIT_CLUSTER_PERSISTENT || plan.variant == CREDIT_CLUSTER_PIPELINED ||
-         plan.rows_per_cluster != 1)) {
+         plan.variant == CREDIT_WARP_ROWS || plan.rows_per_cluster != 1)) {
         // bulk copies need 16-byte alignment: misaligned or ragged rows take
         // the one-row-per-cluster kernel's element path instead
         const int32_t xchg = plan.exchange;
@@ -327,6 +327,16 @@ credit_status_t run(const OpCall& c) {
         // exists; cluster_kernel falls back to the regular one otherwise)
         const DevInfo* di = device_info(dev);
         key.deep = di && plan.smem_bytes > (int64_t)di->smem_per_sm / 3 - 4096;
+    }
+    if (plan.variant == CREDIT_WARP_ROWS) {
+        WarpRowsArgs a;
+        a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;
+        a.rows = c.rows;
+        a.cols = c.cols;
+        a.eps = c.eps;
+        const void* fn = warp_rows_kernel(key);
+        if (!fn || !kernel_info(dev, fn, false)) return CREDIT_ERR_CUDA;
+        return from_cuda(launch_warp_rows(key, a, plan.active_clusters, c.stream));
     }
     if (plan.variant == CREDIT_CLUSTER_PERSISTENT || plan.variant == CREDIT_CLUSTER_PIPELINED) {
         const bool piped = plan.variant == CREDIT_CLUSTER_PIPELINED;
@@ -398,7 +408,8 @@ credit_status_t credit_plan_for(credit_op_t op, int64_t rows, int64_t cols, cred
                                 credit_plan_t* out) {
     if (!out) return CREDIT_ERR_INVALID_ARG;
     if (variant != CREDIT_CLUSTER && variant != CREDIT_TWO_PASS &&
-        variant != CREDIT_CLUSTER_PERSISTENT && variant != CREDIT_CLUSTER_PIPELINED)
+        variant != CREDIT_CLUSTER_PERSISTENT && variant != CREDIT_CLUSTER_PIPELINED &&
+        variant != CREDIT_WARP_ROWS)
         return CREDIT_ERR_INVALID_ARG;
     return make_plan(device, op, rows, cols, dtype, variant, cluster_size, 0, 0, out);
 }

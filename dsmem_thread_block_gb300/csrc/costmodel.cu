@@ -233,8 +233,9 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
     const int64_t rt = std::max<int64_t>(1, std::min<int64_t>(rows, ((int64_t)1 << 30) / (cols * es)));
     const double mat = (double)rt * (double)cols * es;
 
-    // the baseline: the faster of local staging (when one CTA can hold a
-    // row) and the two-pass re-read pair
+    // the baseline: the fastest of local staging (when one CTA can hold a
+    // row), one warp per row in registers (rows of at most 4 KiB) and the
+    // two-pass re-read pair
     credit_plan_t base;
     const int64_t row_bytes = cols * es;
     const int Rb = row_bytes * 4 <= 65536 ? 4 : 1;
@@ -291,12 +292,28 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
             t_base = t_rr;
         }
     }
+    credit_plan_t wrows;
+    if (make_plan(device, op, rt, cols, dtype, CREDIT_WARP_ROWS, 1, 0, 0, &wrows) == CREDIT_OK) {
+        double t_wr = 0.0;
+        st = time_op(op, x.p, y.p, rt, cols, dtype, g.p, b.p, param_dtype, &wrows, nullptr, 0,
+                     runs, &t_wr, auxp);
+        if (st != CREDIT_OK) return st;
+        if (t_wr < t_base) {
+            staging = true;  // one read of the row: no re-read to avoid
+            base = wrows;
+            t_base = t_wr;
+        }
+    }
     const double b_base = staging ? b_credit : b_credit + b_read;
     const double r_base = b_base / t_base;  // bytes per microsecond
 
     // the baseline's control: its grid, footprint and barriers, no work
     double ctrl_base = 0.0;
-    if (staging) {
+    if (base.variant == CREDIT_WARP_ROWS) {
+        // a grid of row-striding CTAs: one launch, no staging, no barrier
+        st = credit_control_time(device, base.active_clusters, 1, base.threads, 0, 1, 0, runs,
+                                 &ctrl_base);
+    } else if (staging) {
         st = credit_control_time(device, ceil_div64(rt, base.rows_per_cluster), 1, base.threads,
                                  base.smem_bytes, 1, 2, runs, &ctrl_base);
     } else {
@@ -309,7 +326,7 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
 
     credit_model_report_t rep;
     std::memset(&rep, 0, sizeof(rep));
-    rep.baseline_variant = staging ? CREDIT_CLUSTER : CREDIT_TWO_PASS;
+    rep.baseline_variant = base.variant;
     rep.t_base_us = t_base;
     rep.b_base_bytes = b_base;
     rep.b_credit_bytes = b_credit;

@@ -68,6 +68,20 @@ struct PersistArgs {
 constexpr int kPersistMaxSlots = 32;
 constexpr int kPersistMaxThreads = 544;  // 16 consumer warps + 1 producer warp
 
+// Arguments of the warp-per-row kernel (rows that fit one warp's registers).
+struct WarpRowsArgs {
+    const void* x;
+    void* y;
+    const void* p0;
+    const void* p1;
+    int64_t rows;
+    int64_t cols;
+    float eps;
+};
+
+constexpr int kWarpRowNV = 8;          // 16-byte vectors per lane: rows up to 4 KiB
+constexpr int kWarpRowThreads = 256;
+
 // Kernel selector: op 0..2, dtype 0 = fp32 / 1 = bf16, pdtype likewise,
 // vec = aligned 16-byte path, rows = rows per cluster (1, 2 or 4; the
 // element path has 1).
@@ -88,6 +102,7 @@ const void* pipelined_kernel(KernelKey k);  // warp-specialised persistent form
 // Reducer warps of the warp-specialised kernel for `consumer_warps` consumer warps.
 int pipelined_reducers(int op, int dtype, int consumer_warps);
 const void* two_pass_stats_kernel(KernelKey k);
+const void* warp_rows_kernel(KernelKey k);
 const void* two_pass_apply_kernel(KernelKey k);
 
 cudaError_t launch_cluster(KernelKey k, const ClusterArgs& a, int P, int threads, size_t smem,
@@ -96,6 +111,7 @@ cudaError_t launch_persistent(KernelKey k, const PersistArgs& a, int P, int thre
                               size_t smem, cudaStream_t s);
 cudaError_t launch_two_pass(KernelKey k, const TwoPassArgs& a, int64_t rows,
                             int threads, cudaStream_t s);
+cudaError_t launch_warp_rows(KernelKey k, const WarpRowsArgs& a, int blocks, cudaStream_t s);
 
 unsigned* device_error_word();  // address of this device's error word
 

@@ -158,7 +158,8 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
     p.ctas_per_sm = 1;
     // st.async deposits for both clustered kernels (measured faster than
     // the push + barrier exchange in each)
-    p.exchange = variant == CREDIT_TWO_PASS ? CREDIT_EXCHANGE_DEFAULT : CREDIT_EXCHANGE_ASYNC;
+    p.exchange = (variant == CREDIT_TWO_PASS || variant == CREDIT_WARP_ROWS)
+                     ? CREDIT_EXCHANGE_DEFAULT : CREDIT_EXCHANGE_ASYNC;
     const double bytes = (op == CREDIT_PEARSON ? 3.0 : 2.0) * (double)rows * (double)cols * es;
 
     if (variant == CREDIT_CLUSTER) {
@@ -210,6 +211,24 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
             }
         }
         if (best != CREDIT_OK) return best;
+    } else if (variant == CREDIT_WARP_ROWS) {
+        // one warp per row, the row in registers: whole rows of at most
+        // 32 lanes x kWarpRowNV vectors
+        if (ceil_div(cols, vec) > 32 * kWarpRowNV) return CREDIT_ERR_NO_LEGAL_PLAN;
+        const void* fn = warp_rows_kernel(KernelKey{(int)op, (int)dtype, 0, true});
+        if (!fn) return CREDIT_ERR_NO_LEGAL_PLAN;  // operator not offered
+        if (!kernel_info(dev, fn, false)) return CREDIT_ERR_CUDA;
+        const int per_sm = occupancy_clusters(dev, fn, 1, kWarpRowThreads, 0, rows);
+        if (per_sm < 1) return CREDIT_ERR_NO_LEGAL_PLAN;
+        const int64_t wpb = kWarpRowThreads / 32;
+        const int64_t blocks = std::min<int64_t>(per_sm, ceil_div(rows, wpb));
+        p.cluster_size = 1;
+        p.threads = kWarpRowThreads;
+        p.slice_elems = cols;
+        p.active_clusters = (int32_t)blocks;
+        p.rows_per_cluster = 1;
+        p.waves = (int32_t)std::min<int64_t>(ceil_div(rows, blocks * wpb), INT32_MAX);
+        p.pred_us = (float)(bytes / (kNominalBytesPerUs * 0.9) + kLaunchUs);
     } else if (variant == CREDIT_TWO_PASS) {
         const int64_t per_thread = kTwoPassVpt * vec;
         int t = threads;
@@ -254,12 +273,22 @@ credit_status_t auto_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
     credit_plan_t base;
     credit_status_t st = make_plan(dev, op, rows, cols, dtype, CREDIT_TWO_PASS, 0, 0, 0, &base);
     if (st != CREDIT_OK) return st;
-    // Static choice (no profile for this shape): the one-row-per-cluster
+    // Static choice (no profile for this shape): rows of 2 KiB or less one
+    // warp each in registers (softmax, LayerNorm, RMSNorm; measured 1.5x the
+    // staging kernel for 1024-column bf16 rows); else the one-row-per-cluster
     // kernel with the smallest P whose slice stays within 64 KiB (three
     // 256-thread CTAs per SM), rows of 16 KiB or less batched four to a CTA;
     // the two-pass kernel only when no cluster size fits.
     const int es = dtype == CREDIT_F32 ? 4 : 2;
     const int nops = op == CREDIT_PEARSON ? 2 : 1;  // staged operands per row
+    if (cols * es <= 2048 && (cols * es) % 16 == 0) {
+        credit_plan_t w;
+        if (make_plan(dev, op, rows, cols, dtype, CREDIT_WARP_ROWS, 1, 0, 0, &w) == CREDIT_OK) {
+            w.pred_two_pass_us = base.pred_us;
+            *out = w;
+            return CREDIT_OK;
+        }
+    }
     for (int P = 1; P <= kMaxCluster; ++P) {
         const int64_t slice_bytes = ceil_div(cols, P) * es * nops;
         if (slice_bytes > 65536 && P < kMaxCluster) continue;

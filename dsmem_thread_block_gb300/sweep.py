@@ -110,7 +110,8 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
     tol = max(0.02 * best, measured[best_P]["iqr_us"], measured[pick]["iqr_us"])
     return {
         "cols": cols, "rows": w.rows,
-        "baseline": "local-staging P=1" if rep.baseline_variant == C.CLUSTER else "two-pass",
+        "baseline": {C.CLUSTER: "local-staging P=1", C.WARP_ROWS: "warp-rows",
+                     C.TWO_PASS: "two-pass"}[rep.baseline_variant],
         "t_base_us": rep.t_base_us, "picked_P": pick, "predicted_profitable": bool(rep.profitable),
         "measured_best_P": best_P, "measured_profitable": best_P != 1,
         "picked_us": measured[pick]["us"], "best_us": best,

@@ -73,11 +73,14 @@ typedef enum {
     CREDIT_CLUSTER_PERSISTENT = 3, /* clustered DSMEM kernel, resident clusters
                               loop over rows; a producer warp streams chunks
                               into a ring of shared-memory slots */
-    CREDIT_CLUSTER_PIPELINED = 4   /* the persistent kernel with warp-specialised
+    CREDIT_CLUSTER_PIPELINED = 4,  /* the persistent kernel with warp-specialised
                               consumers: reducer warps fold, exchange and
                               combine row k + 1 while storer warps write row
                               k (softmax, LayerNorm, RMSNorm; ASYNC exchange
                               only) */
+    CREDIT_WARP_ROWS = 5           /* non-clustered: one warp holds a whole row
+                              in registers (rows of at most 4 KiB; softmax,
+                              LayerNorm, RMSNorm; no exchange) */
 } credit_variant_t;
 
 /*
@@ -104,8 +107,10 @@ typedef enum {
  * A launch plan.  Produced by credit_plan / credit_plan_for; may be passed to
  * the operator calls (NULL there means "plan automatically").
  *   variant          CREDIT_CLUSTER, CREDIT_CLUSTER_PERSISTENT,
- *                    CREDIT_CLUSTER_PIPELINED or CREDIT_TWO_PASS (never AUTO
- *                    once planned)
+ *                    CREDIT_CLUSTER_PIPELINED, CREDIT_WARP_ROWS or
+ *                    CREDIT_TWO_PASS (never AUTO once planned); WARP_ROWS
+ *                    plans have cluster_size 1, smem_bytes 0 and
+ *                    active_clusters = the CTAs of their row-striding grid
  *   cluster_size     P, CTAs per row (1..16; 1 = one CTA stages the whole row)
  *   threads          threads per CTA
  *   waves            predicted waves of resident clusters, ceil(rows / active)
@@ -162,7 +167,7 @@ credit_status_t credit_plan(credit_op_t op, int64_t rows, int64_t cols,
 /*
  * Build a plan for a forced variant: CREDIT_CLUSTER, CREDIT_CLUSTER_PERSISTENT
  * or CREDIT_CLUSTER_PIPELINED with the given cluster_size (1..16), or
- * CREDIT_TWO_PASS (cluster_size ignored).
+ * CREDIT_WARP_ROWS / CREDIT_TWO_PASS (cluster_size ignored).
  * Returns CREDIT_ERR_NO_LEGAL_PLAN if the slice does not fit in shared memory
  * or no cluster of that size can be resident.
  */
@@ -173,8 +178,8 @@ credit_status_t credit_plan_for(credit_op_t op, int64_t rows, int64_t cols,
 
 /*
  * Complete a plan from a partial request: `request->variant` (CLUSTER,
- * CLUSTER_PERSISTENT, CLUSTER_PIPELINED or TWO_PASS) and, for the clustered
- * variants,
+ * CLUSTER_PERSISTENT, CLUSTER_PIPELINED, WARP_ROWS or TWO_PASS) and, for the
+ * clustered variants,
  * `request->cluster_size` are required; `threads`, `ctas_per_sm`,
  * `chunk_elems` and `rows_per_cluster` are used when non-zero and chosen
  * otherwise; every other field is ignored.  The operator calls re-derive a
@@ -374,9 +379,10 @@ credit_status_t credit_run_host(const credit_host_call_t *call,
 
 /* ------------------------------------------------------------------------
  * Profitability cost model (CREDIT "D. Profitability and Candidate
- * Selection").  For one shape it times the non-DSMEM baseline -- the faster
+ * Selection").  For one shape it times the non-DSMEM baseline -- the fastest
  * of the one-CTA-per-row local-staging kernel (when a row fits one CTA's
- * shared memory) and the two-pass global re-read pair -- times the work-free
+ * shared memory), the warp-per-row register kernel (rows of at most 4 KiB)
+ * and the two-pass global re-read pair -- times the work-free
  * control kernel of every legal clustered candidate and of the baseline, and
  * predicts
  *     T_CREDIT(P) = T_base - (B_base - B_credit) / R_base + T_ctrl(P) + T_comm(P)
@@ -409,7 +415,8 @@ typedef struct {
 } credit_candidate_t;
 
 typedef struct {
-    int32_t baseline_variant;     /* CREDIT_CLUSTER (P = 1 staging) or CREDIT_TWO_PASS */
+    int32_t baseline_variant;     /* CREDIT_CLUSTER (P = 1 staging), CREDIT_WARP_ROWS
+                                     or CREDIT_TWO_PASS */
     int32_t model_cluster_size;   /* the model's pick (1 = the baseline) */
     int32_t profitable;           /* 1 if a clustered candidate is predicted faster */
     int32_t chosen_cluster_size;  /* after tuning (equals the model's pick if tune = 0) */
