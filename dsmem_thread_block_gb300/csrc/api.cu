@@ -334,7 +334,7 @@ credit_status_t run(const OpCall& c) {
         a.rows = c.rows;
         a.cols = c.cols;
         a.eps = c.eps;
-        const void* fn = warp_rows_kernel(key);
+        const void* fn = warp_rows_kernel(key, c.cols * (int64_t)es / 16);
         if (!fn || !kernel_info(dev, fn, false)) return CREDIT_ERR_CUDA;
         return from_cuda(launch_warp_rows(key, a, plan.active_clusters, c.stream));
     }

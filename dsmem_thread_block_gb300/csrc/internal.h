@@ -102,7 +102,8 @@ const void* pipelined_kernel(KernelKey k);  // warp-specialised persistent form
 // Reducer warps of the warp-specialised kernel for `consumer_warps` consumer warps.
 int pipelined_reducers(int op, int dtype, int consumer_warps);
 const void* two_pass_stats_kernel(KernelKey k);
-const void* warp_rows_kernel(KernelKey k);
+// the instantiation for rows of `nvec` 16-byte vectors (null when none fits)
+const void* warp_rows_kernel(KernelKey k, int64_t nvec);
 const void* two_pass_apply_kernel(KernelKey k);
 
 cudaError_t launch_cluster(KernelKey k, const ClusterArgs& a, int P, int threads, size_t smem,

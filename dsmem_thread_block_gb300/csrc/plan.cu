@@ -215,7 +215,7 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
         // one warp per row, the row in registers: whole rows of at most
         // 32 lanes x kWarpRowNV vectors
         if (ceil_div(cols, vec) > 32 * kWarpRowNV) return CREDIT_ERR_NO_LEGAL_PLAN;
-        const void* fn = warp_rows_kernel(KernelKey{(int)op, (int)dtype, 0, true});
+        const void* fn = warp_rows_kernel(KernelKey{(int)op, (int)dtype, 0, true}, ceil_div(cols, vec));
         if (!fn) return CREDIT_ERR_NO_LEGAL_PLAN;  // operator not offered
         if (!kernel_info(dev, fn, false)) return CREDIT_ERR_CUDA;
         const int per_sm = occupancy_clusters(dev, fn, 1, kWarpRowThreads, 0, rows);

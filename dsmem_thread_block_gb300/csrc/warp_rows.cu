@@ -18,12 +18,14 @@
 
 namespace credit {
 
-template <int OP, typename T, typename PT>
+// NV: vectors per lane the instantiation holds (kWarpRowNV, or half of it
+// for rows of at most 2 KiB, whose smaller register footprint leaves room
+// for more resident warps).
+template <int OP, typename T, typename PT, int NV>
 __global__ void __launch_bounds__(kWarpRowThreads)
 warp_rows(const WarpRowsArgs a) {
     using E = Elem<T>;
     constexpr int VEC = E::kVec;
-    constexpr int NV = kWarpRowNV;
     constexpr int NP = VEC / 2;  // element pairs per vector
     constexpr bool kParams = OP == kLayerNorm || OP == kRMSNorm;
     const int lane = threadIdx.x & 31;
@@ -114,26 +116,33 @@ warp_rows(const WarpRowsArgs a) {
 }
 
 // ----------------------------------------------------------- dispatch
-template <int OP, typename T>
+template <int OP, typename T, int NV>
 static const void* wr_param(int pdtype) {
-    return pdtype == 0 ? (const void*)warp_rows<OP, T, float> : (const void*)warp_rows<OP, T, bf16>;
+    return pdtype == 0 ? (const void*)warp_rows<OP, T, float, NV>
+                       : (const void*)warp_rows<OP, T, bf16, NV>;
 }
 
-const void* warp_rows_kernel(KernelKey k) {
-    if (!k.vec) return nullptr;  // whole 16-byte vectors only
+template <int NV>
+static const void* wr_pick(KernelKey k) {
     switch (k.op) {
-        case kSoftmax: return k.dtype == 0 ? (const void*)warp_rows<kSoftmax, float, float>
-                                           : (const void*)warp_rows<kSoftmax, bf16, float>;
-        case kLayerNorm: return k.dtype == 0 ? wr_param<kLayerNorm, float>(k.pdtype)
-                                             : wr_param<kLayerNorm, bf16>(k.pdtype);
-        case kRMSNorm: return k.dtype == 0 ? wr_param<kRMSNorm, float>(k.pdtype)
-                                           : wr_param<kRMSNorm, bf16>(k.pdtype);
+        case kSoftmax: return k.dtype == 0 ? (const void*)warp_rows<kSoftmax, float, float, NV>
+                                           : (const void*)warp_rows<kSoftmax, bf16, float, NV>;
+        case kLayerNorm: return k.dtype == 0 ? wr_param<kLayerNorm, float, NV>(k.pdtype)
+                                             : wr_param<kLayerNorm, bf16, NV>(k.pdtype);
+        case kRMSNorm: return k.dtype == 0 ? wr_param<kRMSNorm, float, NV>(k.pdtype)
+                                           : wr_param<kRMSNorm, bf16, NV>(k.pdtype);
     }
     return nullptr;
 }
 
+const void* warp_rows_kernel(KernelKey k, int64_t nvec) {
+    if (!k.vec || nvec < 1 || nvec > 32 * kWarpRowNV) return nullptr;  // whole vectors only
+    return nvec <= 32 * (kWarpRowNV / 2) ? wr_pick<kWarpRowNV / 2>(k) : wr_pick<kWarpRowNV>(k);
+}
+
 cudaError_t launch_warp_rows(KernelKey k, const WarpRowsArgs& a, int blocks, cudaStream_t s) {
-    const void* fn = warp_rows_kernel(k);
+    const int es = k.dtype == 0 ? 4 : 2;
+    const void* fn = warp_rows_kernel(k, a.cols * es / 16);
     if (!fn) return cudaErrorInvalidDeviceFunction;
     WarpRowsArgs b = a;
     void* args[] = {&b};
