@@ -275,9 +275,10 @@ credit_status_t auto_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
     if (st != CREDIT_OK) return st;
     // Static choice (no profile for this shape): rows of 2 KiB or less one
     // warp each in registers (softmax, LayerNorm, RMSNorm; measured 1.5x the
-    // staging kernel for 1024-column bf16 rows); else the one-row-per-cluster
-    // kernel with the smallest P whose slice stays within 64 KiB (three
-    // 256-thread CTAs per SM), rows of 16 KiB or less batched four to a CTA;
+    // staging kernel for 1024-column bf16 softmax and LayerNorm rows); else the
+    // one-row-per-cluster kernel with the smallest P whose slice stays within
+    // 64 KiB (three 256-thread CTAs per SM), rows of 16 KiB or less batched
+    // four to a CTA;
     // the two-pass kernel only when no cluster size fits.
     const int es = dtype == CREDIT_F32 ? 4 : 2;
     const int nops = op == CREDIT_PEARSON ? 2 : 1;  // staged operands per row

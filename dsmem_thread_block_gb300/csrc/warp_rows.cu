@@ -19,8 +19,9 @@
 namespace credit {
 
 // NV: vectors per lane the instantiation holds (kWarpRowNV, or half of it
-// for rows of at most 2 KiB, whose smaller register footprint leaves room
-// for more resident warps).
+// for the norms' rows of at most 2 KiB, whose smaller register footprint
+// leaves room for more resident warps: measured faster for LayerNorm and
+// RMSNorm, slower for softmax, which keeps the full size).
 template <int OP, typename T, typename PT, int NV>
 __global__ void __launch_bounds__(kWarpRowThreads)
 warp_rows(const WarpRowsArgs a) {
@@ -137,7 +138,8 @@ static const void* wr_pick(KernelKey k) {
 
 const void* warp_rows_kernel(KernelKey k, int64_t nvec) {
     if (!k.vec || nvec < 1 || nvec > 32 * kWarpRowNV) return nullptr;  // whole vectors only
-    return nvec <= 32 * (kWarpRowNV / 2) ? wr_pick<kWarpRowNV / 2>(k) : wr_pick<kWarpRowNV>(k);
+    const bool half = k.op != kSoftmax && nvec <= 32 * (kWarpRowNV / 2);
+    return half ? wr_pick<kWarpRowNV / 2>(k) : wr_pick<kWarpRowNV>(k);
 }
 
 cudaError_t launch_warp_rows(KernelKey k, const WarpRowsArgs& a, int blocks, cudaStream_t s) {
