@@ -104,10 +104,20 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     # exchanges exist only for the clustered kernels
     out = C.Plan()
     for variant, exchange in ((C.TWO_PASS, C.EXCHANGE_ASYNC), (C.TWO_PASS, C.EXCHANGE_BARRIER),
-                              (C.CLUSTER_PERSISTENT, 3), (C.CLUSTER, 3), (C.CLUSTER, -1)):
+                              (C.CLUSTER_PERSISTENT, 3), (C.CLUSTER, 3), (C.CLUSTER, -1),
+                              (C.WARP_ROWS, C.EXCHANGE_ASYNC), (C.WARP_ROWS, C.EXCHANGE_BARRIER),
+                              # the warp-specialised kernel exchanges with st.async only
+                              (C.CLUSTER_PIPELINED, C.EXCHANGE_BARRIER)):
         req = C.Plan(variant=variant, cluster_size=2, exchange=exchange)
         assert lib.credit_plan_with(C.SOFTMAX, 4, 4, C.F32, 0, ctypes.byref(req),
                                     ctypes.byref(out)) == C.ERR_INVALID_ARG
+    # unknown variants, in a request and in a forced plan
+    for variant in (C.AUTO, 6, -1):
+        req = C.Plan(variant=variant, cluster_size=2)
+        assert lib.credit_plan_with(C.SOFTMAX, 4, 4, C.F32, 0, ctypes.byref(req),
+                                    ctypes.byref(out)) == C.ERR_INVALID_ARG
+        assert lib.credit_plan_for(C.SOFTMAX, 4, 4, C.F32, 0, variant, 2,
+                                   ctypes.byref(out)) == C.ERR_INVALID_ARG
 
 
 def test_library_fails_loudly_when_missing(monkeypatch, tmp_path):
