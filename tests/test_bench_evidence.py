@@ -1,0 +1,46 @@
+"""Host logic of the benchmark's evidence fields (no GPU): the roofline
+denominator comes from the measured peaks file, else the stated fallback;
+stored ncu traffic is reported only while the kernel sources still hash to
+the value recorded with it; the whole-job rate divides all ranks' bytes by
+the slowest rank's time."""
+import json
+import os
+
+import bench
+
+
+def test_traffic_is_reported_only_for_matching_kernel_sources(monkeypatch):
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        d = json.load(f)
+    key = next(iter(d["entries"]))
+    workload, variant = key.split("|")
+    if d["kernel_source_hash"] == bench.kernel_source_hash():
+        assert bench.stored_traffic(workload, variant) == d["entries"][key]["dram_bytes_per_launch"]
+    assert bench.stored_traffic(workload, "cluster:99") is None  # never captured
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.stored_traffic(workload, variant) is None  # sources changed since the capture
+
+
+def test_kernel_source_hash_covers_every_source_file(tmp_path, monkeypatch):
+    csrc = tmp_path / "dsmem_thread_block_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "a.cu").write_text("one")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h1 = bench.kernel_source_hash()
+    (csrc / "b.cuh").write_text("two")
+    h2 = bench.kernel_source_hash()
+    (csrc / "b.cuh").write_text("two, edited")
+    h3 = bench.kernel_source_hash()
+    assert len({h1, h2, h3}) == 3
+
+
+def test_peak_from_the_measured_file_else_the_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_peak() == (bench.FALLBACK_HBM_GBS, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6781.4}))
+    assert bench.measured_peak() == (6781.4, "measured")
+
+
+def test_job_rate_uses_the_slowest_rank():
+    # 2 ranks, 1 GB each per step, the slowest rank 2 ms per step: 1000 GB/s
+    assert abs(bench.job_rate(1e9, 2.0, 2) - 1000.0) < 1e-9
