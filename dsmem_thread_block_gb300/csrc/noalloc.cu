@@ -29,12 +29,29 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices];  // device address of g_static_scratch, per device
 
-// Device address of the array on the current device `dev` (once per device).
-// In host code `g_static_scratch` names a host-side shadow, not device
-// memory, so the address has to come from the runtime.
+// Per-device set-up, once per device with `dev` current: the device address
+// of the array (in host code `g_static_scratch` names a host-side shadow, not
+// device memory, so the address has to come from the runtime) and the kernel
+// attributes of every two-pass kernel this entry point can launch for `op`
+// (both data types, aligned and element paths, both parameter types), so
+// that no later call does lazy per-device work.
 void* scratch_address(int dev) {
     std::lock_guard<std::mutex> lk(g_setup_mu);
     if (!g_scratch_addr[dev]) {
+        for (int op : {(int)kSoftmax, (int)kLayerNorm, (int)kRMSNorm}) {
+            for (int dt = 0; dt < 2; ++dt) {
+                for (int pdt = 0; pdt < 2; ++pdt) {
+                    for (bool vec : {true, false}) {
+                        const KernelKey k{op, dt, pdt, vec};
+                        const void* fs = two_pass_stats_kernel(k);
+                        const void* fa = two_pass_apply_kernel(k);
+                        if ((fs && !kernel_info(dev, fs, false)) ||
+                            (fa && !kernel_info(dev, fa, false)))
+                            return nullptr;
+                    }
+                }
+            }
+        }
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) {
             cudaGetLastError();
@@ -84,7 +101,7 @@ extern "C" credit_status_t credit_two_pass_noalloc(credit_op_t op, const void* x
     const bool vec = a16(x) && a16(y) && (cols * es) % 16 == 0 && (!p0 || a16(p0)) &&
                      (!p1 || a16(p1));
     const KernelKey key{(int)op, (int)dtype, (p0 || p1) ? (int)param_dtype : 0, vec};
-    TwoPassArgs a;
+    TwoPassArgs a{};  // aux (per-row outputs) stays null: these operators write none
     a.x = x; a.y = y; a.p0 = p0; a.p1 = p1;
     a.cols = cols;
     a.chunk = (int32_t)plan.slice_elems;

@@ -2,7 +2,8 @@
 cudaMalloc: memory already handed to their own pool, hot loops that must not
 synchronise the device, plug-in hosts without an allocator) gives the same
 results as the regular two-pass call with a caller-provided workspace, on two
-calls in a row that share the library's fixed scratch array.
+calls in a row that share the library's fixed scratch array, and both match
+the fp64 oracle within the parity tolerances.
 
 This file is collected last on purpose."""
 import numpy as np
@@ -12,7 +13,7 @@ import torch
 from dsmem_thread_block_gb300 import _credit as C
 from dsmem_thread_block_gb300 import workloads as wl
 
-from gpu_helpers import DT, OPS, RTOL, call, make_plan, to_device, to_host
+from gpu_helpers import DT, OPS, RTOL, call, check, make_plan, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -50,6 +51,8 @@ def test_noalloc_matches_workspace_two_pass(w):
             wl.bf16_bits_to_f32(to_host(ref)).astype(np.float64)
         assert np.isfinite(a).all()
         assert (np.abs(a - b) <= RTOL[w.dtype] * np.abs(b) + 1e-30).all()
+        # and against the oracle itself, not only the other CUDA path
+        check(w2, to_host(got), inp)
 
 
 def test_noalloc_size_limit():
@@ -75,3 +78,4 @@ def test_noalloc_size_limit():
     a = dy[:131072].double().cpu().numpy()
     b = ref[:131072].double().cpu().numpy()
     assert (np.abs(a - b) <= RTOL["f32"] * np.abs(b)).all()
+    check(w1, to_host(dy)[:131072], {"x": inp["x"][:131072]})
