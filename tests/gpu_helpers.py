@@ -5,20 +5,44 @@ the fp64 oracle under the stated tolerances.
 Tolerances (per element, o = oracle value in fp64, g = GPU value widened):
   fp32 outputs   |g - o| <= 1e-5   * |o|
   bf16 outputs   |g - o| <= 2^-7   * |o|        (one bf16 ulp at a binade top)
-LayerNorm adds a cancellation term.  fp32 cannot hold the row mean mu to
-better than ~2^-24 |mu|, so z = (x - mu) / sigma carries an absolute error of
-order 2^-24 (|z| + |mu| / sigma) however it is computed, and the final
-y = z * gamma + beta can cancel to a tiny |o|.  Its bound is therefore
-  |g - o| <= rtol * |o| + 1e-5 * (|gamma| (|z| + |mu| / sigma) + |beta|)
-with sigma = sqrt(var + eps) of the row (1e-5 is ~170 fp32 ulps: room for
-the summation error of the statistics), and the tests report how many
-elements pass only through that term.
-Pearson's y = zx zu (z the deviations over sqrt(var + eps)) carries that
-error in both factors.  A short row's fp32 mean is off by about 2^-24 times
-the row's typical magnitude rather than |mean| (a mean near zero of values
-near +-2 still errs by ~2^-24 * 2), so the term uses the row's rms:
-  |g - o| <= rtol * |o| + 1e-5 * (|zu| (|zx| + rms_x / sx) + |zx| (|zu| + rms_u / su))
-and its fp32 correlation r is held to |g - o| <= 1e-5 (r lies in [-1, 1]).
+  quantization   bit-exact codes and scales
+
+Cancellation (LayerNorm, weighted standardization, Pearson).  These outputs
+are a difference of O(1) quantities: y = z gamma + beta with z = (x - mu) /
+sigma, and z itself is x - mu over sigma.  Any fp32 evaluation rounds its
+intermediates at their own magnitude, so its absolute error scales with
+  S = |gamma| (|z| + rms / sigma) + |beta|      (rms = sqrt(mean x^2))
+and not with |o|, which can be arbitrarily small: |mu| / sigma enters
+through the fp32 row mean (its rounding is relative to the summands, i.e.
+to rms), |z| through the rounding of z and of 1/sigma, |beta| and the final
+rounding through the last fused multiply-add.  An element is therefore held
+to the relative bound unless it lies in the cancellation zone, where the
+bound becomes the fp32 evaluation error instead:
+  |g - o| <= max(rtol |o|,  u_out |o| + C u S),   u = 2^-24,  C = 16,
+u_out the output's own rounding (0 for fp32 outputs -- it is part of C u S --
+and 2^-8 for bf16).  C counts the roundings after the statistics (the two
+fused multiply-adds, the product mu r and the four correctly rounded steps
+of r = 1 / sqrt(M2 / N + eps): at most 3.5 u S together, whatever the
+kernel) and leaves 12.5 u S for the fp32 mean and M2.  Those are recursive
+sums that the kernels split over at most a few hundred terms per thread
+before an ordered fold; their worst-case first-order bound grows with the
+term count, but their rounding errors are unbiased and cancel (Higham and
+Mary's probabilistic bound grows with its square root), and the largest
+total error measured over the whole GPU suite is 2.7 u S.  For
+Pearson, y = zx zu, S = |zu| (|zx| + rms_x / sx) + |zx| (|zu| + rms_u / su),
+and r is held to 1e-5 absolute (r lies in [-1, 1]).
+Outside the zone (rtol |o| >= C u S) the bound is exactly rtol |o|.  Each
+check reports the elements that pass only through the zone term and the
+largest error in units of u S; for fp32 inputs it asserts that they are at
+most a quarter of the zone's elements (bf16 inputs take few distinct values
+near a large mean, so their zone elements come in clumps and a share means
+little).  How many there are depends on the rows: for fp32
+outputs a pure relative bound is out of reach for any fp32 evaluation -- even
+an ideal one (exact statistics, one rounding per operation) misses 1e-5 |o|
+on about 0.2 % of LayerNorm elements of N(0.5, 2) rows (pinned on the CPU in
+tests/test_tolerance.py), and on more where the mean is large against sigma
+(rms / sigma large); the bf16 workloads' full-size tests also assert that
+fewer than 1e-4 of their elements need the zone term.
 """
 from __future__ import annotations
 
@@ -30,7 +54,10 @@ from dsmem_thread_block_gb300 import _credit as C
 from dsmem_thread_block_gb300 import workloads as wl
 
 RTOL = {"f32": 1e-5, "bf16": 2.0 ** -7}
-LN_CANCEL = 1e-5
+U32 = 2.0 ** -24       # fp32 unit roundoff
+C_ZONE = 16            # fp32 evaluation error in units of u S (see above)
+U_OUT = {"f32": 0.0, "bf16": 2.0 ** -8}
+ZONE_SHARE = 0.25      # elements passing only through the zone term, share of the zone
 OPS = {wl.SOFTMAX: C.SOFTMAX, wl.LAYERNORM: C.LAYERNORM, wl.RMSNORM: C.RMSNORM,
        wl.QUANTIZE: C.QUANTIZE, wl.WEIGHTED_STD: C.WEIGHTED_STD, wl.PEARSON: C.PEARSON}
 DT = {"f32": C.F32, "bf16": C.BF16}
@@ -145,33 +172,66 @@ def oracle_rows(w: wl.Workload, inputs: dict, rows=None, want_z=False):
     return oracle.rmsnorm(x, inputs.get("weight"), eps=w.eps), None
 
 
-def check(w: wl.Workload, got: np.ndarray, inputs: dict, rows=None, scale=1.0) -> dict:
-    """Compare GPU output bytes with the oracle; assert the tolerance."""
+def cancel_scale(w: wl.Workload, inputs: dict, z: np.ndarray, rows=None) -> np.ndarray:
+    """S of the cancellation bound for LayerNorm / weighted standardization:
+    |gamma| (|z| + rms / sigma) + |beta|, rms and sigma (weighted for the
+    weighted standardization) of each row."""
+    gam = oracle.widen(inputs["gamma"]) if "gamma" in inputs else 1.0
+    bet = oracle.widen(inputs["beta"]) if "beta" in inputs else 0.0
+    xw = oracle.widen(inputs["x"] if rows is None else inputs["x"][rows])
+    wts = oracle.widen(inputs["weight"]) if w.op == wl.WEIGHTED_STD else np.ones(xw.shape[1])
+    W = wts.sum()
+    mean = (xw * wts).sum(axis=1, keepdims=True) / W
+    var = (wts * (xw - mean) ** 2).sum(axis=1, keepdims=True) / W
+    rms = np.sqrt((wts * xw * xw).sum(axis=1, keepdims=True) / W)
+    return np.abs(gam) * (np.abs(z) + rms / np.sqrt(var + w.eps)) + np.abs(bet)
+
+
+def bounds(w: wl.Workload, inputs: dict, rows=None, scale=1.0, with_scale=False):
+    """(oracle values, per-element bound, strict relative bound[, u S or None])."""
     want, z = oracle_rows(w, inputs, rows)
-    g = oracle.widen(got if rows is None else got[rows])
-    rtol = RTOL[w.dtype] * scale
-    err = np.abs(g - want)
-    bound = rtol * np.abs(want)
-    only_cancel = 0
+    strict = RTOL[w.dtype] * scale * np.abs(want)
     if w.op in (wl.LAYERNORM, wl.WEIGHTED_STD):
-        gam = oracle.widen(inputs["gamma"]) if "gamma" in inputs else 1.0
-        bet = oracle.widen(inputs["beta"]) if "beta" in inputs else 0.0
-        xw = oracle.widen(inputs["x"] if rows is None else inputs["x"][rows])
-        wts = oracle.widen(inputs["weight"]) if w.op == wl.WEIGHTED_STD else np.ones(xw.shape[1])
-        mean = (xw * wts).sum(axis=1, keepdims=True) / wts.sum()
-        var = (wts * (xw - mean) ** 2).sum(axis=1, keepdims=True) / wts.sum()
-        mu_over_sigma = np.abs(mean) / np.sqrt(var + w.eps)
-        extra = LN_CANCEL * scale * (np.abs(gam) * (np.abs(z) + mu_over_sigma) + np.abs(bet))
-        only_cancel = int(((err > bound) & (err <= bound + extra)).sum())
-        bound = bound + extra
+        uS = U32 * cancel_scale(w, inputs, z, rows)
+        zone = U_OUT[w.dtype] * np.abs(want) + C_ZONE * scale * uS
+        out = (want, np.maximum(strict, zone), strict, uS)
+    else:
+        out = (want, strict, strict, None)
+    return out if with_scale else out[:3]
+
+
+def _report(name: str, err, bound, strict, want, dtype: str, uS=None,
+            in_dtype: str = "f32") -> dict:
     bad = err > bound
     if bad.any():
         i = np.unravel_index(np.argmax(err - bound), err.shape)
         raise AssertionError(
-            f"{w.name}: {int(bad.sum())} of {err.size} elements out of tolerance; worst at "
-            f"{i}: got {g[i]!r} want {want[i]!r} err {err[i]:.3e} bound {bound[i]:.3e}")
+            f"{name}: {int(bad.sum())} of {err.size} elements out of tolerance; worst at "
+            f"{i}: want {want[i]!r} err {err[i]:.3e} bound {bound[i]:.3e}")
+    only_zone = int((err > strict).sum())
+    in_zone = bound > strict
     rel = err / np.maximum(np.abs(want), 1e-300)
-    return {"max_rel": float(rel.max()), "only_cancel": only_cancel, "n": int(err.size)}
+    res = {"max_rel": float(rel[~in_zone].max()) if (~in_zone).any() else 0.0,
+           "only_cancel": only_zone, "zone": int(in_zone.sum()), "n": int(err.size),
+           "only_cancel_frac": only_zone / max(1, err.size)}
+    if uS is not None:
+        res["max_c"] = float((np.maximum(err - U_OUT[dtype] * np.abs(want), 0) / uS).max())
+    if in_dtype == "f32":
+        assert only_zone <= ZONE_SHARE * res["zone"], \
+            f"{name}: {only_zone} of the zone's {res['zone']} elements need the cancellation term"
+    if only_zone:
+        print(f"[parity] {name}: max_rel {res['max_rel']:.3e} outside the zone; "
+              f"{only_zone} of {err.size} ({100 * res['only_cancel_frac']:.4f} %; zone "
+              f"{res['zone']}) pass only through the cancellation term; "
+              f"max err {res.get('max_c', float('nan')):.2f} u S")
+    return res
+
+
+def check(w: wl.Workload, got: np.ndarray, inputs: dict, rows=None, scale=1.0) -> dict:
+    """Compare GPU output bytes with the oracle; assert the tolerance."""
+    want, bound, strict, uS = bounds(w, inputs, rows, scale, with_scale=True)
+    g = oracle.widen(got if rows is None else got[rows])
+    return _report(w.name, np.abs(g - want), bound, strict, want, w.dtype, uS, w.dtype)
 
 
 def check_quant(got, inputs: dict, rows=None):
@@ -186,7 +246,6 @@ def check_quant(got, inputs: dict, rows=None):
     assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[0]}: {q[tuple(bad[0])]} vs {qo[tuple(bad[0])]}"
 
 
-PEARSON_CANCEL = 1e-5
 R_ATOL = 1e-5
 
 
@@ -203,18 +262,14 @@ def check_pearson(w: wl.Workload, got, inputs: dict, rows=None, scale=1.0) -> di
     sx = np.sqrt(((xw - mx) ** 2).mean(axis=1, keepdims=True) + w.eps)
     su = np.sqrt(((uw - mu) ** 2).mean(axis=1, keepdims=True) + w.eps)
     zx, zu = (xw - mx) / sx, (uw - mu) / su
-    err = np.abs(g - want)
     rms_x = np.sqrt((xw ** 2).mean(axis=1, keepdims=True))
     rms_u = np.sqrt((uw ** 2).mean(axis=1, keepdims=True))
-    bound = RTOL[w.dtype] * scale * np.abs(want) + PEARSON_CANCEL * scale * (
-        np.abs(zu) * (np.abs(zx) + rms_x / sx) + np.abs(zx) * (np.abs(zu) + rms_u / su))
-    bad = err > bound
-    if bad.any():
-        i = np.unravel_index(np.argmax(err - bound), err.shape)
-        raise AssertionError(
-            f"{w.name}: {int(bad.sum())} of {err.size} outputs out of tolerance; worst at {i}: "
-            f"got {g[i]!r} want {want[i]!r} err {err[i]:.3e} bound {bound[i]:.3e}")
+    S = np.abs(zu) * (np.abs(zx) + rms_x / sx) + np.abs(zx) * (np.abs(zu) + rms_u / su)
+    strict = RTOL[w.dtype] * scale * np.abs(want)
+    bound = np.maximum(strict, U_OUT[w.dtype] * np.abs(want) + C_ZONE * U32 * scale * S)
+    res = _report(w.name, np.abs(g - want), bound, strict, want, w.dtype, U32 * S, w.dtype)
     rerr = np.abs(rg - rw)
     assert (rerr <= R_ATOL * scale).all(), \
         f"{w.name}: r differs by {rerr.max():.3e} at row {int(np.argmax(rerr))}"
-    return {"max_r_err": float(rerr.max()), "n": int(err.size)}
+    res["max_r_err"] = float(rerr.max())
+    return res
