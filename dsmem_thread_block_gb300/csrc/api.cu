@@ -17,6 +17,12 @@ namespace credit {
 
 __device__ unsigned g_device_error;
 
+#ifdef CREDIT_DEBUG
+// Checked build: the per-(row, rank) combined statistics record
+// (debug_row_stats); read and reset by credit_debug_stats.
+__device__ float g_dbg_stats[kDbgStatsRows * kMaxCluster * kDbgStatsWidth];
+#endif
+
 // Self-test of the bounded-wait path: one thread waits on an mbarrier that
 // nothing ever completes, gives up after `limit_ns` and records the timeout
 // in the device error word, exactly as the kernels' waits do.  No copy is in
@@ -105,6 +111,16 @@ const KernelInfo* kernel_info(int dev, const void* fn, bool cluster) {
         return nullptr;
     }
     return &g_kinfo.emplace(key, ki).first->second;
+}
+
+float* debug_stats_buffer() {
+#ifdef CREDIT_DEBUG
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dbg_stats) != cudaSuccess) { cudaGetLastError(); return nullptr; }
+    return static_cast<float*>(p);
+#else
+    return nullptr;
+#endif
 }
 
 unsigned* device_error_word() {
@@ -329,7 +345,7 @@ credit_status_t run(const OpCall& c) {
         key.deep = di && plan.smem_bytes > (int64_t)di->smem_per_sm / 3 - 4096;
     }
     if (plan.variant == CREDIT_WARP_ROWS) {
-        WarpRowsArgs a;
+        WarpRowsArgs a{};
         a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;
         a.rows = c.rows;
         a.cols = c.cols;
@@ -340,7 +356,7 @@ credit_status_t run(const OpCall& c) {
     }
     if (plan.variant == CREDIT_CLUSTER_PERSISTENT || plan.variant == CREDIT_CLUSTER_PIPELINED) {
         const bool piped = plan.variant == CREDIT_CLUSTER_PIPELINED;
-        PersistArgs a;
+        PersistArgs a{};
         a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;
         a.rows = c.rows;
         a.cols = c.cols;
@@ -351,6 +367,7 @@ credit_status_t run(const OpCall& c) {
         a.eps = c.eps;
         a.err = err;
         a.exchange = (piped || plan.exchange == CREDIT_EXCHANGE_ASYNC) ? 1 : 0;
+        a.dbg_stats = debug_stats_buffer();
         a.reducers = piped ? pipelined_reducers(key.op, key.dtype, plan.threads / 32 - 1) : 0;
         // the parameter room follows the ring (warp-specialised plans only)
         const int64_t ring_bytes = (int64_t)plan.ring_slots * plan.chunk_elems * (int64_t)es;
@@ -363,7 +380,7 @@ credit_status_t run(const OpCall& c) {
     }
 
     if (plan.variant == CREDIT_CLUSTER) {
-        ClusterArgs a;
+        ClusterArgs a{};
         a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;
         a.rows = c.rows;
         a.cols = c.cols;
@@ -374,6 +391,7 @@ credit_status_t run(const OpCall& c) {
         a.err = err;
         a.aux = c.aux;
         a.exchange = plan.exchange == CREDIT_EXCHANGE_ASYNC ? 1 : 0;
+        a.dbg_stats = debug_stats_buffer();
         const void* fn = cluster_kernel(key);
         if (!kernel_info(dev, fn, true)) return CREDIT_ERR_CUDA;
         return from_cuda(launch_cluster(key, a, plan.cluster_size, plan.threads,
@@ -382,7 +400,7 @@ credit_status_t run(const OpCall& c) {
     // two-pass baseline
     if (!c.ws || c.ws_bytes < (size_t)plan.workspace_bytes || !aligned16(c.ws))
         return CREDIT_ERR_INVALID_ARG;
-    TwoPassArgs a;
+    TwoPassArgs a{};
     a.x = c.x; a.y = c.y; a.p0 = c.p0; a.p1 = c.p1;
     a.cols = c.cols;
     a.chunk = (int32_t)plan.slice_elems;
@@ -520,6 +538,26 @@ credit_status_t credit_selftest_bounds(int device) {
     return credit_get_device_error(device);
 #else
     (void)device;
+    return CREDIT_ERR_UNSUPPORTED;
+#endif
+}
+
+credit_status_t credit_debug_stats(void* host, int64_t rows) {
+#ifdef CREDIT_DEBUG
+    if (!host || rows < 1 || rows > kDbgStatsRows) return CREDIT_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)rows * kMaxCluster * kDbgStatsWidth * sizeof(float);
+    float* d = debug_stats_buffer();
+    if (!d || cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(host, d, bytes, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(d, 0xff, sizeof(g_dbg_stats)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
+    return CREDIT_OK;
+#else
+    (void)host;
+    (void)rows;
     return CREDIT_ERR_UNSUPPORTED;
 #endif
 }

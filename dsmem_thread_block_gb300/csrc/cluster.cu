@@ -218,6 +218,9 @@ cluster_reduce_reuse(const ClusterArgs a) {
         }
     }
 
+    if (tid == 0) {
+        for (int i = 0; i < rows; ++i) debug_row_stats(a.dbg_stats, row0 + i, rank, P, stv[i], 3);
+    }
     CREDIT_TRACE(4);
     // ------------------------------------------------------- a7 output
     constexpr bool kParams = OP == kLayerNorm || OP == kRMSNorm;

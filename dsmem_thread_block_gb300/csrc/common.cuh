@@ -303,6 +303,27 @@ __device__ __forceinline__ bool in_bounds(bool ok, unsigned* err) {
 #endif
 }
 
+// Checked build: the combined statistics every CTA rebuilt for a row, so a
+// test can see that all P CTAs of a cluster hold bit-identical values (the
+// premise of the replicated push: "C. Cluster Reduction and Reuse Protocol",
+// All-Gather Trade-off).  Rows [0, kDbgStatsRows) of a launch, one record of
+// kDbgStatsWidth floats per (row, rank): the statistics, then P in the last.
+constexpr int kDbgStatsRows = 64;
+constexpr int kDbgStatsWidth = 8;
+
+__device__ __forceinline__ void debug_row_stats(float* buf, int64_t row, uint32_t rank,
+                                                uint32_t P, const float* v, int nv) {
+#ifdef CREDIT_DEBUG
+    if (buf && row >= 0 && row < kDbgStatsRows && rank < (uint32_t)kMaxCluster) {
+        float* d = buf + ((size_t)row * kMaxCluster + rank) * kDbgStatsWidth;
+        for (int i = 0; i < nv && i < kDbgStatsWidth - 1; ++i) d[i] = v[i];
+        d[kDbgStatsWidth - 1] = (float)P;
+    }
+#else
+    (void)buf; (void)row; (void)rank; (void)P; (void)v; (void)nv;
+#endif
+}
+
 // Dynamic shared memory of the running launch, bytes.
 __device__ __forceinline__ uint32_t dyn_smem_bytes() {
     uint32_t r;

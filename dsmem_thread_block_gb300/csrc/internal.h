@@ -22,6 +22,7 @@ struct ClusterArgs {
     unsigned* err;        // device error word
     float* aux;           // per-row scales (quantization) or r (Pearson) out
     int32_t exchange;     // 0: push + cluster barrier; 1: st.async deposits + mbarrier
+    float* dbg_stats;     // checked build: per-(row, rank) combined statistics out (or null)
 };
 
 constexpr int kMaxRowsPerCluster = 4;
@@ -63,6 +64,7 @@ struct PersistArgs {
     int32_t param_off;    // warp-specialised kernel: byte offset of the parameter room in
                           // dynamic shared memory (0 = none)
     int32_t param_room;   // bytes of that room
+    float* dbg_stats;     // checked build: per-(row, rank) combined statistics out (or null)
 };
 
 constexpr int kPersistMaxSlots = 32;
@@ -115,5 +117,8 @@ cudaError_t launch_two_pass(KernelKey k, const TwoPassArgs& a, int64_t rows,
 cudaError_t launch_warp_rows(KernelKey k, const WarpRowsArgs& a, int blocks, cudaStream_t s);
 
 unsigned* device_error_word();  // address of this device's error word
+// checked build: this device's per-(row, rank) statistics record (null in the
+// regular build)
+float* debug_stats_buffer();
 
 }  // namespace credit

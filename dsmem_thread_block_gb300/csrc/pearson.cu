@@ -260,6 +260,10 @@ cluster_pearson(const ClusterArgs a) {
         });
     }
 
+    if (tid == 0) {
+        const float v[6] = {tot.n, tot.mx, tot.mu, tot.mxx, tot.muu, tot.cxu};
+        debug_row_stats(a.dbg_stats, row, rank, P, v, 6);
+    }
     // ---------------------------------------------------------- output
     const CoOut h(tot, a.cols, a.eps);
     if (rank == 0 && tid == 0) a.aux[row] = h.r;

@@ -175,6 +175,10 @@ cluster_persistent(const PersistArgs a) {
             }
             combine_slots<OP>(sl, P, st0, st1, st2);
         }
+        if (tid == 0) {
+            const float v[3] = {st0, st1, st2};
+            debug_row_stats(a.dbg_stats, row, rank, P, v, 3);
+        }
 
         // a7: apply h to the staged slice; each chunk slot goes back to the
         // producer as soon as this warp's tiles have moved past it, so the
@@ -363,6 +367,8 @@ cluster_pipelined(const PersistArgs a) {
                 combine_slots<OP>(sl, P, st0, st1, st2);
             }
             if (tid == 0) {
+                const float v[3] = {st0, st1, st2};
+                debug_row_stats(a.dbg_stats, cid + k * a.nclusters, rank, P, v, 3);
                 // the hand-off buffer of row k was last read for row k - 2
                 if (k >= 2)
                     wait(&hand_empty[k & 1], (uint32_t)((k >> 1) - 1) & 1u);

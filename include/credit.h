@@ -258,8 +258,9 @@ credit_status_t credit_rmsnorm(const void *x, void *y, int64_t rows,
  * the array holds (rows * ceil(cols / chunk) * 16 bytes > 2 MiB; the chunk
  * is the plan's slice_elems from credit_plan_for(..., CREDIT_TWO_PASS, ...)).
  * The first call on a device looks up the array's device address and sets
- * kernel attributes for that device; make that first call before any stream
- * capture.  All calls share the one array and it keeps the last call's
+ * the kernel attributes of every two-pass kernel this entry point can launch
+ * (all three operators, both data and parameter types, aligned and element
+ * paths) for that device; make that first call before any stream capture.  All calls share the one array and it keeps the last call's
  * contents (nothing in it needs clearing: every partial is written before it
  * is read); calls whose executions overlap on the GPU, e.g. on two streams,
  * race on it and must be serialised by the caller.
@@ -593,6 +594,25 @@ credit_status_t credit_selftest_bounds(int device);
  */
 #define CREDIT_TRACE_CTAS 8192
 credit_status_t credit_debug_trace(void *host, int64_t ctas);
+
+/*
+ * Combined statistics every CTA rebuilt (checked build only).  The protocol's
+ * all-gather rests on each of a cluster's P CTAs reconstructing the full row
+ * statistic on its own from the same P partials in the same rank order
+ * (CREDIT "C. Cluster Reduction and Reuse Protocol", All-Gather Trade-off and
+ * Output Generation), so every CTA must hold bit-identical values.  The
+ * clustered, persistent, warp-specialised and Pearson kernels record, for
+ * rows r < CREDIT_DEBUG_STATS_ROWS of a launch, from thread 0 of CTA `rank`,
+ * 8 floats at host[(r * 16 + rank) * 8]: the statistics (softmax m, s;
+ * LayerNorm / weighted standardization n, mean, M2; RMSNorm sum of squares;
+ * quantization absmax; Pearson n, mean x, mean u, Mxx, Muu, Cxu), unused
+ * slots, and the cluster size P in the last.  Copies `rows` (<=
+ * CREDIT_DEBUG_STATS_ROWS) rows of 16 records into `host`, then resets the
+ * record to all-ones bytes (NaN), so entries no CTA wrote read as NaN.
+ * CREDIT_ERR_UNSUPPORTED in the regular build.  Synchronises the device.
+ */
+#define CREDIT_DEBUG_STATS_ROWS 64
+credit_status_t credit_debug_stats(void *host, int64_t rows);
 
 /* Library version as "major.minor.patch" (static storage). */
 const char *credit_version(void);
