@@ -1,14 +1,17 @@
 #!/usr/bin/env python3
 """Benchmark of the clustered DSMEM reduce-reuse path on one GB300.
 
-A step is one library call over the whole workload: bf16 LayerNorm with fp32
-gamma/beta, 1024 rows x 262144 columns (512 KiB per row), eps 1e-5, x drawn
-from N(0.5, 2) with seed 1.  `value` is the algorithmic HBM rate of the timed
-steps: one read plus one write of the matrix, gamma/beta once, divided by the
-device time per step (CUDA events on the launching stream).  The input (512
-MiB) is larger than the 129 MB L2, so no flush is needed between steps.
+A step is one library call over the whole workload.  The default workload is
+the widest one: bf16 RMSNorm with a bf16 weight, 2048 rows x 786432 columns
+(1.5 MiB per row, a slice of 96-192 KiB per CTA for clusters of 8-16),
+eps 1e-6, x drawn from N(0, 1) with seed 3.  `value` is the algorithmic HBM
+rate of the timed steps: one read plus one write of the matrix, the weight
+once, divided by the device time per step (CUDA events on the launching
+stream).  The input (3.2 GB) is far larger than the 129 MB L2, so no flush
+is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload NAME]
 
 Prints ONE JSON line.  Under torchrun (N > 1) every rank runs its own replica
 of the workload on its own GPU (rows are independent: weak scaling, no
@@ -82,8 +85,75 @@ def stored_traffic(workload: str, variant_key: str):
 
 
 # ------------------------------------------------------------------ clocks
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class NvmlClockSampler:
+    """SM clock, maximum SM clock, power and clock-event reasons, polled every
+    `period_ms` through NVML (read-only queries) from a host thread, with
+    host timestamps: fine enough for a timed region of a few milliseconds."""
+
+    def __init__(self, uuid: str | None, period_ms: float = 1.0):
+        import ctypes
+        self.samples = []
+        self.error = None
+        self._stop = threading.Event()
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if uuid:
+                rc = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h))
+            else:
+                rc = lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h))
+            if rc != 0:
+                raise RuntimeError(f"no NVML handle (rc {rc})")
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception as e:  # no NVML: the caller falls back to nvidia-smi
+            self.error = str(e)
+            return
+        self.lib, self.h, self.reasons_fn = lib, h, reasons
+        self.period = period_ms / 1e3
+        self.t = threading.Thread(target=self._poll, daemon=True)
+        self.t.start()
+
+    def _poll(self):
+        import ctypes
+        sm, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.time()
+            ok = (self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(sm)) == 0 and
+                  self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 and
+                  self.reasons_fn(self.h, ctypes.byref(rs)) == 0)
+            if ok:
+                p = pw.value if self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw)) == 0 else 0
+                self.samples.append((t, sm.value, mx.value, rs.value, p / 1e3))
+            time.sleep(self.period)
+
+    def stop(self):
+        self._stop.set()
+        if self.error is None:
+            self.t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
+        reasons = sorted({name for s in inside for bit, name in _NVML_REASONS.items()
+                          if s[3] & bit})
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
+                "samples": len(inside), "power_w_max": max(s[4] for s in inside),
+                "note": "NVML, polled every ~1 ms during the timed region"}
+
+
 class ClockSampler:
-    """nvidia-smi SM clock and throttle-reason samples, host-timestamped."""
+    """nvidia-smi SM clock and throttle-reason samples, host-timestamped
+    (used when NVML cannot be loaded)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -145,6 +215,11 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
                 "samples": len(inside), "note": note}
+
+
+def clock_sampler(uuid: str | None):
+    s = NvmlClockSampler(uuid)
+    return s if s.error is None else ClockSampler(uuid)
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -243,9 +318,9 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="layernorm_bf16_1024x262144")
+    ap.add_argument("--workload", default="rmsnorm_bf16_2048x786432")
     ap.add_argument("--variant", default="auto",
-                    help="auto (cost model + tuning) | static | cluster:P | persist:P | pipe:P | warp_rows | two_pass")
+                    help="auto (cost model + tuning) | static | cluster:P[xR] | persist:P | pipe:P | warp_rows | two_pass")
     ap.add_argument("--cps", type=int, default=0, help="persistent CTAs per SM (0 = planner)")
     ap.add_argument("--exchange", default="plan", choices=["plan", "barrier", "async"],
                     help="partial exchange of a one-pass clustered plan (plan = as planned)")
@@ -305,8 +380,7 @@ def main():
         # step times every legal candidate; planning and tuning happen once,
         # before (and outside) the timed region
         pdt_model = DT[w.param_dtype] if w.param_dtype else -1
-        plan, report = C.credit_plan_profiled(OPS[w.op], w.rows, w.cols, DT[w.dtype], pdt_model,
-                                              dev, 15, 16)
+        plan, report = C.tuned_plan(OPS[w.op], w.rows, w.cols, DT[w.dtype], pdt_model, dev)
         tuning = {"model_P": report.model_cluster_size, "baseline_us": round(report.t_base_us, 2)}
         for c in report.cand:
             if c.legal and c.measured_us > 0 and c.cluster_size > 1:
@@ -322,10 +396,14 @@ def main():
     elif args.variant == "warp_rows":
         plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.WARP_ROWS, 1)
     else:
-        kind, P = args.variant.split(":")
+        kind, P = args.variant.split(":")[:2]
+        R = 0
+        if "x" in P:
+            P, R = P.split("x")
         var = {"cluster": C.CLUSTER, "persist": C.CLUSTER_PERSISTENT,
                "pipe": C.CLUSTER_PIPELINED}[kind]
-        plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, var, int(P))
+        plan = C.credit_plan_with(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, var, int(P),
+                                  rows_per_cluster=int(R))
     if args.cps:
         plan.ctas_per_sm = args.cps
         plan = C.Plan.from_buffer_copy(plan)
@@ -381,7 +459,7 @@ def main():
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
-    sampler = ClockSampler(uuid)
+    sampler = clock_sampler(uuid)
     time.sleep(0.3)  # let the sampler start before the timed region
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -456,12 +534,7 @@ def main():
     e2e_value = job_rate(bytes_step, te / e2e_steps, world)
 
     peak, peak_kind = measured_peak()
-    variant_key = {C.TWO_PASS: "two_pass", C.CLUSTER: f"cluster:{plan.cluster_size}",
-                   C.CLUSTER_PERSISTENT: f"persist:{plan.cluster_size}",
-                   C.CLUSTER_PIPELINED: f"pipe:{plan.cluster_size}",
-                   C.WARP_ROWS: "warp_rows"}[plan.variant]
-    if plan.variant == C.CLUSTER and plan.exchange == C.EXCHANGE_BARRIER:
-        variant_key += ":barrier"
+    variant_key = C.variant_name(plan)
     launches_per_step = 2 if plan.variant == C.TWO_PASS else 1
     traffic = stored_traffic(w.name, variant_key)
     # the dominant kernel is the only kernel of a clustered step

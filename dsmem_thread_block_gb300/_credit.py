@@ -142,6 +142,7 @@ SIGNATURES = {
     "credit_debug_build": (_i32, []),
     "credit_selftest_bounds": (_i32, [_i32]),
     "credit_debug_trace": (_i32, [_vp, _i64]),
+    "credit_debug_stats": (_i32, [_vp, _i64]),
     "credit_version": (ctypes.c_char_p, []),
 }
 
@@ -327,6 +328,33 @@ def credit_plan_profiled(op: int, rows: int, cols: int, dtype: int, param_dtype:
     return p, r
 
 
+def variant_name(plan) -> str:
+    """Short name of a plan's kernel and cluster size, as the benchmark
+    prints it: cluster:P[xR][:barrier], persist:P, pipe:P, warp_rows, two_pass."""
+    if plan.variant == TWO_PASS:
+        return "two_pass"
+    if plan.variant == WARP_ROWS:
+        return "warp_rows"
+    kind = {CLUSTER: "cluster", CLUSTER_PERSISTENT: "persist", CLUSTER_PIPELINED: "pipe"}[plan.variant]
+    s = f"{kind}:{plan.cluster_size}"
+    if plan.variant == CLUSTER and plan.rows_per_cluster > 1:
+        s += f"x{plan.rows_per_cluster}"
+    if plan.variant == CLUSTER and plan.exchange == EXCHANGE_BARRIER:
+        s += ":barrier"
+    return s
+
+
+TUNE_RUNS = 15  # timed runs per candidate
+TUNE_ALL = 16   # best-predicted candidates to time: every legal cluster size
+
+
+def tuned_plan(op: int, rows: int, cols: int, dtype: int, param_dtype: int = -1,
+               device: int = 0):
+    """The plan the benchmark times for a shape: credit_plan_profiled with
+    every legal candidate timed; (plan, report)."""
+    return credit_plan_profiled(op, rows, cols, dtype, param_dtype, device, TUNE_RUNS, TUNE_ALL)
+
+
 def credit_stage_copy_rate(device: int, ctas_per_sm: int, runs: int = 7):
     """(GB/s, resident CTAs per SM) of the staged-copy primitive."""
     g, k = ctypes.c_double(), ctypes.c_int32()
@@ -379,6 +407,19 @@ def credit_debug_trace(ctas: int):
     out = np.zeros((ctas, 8), dtype=np.uint64)
     _check(load().credit_debug_trace(out.ctypes.data, ctas), "credit_debug_trace")
     return out.astype(np.int64)
+
+
+DEBUG_STATS_ROWS = 64
+
+
+def credit_debug_stats(rows: int = DEBUG_STATS_ROWS):
+    """The checked build's record of the combined statistics each CTA rebuilt:
+    a float32 array [rows, 16 ranks, 8] (the statistics, then P in the last
+    slot; NaN where no CTA wrote).  Reading resets the record."""
+    import numpy as np
+    out = np.zeros((rows, 16, 8), dtype=np.float32)
+    _check(load().credit_debug_stats(out.ctypes.data, rows), "credit_debug_stats")
+    return out
 
 
 def credit_version() -> str:

@@ -10,6 +10,8 @@ holds at least one CTA.  The checked build also runs its index checks, so the
 phase times include them; use it for where the time goes, not for rates.
 
     python -m dsmem_thread_block_gb300.trace --workload softmax_bf16_sweep_1048576 --cluster-size 10
+
+`--rows R` traces the workload's first R rows (the trace holds 8192 CTAs).
 """
 from __future__ import annotations
 
@@ -64,10 +66,13 @@ def summarize(stamps: np.ndarray) -> dict:
     return out
 
 
-def run(workload: str, cluster_size: int, device: int = 0, warmup: int = 3) -> dict:
+def run(workload: str, cluster_size: int, device: int = 0, warmup: int = 3,
+        rows: int = 0) -> dict:
     import torch
 
     w = _table()[workload]
+    if rows:
+        w = w.with_rows(rows)
     torch.cuda.set_device(device)
     inp = w.generate()
 
@@ -123,8 +128,9 @@ def main():
     ap.add_argument("--workload", required=True)
     ap.add_argument("--cluster-size", type=int, required=True)
     ap.add_argument("--device", type=int, default=0)
+    ap.add_argument("--rows", type=int, default=0, help="trace the first ROWS rows (0 = all)")
     a = ap.parse_args()
-    print(json.dumps(run(a.workload, a.cluster_size, a.device)))
+    print(json.dumps(run(a.workload, a.cluster_size, a.device, rows=a.rows)))
 
 
 if __name__ == "__main__":
