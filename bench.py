@@ -320,7 +320,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="rmsnorm_bf16_2048x786432")
     ap.add_argument("--variant", default="auto",
-                    help="auto (cost model + tuning) | static | cluster:P[xR] | persist:P | pipe:P | warp_rows | two_pass")
+                    help="auto (cost model + tuning) | static | cluster:P[xR][:sSTAGED] | persist:P | pipe:P | "
+                         "warp_rows | two_pass")
     ap.add_argument("--cps", type=int, default=0, help="persistent CTAs per SM (0 = planner)")
     ap.add_argument("--exchange", default="plan", choices=["plan", "barrier", "async"],
                     help="partial exchange of a one-pass clustered plan (plan = as planned)")
@@ -384,7 +385,9 @@ def main():
         tuning = {"model_P": report.model_cluster_size, "baseline_us": round(report.t_base_us, 2)}
         for c in report.cand:
             if c.legal and c.measured_us > 0 and c.cluster_size > 1:
-                tuning[f"cluster:{c.cluster_size}"] = round(c.measured_us, 2)
+                tuning[C.variant_name(c.plan)] = round(c.measured_us, 2)
+            if c.legal and c.tail_us > 0:
+                tuning[f"cluster:{c.cluster_size}:s{c.tail_staged_elems}"] = round(c.tail_us, 2)
             if c.legal and c.persistent_us > 0:
                 tuning[f"persist:{c.cluster_size}"] = round(c.persistent_us, 2)
             if c.legal and c.pipelined_us > 0:
@@ -396,14 +399,15 @@ def main():
     elif args.variant == "warp_rows":
         plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.WARP_ROWS, 1)
     else:
-        kind, P = args.variant.split(":")[:2]
+        kind, P, *rest = args.variant.split(":")
         R = 0
         if "x" in P:
             P, R = P.split("x")
+        staged = int(rest[0][1:]) if rest and rest[0].startswith("s") else 0
         var = {"cluster": C.CLUSTER, "persist": C.CLUSTER_PERSISTENT,
                "pipe": C.CLUSTER_PIPELINED}[kind]
         plan = C.credit_plan_with(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, var, int(P),
-                                  rows_per_cluster=int(R))
+                                  rows_per_cluster=int(R), staged_elems=staged)
     if args.cps:
         plan.ctas_per_sm = args.cps
         plan = C.Plan.from_buffer_copy(plan)

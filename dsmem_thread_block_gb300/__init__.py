@@ -42,12 +42,13 @@ def _dtype(t):
 
 def plan(op: str, rows: int, cols: int, dtype, device: int | None = None,
          variant: str | None = None, cluster_size: int = 1, rows_per_cluster: int = 0,
-         exchange: str | None = None) -> Plan:
+         exchange: str | None = None, staged_elems: int = 0) -> Plan:
     """Plan a call: automatically (variant None) or for a forced variant
-    ("cluster" with `cluster_size` and optionally `rows_per_cluster`,
-    "persistent" or "pipelined" with `cluster_size`, "warp_rows" or "two_pass");
-    `exchange` ("async" or
-    "barrier") picks how a clustered plan exchanges its partials."""
+    ("cluster" with `cluster_size` and optionally `rows_per_cluster` or
+    `staged_elems` (an L2-tail plan staging that many elements of each
+    slice), "persistent" or "pipelined" with `cluster_size`, "warp_rows" or
+    "two_pass"); `exchange` ("async" or "barrier") picks how a clustered plan
+    exchanges its partials."""
     import torch
     dev = torch.cuda.current_device() if device is None else int(device)
     code = _OPS[op]
@@ -59,7 +60,8 @@ def plan(op: str, rows: int, cols: int, dtype, device: int | None = None,
     x = {None: C.EXCHANGE_DEFAULT, "async": C.EXCHANGE_ASYNC,
          "barrier": C.EXCHANGE_BARRIER}[exchange]
     return C.credit_plan_with(code, rows, cols, _dtype(dtype), dev, v, cluster_size,
-                              rows_per_cluster=rows_per_cluster, exchange=x)
+                              rows_per_cluster=rows_per_cluster, exchange=x,
+                              staged_elems=staged_elems)
 
 
 def _prep(x, out):

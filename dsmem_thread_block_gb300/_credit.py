@@ -35,7 +35,7 @@ class Plan(ctypes.Structure):
                 ("ctas_per_sm", ctypes.c_int32), ("chunk_elems", ctypes.c_int32),
                 ("ring_slots", ctypes.c_int32), ("rows_per_cluster", ctypes.c_int32),
                 ("exchange", ctypes.c_int32), ("pred_us", ctypes.c_float),
-                ("pred_two_pass_us", ctypes.c_float)]
+                ("pred_two_pass_us", ctypes.c_float), ("staged_elems", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -64,7 +64,16 @@ class Candidate(ctypes.Structure):
                 ("t_ctrl_us", ctypes.c_double), ("t_comm_us", ctypes.c_double),
                 ("pred_us", ctypes.c_double), ("measured_us", ctypes.c_double),
                 ("persistent_us", ctypes.c_double),
-                ("pipelined_us", ctypes.c_double)]
+                ("pipelined_us", ctypes.c_double), ("tail_us", ctypes.c_double),
+                ("tail_staged_elems", ctypes.c_int64)]
+
+
+class DeviceKey(ctypes.Structure):
+    """Mirror of credit_device_key_t."""
+    _fields_ = [("gpu_name", ctypes.c_char * 96), ("sms", ctypes.c_int32),
+                ("sm_clock_mhz", ctypes.c_int32), ("mem_clock_mhz", ctypes.c_int32),
+                ("cc_major", ctypes.c_int32), ("cc_minor", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class HostCall(ctypes.Structure):
@@ -131,6 +140,11 @@ SIGNATURES = {
     "credit_plan_profiled": (_i32, [_i32, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
                                     ctypes.POINTER(Plan), ctypes.POINTER(ModelReport)]),
     "credit_status_string": (ctypes.c_char_p, [_i32]),
+    "credit_l2_read_rate": (_i32, [_i32, _i64, _i32, ctypes.POINTER(ctypes.c_double)]),
+    "credit_device_key": (_i32, [_i32, ctypes.POINTER(DeviceKey)]),
+    "credit_save_profile": (_i32, [_i32, ctypes.c_char_p]),
+    "credit_load_profile": (_i32, [_i32, ctypes.c_char_p]),
+    "credit_profile_check": (_i32, [ctypes.c_char_p, ctypes.POINTER(DeviceKey)]),
     "credit_stage_copy_rate": (_i32, [_i32, _i32, _i32, ctypes.POINTER(ctypes.c_double),
                                       ctypes.POINTER(ctypes.c_int32)]),
     "credit_host_buffer_bytes": (_i32, [ctypes.POINTER(HostCall), ctypes.POINTER(Plan), _i64,
@@ -234,10 +248,11 @@ def credit_plan_for(op: int, rows: int, cols: int, dtype: int, device: int,
 def credit_plan_with(op: int, rows: int, cols: int, dtype: int, device: int, variant: int,
                      cluster_size: int = 1, threads: int = 0, ctas_per_sm: int = 0,
                      chunk_elems: int = 0, rows_per_cluster: int = 0,
-                     exchange: int = EXCHANGE_DEFAULT) -> Plan:
+                     exchange: int = EXCHANGE_DEFAULT, staged_elems: int = 0) -> Plan:
     req = Plan(variant=variant, cluster_size=cluster_size, threads=threads,
                ctas_per_sm=ctas_per_sm, chunk_elems=chunk_elems,
-               rows_per_cluster=rows_per_cluster, exchange=exchange)
+               rows_per_cluster=rows_per_cluster, exchange=exchange,
+               staged_elems=staged_elems)
     p = Plan()
     _check(load().credit_plan_with(op, rows, cols, dtype, device, ctypes.byref(req),
                                    ctypes.byref(p)), "credit_plan_with")
@@ -330,7 +345,8 @@ def credit_plan_profiled(op: int, rows: int, cols: int, dtype: int, param_dtype:
 
 def variant_name(plan) -> str:
     """Short name of a plan's kernel and cluster size, as the benchmark
-    prints it: cluster:P[xR][:barrier], persist:P, pipe:P, warp_rows, two_pass."""
+    prints it: cluster:P[xR][:sSTAGED][:barrier], persist:P, pipe:P, warp_rows,
+    two_pass (sSTAGED: an L2-tail plan staging STAGED elements per CTA)."""
     if plan.variant == TWO_PASS:
         return "two_pass"
     if plan.variant == WARP_ROWS:
@@ -339,6 +355,8 @@ def variant_name(plan) -> str:
     s = f"{kind}:{plan.cluster_size}"
     if plan.variant == CLUSTER and plan.rows_per_cluster > 1:
         s += f"x{plan.rows_per_cluster}"
+    if plan.variant == CLUSTER and 0 < plan.staged_elems < plan.slice_elems:
+        s += f":s{plan.staged_elems}"
     if plan.variant == CLUSTER and plan.exchange == EXCHANGE_BARRIER:
         s += ":barrier"
     return s
@@ -353,6 +371,34 @@ def tuned_plan(op: int, rows: int, cols: int, dtype: int, param_dtype: int = -1,
     """The plan the benchmark times for a shape: credit_plan_profiled with
     every legal candidate timed; (plan, report)."""
     return credit_plan_profiled(op, rows, cols, dtype, param_dtype, device, TUNE_RUNS, TUNE_ALL)
+
+
+def credit_device_key(device: int = 0) -> DeviceKey:
+    k = DeviceKey()
+    _check(load().credit_device_key(device, ctypes.byref(k)), "credit_device_key")
+    return k
+
+
+def credit_save_profile(device: int, path: str) -> int:
+    return load().credit_save_profile(device, path.encode())
+
+
+def credit_load_profile(device: int, path: str) -> int:
+    """Status: OK, ERR_NOT_CALIBRATED (stale profile) or ERR_INVALID_ARG."""
+    return load().credit_load_profile(device, path.encode())
+
+
+def credit_profile_check(path: str, key: DeviceKey) -> int:
+    """Status: OK, ERR_NOT_CALIBRATED (stale for `key`) or ERR_INVALID_ARG."""
+    return load().credit_profile_check(path.encode(), ctypes.byref(key))
+
+
+def credit_l2_read_rate(device: int, window_bytes: int, runs: int = 7) -> float:
+    """GB/s at which all SMs read a window of `window_bytes` from L2."""
+    g = ctypes.c_double()
+    _check(load().credit_l2_read_rate(device, window_bytes, runs, ctypes.byref(g)),
+           "credit_l2_read_rate")
+    return g.value
 
 
 def credit_stage_copy_rate(device: int, ctas_per_sm: int, runs: int = 7):

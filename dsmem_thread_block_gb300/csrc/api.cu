@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -192,6 +193,15 @@ struct OpCall {
 };
 
 // Complete / re-derive a plan from the fields a caller may set.
+// The L2-tail length a request asks for: its staged_elems when that is
+// below its own slice_elems (a tail plan as derived) or when the request
+// carries no slice_elems (a fresh request); 0 (the whole slice) otherwise,
+// so a whole-slice plan stays one when its cluster size is edited.
+int64_t tail_request(const credit_plan_t& r) {
+    if (r.staged_elems <= 0) return 0;
+    return (r.slice_elems <= 0 || r.staged_elems < r.slice_elems) ? r.staged_elems : 0;
+}
+
 credit_status_t plan_from_request(int dev, credit_op_t op, int64_t rows, int64_t cols,
                                   credit_dtype_t dtype, const credit_plan_t& r,
                                   credit_plan_t* out) {
@@ -209,10 +219,12 @@ credit_status_t plan_from_request(int dev, credit_op_t op, int64_t rows, int64_t
     if (v == CREDIT_CLUSTER_PIPELINED && r.exchange == CREDIT_EXCHANGE_BARRIER)
         return CREDIT_ERR_INVALID_ARG;
     const bool pers = v == CREDIT_CLUSTER_PERSISTENT || v == CREDIT_CLUSTER_PIPELINED;
+    if (r.staged_elems < 0) return CREDIT_ERR_INVALID_ARG;
     const credit_status_t st =
         make_plan(dev, op, rows, cols, dtype, v, r.cluster_size, r.threads,
                   pers ? r.ctas_per_sm : 0, out, pers ? r.chunk_elems : 0,
-                  v == CREDIT_CLUSTER ? r.rows_per_cluster : 0);
+                  v == CREDIT_CLUSTER ? r.rows_per_cluster : 0,
+                  v == CREDIT_CLUSTER ? tail_request(r) : 0);
     if (st == CREDIT_OK && r.exchange != CREDIT_EXCHANGE_DEFAULT) out->exchange = r.exchange;
     return st;
 }
@@ -224,7 +236,7 @@ credit_status_t plan_from_request(int dev, credit_op_t op, int64_t rows, int64_t
 // calibration may change) has been looked up.
 struct PlanKey {
     int dev, op, dtype, variant, cluster_size, threads, cps, chunk, rpc, exchange;
-    int64_t rows, cols;
+    int64_t rows, cols, staged;
     bool operator==(const PlanKey& o) const {
         return std::memcmp(this, &o, sizeof(PlanKey)) == 0;
     }
@@ -243,7 +255,9 @@ std::unordered_map<PlanKey, credit_plan_t, PlanKeyHash> g_plans;
 credit_status_t cached_plan(int dev, const OpCall& c, credit_plan_t* out) {
     credit_plan_t profiled;
     const bool automatic = !(c.plan && c.plan->variant != CREDIT_AUTO);
-    if (automatic && lookup_profiled_plan(dev, c.op, c.rows, c.cols, c.dtype, &profiled)) {
+    const char* force = std::getenv("CREDIT_FORCE");  // a forced plan outranks a profiled one
+    if (automatic && !(force && *force) &&
+        lookup_profiled_plan(dev, c.op, c.rows, c.cols, c.dtype, &profiled)) {
         *out = profiled;
         return CREDIT_OK;
     }
@@ -254,7 +268,7 @@ credit_status_t cached_plan(int dev, const OpCall& c, credit_plan_t* out) {
         const credit_plan_t& r = *c.plan;
         k.variant = r.variant; k.cluster_size = r.cluster_size; k.threads = r.threads;
         k.cps = r.ctas_per_sm; k.chunk = r.chunk_elems; k.rpc = r.rows_per_cluster;
-        k.exchange = r.exchange;
+        k.exchange = r.exchange; k.staged = tail_request(r);
     }
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
@@ -327,9 +341,11 @@ credit_status_t run(const OpCall& c) {
     if (!err) return CREDIT_ERR_CUDA;
     if (!vec && plan.variant != CREDIT_TWO_PASS &&
         (plan.variant == CREDIT_CLUSTER_PERSISTENT || plan.variant == CREDIT_CLUSTER_PIPELINED ||
-         plan.variant == CREDIT_WARP_ROWS || plan.rows_per_cluster != 1)) {
+         plan.variant == CREDIT_WARP_ROWS || plan.rows_per_cluster != 1 ||
+         (plan.staged_elems > 0 && plan.staged_elems < plan.slice_elems))) {
         // bulk copies need 16-byte alignment: misaligned or ragged rows take
-        // the one-row-per-cluster kernel's element path instead
+        // the one-row-per-cluster kernel's element path instead, which stages
+        // the whole slice (no L2 tail)
         const int32_t xchg = plan.exchange;
         st = make_plan(dev, c.op, c.rows, c.cols, c.dtype, CREDIT_CLUSTER, plan.cluster_size, 0, 0,
                        &plan, 0, 1);
@@ -392,6 +408,7 @@ credit_status_t run(const OpCall& c) {
         a.aux = c.aux;
         a.exchange = plan.exchange == CREDIT_EXCHANGE_ASYNC ? 1 : 0;
         a.dbg_stats = debug_stats_buffer();
+        a.staged = plan.staged_elems > 0 ? plan.staged_elems : plan.slice_elems;
         const void* fn = cluster_kernel(key);
         if (!kernel_info(dev, fn, true)) return CREDIT_ERR_CUDA;
         return from_cuda(launch_cluster(key, a, plan.cluster_size, plan.threads,
@@ -573,6 +590,6 @@ credit_status_t credit_selftest_wait_timeout(int device, int64_t limit_ns) {
     return credit_get_device_error(device);
 }
 
-const char* credit_version(void) { return "0.4.0"; }
+const char* credit_version(void) { return "0.5.0"; }
 
 }  // extern "C"

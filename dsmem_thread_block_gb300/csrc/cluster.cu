@@ -69,16 +69,22 @@ cluster_reduce_reuse(const ClusterArgs a) {
     const bool async_x = a.exchange == 1 && P > 1;
     const int64_t row0 = (blockIdx.x / P) * (int64_t)R;
     const int rows = (int)min((int64_t)R, a.rows - row0);  // live rows of this cluster
+    // L2 tail: one row per cluster may stage only the first a.staged
+    // elements of its slice; the rest is read from HBM once for the
+    // statistics (kept in L2) and once more, from L2, for the output
+    constexpr bool kTail = BULK && R == 1 && tail_capable(OP, (int)sizeof(T));
     const int64_t start = (int64_t)rank * a.slice;
-    const int n_slice = (int)max((int64_t)0, min(a.cols - start, a.slice));
+    const int n_full = (int)max((int64_t)0, min(a.cols - start, a.slice));
+    const int n_slice = kTail ? (int)min((int64_t)n_full, a.staged) : n_full;
     // checked build: the live rows' staged slices and their chunk mbarriers
     // must fit the launch
-    const int n = layout_fits(BULK ? (uint64_t)(rows - 1) * a.pitch + (uint64_t)n_slice * sizeof(T)
-                                   : (uint64_t)n_slice * sizeof(T),
-                              BULK ? (int64_t)rows * ((n_slice + a.chunk_elems - 1) / a.chunk_elems)
-                                   : 0,
-                              kMaxChunks, a.err)
-                      ? n_slice : 0;
+    const bool fits =
+        layout_fits(BULK ? (uint64_t)(rows - 1) * a.pitch + (uint64_t)n_slice * sizeof(T)
+                         : (uint64_t)n_slice * sizeof(T),
+                    BULK ? (int64_t)rows * ((n_slice + a.chunk_elems - 1) / a.chunk_elems) : 0,
+                    kMaxChunks, a.err);
+    const int n = fits ? n_slice : 0;                       // staged elements
+    const int ntail = kTail && fits ? n_full - n_slice : 0;  // L2-tail elements
     const T* xs = static_cast<const T*>(a.x) + row0 * a.cols + start;
     const int tid = threadIdx.x, nt = blockDim.x;
     const int warp = tid >> 5, lane = tid & 31, nwarps = nt >> 5;
@@ -134,8 +140,14 @@ cluster_reduce_reuse(const ClusterArgs a) {
 
     // --------------------------------------------- a3 local partials
     // each chunk is folded into the threads' statistics as soon as it lands
+    // (the L2 tail first, while the bulk copies are in flight)
     const PT* wp = OP == kWStd ? static_cast<const PT*>(a.p0) + start : nullptr;  // weights
     Stats<OP, T> st[R];
+    if constexpr (kTail) {
+        if (ntail > 0)
+            stats_global(st[0], reinterpret_cast<const unsigned char*>(xs + n), ntail / VEC, warp,
+                         nwarps, lane, l2_policy_evict_last());
+    }
 #pragma unroll
     for (int i = 0; i < R; ++i) {
         if (i < rows) {
@@ -244,6 +256,14 @@ cluster_reduce_reuse(const ClusterArgs a) {
         T* yrow[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) yrow[i] = static_cast<T*>(a.y) + (row0 + i) * a.cols + start;
+        if constexpr (kTail) {
+            // the L2 tail first: its lines leave L2 as early as possible
+            if (ntail > 0)
+                output_tiles<OP, T, PT, NoRelease, false, true>(
+                    h[0], reinterpret_cast<const unsigned char*>(xs + n), yrow[0] + n,
+                    g ? g + start + n : nullptr, b ? b + start + n : nullptr, ntail / VEC, warp,
+                    nwarps, lane, NoRelease(), l2_policy_evict_first());
+        }
         // RMSNorm with bf16 data and bf16 weights gains from the pipelined
         // pass (measured); the other operator / type combinations do not
         constexpr bool kPipe = BULK && R == 1 && OP == kRMSNorm && Granule<OP, T, PT>::kPairs == 4;

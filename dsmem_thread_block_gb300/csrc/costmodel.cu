@@ -92,11 +92,55 @@ double median_of(std::vector<double> v) {
 
 bool lookup_profiled_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
                           credit_dtype_t dtype, credit_plan_t* out) {
+    profile_env_load(dev);  // CREDIT_PROFILE: the saved choices, once per device
     std::lock_guard<std::mutex> lk(g_cm_mu);
     auto it = g_chosen.find(std::make_tuple(dev, (int)op, (int)dtype, rows, cols));
     if (it == g_chosen.end()) return false;
     *out = it->second;
     return true;
+}
+
+bool dsmem_profile_get(int dev, double* barrier_ns, double* exchange_ns, double* async_ns) {
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(g_cm_mu);
+    const DsmemProfile& p = g_profile[dev];
+    if (!p.valid) return false;
+    for (int P = 0; P <= kMaxCluster; ++P) {
+        barrier_ns[P] = p.barrier_ns[P];
+        exchange_ns[P] = p.exchange_ns[P];
+        async_ns[P] = p.async_exchange_ns[P];
+    }
+    return true;
+}
+
+void dsmem_profile_set(int dev, const double* barrier_ns, const double* exchange_ns,
+                       const double* async_ns) {
+    if (dev < 0 || dev >= kMaxDevices) return;
+    DsmemProfile p;
+    for (int P = 0; P <= kMaxCluster; ++P) {
+        p.barrier_ns[P] = barrier_ns[P];
+        p.exchange_ns[P] = exchange_ns[P];
+        p.async_exchange_ns[P] = async_ns[P];
+    }
+    p.valid = true;
+    std::lock_guard<std::mutex> lk(g_cm_mu);
+    g_profile[dev] = p;
+}
+
+std::vector<ChosenPlan> chosen_plans(int dev) {
+    std::vector<ChosenPlan> out;
+    std::lock_guard<std::mutex> lk(g_cm_mu);
+    for (const auto& kv : g_chosen) {
+        if (std::get<0>(kv.first) != dev) continue;
+        out.push_back(ChosenPlan{std::get<1>(kv.first), std::get<2>(kv.first),
+                                 std::get<3>(kv.first), std::get<4>(kv.first), kv.second});
+    }
+    return out;
+}
+
+void chosen_plan_put(int dev, const ChosenPlan& c) {
+    std::lock_guard<std::mutex> lk(g_cm_mu);
+    g_chosen[std::make_tuple(dev, c.op, c.dtype, c.rows, c.cols)] = c.plan;
 }
 
 }  // namespace credit
@@ -124,20 +168,10 @@ extern "C" credit_status_t credit_calibrate(int device, int runs, const char* pr
         g_profile[device] = prof;
     }
     if (profile_path) {
-        FILE* f = std::fopen(profile_path, "w");
-        if (!f) return CREDIT_ERR_INVALID_ARG;
-        std::fprintf(f, "{\"device\": %d, \"runs\": %d, \"barrier_ns\": {", device, runs);
-        for (int P = 2; P <= kMaxCluster; ++P)
-            std::fprintf(f, "%s\"%d\": %.2f", P > 2 ? ", " : "", P, prof.barrier_ns[P]);
-        std::fprintf(f, "}, \"exchange_ns\": {");
-        for (int P = 2; P <= kMaxCluster; ++P)
-            std::fprintf(f, "%s\"%d\": %.2f", P > 2 ? ", " : "", P, prof.exchange_ns[P]);
-        std::fprintf(f, "}, \"async_exchange_ns\": {");
-        for (int P = 2; P <= kMaxCluster; ++P)
-            std::fprintf(f, "%s\"%d\": %.2f", P > 2 ? ", " : "", P, prof.async_exchange_ns[P]);
-        std::fprintf(f, "}}\n");
-        std::fclose(f);
+        const credit_status_t st = credit_save_profile(device, profile_path);
+        if (st != CREDIT_OK) return st;
     }
+    profile_env_save(device);
     return CREDIT_OK;
 }
 
@@ -207,6 +241,7 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
     if (dtype != CREDIT_F32 && dtype != CREDIT_BF16) return CREDIT_ERR_UNSUPPORTED;
     if (param_dtype != -1 && param_dtype != CREDIT_F32 && param_dtype != CREDIT_BF16)
         return CREDIT_ERR_UNSUPPORTED;
+    profile_env_load(device);  // CREDIT_PROFILE: a saved DSMEM profile spares the calibration
     DsmemProfile prof;
     {
         std::lock_guard<std::mutex> lk(g_cm_mu);
@@ -343,8 +378,15 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         credit_candidate_t& c = rep.cand[P - 1];
         c.cluster_size = P;
         credit_plan_t p;
-        if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1) != CREDIT_OK)
-            continue;
+        if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1) != CREDIT_OK) {
+            // a slice too large for shared memory is a candidate through its
+            // L2-tail plan (two CTAs per SM)
+            const int64_t held = tail_staged_for(device, op, cols, dtype, P, 2);
+            if (held == 0 ||
+                make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1, held) !=
+                    CREDIT_OK)
+                continue;
+        }
         if ((int64_t)(P - 1) * p.slice_elems >= cols) continue;  // an idle CTA
         double ctrl = 0.0;
         st = credit_control_time(device, rt, P, p.threads, p.smem_bytes, 1, 2, runs, &ctrl);
@@ -399,6 +441,28 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
                 best_plan = c.plan;
                 best_meas_P = P;
             }
+            // L2-tail plans sized for two and three CTAs per SM
+            for (int cps : {2, 3}) {
+                const int64_t held = tail_staged_for(device, op, cols, dtype, P, cps);
+                if (held == 0 || held == c.plan.staged_elems) continue;
+                credit_plan_t tp;
+                if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &tp, 0, 1,
+                              held) != CREDIT_OK)
+                    continue;
+                double us = 0.0;
+                st = time_op(op, x.p, y.p, rt, cols, dtype, g.p, b.p, param_dtype, &tp, nullptr,
+                             0, runs, &us, auxp);
+                if (st != CREDIT_OK) return st;
+                if (c.tail_us == 0.0 || us < c.tail_us) {
+                    c.tail_us = us;
+                    c.tail_staged_elems = held;
+                }
+                if (us < best_meas) {
+                    best_meas = us;
+                    best_plan = tp;
+                    best_meas_P = P;
+                }
+            }
             for (credit_variant_t rv : {CREDIT_CLUSTER_PERSISTENT, CREDIT_CLUSTER_PIPELINED}) {
                 credit_plan_t pp;
                 if (make_plan(device, op, rt, cols, dtype, rv, P, 0, 0, &pp) != CREDIT_OK) continue;
@@ -427,7 +491,8 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         const bool pers = v == CREDIT_CLUSTER_PERSISTENT || v == CREDIT_CLUSTER_PIPELINED;
         if (make_plan(device, op, rows, cols, dtype, v, chosen.cluster_size, chosen.threads,
                       pers ? chosen.ctas_per_sm : 0, &full, pers ? chosen.chunk_elems : 0,
-                      v == CREDIT_CLUSTER ? chosen.rows_per_cluster : 0) == CREDIT_OK) {
+                      v == CREDIT_CLUSTER ? chosen.rows_per_cluster : 0,
+                      v == CREDIT_CLUSTER ? chosen.staged_elems : 0) == CREDIT_OK) {
             const double scale = (double)rows / (double)rt;
             full.exchange = chosen.exchange;
             full.pred_us = (float)(chosen.pred_us * scale);
@@ -439,6 +504,7 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         std::lock_guard<std::mutex> lk(g_cm_mu);
         g_chosen[std::make_tuple(device, (int)op, (int)dtype, rows, cols)] = chosen;
     }
+    profile_env_save(device);
     *out = chosen;
     if (report) *report = rep;
     return CREDIT_OK;

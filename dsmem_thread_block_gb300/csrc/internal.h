@@ -23,9 +23,18 @@ struct ClusterArgs {
     float* aux;           // per-row scales (quantization) or r (Pearson) out
     int32_t exchange;     // 0: push + cluster barrier; 1: st.async deposits + mbarrier
     float* dbg_stats;     // checked build: per-(row, rank) combined statistics out (or null)
+    int64_t staged;       // elements of a CTA's slice staged in shared memory (>= slice: all);
+                          // the rest, the L2 tail, is read twice through L2
 };
 
 constexpr int kMaxRowsPerCluster = 4;
+
+// Operators and data types whose one-row-per-cluster kernel can leave an L2
+// tail of its slice unstaged (not fp32 softmax, whose stash pass rewrites
+// the staged slice in place).
+__host__ __device__ constexpr bool tail_capable(int op, int dtype_bytes) {
+    return op == 1 /* LayerNorm */ || op == 2 /* RMSNorm */ || (op == 0 && dtype_bytes == 2);
+}
 
 // Arguments of the two-pass (global re-read) kernel pair.
 struct TwoPassArgs {

@@ -420,6 +420,94 @@ extern "C" credit_status_t credit_control_time(int device, int64_t nclusters, in
     return status;
 }
 
+// L2 read primitive: every CTA reads the whole `window` (16-byte vectors,
+// eight loads in flight per thread, past L1), starting at a CTA-dependent
+// offset so the CTAs spread over the L2 slices.  With a window far smaller
+// than L2 every read after the first launch is an L2 hit: the rate is what
+// the SMs can pull from L2 at once -- the ceiling of a stream that re-reads
+// the same per-column vectors row after row.
+__global__ void __launch_bounds__(512) l2_read_kernel(const uint4* window, int64_t nvec,
+                                                      unsigned* sink) {
+    constexpr int U = 8;
+    const int64_t start = ((int64_t)blockIdx.x * 9973) % nvec;
+    uint32_t fold = 0;
+    for (int64_t i0 = threadIdx.x; i0 < nvec; i0 += (int64_t)U * blockDim.x) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            int64_t i = i0 + (int64_t)u * blockDim.x;
+            if (i < nvec) {
+                i += start;
+                if (i >= nvec) i -= nvec;
+                v[u] = ld_global_nc_l1na_v4(window + i);
+            } else {
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) fold += v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+    }
+    // keeps the loads live (nvec is never negative, which the compiler
+    // cannot know)
+    if (nvec < 0) sink[0] = fold;
+}
+
+extern "C" credit_status_t credit_l2_read_rate(int device, int64_t window_bytes, int runs,
+                                               double* gbps) {
+    if (!gbps || window_bytes < 65536 || window_bytes > ((int64_t)64 << 20) || window_bytes % 16 ||
+        runs < 1 || runs > 1000)
+        return CREDIT_ERR_INVALID_ARG;
+    const DevInfo* d = device_info(device);
+    if (!d) return CREDIT_ERR_CUDA;
+    const KernelInfo* ki = kernel_info(device, (const void*)l2_read_kernel, false);
+    if (!ki) return CREDIT_ERR_CUDA;
+    int old = 0;
+    if (cudaGetDevice(&old) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
+    struct Restore { int d; ~Restore() { cudaSetDevice(d); } } restore{old};
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, l2_read_kernel, 512, 0) != cudaSuccess ||
+        occ < 1) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
+    const int64_t ctas = (int64_t)occ * d->sms;
+    unsigned* err = device_error_word();
+    if (!err) return CREDIT_ERR_CUDA;
+    void* w = nullptr;
+    if (cudaMalloc(&w, (size_t)window_bytes) != cudaSuccess ||
+        cudaMemset(w, 0x5a, (size_t)window_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        if (w) cudaFree(w);
+        return CREDIT_ERR_CUDA;
+    }
+    const int64_t nvec = window_bytes / 16;
+    credit_status_t status = CREDIT_OK;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    std::vector<double> t;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) status = CREDIT_ERR_CUDA;
+    for (int r = 0; status == CREDIT_OK && r < runs + 1; ++r) {  // run 0 warms up (fills L2)
+        float ms = 0.f;
+        if (cudaEventRecord(e0, 0) != cudaSuccess) { status = CREDIT_ERR_CUDA; break; }
+        l2_read_kernel<<<(unsigned)ctas, 512>>>(static_cast<const uint4*>(w), nvec, err);
+        if (cudaGetLastError() != cudaSuccess || cudaEventRecord(e1, 0) != cudaSuccess ||
+            cudaEventSynchronize(e1) != cudaSuccess || cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) {
+            cudaGetLastError();
+            status = CREDIT_ERR_CUDA;
+            break;
+        }
+        if (r > 0) t.push_back(1e3 * ms);
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaFree(w);
+    if (status != CREDIT_OK) return status;
+    *gbps = (double)ctas * (double)window_bytes / median(t) / 1e3;  // bytes / us / 1e3 = GB/s
+    return CREDIT_OK;
+}
+
 extern "C" credit_status_t credit_stage_copy_rate(int device, int ctas_per_sm, int runs,
                                                   double* gbps, int* resident) {
     if (!gbps || ctas_per_sm < 1 || ctas_per_sm > 8 || runs < 1 || runs > 1000)

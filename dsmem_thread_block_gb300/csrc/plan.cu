@@ -51,6 +51,22 @@ int64_t bulk_chunk_elems(int64_t slice_elems, int elem_bytes, int rows_per_clust
     return round_up(std::max(target, ceil_div(slice_elems, kMaxChunks / rows_per_cluster)), vec);
 }
 
+int64_t tail_staged_for(int dev, credit_op_t op, int64_t cols, credit_dtype_t dtype, int P,
+                        int cps) {
+    const int es = dtype == CREDIT_F32 ? 4 : 2;
+    if (P < 1 || P > kMaxCluster || cps < 1 || !tail_capable((int)op, es)) return 0;
+    const DevInfo* d = device_info(dev);
+    const void* fn = cluster_kernel(KernelKey{(int)op, (int)dtype, 0, true, 1});
+    const KernelInfo* ki = d ? kernel_info(dev, fn, true) : nullptr;
+    if (!ki) return 0;
+    const int64_t vec = 16 / es;
+    const int64_t slice = round_up(ceil_div(cols, P), vec);
+    const int64_t budget = std::min<int64_t>(
+        (int64_t)d->smem_per_sm / cps - ki->static_smem - d->reserved_smem, ki->max_dyn_smem);
+    const int64_t held = budget / (vec * es) * vec;  // whole 16-byte vectors
+    return held >= vec && held < slice ? held : 0;
+}
+
 int64_t row_pitch(int64_t slice_elems, int elem_bytes) {
     return round_up(slice_elems * elem_bytes, 128);
 }
@@ -138,7 +154,7 @@ credit_status_t persistent_plan(int dev, const DevInfo* d, credit_op_t op, int64
 credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
                           credit_dtype_t dtype, credit_variant_t variant, int P,
                           int threads, int cps, credit_plan_t* out, int64_t chunk,
-                          int rows_per_cluster) {
+                          int rows_per_cluster, int64_t staged_req) {
     if (!out || rows < 1 || cols < 1) return CREDIT_ERR_INVALID_ARG;
     if (!op_ok(op)) return CREDIT_ERR_UNSUPPORTED;
     if (dtype != CREDIT_F32 && dtype != CREDIT_BF16) return CREDIT_ERR_UNSUPPORTED;
@@ -171,8 +187,15 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
         if (two_ops && R != 1) return CREDIT_ERR_INVALID_ARG;
         const int staged = two_ops ? 2 : R;  // slices held per CTA
         const int64_t slice = round_up(ceil_div(cols, P), vec);
+        // an L2 tail: stage only the first `held` elements of the slice (one
+        // row per cluster, operators without an in-place stash pass)
+        int64_t held = slice;
+        if (staged_req > 0 && staged_req < slice) {
+            if (R != 1 || two_ops || !tail_capable((int)op, es)) return CREDIT_ERR_INVALID_ARG;
+            held = round_up(staged_req, vec);
+        }
         const int64_t pitch = row_pitch(slice, es);
-        const int64_t smem = staged == 1 ? round_up(slice * es, 16) : staged * pitch;
+        const int64_t smem = staged == 1 ? round_up(held * es, 16) : staged * pitch;
         const void* fn = cluster_kernel(KernelKey{(int)op, (int)dtype, 0, true, R});
         const KernelInfo* ki = kernel_info(dev, fn, true);
         if (!ki) return CREDIT_ERR_CUDA;
@@ -184,7 +207,8 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
         p.threads = t;
         p.smem_bytes = smem;
         p.slice_elems = slice;
-        p.chunk_elems = (int32_t)bulk_chunk_elems(slice, es, staged);
+        p.staged_elems = held;
+        p.chunk_elems = (int32_t)bulk_chunk_elems(held, es, staged);
         p.rows_per_cluster = R;
         p.active_clusters = active;
         p.ctas_per_sm = std::max(1, (int)((int64_t)active * P / d->sms));
@@ -265,6 +289,7 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
 credit_status_t auto_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
                           credit_dtype_t dtype, credit_plan_t* out) {
     if (!out || rows < 1 || cols < 1) return CREDIT_ERR_INVALID_ARG;
+    if (forced_plan(dev, op, rows, cols, dtype, out)) return CREDIT_OK;  // CREDIT_FORCE
     credit_plan_t profiled;
     if (lookup_profiled_plan(dev, op, rows, cols, dtype, &profiled)) {
         *out = profiled;

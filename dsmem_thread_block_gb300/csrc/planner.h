@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <vector>
 
 #include "credit.h"
 
@@ -39,10 +40,18 @@ int64_t bulk_chunk_elems(int64_t slice_elems, int elem_bytes, int rows_per_clust
 // choose).  cps is the number of persistent CTAs meant to share one SM (1 or
 // 2); chunk the persistent ring's slot size in elements (a power-of-two
 // number of 16-byte vectors).
+// staged: CREDIT_CLUSTER with one row per cluster, the elements of each
+// CTA's slice to stage in shared memory (0 = all); the rest is an L2 tail.
 credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
                           credit_dtype_t dtype, credit_variant_t variant, int P,
                           int threads, int cps, credit_plan_t* out, int64_t chunk = 0,
-                          int rows_per_cluster = 0);
+                          int rows_per_cluster = 0, int64_t staged = 0);
+
+// Staged elements of an L2-tail plan of cluster size P that lets `cps` CTAs
+// share an SM (one-row-per-cluster kernel), or 0 when the operator has no
+// L2-tail form or the whole slice already fits that budget.
+int64_t tail_staged_for(int dev, credit_op_t op, int64_t cols, credit_dtype_t dtype, int P,
+                        int cps);
 
 // Bytes between the staged row slices of a multi-row CTA.
 int64_t row_pitch(int64_t slice_elems, int elem_bytes);
@@ -50,6 +59,28 @@ int64_t row_pitch(int64_t slice_elems, int elem_bytes);
 // The plan the profiled cost model chose for this shape, if it has run.
 bool lookup_profiled_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
                           credit_dtype_t dtype, credit_plan_t* out);
+
+// Calibration-profile state of the cost model (costmodel.cu) and its
+// persistence (profile.cu).
+struct ChosenPlan {
+    int op, dtype;
+    int64_t rows, cols;
+    credit_plan_t plan;
+};
+// DSMEM profile arrays are indexed by cluster size, kMaxCluster + 1 entries.
+bool dsmem_profile_get(int dev, double* barrier_ns, double* exchange_ns, double* async_ns);
+void dsmem_profile_set(int dev, const double* barrier_ns, const double* exchange_ns,
+                       const double* async_ns);
+std::vector<ChosenPlan> chosen_plans(int dev);
+void chosen_plan_put(int dev, const ChosenPlan& c);
+// CREDIT_PROFILE: load the named profile once per device (if it exists and
+// matches this device and library), and save the state back after a
+// calibration or a profiled plan.  No-ops when the variable is unset.
+void profile_env_load(int dev);
+void profile_env_save(int dev);
+// CREDIT_FORCE: the plan it names for this shape, if set and legal.
+bool forced_plan(int dev, credit_op_t op, int64_t rows, int64_t cols, credit_dtype_t dtype,
+                 credit_plan_t* out);
 
 // The automatic plan: the profiled choice when there is one, else a static
 // rule.

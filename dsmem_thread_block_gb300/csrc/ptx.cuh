@@ -128,6 +128,28 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+// L2 policy: data read twice a few microseconds apart (the L2 tail of a
+// staged slice), kept ahead of streamed lines until its second read.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 16- and 8-byte global loads that bypass L1 and carry an L2 cache policy.
+__device__ __forceinline__ uint4 ld_global_l2hint_v4(const void* p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(policy));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_global_l2hint_v2(const void* p, uint64_t policy) {
+    uint2 v;
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(policy));
+    return v;
+}
+
 // Non-multicast bulk copy of `bytes` (multiple of 16, both addresses 16-byte
 // aligned) from global memory into this CTA's shared memory; completion is
 // signalled as transaction bytes on mbarrier `bar`.
@@ -159,6 +181,14 @@ __device__ __forceinline__ void st_global_cs_v4(void* p, uint4 v) {
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+// Read-only 16-byte global load that does not allocate in L1 (every hit is
+// an L2 hit).
+__device__ __forceinline__ uint4 ld_global_nc_l1na_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }

@@ -355,6 +355,34 @@ __device__ __forceinline__ void stats_tiles(Stats<OP, T>& st, const unsigned cha
     }
 }
 
+// Statistics over [0, n) 16-byte vectors in global memory at `g` (the L2
+// tail of a slice: its first read, from HBM, with the L2 policy `pol`).
+// Each warp tile issues all its loads before folding any of them.
+template <int OP, typename T>
+__device__ __forceinline__ void stats_global(Stats<OP, T>& st, const unsigned char* g, int n,
+                                             int warp, int nwarps, int lane, uint64_t pol) {
+    constexpr int U = 4, kTile = 32 * U;
+    int t = warp * kTile;
+    for (; t + kTile <= n; t += nwarps * kTile) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) r[u] = ld_global_l2hint_v4(g + (size_t)(t + lane + 32 * u) * 16, pol);
+#pragma unroll
+        for (int u = 0; u < U; ++u) st.add(r[u]);
+    }
+    if (t < n) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = t + lane + 32 * u;
+            if (i < n) r[u] = ld_global_l2hint_v4(g + (size_t)i * 16, pol);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (t + lane + 32 * u < n) st.add(r[u]);
+    }
+}
+
 // Output granule of an operator: 4 elements for bf16 data with fp32
 // parameters (so one 16-byte gamma load and one 16-byte beta load cover it),
 // else one 16-byte vector of data.
@@ -408,12 +436,16 @@ struct NoRelease {
 // each tile `release(v)` is told the first staged vector the warp may still
 // read (the start of its next tile; nvec at the end), so a caller can hand
 // back the shared memory the warp has finished with.  SMEM: gp / bp point to
-// a copy of the slice's parameters in shared memory.
-template <int OP, typename T, typename PT, typename Release = NoRelease, bool SMEM = false>
+// a copy of the slice's parameters in shared memory.  XG: `base` is global
+// memory (the L2 tail of a slice, read a second time), loaded past L1 with
+// the L2 policy `xpol`; each element is loaded before the same lane stores
+// its output, so y may alias x.
+template <int OP, typename T, typename PT, typename Release = NoRelease, bool SMEM = false,
+          bool XG = false>
 __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const unsigned char* base,
                                              T* yrow, const PT* gp, const PT* bp, int nvec,
                                              int warp, int nwarps, int lane,
-                                             Release release = Release()) {
+                                             Release release = Release(), uint64_t xpol = 0) {
     using G = Granule<OP, T, PT>;
     constexpr int U = (OP != kSoftmax && G::kPairs == 4) ? 2 : 4, NP = G::kPairs, kTile = 32 * U;
     const int ngran = nvec * (16 / G::kBytes);
@@ -429,10 +461,13 @@ __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const un
             const int q = t + lane + 32 * u;
             if (full || q < ngran) {
                 if constexpr (G::kBytes == 8) {
-                    const uint2 w = *reinterpret_cast<const uint2*>(base + (size_t)q * 8);
+                    uint2 w;
+                    if constexpr (XG) w = ld_global_l2hint_v2(base + (size_t)q * 8, xpol);
+                    else w = *reinterpret_cast<const uint2*>(base + (size_t)q * 8);
                     raw[u] = make_uint4(w.x, w.y, 0u, 0u);
                 } else {
-                    raw[u] = lds16(base + (size_t)q * 16);
+                    if constexpr (XG) raw[u] = ld_global_l2hint_v4(base + (size_t)q * 16, xpol);
+                    else raw[u] = lds16(base + (size_t)q * 16);
                 }
                 if constexpr (kParams) {
                     if (has_g) granule_params<PT, NP, SMEM>(gp, q, gv[u]);

@@ -3,7 +3,8 @@
 Measures, on one GPU, the cluster-barrier round trip, the replicated-push
 exchange and the st.async exchange (deposits counted on each receiver's
 mbarrier, no cluster barrier) for every cluster size 2..16, the staged-copy
-rate (HBM -> shared memory -> HBM, bulk copies) at 1..8 CTAs per SM, remote and local shared-memory load
+rate (HBM -> shared memory -> HBM, bulk copies) at 1..8 CTAs per SM, the L2
+read rate of every SM re-reading a 2, 8 and 32 MiB window, remote and local shared-memory load
 latency (pointer chase), and remote / local 16-byte load and store throughput
 of one CTA, each as the median of 15 launches (CREDIT summary page, "C.
 Positioning": latency, throughput and repeated cluster-synchronisation
@@ -37,6 +38,8 @@ def run_suite(device: int = 0, runs: int = 15, sizes=range(2, 17)) -> dict:
     for k in (1, 2, 3, 4, 6, 8):
         g, res = C.credit_stage_copy_rate(device, k, min(runs, 7))
         out["stage_copy"][k] = {"gbps": g, "resident": res}
+    out["l2_read_gbps"] = {str(b): C.credit_l2_read_rate(device, b, min(runs, 7))
+                           for b in (1 << 21, 1 << 23, 1 << 25)}
     return out
 
 

@@ -149,6 +149,17 @@ typedef struct {
     int32_t exchange;
     float pred_us;
     float pred_two_pass_us;
+    int64_t staged_elems;    /* CREDIT_CLUSTER, one row per cluster: elements of
+                                each CTA's slice staged in shared memory; the
+                                rest of the slice (the L2 tail) is read from
+                                HBM once with an L2 evict-last hint, folded
+                                from registers, and read again from L2 by the
+                                output pass.  In a request it asks for an
+                                L2 tail when it lies below the request's own
+                                slice_elems, or when slice_elems is 0 (a
+                                fresh request); 0, or a value equal to
+                                slice_elems (a whole-slice plan as derived),
+                                stages the whole slice. */
 } credit_plan_t;
 
 /*
@@ -396,9 +407,12 @@ credit_status_t credit_run_host(const credit_host_call_t *call,
  * per-SM input stream.  The candidate with the smallest prediction is kept
  * if it beats T_base, else the baseline.  As on the pages, the model screens
  * and a final tuning step may pick another legal size: with tune > 0 the
- * `tune` best-predicted clustered candidates (one-row-per-cluster, and the
- * persistent and pipelined kernels of the same P) are timed and the fastest
- * measured plan, baseline included, is chosen.
+ * `tune` best-predicted clustered candidates (one-row-per-cluster, its L2-tail
+ * plans sized for two and three CTAs per SM where the slice needs one, and
+ * the persistent and pipelined kernels of the same P) are timed and the
+ * fastest measured plan, baseline included, is chosen.  A cluster size whose
+ * whole slice does not fit shared memory is a candidate through its L2-tail
+ * plan.
  */
 typedef struct {
     int32_t cluster_size;    /* P; 1 = the baseline */
@@ -413,6 +427,9 @@ typedef struct {
     double pipelined_us;     /* tuning: measured time of the warp-specialised
                                 persistent kernel of this P (0 = not timed or
                                 not legal) */
+    double tail_us;          /* tuning: measured time of the fastest L2-tail
+                                plan of this P (0 = none timed) */
+    int64_t tail_staged_elems;  /* that plan's staged_elems */
 } credit_candidate_t;
 
 typedef struct {
@@ -440,6 +457,57 @@ typedef struct {
 credit_status_t credit_calibrate(int device, int runs, const char *profile_path);
 
 /*
+ * The persisted calibration profile.  A profile file holds the DSMEM profile
+ * of credit_calibrate and the plans credit_plan_profiled chose per shape, so
+ * a later process plans without recalibrating or re-timing candidates.  It
+ * is keyed on what produced it: the device key below and the library
+ * version; a profile whose key differs from the loading device's is stale.
+ * Nothing on the CREDIT pages corresponds to this; the pages recalibrate per
+ * run.
+ *
+ * Environment (read by the library):
+ *   CREDIT_PROFILE=<path>  the first planning call on a device loads <path>
+ *                          when it exists and is not stale; every calibration
+ *                          and profiled plan then writes the device's state
+ *                          back to <path> (atomically: a temporary file
+ *                          renamed over it)
+ *   CREDIT_FORCE=<plan>    automatic plans become <plan> where it is legal
+ *                          for the shape (else the automatic choice stands):
+ *                          cluster:P, cluster:PxR (R rows per cluster),
+ *                          cluster:P:sN (an L2-tail plan staging N elements),
+ *                          persist:P, pipe:P, warp_rows or twopass
+ */
+typedef struct {
+    char gpu_name[96];
+    int32_t sms;
+    int32_t sm_clock_mhz;    /* peak SM clock */
+    int32_t mem_clock_mhz;   /* peak memory clock */
+    int32_t cc_major;
+    int32_t cc_minor;
+    int32_t reserved;
+} credit_device_key_t;
+
+/* The key of `device` (host query).  CREDIT_ERR_CUDA if it cannot be read. */
+credit_status_t credit_device_key(int device, credit_device_key_t *out);
+
+/* Write the DSMEM profile (if calibrated) and every chosen plan of `device`
+ * to `path`.  CREDIT_ERR_INVALID_ARG if the file cannot be written. */
+credit_status_t credit_save_profile(int device, const char *path);
+
+/* Load `path` into `device`'s in-memory state: its DSMEM profile and its
+ * chosen plans (each re-derived on this device; one it cannot launch is
+ * skipped).  Returns CREDIT_ERR_INVALID_ARG for a missing, unreadable or
+ * malformed file and CREDIT_ERR_NOT_CALIBRATED, loading nothing, for a
+ * stale profile (another GPU, SM count, clock, compute capability or
+ * library version). */
+credit_status_t credit_load_profile(int device, const char *path);
+
+/* Host-only check of a profile file against a device key: CREDIT_OK if it
+ * matches `key` and this library version, CREDIT_ERR_NOT_CALIBRATED if it is
+ * stale, CREDIT_ERR_INVALID_ARG if it is not a readable profile. */
+credit_status_t credit_profile_check(const char *path, const credit_device_key_t *key);
+
+/*
  * The staged-copy primitive: every CTA moves one footprint of bytes from HBM
  * into its shared memory (non-multicast bulk copies, an mbarrier per 16 KiB),
  * folds it once as the chunks land, meets at a block barrier, and reads it
@@ -454,6 +522,20 @@ credit_status_t credit_calibrate(int device, int runs, const char *profile_path)
  */
 credit_status_t credit_stage_copy_rate(int device, int ctas_per_sm, int runs,
                                        double *gbps, int *resident);
+
+/*
+ * The L2 read primitive: every resident CTA (512 threads, as many per SM as
+ * fit) reads a whole window of window_bytes (64 KiB .. 64 MiB, a multiple of
+ * 16) with 16-byte loads that bypass L1, eight in flight per thread.  The
+ * window lies well inside the L2, so every read after the warm-up launch hits,
+ * so *gbps = (CTAs x window bytes) / median time of `runs` launches is the
+ * rate at which the SMs can pull data from L2 -- the ceiling of an operator
+ * whose per-column parameters are re-read from L2 for every row (CREDIT "D.
+ * Traffic Validation" counts only DRAM bytes; this is the on-chip side).
+ * Allocates and frees the window; synchronises the device.
+ */
+credit_status_t credit_l2_read_rate(int device, int64_t window_bytes, int runs,
+                                    double *gbps);
 
 /*
  * Apply the cost model to one shape on `device` (calibrating first if

@@ -49,7 +49,7 @@ def test_binding_covers_the_abi(lib):
 
 def test_plan_struct_layout_matches_header():
     # int32 x4, int64 x3, int32 x6, float x2 -> 72 bytes, no padding surprises
-    assert ctypes.sizeof(C.Plan) == 72
+    assert ctypes.sizeof(C.Plan) == 80
     assert C.Plan.smem_bytes.offset == 16 and C.Plan.pred_us.offset == 64
     assert C.Plan.exchange.offset == 60
 
@@ -87,7 +87,7 @@ def test_status_strings(lib):
     for s in range(8):
         assert C.status_string(s) != "unknown status"
     assert C.status_string(C.ERR_NO_LEGAL_PLAN).startswith("no legal plan")
-    assert C.credit_version() == "0.4.0"
+    assert C.credit_version() == "0.5.0"
 
 
 def test_host_side_argument_checks_need_no_gpu(lib):

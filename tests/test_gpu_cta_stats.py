@@ -7,7 +7,7 @@ the output is only consistent across a row's slices if every CTA ends up
 with the same bits.  The checked build records, for each row and each rank,
 the combined statistics that CTA holds (credit_debug_stats).  For cluster
 sizes 2, 3 (unequal slices), 8 and 16, both exchanges, one and two rows per
-cluster, the persistent ring and the warp-specialised kernel, every
+cluster, L2-tail plans, the persistent ring and the warp-specialised kernel, every
 operator: the P records of a row are bit-identical, no other rank wrote one,
 and the statistics match the oracle's fp64 values of the same row (max and
 absmax exactly).
@@ -41,6 +41,7 @@ WORKLOADS = [
     _w(wl.PEARSON, "f32", 32768, 406, x_mean=0.5, x_std=2.0, eps=1e-5),
 ]
 RING_OPS = (wl.SOFTMAX, wl.LAYERNORM, wl.RMSNORM)
+TAIL_OPS = (wl.SOFTMAX, wl.LAYERNORM, wl.RMSNORM)
 
 
 def _plans(w, P):
@@ -57,6 +58,11 @@ def _plans(w, P):
 
     for xc, name in ((C.EXCHANGE_BARRIER, "barrier"), (C.EXCHANGE_ASYNC, "async")):
         add(f"cluster:{name}", C.CLUSTER, exchange=xc)
+        if out and w.op in TAIL_OPS and (w.op != wl.SOFTMAX or w.dtype == "bf16"):
+            # an L2-tail plan staging half of the slice
+            vec = 4 if w.dtype == "f32" else 8
+            half = max(vec, out[-1][1].slice_elems // 2 // vec * vec)
+            add(f"tail:{name}", C.CLUSTER, exchange=xc, staged_elems=half)
         if w.op != wl.PEARSON:
             add(f"cluster2:{name}", C.CLUSTER, exchange=xc, rows_per_cluster=2)
         if w.op in RING_OPS:

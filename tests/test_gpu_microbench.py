@@ -60,3 +60,15 @@ def test_microbench_argument_checks():
     with pytest.raises(C.CreditError):
         C.credit_bench_dsmem(0, C.BENCH_BARRIER, 17, 10, 3)
     torch.cuda.synchronize()
+
+
+def test_l2_read_rate_exceeds_the_hbm_copy_rate():
+    # a 2 MiB window stays in L2: all SMs read it faster than the staged
+    # copy streams HBM (read + write)
+    small = C.credit_l2_read_rate(0, 1 << 21, 5)
+    hbm, _ = C.credit_stage_copy_rate(0, 2, 3)
+    assert small > 1.5 * hbm > 0
+    with pytest.raises(C.CreditError):
+        C.credit_l2_read_rate(0, 1000, 3)  # below 64 KiB
+    with pytest.raises(C.CreditError):
+        C.credit_l2_read_rate(0, 1 << 30, 3)  # beyond 64 MiB: no longer an L2 window
