@@ -142,6 +142,7 @@ SIGNATURES = {
     "credit_status_string": (ctypes.c_char_p, [_i32]),
     "credit_l2_read_rate": (_i32, [_i32, _i64, _i32, ctypes.POINTER(ctypes.c_double)]),
     "credit_device_key": (_i32, [_i32, ctypes.POINTER(DeviceKey)]),
+    "credit_plan_tail": (_i32, [_i32, _i64, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(Plan)]),
     "credit_save_profile": (_i32, [_i32, ctypes.c_char_p]),
     "credit_load_profile": (_i32, [_i32, ctypes.c_char_p]),
     "credit_profile_check": (_i32, [ctypes.c_char_p, ctypes.POINTER(DeviceKey)]),
@@ -242,6 +243,16 @@ def credit_plan_for(op: int, rows: int, cols: int, dtype: int, device: int,
     p = Plan()
     _check(load().credit_plan_for(op, rows, cols, dtype, device, variant, cluster_size,
                                   ctypes.byref(p)), "credit_plan_for")
+    return p
+
+
+def credit_plan_tail(op: int, rows: int, cols: int, dtype: int, device: int, cluster_size: int,
+                     ctas_per_sm: int) -> Plan:
+    """The L2-tail plan of cluster size P whose staged part lets ctas_per_sm
+    CTAs share an SM (raises ERR_NO_LEGAL_PLAN where there is none)."""
+    p = Plan()
+    _check(load().credit_plan_tail(op, rows, cols, dtype, device, cluster_size, ctas_per_sm,
+                                   ctypes.byref(p)), "credit_plan_tail")
     return p
 
 

@@ -357,8 +357,7 @@ credit_status_t run(const OpCall& c) {
         // slices too large for three CTAs per SM take the instantiation that
         // spends the spare registers on deeper parameter prefetch (where one
         // exists; cluster_kernel falls back to the regular one otherwise)
-        const DevInfo* di = device_info(dev);
-        key.deep = di && plan.smem_bytes > (int64_t)di->smem_per_sm / 3 - 4096;
+        key.deep = deep_footprint(dev, key, plan.smem_bytes);
     }
     if (plan.variant == CREDIT_WARP_ROWS) {
         WarpRowsArgs a{};
@@ -402,7 +401,8 @@ credit_status_t run(const OpCall& c) {
         a.cols = c.cols;
         a.slice = plan.slice_elems;
         a.chunk_elems = plan.chunk_elems;
-        a.pitch = (int32_t)row_pitch(plan.slice_elems, (int)es);
+        a.pitch = (int32_t)row_pitch(plan.staged_elems > 0 ? plan.staged_elems : plan.slice_elems,
+                                     (int)es);
         a.eps = c.eps;
         a.err = err;
         a.aux = c.aux;
@@ -447,6 +447,18 @@ credit_status_t credit_plan_for(credit_op_t op, int64_t rows, int64_t cols, cred
         variant != CREDIT_WARP_ROWS)
         return CREDIT_ERR_INVALID_ARG;
     return make_plan(device, op, rows, cols, dtype, variant, cluster_size, 0, 0, out);
+}
+
+credit_status_t credit_plan_tail(credit_op_t op, int64_t rows, int64_t cols, credit_dtype_t dtype,
+                                 int device, int cluster_size, int ctas_per_sm,
+                                 credit_plan_t* out) {
+    if (!out || rows < 1 || cols < 1 || ctas_per_sm < 1 || ctas_per_sm > 8) return CREDIT_ERR_INVALID_ARG;
+    if (cluster_size < 1 || cluster_size > kMaxCluster) return CREDIT_ERR_NO_LEGAL_PLAN;
+    if (dtype != CREDIT_F32 && dtype != CREDIT_BF16) return CREDIT_ERR_UNSUPPORTED;
+    const int64_t held = tail_staged_for(device, op, cols, dtype, cluster_size, ctas_per_sm);
+    if (held == 0) return CREDIT_ERR_NO_LEGAL_PLAN;
+    return make_plan(device, op, rows, cols, dtype, CREDIT_CLUSTER, cluster_size, 0, 0, out, 0, 1,
+                     held);
 }
 
 credit_status_t credit_plan_with(credit_op_t op, int64_t rows, int64_t cols, credit_dtype_t dtype,

@@ -69,10 +69,10 @@ cluster_reduce_reuse(const ClusterArgs a) {
     const bool async_x = a.exchange == 1 && P > 1;
     const int64_t row0 = (blockIdx.x / P) * (int64_t)R;
     const int rows = (int)min((int64_t)R, a.rows - row0);  // live rows of this cluster
-    // L2 tail: one row per cluster may stage only the first a.staged
-    // elements of its slice; the rest is read from HBM once for the
-    // statistics (kept in L2) and once more, from L2, for the output
-    constexpr bool kTail = BULK && R == 1 && tail_capable(OP, (int)sizeof(T));
+    // L2 tail: a CTA may stage only the first a.staged elements of each of
+    // its rows' slices; the rest is read from HBM once for the statistics
+    // (kept in L2) and once more, from L2, for the output
+    constexpr bool kTail = BULK && tail_capable(OP, (int)sizeof(T));
     const int64_t start = (int64_t)rank * a.slice;
     const int n_full = (int)max((int64_t)0, min(a.cols - start, a.slice));
     const int n_slice = kTail ? (int)min((int64_t)n_full, a.staged) : n_full;
@@ -144,9 +144,14 @@ cluster_reduce_reuse(const ClusterArgs a) {
     const PT* wp = OP == kWStd ? static_cast<const PT*>(a.p0) + start : nullptr;  // weights
     Stats<OP, T> st[R];
     if constexpr (kTail) {
-        if (ntail > 0)
-            stats_global(st[0], reinterpret_cast<const unsigned char*>(xs + n), ntail / VEC, warp,
-                         nwarps, lane, l2_policy_evict_last());
+        if (ntail > 0) {
+            const uint64_t keep = l2_policy_evict_last();
+#pragma unroll
+            for (int i = 0; i < R; ++i)
+                if (i < rows)
+                    stats_global(st[i], reinterpret_cast<const unsigned char*>(xs + i * a.cols + n),
+                                 ntail / VEC, warp, nwarps, lane, keep);
+        }
     }
 #pragma unroll
     for (int i = 0; i < R; ++i) {
@@ -258,11 +263,23 @@ cluster_reduce_reuse(const ClusterArgs a) {
         for (int i = 0; i < R; ++i) yrow[i] = static_cast<T*>(a.y) + (row0 + i) * a.cols + start;
         if constexpr (kTail) {
             // the L2 tail first: its lines leave L2 as early as possible
-            if (ntail > 0)
-                output_tiles<OP, T, PT, NoRelease, false, true>(
-                    h[0], reinterpret_cast<const unsigned char*>(xs + n), yrow[0] + n,
-                    g ? g + start + n : nullptr, b ? b + start + n : nullptr, ntail / VEC, warp,
-                    nwarps, lane, NoRelease(), l2_policy_evict_first());
+            if (ntail > 0) {
+                if constexpr (R == 1) {
+                    output_tiles<OP, T, PT, NoRelease, false, true>(
+                        h[0], reinterpret_cast<const unsigned char*>(xs + n), yrow[0] + n,
+                        g ? g + start + n : nullptr, b ? b + start + n : nullptr, ntail / VEC,
+                        warp, nwarps, lane, NoRelease(), l2_policy_evict_first());
+                } else {
+                    T* ytail[R];
+#pragma unroll
+                    for (int i = 0; i < R; ++i) ytail[i] = yrow[i] + n;
+                    output_tiles_rows<OP, T, PT, R, true>(
+                        h, reinterpret_cast<const unsigned char*>(xs + n),
+                        a.cols * (int64_t)sizeof(T), ytail, rows, g ? g + start + n : nullptr,
+                        b ? b + start + n : nullptr, ntail / VEC, warp, nwarps, lane,
+                        l2_policy_evict_first());
+                }
+            }
         }
         // RMSNorm with bf16 data and bf16 weights gains from the pipelined
         // pass (measured); the other operator / type combinations do not

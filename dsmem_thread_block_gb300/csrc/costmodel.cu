@@ -30,16 +30,21 @@
 namespace credit {
 namespace {
 
+static_assert(kProfileSizes == kMaxCluster + 1, "one profile entry per cluster size");
+
 struct DsmemProfile {
     bool valid = false;
     double barrier_ns[kMaxCluster + 1] = {};
     double exchange_ns[kMaxCluster + 1] = {};
     double async_exchange_ns[kMaxCluster + 1] = {};
+    double local_load_ns = 0.0;  // one shared-memory hop: the local replay's unit
 };
 
 std::mutex g_cm_mu;
 DsmemProfile g_profile[kMaxDevices];
 std::map<std::tuple<int, int, int, int64_t, int64_t>, credit_plan_t> g_chosen;
+// local-work primitive rates per (device, op, dtype, parameter dtype)
+std::map<std::tuple<int, int, int, int>, LocalRates> g_local;
 
 int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -100,31 +105,45 @@ bool lookup_profiled_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
     return true;
 }
 
-bool dsmem_profile_get(int dev, double* barrier_ns, double* exchange_ns, double* async_ns) {
+bool dsmem_profile_get(int dev, DsmemData* out) {
     if (dev < 0 || dev >= kMaxDevices) return false;
     std::lock_guard<std::mutex> lk(g_cm_mu);
     const DsmemProfile& p = g_profile[dev];
     if (!p.valid) return false;
     for (int P = 0; P <= kMaxCluster; ++P) {
-        barrier_ns[P] = p.barrier_ns[P];
-        exchange_ns[P] = p.exchange_ns[P];
-        async_ns[P] = p.async_exchange_ns[P];
+        out->barrier_ns[P] = p.barrier_ns[P];
+        out->exchange_ns[P] = p.exchange_ns[P];
+        out->async_ns[P] = p.async_exchange_ns[P];
     }
+    out->local_load_ns = p.local_load_ns;
     return true;
 }
 
-void dsmem_profile_set(int dev, const double* barrier_ns, const double* exchange_ns,
-                       const double* async_ns) {
+void dsmem_profile_set(int dev, const DsmemData& d) {
     if (dev < 0 || dev >= kMaxDevices) return;
     DsmemProfile p;
     for (int P = 0; P <= kMaxCluster; ++P) {
-        p.barrier_ns[P] = barrier_ns[P];
-        p.exchange_ns[P] = exchange_ns[P];
-        p.async_exchange_ns[P] = async_ns[P];
+        p.barrier_ns[P] = d.barrier_ns[P];
+        p.exchange_ns[P] = d.exchange_ns[P];
+        p.async_exchange_ns[P] = d.async_ns[P];
     }
+    p.local_load_ns = d.local_load_ns;
     p.valid = true;
     std::lock_guard<std::mutex> lk(g_cm_mu);
     g_profile[dev] = p;
+}
+
+std::vector<LocalRates> local_rates(int dev) {
+    std::vector<LocalRates> out;
+    std::lock_guard<std::mutex> lk(g_cm_mu);
+    for (const auto& kv : g_local)
+        if (std::get<0>(kv.first) == dev) out.push_back(kv.second);
+    return out;
+}
+
+void local_rates_put(int dev, const LocalRates& r) {
+    std::lock_guard<std::mutex> lk(g_cm_mu);
+    g_local[std::make_tuple(dev, r.op, r.dtype, r.pdt)] = r;
 }
 
 std::vector<ChosenPlan> chosen_plans(int dev) {
@@ -149,6 +168,9 @@ using namespace credit;
 
 extern "C" credit_status_t credit_calibrate(int device, int runs, const char* profile_path) {
     if (device < 0 || device >= kMaxDevices || runs < 1) return CREDIT_ERR_INVALID_ARG;
+    // CREDIT_PROFILE: read what the file already holds first, so the write
+    // below keeps it (plans and primitive rates) instead of replacing it
+    profile_env_load(device);
     DsmemProfile prof;
     for (int P = 2; P <= kMaxCluster; ++P) {
         credit_bench_result_t b, e, x;
@@ -161,6 +183,13 @@ extern "C" credit_status_t credit_calibrate(int device, int runs, const char* pr
         prof.barrier_ns[P] = b.median_ns;
         prof.exchange_ns[P] = e.median_ns;
         prof.async_exchange_ns[P] = x.median_ns;
+    }
+    {
+        credit_bench_result_t l;
+        const credit_status_t st =
+            credit_bench_dsmem(device, CREDIT_BENCH_LOCAL_LOAD_LATENCY, 2, 2000, runs, &l);
+        if (st != CREDIT_OK) return st;
+        prof.local_load_ns = l.median_ns;
     }
     prof.valid = true;
     {
@@ -227,6 +256,168 @@ credit_status_t time_op(credit_op_t op, const void* x, void* y, int64_t rows, in
     cudaEventDestroy(e1);
     if (st == CREDIT_OK) *us = median_of(t);
     return st;
+}
+
+// Elements of one CTA's staged slice that let `cps` CTAs share an SM (the
+// one-row-per-cluster kernel's budget for one staged operand).
+int64_t staged_budget(int dev, credit_op_t op, credit_dtype_t dtype, int cps) {
+    const int es = dtype == CREDIT_F32 ? 4 : 2;
+    const DevInfo* d = device_info(dev);
+    const void* fn = cluster_kernel(KernelKey{(int)op, (int)dtype, 0, true, 1});
+    const KernelInfo* ki = d ? kernel_info(dev, fn, true) : nullptr;
+    if (!ki) return 0;
+    const int64_t vec = 16 / es;
+    int64_t budget = std::min<int64_t>(tail_budget_bytes(*d, ki->static_smem, cps),
+                                       ki->max_dyn_smem);
+    if (op == CREDIT_PEARSON) budget = budget / 2 - 128;  // x and u, one pitch apart
+    return budget / (vec * es) * vec;
+}
+
+// The local-work primitive (a candidate's per-CTA work replayed without
+// DSMEM; CREDIT "D. Profitability and Candidate Selection": matched
+// primitive measurements): the one-CTA-per-row kernel at cluster size 1 --
+// no exchange -- on a calibration matrix whose rows are one staged budget
+// wide, so that `cps` CTAs share an SM, and `tails` more budgets of L2 tail
+// (0: fully staged; 1: half the row in the tail; 3: three quarters).  GB/s of
+// one read and one write of the matrix.
+credit_status_t local_rate(int dev, credit_op_t op, credit_dtype_t dtype, int pdt, int cps,
+                           int tails, int runs, double* gbps, int P = 1,
+                           double* c_eff = nullptr) {
+    const int es = dtype == CREDIT_F32 ? 4 : 2;
+    const int64_t held = staged_budget(dev, op, dtype, cps);
+    if (held < 16 / es) return CREDIT_ERR_NO_LEGAL_PLAN;
+    const bool tail = tails > 0;
+    const int64_t cols = held * (1 + tails) * P;
+    const DevInfo* d = device_info(dev);
+    if (!d) return CREDIT_ERR_CUDA;
+    const int64_t row_bytes = cols * es;
+    const int64_t rows = std::max<int64_t>((int64_t)8 * cps * d->sms,
+                                           ceil_div64((int64_t)256 << 20, row_bytes));
+    credit_plan_t p;
+    credit_status_t st = make_plan(dev, op, rows, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1,
+                                   tail ? held : 0);
+    if (st != CREDIT_OK) return st;
+    if (p.slice_elems != held * (1 + tails)) return CREDIT_ERR_NO_LEGAL_PLAN;
+    if (c_eff) *c_eff = (double)p.active_clusters * P / (double)d->sms;
+    {
+        // a residency the footprint allows but threads or registers do not:
+        // not a level of this primitive
+        KernelKey key{(int)op, (int)dtype, pdt == CREDIT_BF16 ? 1 : 0, true, 1};
+        key.deep = deep_footprint(dev, key, p.smem_bytes);
+        const void* fn = cluster_kernel(key);
+        int per_sm = 0;
+        // kernel_info raises the instantiation's dynamic-SMEM limit first
+        // (the occupancy calculator counts zero blocks otherwise)
+        if (!fn || !kernel_info(dev, fn, true) ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, p.threads,
+                                                          (size_t)p.smem_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return CREDIT_ERR_CUDA;
+        }
+        if (per_sm < cps) return CREDIT_ERR_NO_LEGAL_PLAN;
+    }
+    const bool pearson = op == CREDIT_PEARSON;
+    const size_t mat = (size_t)rows * (size_t)row_bytes;
+    const size_t pbytes = (size_t)cols * (pdt == CREDIT_F32 ? 4 : 2);
+    Scratch x, y, g, b, aux;
+    if (!x.alloc(mat) || !y.alloc(mat) || !aux.alloc((size_t)rows * 4) ||
+        (pearson && !g.alloc(mat)) || (!pearson && pdt >= 0 && (!g.alloc(pbytes) || !b.alloc(pbytes))))
+        return CREDIT_ERR_CUDA;
+    const credit_dtype_t pd = pdt == CREDIT_BF16 ? CREDIT_BF16 : CREDIT_F32;
+    if (!fill(x.p, rows * cols, dtype, -2.f, 2.f, 11u) ||
+        (pearson && !fill(g.p, rows * cols, dtype, -2.f, 2.f, 12u)) ||
+        (!pearson && pdt >= 0 &&
+         (!fill(g.p, cols, pd, 0.5f, 1.5f, 13u) || !fill(b.p, cols, pd, -0.5f, 0.5f, 14u))) ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return CREDIT_ERR_CUDA;
+    }
+    double us = 0.0;
+    st = time_op(op, x.p, y.p, rows, cols, dtype, g.p, b.p, pdt, &p, nullptr, 0, runs, &us,
+                 static_cast<float*>(aux.p));
+    if (st != CREDIT_OK) return st;
+    const double bytes = (pearson ? 3.0 : (op == CREDIT_QUANTIZE ? 1.0 + 1.0 / es : 2.0)) * (double)mat;
+    *gbps = bytes / us / 1e3;
+    return CREDIT_OK;
+}
+
+double local_gbps(const LocalRates& r, double c_eff, double f);
+
+// The primitive's rates of (op, dtype, pdt) at 1..4 CTAs per SM, measured once
+// per device and kept (and persisted with the profile).
+credit_status_t local_rates_for(int dev, credit_op_t op, credit_dtype_t dtype, int pdt, int runs,
+                                LocalRates* out) {
+    {
+        std::lock_guard<std::mutex> lk(g_cm_mu);
+        auto it = g_local.find(std::make_tuple(dev, (int)op, (int)dtype, pdt));
+        if (it != g_local.end()) {
+            *out = it->second;
+            return CREDIT_OK;
+        }
+    }
+    LocalRates r;
+    std::memset(&r, 0, sizeof(r));
+    r.op = (int)op;
+    r.dtype = (int)dtype;
+    r.pdt = pdt;
+    const bool tails = tail_capable((int)op, dtype == CREDIT_F32 ? 4 : 2);
+    for (int c = 1; c <= kLocalMaxCps; ++c) {
+        credit_status_t st = local_rate(dev, op, dtype, pdt, c, 0, runs, &r.full[c]);
+        if (st == CREDIT_ERR_NO_LEGAL_PLAN) continue;
+        if (st != CREDIT_OK) return st;
+        if (tails) {
+            st = local_rate(dev, op, dtype, pdt, c, 1, runs, &r.tail50[c]);
+            if (st != CREDIT_OK && st != CREDIT_ERR_NO_LEGAL_PLAN) return st;
+            st = local_rate(dev, op, dtype, pdt, c, 3, runs, &r.tail75[c]);
+            if (st != CREDIT_OK && st != CREDIT_ERR_NO_LEGAL_PLAN) return st;
+        }
+    }
+    // the synchronisation factor of each cluster size: the clustered kernel
+    // on rows of P calibration slices (three CTAs per SM) against the local
+    // rate at the effective residency its clusters reach
+    for (int P = 2; P <= kMaxCluster; ++P) {
+        double g = 0.0, ce = 0.0;
+        const credit_status_t st = local_rate(dev, op, dtype, pdt, 3, 0, runs, &g, P, &ce);
+        if (st == CREDIT_ERR_NO_LEGAL_PLAN) continue;
+        if (st != CREDIT_OK) return st;
+        const double ref = local_gbps(r, ce, 0.0);
+        if (ref > 0.0) r.sync[P] = std::min(1.0, g / ref);
+    }
+    local_rates_put(dev, r);
+    *out = r;
+    return CREDIT_OK;
+}
+
+// The primitive's rate at one whole residency c and L2-tail fraction f of
+// the slice: piecewise linear in f through the fully staged rate and the
+// rates with half and three quarters of the row in the tail, continued along
+// the last piece beyond three quarters (floored at a tenth of the staged
+// rate).
+double local_gbps_at(const LocalRates& r, int c, double f) {
+    const double full = r.full[c];
+    if (f <= 0.0 || r.tail50[c] <= 0.0) return full;
+    if (f <= 0.5) return full + (r.tail50[c] - full) * (f / 0.5);
+    const double t75 = r.tail75[c] > 0.0 ? r.tail75[c] : r.tail50[c];
+    return std::max(0.1 * full, r.tail50[c] + (t75 - r.tail50[c]) * ((f - 0.5) / 0.25));
+}
+
+// ... at an effective residency c_eff (resident CTAs per SM, fractional):
+// linear between the measured residencies around it, proportional below one
+// CTA per SM (idle SMs stream nothing), saturated at the highest residency
+// measured.
+double local_gbps(const LocalRates& r, double c_eff, double f) {
+    if (r.full[1] <= 0.0) return 0.0;
+    if (c_eff <= 1.0) return local_gbps_at(r, 1, f) * std::max(0.0, c_eff);
+    int lo = 1;
+    for (int c = 2; c <= kLocalMaxCps; ++c) {
+        if (r.full[c] <= 0.0) continue;
+        if (c >= c_eff) {
+            const double w = (c_eff - lo) / (double)(c - lo);
+            return local_gbps_at(r, lo, f) * (1.0 - w) + local_gbps_at(r, c, f) * w;
+        }
+        lo = c;
+    }
+    return local_gbps_at(r, lo, f);
 }
 
 }  // namespace
@@ -340,7 +531,6 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         }
     }
     const double b_base = staging ? b_credit : b_credit + b_read;
-    const double r_base = b_base / t_base;  // bytes per microsecond
 
     // the baseline's control: its grid, footprint and barriers, no work
     double ctrl_base = 0.0;
@@ -371,41 +561,96 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
     rep.cand[0].plan = base;
     rep.cand[0].pred_us = t_base;
 
+    // The candidates' local work, valued by the local-work primitive at each
+    // candidate's effective residency and L2-tail fraction instead of at the
+    // baseline's achieved rate: a clustered plan moves its bytes at the rate
+    // of the CTAs per SM its clusters keep resident.
+    LocalRates lr;
+    st = local_rates_for(device, op, dtype, param_dtype, runs, &lr);
+    if (st != CREDIT_OK) return st;
+    const int pkey = param_dtype == CREDIT_BF16 ? 1 : 0;
+
     double best = t_base;
     int best_P = 1;
     credit_plan_t chosen = base;
     for (int P = 2; P <= kMaxCluster; ++P) {
         credit_candidate_t& c = rep.cand[P - 1];
         c.cluster_size = P;
+        // the whole slice staged (where it fits) and the L2-tail plans sized
+        // for two and three CTAs per SM
+        std::vector<credit_plan_t> plans;
         credit_plan_t p;
-        if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1) != CREDIT_OK) {
-            // a slice too large for shared memory is a candidate through its
-            // L2-tail plan (two CTAs per SM)
-            const int64_t held = tail_staged_for(device, op, cols, dtype, P, 2);
-            if (held == 0 ||
-                make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1, held) !=
+        if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1) == CREDIT_OK)
+            plans.push_back(p);
+        for (int cps : {2, 3}) {
+            const int64_t held = tail_staged_for(device, op, cols, dtype, P, cps);
+            if (held > 0 &&
+                make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1, held) ==
                     CREDIT_OK)
-                continue;
+                plans.push_back(p);
         }
-        if ((int64_t)(P - 1) * p.slice_elems >= cols) continue;  // an idle CTA
-        double ctrl = 0.0;
-        st = credit_control_time(device, rt, P, p.threads, p.smem_bytes, 1, 2, runs, &ctrl);
-        if (st == CREDIT_ERR_NO_LEGAL_PLAN) continue;
-        if (st != CREDIT_OK) return st;
-        c.legal = 1;
-        c.plan = p;
-        c.t_ctrl_us = ctrl - ctrl_base;
-        // the control kernel already pays the exchange's barrier; the push
-        // costs what the measured exchange adds to it (with st.async
-        // deposits the exchange replaces that barrier on the critical path)
-        const double xchg_ns = p.exchange == CREDIT_EXCHANGE_ASYNC ? prof.async_exchange_ns[P]
-                                                                   : prof.exchange_ns[P];
-        const double push_ns = std::max(0.0, xchg_ns - prof.barrier_ns[P]);
-        c.t_comm_us = (double)p.waves * push_ns * 1e-3;
-        c.pred_us = t_base - (b_base - b_credit) / r_base + c.t_ctrl_us + c.t_comm_us;
-        c.plan.pred_us = (float)c.pred_us;
-        c.plan.pred_two_pass_us = (float)t_base;
-        if (c.pred_us < best) {
+        for (const credit_plan_t& q : plans) {
+            if ((int64_t)(P - 1) * q.slice_elems >= cols) continue;  // an idle CTA
+            // residency: CTAs per SM the footprint allows, free of clusters
+            KernelKey key{(int)op, (int)dtype, pkey, true, 1};
+            key.deep = deep_footprint(device, key, q.smem_bytes);
+            const void* fn = cluster_kernel(key);
+            int per_sm = 0;
+            if (!fn || !kernel_info(device, fn, true) ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, q.threads,
+                                                              (size_t)q.smem_bytes) !=
+                    cudaSuccess ||
+                per_sm < 1) {
+                cudaGetLastError();
+                continue;
+            }
+            // the CTAs per SM the candidate's clusters actually keep
+            // resident: at most what the footprint allows, fewer where
+            // clusters (which live in one GPC) cannot fill every slot
+            const double c_eff = std::min<double>(
+                per_sm, (double)q.active_clusters * P / (double)d->sms);
+            const double f = q.staged_elems < q.slice_elems
+                                 ? (double)(q.slice_elems - q.staged_elems) / (double)q.slice_elems
+                                 : 0.0;
+            // the cluster's synchronisation factor (a cluster waits for its
+            // slowest CTA at the exchange), measured per cluster size
+            const double sync = lr.sync[P] > 0.0 ? lr.sync[P] : 1.0;
+            const double rate = local_gbps(lr, c_eff, f) * sync * 1e3;  // bytes per us
+            if (rate <= 0.0) continue;
+            const double waves = (double)ceil_div64(rt, q.active_clusters);
+            const double quant = waves * q.active_clusters / (double)rt;  // last-wave fill
+            const double t_local = b_credit / rate * quant;
+            // DSMEM control: the cluster launch with its two barriers per row
+            // over the same grid without clusters
+            double ctrl = 0.0, ctrl1 = 0.0;
+            st = credit_control_time(device, rt, P, q.threads, q.smem_bytes, 1, 2, runs, &ctrl);
+            if (st == CREDIT_ERR_NO_LEGAL_PLAN) continue;
+            if (st != CREDIT_OK) return st;
+            st = credit_control_time(device, rt * P, 1, q.threads, q.smem_bytes, 1, 0, runs, &ctrl1);
+            if (st != CREDIT_OK && st != CREDIT_ERR_NO_LEGAL_PLAN) return st;
+            // the control kernel already pays the exchange's barrier; the push
+            // costs what the measured exchange adds to it (with st.async
+            // deposits the exchange replaces that barrier on the critical path)
+            const double xchg_ns = q.exchange == CREDIT_EXCHANGE_ASYNC ? prof.async_exchange_ns[P]
+                                                                       : prof.exchange_ns[P];
+            const double push_ns = std::max(0.0, xchg_ns - prof.barrier_ns[P]);
+            const double t_ctrl = std::max(0.0, ctrl - ctrl1);
+            const double t_comm = waves * push_ns * 1e-3;
+            // local replay: every CTA folds the P partials from its own shared
+            // memory, one slot read per peer
+            const double t_replay = waves * P * prof.local_load_ns * 1e-3;
+            const double pred = t_local + t_ctrl + t_comm + t_replay;
+            if (!c.legal || pred < c.pred_us) {
+                c.legal = 1;
+                c.plan = q;
+                c.t_ctrl_us = t_ctrl;
+                c.t_comm_us = t_comm + t_replay;
+                c.pred_us = pred;
+                c.plan.pred_us = (float)pred;
+                c.plan.pred_two_pass_us = (float)t_base;
+            }
+        }
+        if (c.legal && c.pred_us < best) {
             best = c.pred_us;
             best_P = P;
             chosen = c.plan;
@@ -433,34 +678,61 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         rep.cand[0].measured_us = t_base;
         for (int P : order) {
             credit_candidate_t& c = rep.cand[P - 1];
-            st = time_op(op, x.p, y.p, rt, cols, dtype, g.p, b.p, param_dtype, &c.plan, nullptr,
-                         0, runs, &c.measured_us, auxp);
-            if (st != CREDIT_OK) return st;
-            if (c.measured_us < best_meas) {
-                best_meas = c.measured_us;
-                best_plan = c.plan;
-                best_meas_P = P;
-            }
-            // L2-tail plans sized for two and three CTAs per SM
+            // the model's plan of this P, then its other staging forms: the
+            // whole slice (where it fits) and the L2-tail plans for two and
+            // three CTAs per SM
+            std::vector<credit_plan_t> plans{c.plan};
+            credit_plan_t tp;
+            if (c.plan.staged_elems < c.plan.slice_elems &&
+                make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &tp, 0, 1) == CREDIT_OK)
+                plans.push_back(tp);
             for (int cps : {2, 3}) {
                 const int64_t held = tail_staged_for(device, op, cols, dtype, P, cps);
-                if (held == 0 || held == c.plan.staged_elems) continue;
-                credit_plan_t tp;
-                if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &tp, 0, 1,
-                              held) != CREDIT_OK)
-                    continue;
+                if (held > 0 && held != c.plan.staged_elems &&
+                    make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &tp, 0, 1,
+                              held) == CREDIT_OK)
+                    plans.push_back(tp);
+            }
+            for (size_t i = 0; i < plans.size(); ++i) {
                 double us = 0.0;
-                st = time_op(op, x.p, y.p, rt, cols, dtype, g.p, b.p, param_dtype, &tp, nullptr,
-                             0, runs, &us, auxp);
+                st = time_op(op, x.p, y.p, rt, cols, dtype, g.p, b.p, param_dtype, &plans[i],
+                             nullptr, 0, runs, &us, auxp);
                 if (st != CREDIT_OK) return st;
-                if (c.tail_us == 0.0 || us < c.tail_us) {
+                if (i == 0) c.measured_us = us;
+                if (plans[i].staged_elems < plans[i].slice_elems &&
+                    (c.tail_us == 0.0 || us < c.tail_us)) {
                     c.tail_us = us;
-                    c.tail_staged_elems = held;
+                    c.tail_staged_elems = plans[i].staged_elems;
                 }
                 if (us < best_meas) {
                     best_meas = us;
-                    best_plan = tp;
+                    best_plan = plans[i];
                     best_meas_P = P;
+                }
+            }
+            // operators with per-column parameters: two rows per cluster
+            // share one parameter load; their L2-tail plans keep the CTAs
+            // per SM of a one-row plan
+            if ((op == CREDIT_LAYERNORM || op == CREDIT_RMSNORM) && param_dtype >= 0 && rt >= 2) {
+                for (int cps : {2, 3}) {
+                    const int64_t held = tail_staged_for(device, op, cols, dtype, P, cps, 2);
+                    credit_plan_t rp;
+                    if (held == 0 || make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0,
+                                               0, &rp, 0, 2, held) != CREDIT_OK)
+                        continue;
+                    double us = 0.0;
+                    st = time_op(op, x.p, y.p, rt, cols, dtype, g.p, b.p, param_dtype, &rp,
+                                 nullptr, 0, runs, &us, auxp);
+                    if (st != CREDIT_OK) return st;
+                    if (c.tail_us == 0.0 || us < c.tail_us) {
+                        c.tail_us = us;
+                        c.tail_staged_elems = held;
+                    }
+                    if (us < best_meas) {
+                        best_meas = us;
+                        best_plan = rp;
+                        best_meas_P = P;
+                    }
                 }
             }
             for (credit_variant_t rv : {CREDIT_CLUSTER_PERSISTENT, CREDIT_CLUSTER_PIPELINED}) {

@@ -51,19 +51,38 @@ int64_t bulk_chunk_elems(int64_t slice_elems, int elem_bytes, int rows_per_clust
     return round_up(std::max(target, ceil_div(slice_elems, kMaxChunks / rows_per_cluster)), vec);
 }
 
-int64_t tail_staged_for(int dev, credit_op_t op, int64_t cols, credit_dtype_t dtype, int P,
-                        int cps) {
-    const int es = dtype == CREDIT_F32 ? 4 : 2;
-    if (P < 1 || P > kMaxCluster || cps < 1 || !tail_capable((int)op, es)) return 0;
+bool deep_footprint(int dev, KernelKey k, int64_t smem_bytes) {
     const DevInfo* d = device_info(dev);
-    const void* fn = cluster_kernel(KernelKey{(int)op, (int)dtype, 0, true, 1});
+    k.deep = false;
+    const KernelInfo* ki = d ? kernel_info(dev, cluster_kernel(k), true) : nullptr;
+    if (!ki) return false;
+    return smem_bytes + ki->static_smem + d->reserved_smem > (int64_t)d->smem_per_sm / 3;
+}
+
+int64_t tail_budget_bytes(const DevInfo& d, int static_smem, int cps) {
+    const int64_t per_cta = (int64_t)d.smem_per_sm / cps - d.reserved_smem;
+    const int64_t kb = 1024;
+    return per_cta / kb * kb - (static_smem + kb - 1) / kb * kb - kb;
+}
+
+int64_t tail_staged_for(int dev, credit_op_t op, int64_t cols, credit_dtype_t dtype, int P,
+                        int cps, int rows_per_cluster) {
+    const int es = dtype == CREDIT_F32 ? 4 : 2;
+    const int R = rows_per_cluster;
+    if (P < 1 || P > kMaxCluster || cps < 1 || (R != 1 && R != 2 && R != 4) ||
+        !tail_capable((int)op, es))
+        return 0;
+    const DevInfo* d = device_info(dev);
+    const void* fn = cluster_kernel(KernelKey{(int)op, (int)dtype, 0, true, R});
     const KernelInfo* ki = d ? kernel_info(dev, fn, true) : nullptr;
     if (!ki) return 0;
     const int64_t vec = 16 / es;
     const int64_t slice = round_up(ceil_div(cols, P), vec);
-    const int64_t budget = std::min<int64_t>(
-        (int64_t)d->smem_per_sm / cps - ki->static_smem - d->reserved_smem, ki->max_dyn_smem);
-    const int64_t held = budget / (vec * es) * vec;  // whole 16-byte vectors
+    const int64_t budget = std::min<int64_t>(tail_budget_bytes(*d, ki->static_smem, cps),
+                                             ki->max_dyn_smem);
+    // one row: whole 16-byte vectors; several rows: each staged slice
+    // starts on a 128-byte pitch
+    const int64_t held = R == 1 ? budget / (vec * es) * vec : budget / R / 128 * 128 / es;
     return held >= vec && held < slice ? held : 0;
 }
 
@@ -187,14 +206,14 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
         if (two_ops && R != 1) return CREDIT_ERR_INVALID_ARG;
         const int staged = two_ops ? 2 : R;  // slices held per CTA
         const int64_t slice = round_up(ceil_div(cols, P), vec);
-        // an L2 tail: stage only the first `held` elements of the slice (one
-        // row per cluster, operators without an in-place stash pass)
+        // an L2 tail: stage only the first `held` elements of each row's
+        // slice (operators without an in-place stash pass)
         int64_t held = slice;
         if (staged_req > 0 && staged_req < slice) {
-            if (R != 1 || two_ops || !tail_capable((int)op, es)) return CREDIT_ERR_INVALID_ARG;
+            if (two_ops || !tail_capable((int)op, es)) return CREDIT_ERR_INVALID_ARG;
             held = round_up(staged_req, vec);
         }
-        const int64_t pitch = row_pitch(slice, es);
+        const int64_t pitch = row_pitch(held, es);
         const int64_t smem = staged == 1 ? round_up(held * es, 16) : staged * pitch;
         const void* fn = cluster_kernel(KernelKey{(int)op, (int)dtype, 0, true, R});
         const KernelInfo* ki = kernel_info(dev, fn, true);

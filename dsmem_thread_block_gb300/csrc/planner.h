@@ -5,6 +5,7 @@
 #include <vector>
 
 #include "credit.h"
+#include "internal.h"
 
 namespace credit {
 
@@ -47,11 +48,22 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
                           int threads, int cps, credit_plan_t* out, int64_t chunk = 0,
                           int rows_per_cluster = 0, int64_t staged = 0);
 
-// Staged elements of an L2-tail plan of cluster size P that lets `cps` CTAs
-// share an SM (one-row-per-cluster kernel), or 0 when the operator has no
-// L2-tail form or the whole slice already fits that budget.
+// Dynamic shared memory of one CTA of an L2-tail plan that `cps` CTAs can
+// share an SM with: whole kilobytes, the kernel's static shared memory
+// rounded up to one, and a kilobyte of slack.
+int64_t tail_budget_bytes(const DevInfo& d, int static_smem, int cps);
+
+// Does a one-row-per-cluster launch of `smem_bytes` dynamic shared memory
+// leave room for fewer than three CTAs per SM?  Then it takes the deep
+// instantiation (where the operator has one), whose launch bounds allow two
+// CTAs per SM and twice the registers.
+bool deep_footprint(int dev, KernelKey k, int64_t smem_bytes);
+
+// Staged elements per row of an L2-tail plan of cluster size P with
+// rows_per_cluster rows per cluster that lets `cps` CTAs share an SM, or 0
+// when the operator has no L2-tail form or the whole slice already fits.
 int64_t tail_staged_for(int dev, credit_op_t op, int64_t cols, credit_dtype_t dtype, int P,
-                        int cps);
+                        int cps, int rows_per_cluster = 1);
 
 // Bytes between the staged row slices of a multi-row CTA.
 int64_t row_pitch(int64_t slice_elems, int elem_bytes);
@@ -67,10 +79,37 @@ struct ChosenPlan {
     int64_t rows, cols;
     credit_plan_t plan;
 };
-// DSMEM profile arrays are indexed by cluster size, kMaxCluster + 1 entries.
-bool dsmem_profile_get(int dev, double* barrier_ns, double* exchange_ns, double* async_ns);
-void dsmem_profile_set(int dev, const double* barrier_ns, const double* exchange_ns,
-                       const double* async_ns);
+// The DSMEM profile: per cluster size (index P, 17 entries) the cluster
+// barrier, the replicated push + barrier exchange and the st.async exchange;
+// and the local replay cost, one hop of a shared-memory pointer chase.
+constexpr int kProfileSizes = 17;
+struct DsmemData {
+    double barrier_ns[kProfileSizes];
+    double exchange_ns[kProfileSizes];
+    double async_ns[kProfileSizes];
+    double local_load_ns;
+};
+bool dsmem_profile_get(int dev, DsmemData* out);
+void dsmem_profile_set(int dev, const DsmemData& d);
+// The local-work primitive of one (operator, dtype, parameter dtype): GB/s
+// (one read and one write of the matrix) of the one-CTA-per-row kernel at
+// 1..kLocalMaxCps CTAs per SM ([0] unused), fully staged and with an L2 tail
+// of a half and of three quarters of each row (0 where the operator has no
+// L2-tail form or the residency cannot be reached).
+// sync[P] (P = 2..16) is the clustered kernel's synchronisation factor: its
+// rate at cluster size P on calibration rows that give three CTAs per SM
+// over the local rate at the same effective residency (1 = no cost; 0 =
+// not measured).
+constexpr int kLocalMaxCps = 8;
+struct LocalRates {
+    int op, dtype, pdt;
+    double full[kLocalMaxCps + 1];
+    double tail50[kLocalMaxCps + 1];
+    double tail75[kLocalMaxCps + 1];
+    double sync[kProfileSizes];
+};
+std::vector<LocalRates> local_rates(int dev);
+void local_rates_put(int dev, const LocalRates& r);
 std::vector<ChosenPlan> chosen_plans(int dev);
 void chosen_plan_put(int dev, const ChosenPlan& c);
 // CREDIT_PROFILE: load the named profile once per device (if it exists and

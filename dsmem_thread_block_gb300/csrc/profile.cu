@@ -396,10 +396,10 @@ credit_status_t credit_save_profile(int device, const char* path) {
                  "\"mem_clock_mhz\": %d, \"cc_major\": %d, \"cc_minor\": %d},\n",
                  escaped(key.gpu_name).c_str(), key.sms, key.sm_clock_mhz, key.mem_clock_mhz,
                  key.cc_major, key.cc_minor);
-    double bar[kMaxCluster + 1], xch[kMaxCluster + 1], asx[kMaxCluster + 1];
-    if (dsmem_profile_get(device, bar, xch, asx)) {
+    DsmemData dd;
+    if (dsmem_profile_get(device, &dd)) {
         const char* names[3] = {"barrier_ns", "exchange_ns", "async_exchange_ns"};
-        const double* arrs[3] = {bar, xch, asx};
+        const double* arrs[3] = {dd.barrier_ns, dd.exchange_ns, dd.async_ns};
         std::fprintf(f, " \"dsmem\": {");
         for (int k = 0; k < 3; ++k) {
             std::fprintf(f, "%s\"%s\": [", k ? ", " : "", names[k]);
@@ -407,8 +407,24 @@ credit_status_t credit_save_profile(int device, const char* path) {
                 std::fprintf(f, "%s%.3f", P ? ", " : "", arrs[k][P]);
             std::fprintf(f, "]");
         }
-        std::fprintf(f, "},\n");
+        std::fprintf(f, ", \"local_load_ns\": %.3f},\n", dd.local_load_ns);
     }
+    std::fprintf(f, " \"local_rates\": [");
+    const std::vector<LocalRates> lr = local_rates(device);
+    for (size_t i = 0; i < lr.size(); ++i) {
+        const LocalRates& r = lr[i];
+        std::fprintf(f, "%s\n  {\"op\": %d, \"dtype\": %d, \"pdtype\": %d, \"full\": [",
+                     i ? "," : "", r.op, r.dtype, r.pdt);
+        for (int c = 0; c <= kLocalMaxCps; ++c) std::fprintf(f, "%s%.3f", c ? ", " : "", r.full[c]);
+        std::fprintf(f, "], \"tail50\": [");
+        for (int c = 0; c <= kLocalMaxCps; ++c) std::fprintf(f, "%s%.3f", c ? ", " : "", r.tail50[c]);
+        std::fprintf(f, "], \"tail75\": [");
+        for (int c = 0; c <= kLocalMaxCps; ++c) std::fprintf(f, "%s%.3f", c ? ", " : "", r.tail75[c]);
+        std::fprintf(f, "], \"sync\": [");
+        for (int P = 0; P < kProfileSizes; ++P) std::fprintf(f, "%s%.5f", P ? ", " : "", r.sync[P]);
+        std::fprintf(f, "]}");
+    }
+    std::fprintf(f, "],\n");
     std::fprintf(f, " \"plans\": [");
     const std::vector<ChosenPlan> plans = chosen_plans(device);
     for (size_t i = 0; i < plans.size(); ++i) {
@@ -441,7 +457,8 @@ credit_status_t credit_load_profile(int device, const char* path) {
     if (st != CREDIT_OK) return st;
     if (const Json* d = root.get("dsmem")) {
         const char* names[3] = {"barrier_ns", "exchange_ns", "async_exchange_ns"};
-        double arrs[3][kMaxCluster + 1];
+        DsmemData dd;
+        double* arrs[3] = {dd.barrier_ns, dd.exchange_ns, dd.async_ns};
         bool good = d->kind == Json::kObj;
         for (int k = 0; good && k < 3; ++k) {
             const Json* a = d->get(names[k]);
@@ -451,8 +468,38 @@ credit_status_t credit_load_profile(int device, const char* path) {
                 if (good) arrs[k][P] = a->arr[P].num;
             }
         }
-        if (!good) return CREDIT_ERR_INVALID_ARG;
-        dsmem_profile_set(device, arrs[0], arrs[1], arrs[2]);
+        dd.local_load_ns = num_or(d->get("local_load_ns"), -1.0);
+        if (!good || dd.local_load_ns < 0.0) return CREDIT_ERR_INVALID_ARG;
+        dsmem_profile_set(device, dd);
+    }
+    if (const Json* l = root.get("local_rates")) {
+        if (l->kind != Json::kArr) return CREDIT_ERR_INVALID_ARG;
+        for (const Json& e : l->arr) {
+            LocalRates r;
+            r.op = (int)num_or(e.get("op"), -1);
+            r.dtype = (int)num_or(e.get("dtype"), -1);
+            r.pdt = (int)num_or(e.get("pdtype"), -2);
+            const Json* arrs[3] = {e.get("full"), e.get("tail50"), e.get("tail75")};
+            double* dst[3] = {r.full, r.tail50, r.tail75};
+            bool good = r.op >= 0 && r.op <= CREDIT_PEARSON && (r.dtype == 0 || r.dtype == 1) &&
+                        r.pdt >= -1 && r.pdt <= 1;
+            for (int k = 0; good && k < 3; ++k) {
+                good = arrs[k] && arrs[k]->kind == Json::kArr &&
+                       arrs[k]->arr.size() == (size_t)kLocalMaxCps + 1;
+                for (int c = 0; good && c <= kLocalMaxCps; ++c) {
+                    good = arrs[k]->arr[c].kind == Json::kNum && arrs[k]->arr[c].num >= 0.0;
+                    if (good) dst[k][c] = arrs[k]->arr[c].num;
+                }
+            }
+            const Json* sy = e.get("sync");
+            good = good && sy && sy->kind == Json::kArr && sy->arr.size() == (size_t)kProfileSizes;
+            for (int P = 0; good && P < kProfileSizes; ++P) {
+                good = sy->arr[P].kind == Json::kNum && sy->arr[P].num >= 0.0;
+                if (good) r.sync[P] = sy->arr[P].num;
+            }
+            if (!good) return CREDIT_ERR_INVALID_ARG;
+            local_rates_put(device, r);
+        }
     }
     if (const Json* plans = root.get("plans")) {
         if (plans->kind != Json::kArr) return CREDIT_ERR_INVALID_ARG;

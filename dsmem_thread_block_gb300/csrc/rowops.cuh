@@ -357,11 +357,11 @@ __device__ __forceinline__ void stats_tiles(Stats<OP, T>& st, const unsigned cha
 
 // Statistics over [0, n) 16-byte vectors in global memory at `g` (the L2
 // tail of a slice: its first read, from HBM, with the L2 policy `pol`).
-// Each warp tile issues all its loads before folding any of them.
+// Each warp tile issues all its loads (eight per lane) before folding any.
 template <int OP, typename T>
 __device__ __forceinline__ void stats_global(Stats<OP, T>& st, const unsigned char* g, int n,
                                              int warp, int nwarps, int lane, uint64_t pol) {
-    constexpr int U = 4, kTile = 32 * U;
+    constexpr int U = 8, kTile = 32 * U;
     int t = warp * kTile;
     for (; t + kTile <= n; t += nwarps * kTile) {
         uint4 r[U];
@@ -447,7 +447,10 @@ __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const un
                                              int warp, int nwarps, int lane,
                                              Release release = Release(), uint64_t xpol = 0) {
     using G = Granule<OP, T, PT>;
-    constexpr int U = (OP != kSoftmax && G::kPairs == 4) ? 2 : 4, NP = G::kPairs, kTile = 32 * U;
+    // granules in flight per lane: the L2 tail (XG) is latency-bound on its
+    // loads, so it keeps more of them in flight than the shared-memory pass
+    constexpr int kU = (OP != kSoftmax && G::kPairs == 4) ? 2 : 4;
+    constexpr int U = XG ? (OP == kSoftmax ? 8 : 4) : kU, NP = G::kPairs, kTile = 32 * U;
     const int ngran = nvec * (16 / G::kBytes);
     constexpr bool kParams = OP == kLayerNorm || OP == kRMSNorm;
     const bool has_g = kParams && gp != nullptr;
@@ -720,17 +723,20 @@ __device__ __forceinline__ void output_tiles_pipelined(const OutputMap<OP, T>& h
 
 // Output of R rows that share a column slice: each granule's parameters are
 // loaded once and applied to all live rows (row i staged at base + i * pitch,
-// written to yrow[i]); the first `rows` <= R rows are live.
-template <int OP, typename T, typename PT, int R>
+// written to yrow[i]); the first `rows` <= R rows are live.  XG: the rows are
+// in global memory (the L2 tails of R rows, `pitch` bytes apart), loaded past
+// L1 with the L2 policy `xpol`, each element before its lane stores it.
+template <int OP, typename T, typename PT, int R, bool XG = false>
 __device__ __forceinline__ void output_tiles_rows(const OutputMap<OP, T> (&h)[R],
-                                                  const unsigned char* base, int pitch,
+                                                  const unsigned char* base, int64_t pitch,
                                                   T* const (&yrow)[R], int rows, const PT* gp,
                                                   const PT* bp, int nvec, int warp, int nwarps,
-                                                  int lane) {
+                                                  int lane, uint64_t xpol = 0) {
     using G = Granule<OP, T, PT>;
     // granules in flight per thread: 4, halved when a granule carries 8
-    // parameters, divided among the rows
-    constexpr int kBase = (OP != kSoftmax && G::kPairs == 4) ? 2 : 4;
+    // parameters, divided among the rows (twice as many for an L2 tail,
+    // whose loads are latency-bound)
+    constexpr int kBase = ((OP != kSoftmax && G::kPairs == 4) ? 2 : 4) * (XG ? 2 : 1);
     constexpr int U = kBase / R > 0 ? kBase / R : 1, NP = G::kPairs, kTile = 32 * U;
     const int ngran = nvec * (16 / G::kBytes);
     constexpr bool kParams = OP == kLayerNorm || OP == kRMSNorm;
@@ -749,10 +755,13 @@ __device__ __forceinline__ void output_tiles_rows(const OutputMap<OP, T> (&h)[R]
                     if (i < rows) {
                         const unsigned char* b = base + (size_t)i * pitch;
                         if constexpr (G::kBytes == 8) {
-                            const uint2 w = *reinterpret_cast<const uint2*>(b + (size_t)q * 8);
+                            uint2 w;
+                            if constexpr (XG) w = ld_global_l2hint_v2(b + (size_t)q * 8, xpol);
+                            else w = *reinterpret_cast<const uint2*>(b + (size_t)q * 8);
                             raw[u][i] = make_uint4(w.x, w.y, 0u, 0u);
                         } else {
-                            raw[u][i] = lds16(b + (size_t)q * 16);
+                            if constexpr (XG) raw[u][i] = ld_global_l2hint_v4(b + (size_t)q * 16, xpol);
+                            else raw[u][i] = lds16(b + (size_t)q * 16);
                         }
                     }
                 }

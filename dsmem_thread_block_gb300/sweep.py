@@ -2,9 +2,11 @@
 
 For each width of a sweep (2^28 elements, 1024..1048576 columns; bf16
 softmax by default, or another operator and dtype) the cost model
-(credit_plan_profiled) predicts the time of every legal cluster size and of
-the non-DSMEM baseline and picks one; then every candidate is timed on the
-seeded input (median of `runs` launches, CUDA events).  A point is correct when the pick's measured time is within
+(credit_plan_profiled) predicts the time of every legal cluster size (each
+with its whole slice staged, where it fits, and with L2-tail plans) and of
+the non-DSMEM baseline and picks one; then every candidate -- every staging
+form of every legal cluster size -- is timed on the seeded input (median of
+`runs` launches, CUDA events).  A point is correct when the pick's measured time is within
 max(2 %, the runs' interquartile spread) of the fastest measured candidate
 (CREDIT summary page, "C. Cost-Model Validation": profitability accuracy
 and crossover prediction).  Prints one JSON object per point and a summary.
@@ -81,11 +83,7 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
                                 g.data_ptr() if g is not None else 0, pdt if pdt >= 0 else C.F32,
                                 w.eps, p, ws.data_ptr(), int(p.workspace_bytes), stream)
 
-    measured = {}
-    for cand in rep.cand:
-        if not cand.legal:
-            continue
-        p = cand.plan
+    def timed(p):
         ws = torch.empty(max(1, int(p.workspace_bytes)), dtype=torch.uint8, device=x.device)
 
         def go(p=p, ws=ws):
@@ -93,27 +91,59 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
             if st != C.OK:
                 raise C.CreditError(st, "sweep launch")
 
-        med, iqr = _timed(go, runs)
-        measured[cand.cluster_size] = {"us": med, "iqr_us": iqr, "pred_us": cand.pred_us,
-                                       "t_ctrl_us": cand.t_ctrl_us, "t_comm_us": cand.t_comm_us,
-                                       "active_clusters": p.active_clusters, "waves": p.waves,
-                                       "threads": p.threads, "smem_bytes": p.smem_bytes}
+        return _timed(go, runs)
+
+    # every candidate the model valued: per legal P its chosen staging form
+    # (measured[P]) and the other forms (whole slice, L2-tail plans for two
+    # and three CTAs per SM), all timed; forms[P] keeps the fastest form
+    measured, forms = {}, {}
+    for cand in rep.cand:
+        if not cand.legal:
+            continue
+        P = cand.cluster_size
+        med, iqr = timed(cand.plan)
+        measured[P] = {"us": med, "iqr_us": iqr, "pred_us": cand.pred_us,
+                       "t_ctrl_us": cand.t_ctrl_us, "t_comm_us": cand.t_comm_us,
+                       "variant": C.variant_name(cand.plan),
+                       "active_clusters": cand.plan.active_clusters, "waves": cand.plan.waves,
+                       "threads": cand.plan.threads, "smem_bytes": cand.plan.smem_bytes}
+        forms[P] = {"us": med, "iqr_us": iqr, "variant": C.variant_name(cand.plan)}
+        if P == 1:
+            continue
+        others = []
+        try:
+            others.append(C.credit_plan_for(_OPS[op], w.rows, w.cols, _DT[dtype], device,
+                                            C.CLUSTER, P))
+        except C.CreditError:
+            pass
+        for cps in (2, 3):
+            try:
+                others.append(C.credit_plan_tail(_OPS[op], w.rows, w.cols, _DT[dtype], device, P,
+                                                 cps))
+            except C.CreditError:
+                pass
+        for q in others:
+            if C.variant_name(q) == measured[P]["variant"]:
+                continue
+            med, iqr = timed(q)
+            if med < forms[P]["us"]:
+                forms[P] = {"us": med, "iqr_us": iqr, "variant": C.variant_name(q)}
     # the tuned plan may be a persistent one: time it as chosen
-    ws = torch.empty(max(1, int(plan.workspace_bytes)), dtype=torch.uint8, device=x.device)
-    tuned_us, tuned_iqr = _timed(lambda: launch(plan, ws), runs)
-    best_P = min(measured, key=lambda k: measured[k]["us"])
-    best = min(measured[best_P]["us"], tuned_us)
-    clustered = [v["us"] for k, v in measured.items() if k != 1]
+    tuned_us, tuned_iqr = timed(plan)
+    best_P = min(forms, key=lambda k: forms[k]["us"])
+    best = min(forms[best_P]["us"], tuned_us)
+    clustered = [v["us"] for k, v in forms.items() if k != 1]
     # how far the best clustered candidate is from the baseline (> 0: faster)
     gap = (measured[1]["us"] - min(clustered)) / measured[1]["us"] if clustered else None
     pick = rep.model_cluster_size
-    tol = max(0.02 * best, measured[best_P]["iqr_us"], measured[pick]["iqr_us"])
+    tol = max(0.02 * best, forms[best_P]["iqr_us"], measured[pick]["iqr_us"])
     return {
         "cols": cols, "rows": w.rows,
         "baseline": {C.CLUSTER: "local-staging P=1", C.WARP_ROWS: "warp-rows",
                      C.TWO_PASS: "two-pass"}[rep.baseline_variant],
         "t_base_us": rep.t_base_us, "picked_P": pick, "predicted_profitable": bool(rep.profitable),
-        "measured_best_P": best_P, "measured_profitable": best_P != 1,
+        "measured_best_P": best_P, "measured_best_variant": forms[best_P]["variant"],
+        "measured_profitable": best_P != 1, "picked_variant": measured[pick]["variant"],
         "picked_us": measured[pick]["us"], "best_us": best,
         "tuned_P": rep.chosen_cluster_size, "tuned_variant": int(plan.variant),
         "tuned_us": tuned_us, "tuned_correct": tuned_us <= best + max(tol, tuned_iqr),
@@ -121,6 +151,7 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
         "profitability_correct": bool(rep.profitable) == (best_P != 1),
         "parity_gap": gap,
         "candidates": {str(k): v for k, v in sorted(measured.items())},
+        "fastest_form": {str(k): v for k, v in sorted(forms.items())},
         "gbps_best": w.ideal_bytes() / best / 1e3,
     }
 

@@ -176,6 +176,19 @@ credit_status_t credit_plan(credit_op_t op, int64_t rows, int64_t cols,
                             credit_plan_t *out);
 
 /*
+ * The L2-tail plan of a one-row-per-cluster launch with cluster size
+ * cluster_size whose staged part lets ctas_per_sm (1..8) CTAs share an SM:
+ * staged_elems is the largest whole number of 16-byte vectors of the slice
+ * that fits that share of an SM's shared memory.  CREDIT_ERR_NO_LEGAL_PLAN
+ * if the whole slice already fits that budget, the operator and dtype have
+ * no L2-tail form (fp32 softmax, quantization, weighted standardization,
+ * Pearson), or no such cluster can be resident.  Host only.
+ */
+credit_status_t credit_plan_tail(credit_op_t op, int64_t rows, int64_t cols,
+                                 credit_dtype_t dtype, int device, int cluster_size,
+                                 int ctas_per_sm, credit_plan_t *out);
+
+/*
  * Build a plan for a forced variant: CREDIT_CLUSTER, CREDIT_CLUSTER_PERSISTENT
  * or CREDIT_CLUSTER_PIPELINED with the given cluster_size (1..16), or
  * CREDIT_WARP_ROWS / CREDIT_TWO_PASS (cluster_size ignored).
@@ -394,25 +407,40 @@ credit_status_t credit_run_host(const credit_host_call_t *call,
  * Selection").  For one shape it times the non-DSMEM baseline -- the fastest
  * of the one-CTA-per-row local-staging kernel (when a row fits one CTA's
  * shared memory), the warp-per-row register kernel (rows of at most 4 KiB)
- * and the two-pass global re-read pair -- times the work-free
- * control kernel of every legal clustered candidate and of the baseline, and
- * predicts
- *     T_CREDIT(P) = T_base - (B_base - B_credit) / R_base + T_ctrl(P) + T_comm(P)
- * with R_base = B_base / T_base the baseline's achieved byte rate, T_ctrl(P)
- * the candidate's control time minus the baseline's, and T_comm(P) the
- * measured exchange's cost beyond one cluster barrier (DSMEM profile: the
- * st.async exchange for ASYNC plans, clamped at zero, push + barrier for
- * BARRIER plans) times the candidate's waves of resident clusters.  The deposit residual
- * [T_wSMEM - T_input]+ is zero: a 16-byte push per peer is far below the
- * per-SM input stream.  The candidate with the smallest prediction is kept
- * if it beats T_base, else the baseline.  As on the pages, the model screens
- * and a final tuning step may pick another legal size: with tune > 0 the
- * `tune` best-predicted clustered candidates (one-row-per-cluster, its L2-tail
- * plans sized for two and three CTAs per SM where the slice needs one, and
- * the persistent and pipelined kernels of the same P) are timed and the
- * fastest measured plan, baseline included, is chosen.  A cluster size whose
- * whole slice does not fit shared memory is a candidate through its L2-tail
- * plan.
+ * and the two-pass global re-read pair -- and predicts every legal clustered
+ * candidate (each P with its whole slice staged, where it fits, and with the
+ * L2-tail plans sized for two and three CTAs per SM) from measured
+ * primitives, without timing the candidate:
+ *     T(P) = B_credit / (R_loc(c_eff, f) * S(P)) * q + T_ctrl(P) + T_comm(P)
+ *            + T_replay(P)
+ *   R_loc(c, f)  the local-work primitive: the one-CTA-per-row kernel (no
+ *                DSMEM) timed once per operator and dtype on calibration
+ *                rows that let c = 1..8 CTAs share an SM, fully staged and
+ *                with a half and three quarters of each row an L2 tail;
+ *                piecewise linear in c and in the tail fraction f
+ *   c_eff        the CTAs per SM the candidate keeps resident: resident
+ *                clusters x P / SMs, at most what its footprint allows (a
+ *                cluster lives in one GPC, so clusters may not fill every slot)
+ *   S(P)         the synchronisation factor of cluster size P: the clustered
+ *                kernel timed once per operator on calibration rows of P
+ *                slices (three CTAs per SM), over R_loc at the residency it
+ *                reached -- what waiting for a cluster's slowest CTA costs
+ *   q            the last wave's fill: ceil(rows / clusters) clusters / rows
+ *   T_ctrl(P)    the work-free control kernel with the candidate's grid,
+ *                cluster size, footprint and two barriers per row, minus the
+ *                same grid without clusters
+ *   T_comm(P)    waves x the measured exchange's cost beyond one cluster
+ *                barrier (DSMEM profile: the st.async exchange for ASYNC plans,
+ *                push + barrier for BARRIER plans, clamped at zero)
+ *   T_replay(P)  waves x P shared-memory reads: every CTA folds the P partials
+ *                locally (DSMEM profile: one local load hop)
+ * The deposit residual [T_wSMEM - T_input]+ is zero: a 16-byte push per peer
+ * is far below the per-SM input stream.  The candidate with the smallest
+ * prediction is kept if it beats T_base, else the baseline.  As on the
+ * pages, the model screens and a final tuning step may pick another legal
+ * size: with tune > 0 the `tune` best-predicted cluster sizes are timed (all
+ * their staging forms, and the persistent and pipelined kernels of the same
+ * P) and the fastest measured plan, baseline included, is chosen.
  */
 typedef struct {
     int32_t cluster_size;    /* P; 1 = the baseline */

@@ -63,6 +63,7 @@ def _plans(w, P):
             vec = 4 if w.dtype == "f32" else 8
             half = max(vec, out[-1][1].slice_elems // 2 // vec * vec)
             add(f"tail:{name}", C.CLUSTER, exchange=xc, staged_elems=half)
+            add(f"tail2:{name}", C.CLUSTER, exchange=xc, staged_elems=half, rows_per_cluster=2)
         if w.op != wl.PEARSON:
             add(f"cluster2:{name}", C.CLUSTER, exchange=xc, rows_per_cluster=2)
         if w.op in RING_OPS:

@@ -9,8 +9,8 @@ cluster sizes and staged lengths (including cluster sizes whose whole slice
 does not fit shared memory), unequal last slices, CTAs whose slice ends
 before the tail starts, a staged part of a single vector, in-place calls,
 absent parameters, fp32 data, the checked build, seeded random shapes, and
-the argument rules (operators without an L2-tail form, several rows per
-cluster, misaligned pointers falling back to whole-slice staging)."""
+two and four rows per cluster, and the argument rules (operators without an
+L2-tail form, misaligned pointers falling back to whole-slice staging)."""
 import numpy as np
 import pytest
 import torch
@@ -89,8 +89,9 @@ def test_tail_plan_argument_rules():
         _plan(q, 4, 8192)
     assert e.value.status == C.ERR_INVALID_ARG
     ln = _custom(wl.LAYERNORM, "bf16", 4, 65536, 72, eps=1e-5, param_dtype="f32")
-    with pytest.raises(C.CreditError) as e:  # tails are for one row per cluster
-        _plan(ln, 4, 8192, rows_per_cluster=2)
+    pe = _custom(wl.PEARSON, "f32", 2, 65536, 74)
+    with pytest.raises(C.CreditError) as e:  # two staged operands: no tail form
+        _plan(pe, 4, 8192)
     assert e.value.status == C.ERR_INVALID_ARG
     with pytest.raises(C.CreditError) as e:
         C.credit_plan_with(OPS[ln.op], ln.rows, ln.cols, DT[ln.dtype], dev, C.CLUSTER, 4,
@@ -99,6 +100,28 @@ def test_tail_plan_argument_rules():
     # a staged length at or beyond the slice is a whole-slice plan
     p = _plan(ln, 4, 1 << 20)
     assert p.staged_elems == p.slice_elems
+
+
+MULTI = [
+    (wl.LAYERNORM_BF16_1024x262144.with_rows(5), [(8, 2, 18432), (8, 4, 8192), (16, 2, 12288)]),
+    (wl.RMSNORM_BF16_2048x786432.with_rows(3), [(12, 2, 18432), (16, 2, 16384)]),
+    (wl.sweep_point(1 << 19).with_rows(7), [(8, 2, 18432), (12, 4, 8192)]),
+    (_custom(wl.LAYERNORM, "f32", 5, 100004, 75, x_mean=-0.5, x_std=1.5, eps=1e-5,
+             param_dtype="bf16"), [(7, 2, 6000), (3, 4, 4000)]),
+]
+
+
+@pytest.mark.parametrize("w,cases", MULTI, ids=[c[0].name for c in MULTI])
+def test_tails_with_several_rows_per_cluster(w, cases):
+    # R rows per cluster share one parameter load; each row's slice has its
+    # staged part at its own pitch and its own L2 tail (row counts that are
+    # not a multiple of R leave the last cluster short)
+    inp = w.generate()
+    for P, R, staged in cases:
+        p = _plan(w, P, staged, rows_per_cluster=R)
+        assert p.rows_per_cluster == R and p.staged_elems == staged < p.slice_elems
+        check(w, run(w, inp, p), inp)
+        check(w, run(w, inp, p, in_place=True), inp)
 
 
 def test_misaligned_pointers_fall_back_to_whole_slice_staging():
