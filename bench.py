@@ -326,7 +326,7 @@ def main():
     ap.add_argument("--exchange", default="plan", choices=["plan", "barrier", "async"],
                     help="partial exchange of a one-pass clustered plan (plan = as planned)")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--e2e-chunks", type=int, default=8,
+    ap.add_argument("--e2e-chunks", type=int, default=16,
                     help="row chunks of the host-buffer pipeline")
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the cpu_baseline sample")
