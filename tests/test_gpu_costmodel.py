@@ -1,12 +1,13 @@
 """The profiling-fed cost model: its report is consistent, its choice is a
-legal plan that the automatic planner then reuses, and on a few widths of
-the bf16 softmax sweep (scaled down) the pick is close to the fastest
-measured candidate."""
+legal plan that the automatic planner then reuses, and on the full bf16
+softmax profitability sweep its untimed prediction gets profitability and
+the crossover right and its pick stays close to the fastest candidate."""
 import pytest
 import torch
 
 from dsmem_thread_block_gb300 import _credit as C
 from dsmem_thread_block_gb300 import sweep
+from dsmem_thread_block_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
@@ -45,13 +46,32 @@ def test_tuning_times_the_top_candidates():
     assert abs(plan.pred_us - best) <= 1e-3 * best + 1e-3  # the plan carries its measured time
 
 
-def test_small_sweep_picks_near_best():
-    pts = [sweep.run_point(c, runs=7, total_elements=1 << 24) for c in (4096, 65536, 262144)]
-    for p in pts:
-        # scaled-down shapes run for tens of microseconds: allow timing noise
-        assert p["tuned_us"] <= 1.30 * p["best_us"], p
+def test_softmax_sweep_profitability_and_crossover_at_full_size():
+    # the bf16 softmax profitability sweep as specified: 2^28 elements, 1024 to
+    # 1048576 columns.  The model alone -- primitives measured on calibration
+    # shapes, one timing of the non-DSMEM baseline, no timing of any clustered
+    # candidate -- decides clustered or not; then every staging form of every
+    # legal cluster size is timed ("C. Cost-Model Validation": profitability
+    # accuracy and crossover prediction)
+    C.credit_calibrate(0, 7)
+    pts = [sweep.run_point(c, runs=7) for c in wl.SWEEP_COLS]
     s = sweep.summarize(pts)
-    assert 0.0 <= s["pick_accuracy"] <= 1.0
+    report = [(p["cols"], p["picked_variant"], round(p["picked_us"], 1), p["measured_best_variant"],
+               round(p["best_us"], 1), p["predicted_profitable"], p["measured_profitable"])
+              for p in pts]
+    print(s, report)
+    # profitability right at >= 90 % of the widths; a miss where the best
+    # clustered candidate and the baseline are within 2 % of each other is a
+    # tie that timing noise decides, as the pages count it
+    hard = [p for p in pts if not p["profitability_correct"] and
+            (p["parity_gap"] is None or abs(p["parity_gap"]) > 0.02)]
+    assert len(pts) - len(hard) >= 0.9 * len(pts), (s, report)
+    # the predicted crossover (smallest profitable width) lands within one x2
+    # interval of the measured one
+    assert s["crossover_interval_error"] is not None and s["crossover_interval_error"] <= 1, (s, report)
+    # the model's own pick, untimed, is never far from the fastest candidate
+    for p in pts:
+        assert p["picked_us"] <= 1.15 * p["best_us"], (p["cols"], report)
     torch.cuda.synchronize()
 
 

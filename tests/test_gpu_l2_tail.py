@@ -195,3 +195,28 @@ def test_random_tail_plans(w, P, staged):
     else:
         raise AssertionError(f"{w.name}: no legal plan from P = {P}")
     check(w, run(w, inp, p), inp)
+
+
+
+LARGE = [
+    # footprints that leave room for at most two CTAs per SM: whole slices and
+    # L2 tails of LayerNorm (bf16 data, fp32 parameters) with one and two rows
+    # per cluster, and RMSNorm's bf16 instantiation bounded to two CTAs per SM
+    (wl.LAYERNORM_BF16_1024x262144.with_rows(5), [(12, 2, 0), (10, 2, 0), (8, 2, 24576),
+                                                   (4, 1, 45056)]),
+    (_custom(wl.LAYERNORM, "bf16", 5, 200008, 76, x_mean=-2.0, x_std=0.7, eps=1e-5,
+             param_dtype="f32"), [(9, 2, 0), (5, 2, 20000), (3, 1, 40000)]),
+    (wl.RMSNORM_BF16_2048x786432.with_rows(3), [(16, 1, 0), (8, 1, 45056)]),
+]
+
+
+@pytest.mark.parametrize("w,cases", LARGE, ids=[c[0].name for c in LARGE])
+def test_footprints_of_two_ctas_per_sm(w, cases):
+    inp = w.generate()
+    smem_per_sm = torch.cuda.get_device_properties(0).shared_memory_per_multiprocessor
+    for P, R, staged in cases:
+        p = _plan(w, P, staged, rows_per_cluster=R)
+        assert p.rows_per_cluster == R
+        assert p.smem_bytes > smem_per_sm // 3, (P, R, staged, p.smem_bytes)
+        check(w, run(w, inp, p), inp)
+        check(w, run(w, inp, p, in_place=True), inp)
