@@ -261,7 +261,29 @@ cluster_reduce_reuse(const ClusterArgs a) {
         T* yrow[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) yrow[i] = static_cast<T*>(a.y) + (row0 + i) * a.cols + start;
-        if constexpr (kTail) {
+        // RMSNorm with bf16 data and bf16 weights gains from the pipelined
+        // pass (measured); the other operator / type combinations do not
+        constexpr bool kPipe = BULK && R == 1 && OP == kRMSNorm && Granule<OP, T, PT>::kPairs == 4;
+        // the tail of a slice with 16-byte granules is written from each
+        // warp's ring of freed staged tiles; RMSNorm's pipelined pass, which
+        // keeps its weight loads ahead of its tiles, measured faster with
+        // the tail loaded through registers
+        constexpr bool kRing = kTail && R == 1 && Granule<OP, T, PT>::kBytes == 16 && !kPipe;
+        bool done = false;
+        if constexpr (kRing) {
+            if (ntail > 0) {
+                // staged tiles first, then the tail from each warp's ring
+                // (8 KB of each warp in flight)
+                constexpr int kRingD = (OP != kSoftmax && Granule<OP, T, PT>::kPairs == 4) ? 8 : 4;
+                output_ring<OP, T, PT, kRingD>(
+                    h[0], stage, reinterpret_cast<const unsigned char*>(xs + n), yrow[0],
+                    g ? g + start : nullptr, b ? b + start : nullptr, nvec, ntail / VEC, warp,
+                    nwarps, lane, l2_policy_evict_first());
+                done = true;
+            }
+        }
+        if (done) {
+        } else if constexpr (kTail) {
             // the L2 tail first: its lines leave L2 as early as possible
             if (ntail > 0) {
                 if constexpr (R == 1) {
@@ -281,10 +303,8 @@ cluster_reduce_reuse(const ClusterArgs a) {
                 }
             }
         }
-        // RMSNorm with bf16 data and bf16 weights gains from the pipelined
-        // pass (measured); the other operator / type combinations do not
-        constexpr bool kPipe = BULK && R == 1 && OP == kRMSNorm && Granule<OP, T, PT>::kPairs == 4;
-        if constexpr (kPipe) {
+        if (done) {
+        } else if constexpr (kPipe) {
             if (g) {
                 output_tiles_pipelined<OP, T, PT, kPipeU>(h[0], stage, yrow[0], g + start, nullptr,
                                                           nvec, warp, nwarps, lane);

@@ -273,6 +273,25 @@ int64_t staged_budget(int dev, credit_op_t op, credit_dtype_t dtype, int cps) {
     return budget / (vec * es) * vec;
 }
 
+// The L2-tail staging forms of cluster size P: the staged lengths that let
+// two and three CTAs share an SM, and half the three-CTA length -- a longer
+// tail that each warp writes from a ring of its freed staged tiles, whose
+// loads overlap the staging from the start (measured faster for the widest
+// bf16 softmax rows).  Empty where the operator has no L2-tail form.
+std::vector<int64_t> tail_forms(int dev, credit_op_t op, int64_t cols, credit_dtype_t dtype,
+                                int P) {
+    std::vector<int64_t> out;
+    for (int cps : {2, 3}) {
+        const int64_t h = tail_staged_for(dev, op, cols, dtype, P, cps);
+        if (h > 0) out.push_back(h);
+    }
+    const int64_t vec = dtype == CREDIT_F32 ? 4 : 8;
+    const int64_t h3 = tail_staged_for(dev, op, cols, dtype, P, 3);
+    const int64_t half = h3 / 2 / vec * vec;
+    if (h3 > 0 && half >= vec) out.push_back(half);
+    return out;
+}
+
 // The local-work primitive (a candidate's per-CTA work replayed without
 // DSMEM; CREDIT "D. Profitability and Candidate Selection": matched
 // primitive measurements): the one-CTA-per-row kernel at cluster size 1 --
@@ -576,17 +595,15 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
     for (int P = 2; P <= kMaxCluster; ++P) {
         credit_candidate_t& c = rep.cand[P - 1];
         c.cluster_size = P;
-        // the whole slice staged (where it fits) and the L2-tail plans sized
-        // for two and three CTAs per SM
+        // the whole slice staged (where it fits) and the L2-tail plans
+        // (tail_forms)
         std::vector<credit_plan_t> plans;
         credit_plan_t p;
         if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1) == CREDIT_OK)
             plans.push_back(p);
-        for (int cps : {2, 3}) {
-            const int64_t held = tail_staged_for(device, op, cols, dtype, P, cps);
-            if (held > 0 &&
-                make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1, held) ==
-                    CREDIT_OK)
+        for (int64_t held : tail_forms(device, op, cols, dtype, P)) {
+            if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1, held) ==
+                CREDIT_OK)
                 plans.push_back(p);
         }
         for (const credit_plan_t& q : plans) {
@@ -679,16 +696,14 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         for (int P : order) {
             credit_candidate_t& c = rep.cand[P - 1];
             // the model's plan of this P, then its other staging forms: the
-            // whole slice (where it fits) and the L2-tail plans for two and
-            // three CTAs per SM
+            // whole slice (where it fits) and the L2-tail plans (tail_forms)
             std::vector<credit_plan_t> plans{c.plan};
             credit_plan_t tp;
             if (c.plan.staged_elems < c.plan.slice_elems &&
                 make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &tp, 0, 1) == CREDIT_OK)
                 plans.push_back(tp);
-            for (int cps : {2, 3}) {
-                const int64_t held = tail_staged_for(device, op, cols, dtype, P, cps);
-                if (held > 0 && held != c.plan.staged_elems &&
+            for (int64_t held : tail_forms(device, op, cols, dtype, P)) {
+                if (held != c.plan.staged_elems &&
                     make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &tp, 0, 1,
                               held) == CREDIT_OK)
                     plans.push_back(tp);

@@ -162,6 +162,22 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src,
         :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
 }
 
+// Per-thread asynchronous 16-byte copy global -> this CTA's shared memory
+// (both addresses 16-byte aligned), bypassing L1, with an L2 cache policy.
+// Completion is per thread: a thread's copies land in the order of its
+// commit groups, and cp_async_wait<N> returns once at most N of its groups
+// are still in flight.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+                 :: "r"(dst), "l"(src), "l"(policy) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+
 // ------------------------------------------------------------- vector access
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;

@@ -515,6 +515,115 @@ __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const un
     release(nvec);
 }
 
+// Output of one row slice with an L2 tail, the tail written from shared
+// memory: `stage` holds the first `nvec` vectors of the slice, `xtail` (global
+// memory) the `ntv` vectors that follow them, which the statistics pass read
+// from HBM with an evict-last policy.  Each warp writes its staged tiles
+// first.  A warp's first D full staged tiles, once written, are read by no
+// one else, so they become the warp's private ring: after writing staged
+// tile k < D, each lane copies its own vectors of the warp's tail tile k into
+// its own vectors of that tile (cp.async from L2, evict-first, no registers
+// held while they fly), and after writing tail tile j from its slot it
+// refills the slot with tail tile j + D.  Every copy is read back by the lane
+// that issued it, after its own wait, so no barrier is needed; D tiles of
+// every warp are in flight.  A warp with fewer than D full staged tiles
+// takes a ring of D / 2 (down to two), and with fewer than two reads its
+// tail tiles from global memory instead.  gp / bp point to the slice's
+// first parameter; y may alias x (each tail element is copied before the
+// same lane stores its output, and staged columns never overlap the tail).
+template <int OP, typename T, typename PT, int D>
+__device__ __forceinline__ void output_ring(const OutputMap<OP, T>& h, const unsigned char* stage,
+                                            const unsigned char* xtail, T* yrow, const PT* gp,
+                                            const PT* bp, int nvec, int ntv, int warp,
+                                            int nwarps, int lane, uint64_t tail_pol) {
+    using G = Granule<OP, T, PT>;
+    static_assert(G::kBytes == 16, "the ring copies 16-byte granules");
+    constexpr int U = (OP != kSoftmax && G::kPairs == 4) ? 2 : 4, NP = G::kPairs, kTile = 32 * U;
+    constexpr bool kParams = OP == kLayerNorm || OP == kRMSNorm;
+    const bool has_g = kParams && gp != nullptr;
+    const bool has_b = kParams && bp != nullptr;
+    const int stride = nwarps * kTile, t0 = warp * kTile;
+    const bool ring = t0 + (D - 1) * stride + kTile <= nvec;
+    if constexpr (D > 2) {
+        // too few full staged tiles for this depth: a shallower ring
+        if (!ring) {
+            output_ring<OP, T, PT, D / 2>(h, stage, xtail, yrow, gp, bp, nvec, ntv, warp, nwarps,
+                                          lane, tail_pol);
+            return;
+        }
+    }
+    const uint32_t s0 = smem_u32(stage);
+    // src_t: the tile's first granule in shared memory (xg: read from the
+    // tail in global memory instead); dst_t: the granule index of its output
+    // and parameters within the slice; lim: the granule count at dst
+    auto tile = [&](int src_t, int dst_t, int lim, bool xg) {
+        const bool full = dst_t + kTile <= lim;
+        uint4 raw[U];
+        F2 gv[U][NP], bv[U][NP];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = dst_t + lane + 32 * u;
+            if (full || q < lim) {
+                if (xg) raw[u] = ld_global_l2hint_v4(xtail + (size_t)(q - nvec) * 16, tail_pol);
+                else raw[u] = lds16(stage + (size_t)(src_t + lane + 32 * u) * 16);
+                if constexpr (kParams) {
+                    if (has_g) granule_params<PT, NP>(gp, q, gv[u]);
+                    else for (int i = 0; i < NP; ++i) gv[u][i] = f2(1.f);
+                    if (has_b) granule_params<PT, NP>(bp, q, bv[u]);
+                    else for (int i = 0; i < NP; ++i) bv[u][i] = f2(0.f);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = dst_t + lane + 32 * u;
+            if (full || q < lim) {
+                F2 p[NP];
+                Pairs<T>::unpack(raw[u], p);
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    if constexpr (kParams) p[i] = h(p[i], gv[u][i], bv[u][i]);
+                    else p[i] = h(p[i], p[i], p[i]);
+                }
+                stg16_stream(reinterpret_cast<uint4*>(yrow) + q, Pairs<T>::pack(p));
+            }
+        }
+    };
+    // tail tile k of this warp into ring slot k % D (one commit group, empty
+    // past the tail, so that the groups stay counted)
+    auto prefetch = [&](int k) {
+        const int tt = t0 + k * stride, ts = t0 + (k % D) * stride;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = tt + lane + 32 * u;
+            if (q < ntv)
+                cp_async16(s0 + (uint32_t)(ts + lane + 32 * u) * 16u, xtail + (size_t)q * 16,
+                           tail_pol);
+        }
+        cp_async_commit();
+    };
+    int t = t0, k = 0;
+    for (; t + kTile <= nvec; t += stride, ++k) {
+        tile(t, t, nvec, false);
+        if (ring && k < D) prefetch(k);
+    }
+    if (t < nvec) tile(t, t, nvec, false);
+    const int lim = nvec + ntv;
+    if (ring) {
+        // D groups were committed above and one more per tail tile, so tail
+        // tile j's group is complete once at most D - 1 are pending
+        for (int j = 0; t0 + j * stride < ntv; ++j) {
+            cp_async_wait<D - 1>();
+            const int tt = t0 + j * stride;
+            tile(t0 + (j % D) * stride, nvec + tt, lim, false);
+            prefetch(j + D);
+        }
+        cp_async_wait<0>();
+    } else {
+        for (int tt = t0; tt < ntv; tt += stride) tile(0, nvec + tt, lim, true);
+    }
+}
+
 }  // namespace credit
 
 namespace credit {

@@ -5,8 +5,9 @@ softmax by default, or another operator and dtype) the cost model
 (credit_plan_profiled) predicts the time of every legal cluster size (each
 with its whole slice staged, where it fits, and with L2-tail plans) and of
 the non-DSMEM baseline and picks one; then every candidate -- every staging
-form of every legal cluster size -- is timed on the seeded input (median of
-`runs` launches, CUDA events).  A point is correct when the pick's measured time is within
+form of every legal cluster size (the whole slice, the L2-tail plans for two
+and three CTAs per SM and half the three-CTA staged length) -- is timed on
+the seeded input (median of `runs` launches, CUDA events).  A point is correct when the pick's measured time is within
 max(2 %, the runs' interquartile spread) of the fastest measured candidate
 (CREDIT summary page, "C. Cost-Model Validation": profitability accuracy
 and crossover prediction).  Prints one JSON object per point and a summary.
@@ -95,7 +96,8 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
 
     # every candidate the model valued: per legal P its chosen staging form
     # (measured[P]) and the other forms (whole slice, L2-tail plans for two
-    # and three CTAs per SM), all timed; forms[P] keeps the fastest form
+    # and three CTAs per SM, half the three-CTA staged length), all timed;
+    # forms[P] keeps the fastest form
     measured, forms = {}, {}
     for cand in rep.cand:
         if not cand.legal:
@@ -116,12 +118,25 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
                                             C.CLUSTER, P))
         except C.CreditError:
             pass
+        t3 = None
         for cps in (2, 3):
             try:
-                others.append(C.credit_plan_tail(_OPS[op], w.rows, w.cols, _DT[dtype], device, P,
-                                                 cps))
+                q = C.credit_plan_tail(_OPS[op], w.rows, w.cols, _DT[dtype], device, P, cps)
+                others.append(q)
+                t3 = q if cps == 3 else t3
             except C.CreditError:
                 pass
+        if t3 is not None and t3.staged_elems < t3.slice_elems:
+            # the longer tail the cost model also considers: half the
+            # three-CTA staged length
+            vec = 4 if dtype == "f32" else 8
+            half = int(t3.staged_elems) // 2 // vec * vec
+            if half >= vec:
+                try:
+                    others.append(C.credit_plan_with(_OPS[op], w.rows, w.cols, _DT[dtype], device,
+                                                     C.CLUSTER, P, staged_elems=half))
+                except C.CreditError:
+                    pass
         for q in others:
             if C.variant_name(q) == measured[P]["variant"]:
                 continue

@@ -3,7 +3,9 @@
 An L2-tail plan stages only the first `staged_elems` elements of each CTA's
 slice in shared memory; the rest of the slice is read from HBM once (kept
 in L2 with an evict-last hint) for the statistics and read again, from L2,
-by the output pass.  The results must match the oracle exactly as a fully
+by the output pass -- through registers, or copied by each warp into a ring
+of its freed staged tiles (16-byte granules), including warps with too few
+staged tiles for a ring and tails several rings long.  The results must match the oracle exactly as a fully
 staged plan's do: the workload shapes at reduced row counts for several
 cluster sizes and staged lengths (including cluster sizes whose whole slice
 does not fit shared memory), unequal last slices, CTAs whose slice ends
@@ -33,8 +35,12 @@ WIDE = [
     (wl.LAYERNORM_BF16_1024x262144.with_rows(3), [(8, 16384), (8, 24576), (16, 12288), (4, 36864)]),
     (wl.RMSNORM_BF16_2048x786432.with_rows(2), [(10, 36864), (12, 28672), (16, 24576), (8, 53248),
                                                  (5, 53248)]),
-    (wl.sweep_point(1 << 20).with_rows(2), [(12, 36864), (16, 28672), (10, 53248)]),
-    (wl.sweep_point(1 << 19).with_rows(3), [(12, 36864), (8, 36864)]),
+    (wl.sweep_point(1 << 20).with_rows(2), [(12, 36864), (16, 28672), (10, 53248), (8, 37376),
+                                             (8, 18688)]),
+    # 28,672 staged elements: warps 0-3 have four full staged tiles for a
+    # ring of tail tiles, warps 4-7 read their tail tiles from global memory
+    (wl.sweep_point(1 << 19).with_rows(3), [(12, 36864), (8, 36864), (8, 28672), (8, 18688),
+                                            (8, 4096)]),
 ]
 
 
