@@ -266,8 +266,9 @@ cluster_reduce_reuse(const ClusterArgs a) {
         constexpr bool kPipe = BULK && R == 1 && OP == kRMSNorm && Granule<OP, T, PT>::kPairs == 4;
         // the tail of a slice with 16-byte granules is written from each
         // warp's ring of freed staged tiles; RMSNorm's pipelined pass, which
-        // keeps its weight loads ahead of its tiles, measured faster with
-        // the tail loaded through registers
+        // keeps its weight loads ahead of its tiles, and 8-byte granules
+        // (bf16 data with fp32 parameters, copied 8 bytes at a time) measured
+        // faster with the tail loaded through registers
         constexpr bool kRing = kTail && R == 1 && Granule<OP, T, PT>::kBytes == 16 && !kPipe;
         bool done = false;
         if constexpr (kRing) {

@@ -518,13 +518,15 @@ __device__ __forceinline__ void output_tiles(const OutputMap<OP, T>& h, const un
 // Output of one row slice with an L2 tail, the tail written from shared
 // memory: `stage` holds the first `nvec` vectors of the slice, `xtail` (global
 // memory) the `ntv` vectors that follow them, which the statistics pass read
-// from HBM with an evict-last policy.  Each warp writes its staged tiles
-// first.  A warp's first D full staged tiles, once written, are read by no
-// one else, so they become the warp's private ring: after writing staged
-// tile k < D, each lane copies its own vectors of the warp's tail tile k into
-// its own vectors of that tile (cp.async from L2, evict-first, no registers
-// held while they fly), and after writing tail tile j from its slot it
-// refills the slot with tail tile j + D.  Every copy is read back by the lane
+// from HBM with an evict-last policy.  A warp's first D full staged tiles,
+// once written, are read by no one else, so they become the warp's private
+// ring: after writing staged tile k < D, each lane copies its own vectors of
+// the warp's tail tile k into its own vectors of that tile (cp.async from L2,
+// evict-first, no registers held while they fly), and after writing tail
+// tile j from its slot it refills the slot with tail tile j + D.  The warp
+// writes its tail right after those D tiles, so that the tail's lines are
+// read again soon after the statistics pass left them in L2, and its other
+// staged tiles last.  Every copy is read back by the lane
 // that issued it, after its own wait, so no barrier is needed; D tiles of
 // every warp are in flight.  A warp with fewer than D full staged tiles
 // takes a ring of D / 2 (down to two), and with fewer than two reads its
@@ -602,14 +604,16 @@ __device__ __forceinline__ void output_ring(const OutputMap<OP, T>& h, const uns
         }
         cp_async_commit();
     };
-    int t = t0, k = 0;
-    for (; t + kTile <= nvec; t += stride, ++k) {
-        tile(t, t, nvec, false);
-        if (ring && k < D) prefetch(k);
-    }
-    if (t < nvec) tile(t, t, nvec, false);
     const int lim = nvec + ntv;
+    int t = t0;
     if (ring) {
+        // the first D staged tiles (full), each freeing a ring slot; then the
+        // tail, so that its lines are read again soon after the statistics
+        // pass left them in L2; then the rest of the staged tiles
+        for (int k = 0; k < D; ++k, t += stride) {
+            tile(t, t, nvec, false);
+            prefetch(k);
+        }
         // D groups were committed above and one more per tail tile, so tail
         // tile j's group is complete once at most D - 1 are pending
         for (int j = 0; t0 + j * stride < ntv; ++j) {
@@ -620,8 +624,11 @@ __device__ __forceinline__ void output_ring(const OutputMap<OP, T>& h, const uns
         }
         cp_async_wait<0>();
     } else {
+        // the tail first, from global memory
         for (int tt = t0; tt < ntv; tt += stride) tile(0, nvec + tt, lim, true);
     }
+    for (; t + kTile <= nvec; t += stride) tile(t, t, nvec, false);
+    if (t < nvec) tile(t, t, nvec, false);
 }
 
 }  // namespace credit
