@@ -376,10 +376,10 @@ def main():
 
     tuning = None
     if args.variant == "auto":
-        # the cost model screens profitability (its prediction is nearly
-        # flat across cluster sizes: it is no ranking tool), and the tuning
-        # step times every legal candidate; planning and tuning happen once,
-        # before (and outside) the timed region
+        # the cost model screens profitability and ranks the candidates (to
+        # within a few percent at the wide end), and the tuning step times
+        # every legal candidate; planning and tuning happen once, before
+        # (and outside) the timed region
         pdt_model = DT[w.param_dtype] if w.param_dtype else -1
         plan, report = C.tuned_plan(OPS[w.op], w.rows, w.cols, DT[w.dtype], pdt_model, dev)
         tuning = {"model_P": report.model_cluster_size, "baseline_us": round(report.t_base_us, 2)}

@@ -2,15 +2,17 @@
 // DSMEM profile it reads.
 //
 // CREDIT summary page (arXiv 2609.01864v1), "D. Profitability and Candidate
-// Selection": one timing of the selected non-DSMEM CUDA path is the first
-// screen (no peak-bandwidth assumptions); a work-free control kernel with
-// the candidate's grid, cluster size, dynamic-SMEM footprint and K = 2L
-// barriers measures launch, scheduling, occupancy and synchronisation cost
-// (T_ctrl = its excess over the one-CTA control); communication is charged
-// as local replay plus remote-store issue plus the non-overlapped deposit
-// residual; the avoided source time is valued at the baseline's achieved
-// rate ("D. Traffic Validation", cost accounting).  See include/credit.h for
-// the formula as implemented.
+// Selection".  The model screens a shape with a single timing of the
+// non-DSMEM path (no assumed peak bandwidth).  It prices the cluster's
+// launch, scheduling, occupancy and barrier cost with a control kernel that
+// does no work but has the candidate's grid, cluster size, shared-memory
+// footprint and two barriers per row (T_ctrl: its time beyond the same grid
+// without clusters).  It charges communication as the local replay of the
+// gathered partials, the issue of the remote stores and whatever part of the
+// deposits no other work hides.  The page prices the re-read that clustering
+// avoids at the baseline's own rate ("D. Traffic Validation", cost
+// accounting); this model uses measured local-work rates instead.
+// include/credit.h has the formula as implemented.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -293,10 +295,10 @@ std::vector<int64_t> tail_forms(int dev, credit_op_t op, int64_t cols, credit_dt
 }
 
 // The local-work primitive (a candidate's per-CTA work replayed without
-// DSMEM; CREDIT "D. Profitability and Candidate Selection": matched
-// primitive measurements): the one-CTA-per-row kernel at cluster size 1 --
-// no exchange -- on a calibration matrix whose rows are one staged budget
-// wide, so that `cps` CTAs share an SM, and `tails` more budgets of L2 tail
+// DSMEM; CREDIT "D. Profitability and Candidate Selection" builds its model
+// from primitives matched to the candidate): the one-CTA-per-row kernel at
+// cluster size 1 -- no exchange -- on a calibration matrix whose rows are
+// one staged budget wide, so that `cps` CTAs share an SM, and `tails` more budgets of L2 tail
 // (0: fully staged; 1: half the row in the tail; 3: three quarters).  GB/s of
 // one read and one write of the matrix.
 credit_status_t local_rate(int dev, credit_op_t op, credit_dtype_t dtype, int pdt, int cps,

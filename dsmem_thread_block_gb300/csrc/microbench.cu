@@ -1,12 +1,13 @@
 // microbench.cu -- DSMEM primitive characterisation and the control kernel.
 //
 // CREDIT summary page (arXiv 2609.01864v1), "C. Positioning": DSMEM is
-// profiled with latency, throughput and repeated cluster-synchronisation
-// microbenchmarks that place the CTAs on different SMs, reporting the median
-// of 15 runs; "D. Profitability and Candidate Selection": a work-free control
-// kernel with the real kernel's grid, cluster size, dynamic-SMEM footprint
-// and K = 2L barriers measures launch, scheduling, occupancy and
-// synchronisation cost, and its excess over a one-CTA control is T_ctrl.
+// characterised by latency, throughput and repeated cluster-barrier
+// benchmarks whose CTAs sit on different SMs, each reported as the median of
+// 15 runs.  "D. Profitability and Candidate Selection": a control kernel that
+// does no work but copies the real kernel's grid, cluster size,
+// shared-memory footprint and two barriers per row measures what launching,
+// scheduling, occupancy and synchronisation cost; T_ctrl is its time beyond
+// a control without clusters.
 //
 // Every benchmark kernel requests more than half of an SM's shared memory
 // (or the caller's footprint) so that no two of its CTAs share an SM; the
