@@ -21,17 +21,26 @@ def test_traffic_is_reported_only_for_matching_kernel_sources(monkeypatch):
     assert bench.stored_traffic(workload, variant) is None  # sources changed since the capture
 
 
-def test_kernel_source_hash_covers_every_source_file(tmp_path, monkeypatch):
+def test_kernel_source_hash_covers_the_kernel_sources(tmp_path, monkeypatch):
+    # every file that defines a kernel or its launch changes the hash; the
+    # cost model, microbenchmarks and host pipeline do not
     csrc = tmp_path / "dsmem_thread_block_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    (csrc / "a.cu").write_text("one")
+    for f in bench.KERNEL_SOURCES + ("costmodel.cu", "microbench.cu", "host.cu"):
+        (csrc / f).write_text(f)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    h1 = bench.kernel_source_hash()
-    (csrc / "b.cuh").write_text("two")
-    h2 = bench.kernel_source_hash()
-    (csrc / "b.cuh").write_text("two, edited")
-    h3 = bench.kernel_source_hash()
-    assert len({h1, h2, h3}) == 3
+    seen = {bench.kernel_source_hash()}
+    for f in bench.KERNEL_SOURCES:
+        (csrc / f).write_text(f + " edited")
+        seen.add(bench.kernel_source_hash())
+    assert len(seen) == len(bench.KERNEL_SOURCES) + 1
+    h = bench.kernel_source_hash()
+    for f in ("costmodel.cu", "microbench.cu", "host.cu"):
+        (csrc / f).write_text(f + " edited")
+    assert bench.kernel_source_hash() == h
+    real = set(os.listdir(os.path.join(os.path.dirname(os.path.dirname(__file__)),
+                                       "dsmem_thread_block_gb300", "csrc")))
+    assert set(bench.KERNEL_SOURCES) <= real
 
 
 def test_peak_from_the_measured_file_else_the_fallback(tmp_path, monkeypatch):
