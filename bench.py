@@ -333,7 +333,7 @@ def main():
     ap.add_argument("--cps", type=int, default=0, help="persistent CTAs per SM (0 = planner)")
     ap.add_argument("--exchange", default="plan", choices=["plan", "barrier", "async"],
                     help="partial exchange of a one-pass clustered plan (plan = as planned)")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--e2e-chunks", type=int, default=16,
                     help="row chunks of the host-buffer pipeline")
     ap.add_argument("--cpu-budget", type=float, default=20.0,
@@ -531,19 +531,22 @@ def main():
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # an event after every step (no synchronisation in between) shows how
+    # the steps spread: the host link stalls now and then for everyone
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
     with torch.cuda.stream(stream):
-        f0.record(stream)
-        for _ in range(e2e_steps):
+        marks[0].record(stream)
+        for i in range(e2e_steps):
             for k, v in hparams.items():
                 dparams[k].copy_(v, non_blocking=True)
             st = C.credit_run_host(call, plan, hbuf.data_ptr(), hbytes, rpc, sptr)
             if st != C.OK:
                 raise C.CreditError(st, "credit_run_host")
-        f1.record(stream)
+            marks[i + 1].record(stream)
     torch.cuda.synchronize()
-    te = max_over_ranks(f0.elapsed_time(f1), world, "cuda")
+    te = max_over_ranks(marks[0].elapsed_time(marks[-1]), world, "cuda")
     e2e_value = job_rate(bytes_step, te / e2e_steps, world)
+    step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(e2e_steps)]
 
     peak, peak_kind = measured_peak()
     variant_key = C.variant_name(plan)
@@ -582,7 +585,9 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "step_ms_median": statistics.median(step_ms),
+                    "step_ms_max": max(step_ms)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
