@@ -358,6 +358,8 @@ credit_status_t run(const OpCall& c) {
         // spends the spare registers on deeper parameter prefetch (where one
         // exists; cluster_kernel falls back to the regular one otherwise)
         key.deep = deep_footprint(dev, key, plan.smem_bytes);
+        key.quad = quad_footprint(dev, key, plan.smem_bytes,
+                                  plan.staged_elems < plan.slice_elems);
     }
     if (plan.variant == CREDIT_WARP_ROWS) {
         WarpRowsArgs a{};

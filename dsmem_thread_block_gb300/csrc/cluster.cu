@@ -51,8 +51,9 @@ __device__ unsigned long long g_trace[kTraceCtas][8];
 // DEEP: the instantiation for slices that leave room for at most two CTAs
 // per SM -- it may use twice the registers, which its pipelined output pass
 // spends on twice as many parameter loads in flight per lane.
-template <int OP, typename T, typename PT, bool BULK, int R, bool DEEP = false>
-__global__ void __launch_bounds__(kClusterMaxThreads, DEEP ? 2 : 3)
+template <int OP, typename T, typename PT, bool BULK, int R, bool DEEP = false,
+          bool QUAD = false>
+__global__ void __launch_bounds__(kClusterMaxThreads, DEEP ? 2 : (QUAD ? 4 : 3))
 cluster_reduce_reuse(const ClusterArgs a) {
     constexpr int kPipeU = DEEP ? 4 : 2;  // granules per lane in a pipelined output tile
     static_assert(BULK || R == 1, "the element path stages one row per cluster");
@@ -334,12 +335,17 @@ cluster_reduce_reuse(const ClusterArgs a) {
 
 // ----------------------------------------------------------- dispatch
 template <int OP, typename T, typename PT>
-static const void* pick_rows(bool vec, int rows, bool deep = false) {
+static const void* pick_rows(bool vec, int rows, bool deep = false, bool quad = false) {
     if (!vec) return rows == 1 ? (const void*)cluster_reduce_reuse<OP, T, PT, false, 1> : nullptr;
     // the deep instantiation exists where the output pass is pipelined
     constexpr bool kHasDeep = OP == kRMSNorm && Granule<OP, T, PT>::kPairs == 4;
     if constexpr (kHasDeep) {
         if (deep && rows == 1) return (const void*)cluster_reduce_reuse<OP, T, PT, true, 1, true>;
+    }
+    // the four-CTA instantiation: bf16 softmax (64 registers, no spills)
+    if constexpr (quad_capable(OP, (int)sizeof(T))) {
+        if (quad && rows == 1)
+            return (const void*)cluster_reduce_reuse<OP, T, PT, true, 1, false, true>;
     }
     switch (rows) {
         case 1: return (const void*)cluster_reduce_reuse<OP, T, PT, true, 1>;
@@ -364,7 +370,8 @@ static const void* pick_dtype(int dtype, int pdtype, bool vec, int rows, bool de
 const void* cluster_kernel(KernelKey k) {
     switch (k.op) {
         case kSoftmax: return k.dtype == 0 ? pick_rows<kSoftmax, float, float>(k.vec, k.rows)
-                                           : pick_rows<kSoftmax, bf16, float>(k.vec, k.rows);
+                                           : pick_rows<kSoftmax, bf16, float>(k.vec, k.rows,
+                                                                              false, k.quad);
         case kLayerNorm: return pick_dtype<kLayerNorm>(k.dtype, k.pdtype, k.vec, k.rows);
         case kRMSNorm: return pick_dtype<kRMSNorm>(k.dtype, k.pdtype, k.vec, k.rows, k.deep);
         case kQuant: return k.dtype == 0 ? pick_rows<kQuant, float, float>(k.vec, k.rows)

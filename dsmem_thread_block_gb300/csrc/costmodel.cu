@@ -276,14 +276,17 @@ int64_t staged_budget(int dev, credit_op_t op, credit_dtype_t dtype, int cps) {
 }
 
 // The L2-tail staging forms of cluster size P: the staged lengths that let
-// two and three CTAs share an SM, and half the three-CTA length -- a longer
+// two, three and (bf16 softmax) four CTAs share an SM, and half the
+// three-CTA length -- a longer
 // tail that each warp writes from a ring of its freed staged tiles, whose
 // loads overlap the staging from the start (measured faster for the widest
 // bf16 softmax rows).  Empty where the operator has no L2-tail form.
 std::vector<int64_t> tail_forms(int dev, credit_op_t op, int64_t cols, credit_dtype_t dtype,
                                 int P) {
     std::vector<int64_t> out;
-    for (int cps : {2, 3}) {
+    for (int cps : {2, 3, 4}) {
+        // four CTAs per SM only where the four-CTA instantiation exists
+        if (cps == 4 && !quad_capable((int)op, dtype == CREDIT_F32 ? 4 : 2)) continue;
         const int64_t h = tail_staged_for(dev, op, cols, dtype, P, cps);
         if (h > 0) out.push_back(h);
     }
@@ -325,6 +328,7 @@ credit_status_t local_rate(int dev, credit_op_t op, credit_dtype_t dtype, int pd
         // not a level of this primitive
         KernelKey key{(int)op, (int)dtype, pdt == CREDIT_BF16 ? 1 : 0, true, 1};
         key.deep = deep_footprint(dev, key, p.smem_bytes);
+        key.quad = quad_footprint(dev, key, p.smem_bytes, p.staged_elems < p.slice_elems);
         const void* fn = cluster_kernel(key);
         int per_sm = 0;
         // kernel_info raises the instantiation's dynamic-SMEM limit first
@@ -381,11 +385,15 @@ credit_status_t local_rates_for(int dev, credit_op_t op, credit_dtype_t dtype, i
     r.op = (int)op;
     r.dtype = (int)dtype;
     r.pdt = pdt;
-    const bool tails = tail_capable((int)op, dtype == CREDIT_F32 ? 4 : 2);
+    const int es = dtype == CREDIT_F32 ? 4 : 2;
+    const bool tails = tail_capable((int)op, es);
     for (int c = 1; c <= kLocalMaxCps; ++c) {
         credit_status_t st = local_rate(dev, op, dtype, pdt, c, 0, runs, &r.full[c]);
-        if (st == CREDIT_ERR_NO_LEGAL_PLAN) continue;
-        if (st != CREDIT_OK) return st;
+        if (st != CREDIT_OK && st != CREDIT_ERR_NO_LEGAL_PLAN) return st;
+        if (st != CREDIT_OK) r.full[c] = 0.0;
+        // the tail levels also where only L2-tail plans reach c CTAs per SM
+        // (the four-CTA instantiation)
+        if (st != CREDIT_OK && !quad_capable((int)op, es)) continue;
         if (tails) {
             st = local_rate(dev, op, dtype, pdt, c, 1, runs, &r.tail50[c]);
             if (st != CREDIT_OK && st != CREDIT_ERR_NO_LEGAL_PLAN) return st;
@@ -416,6 +424,14 @@ credit_status_t local_rates_for(int dev, credit_op_t op, credit_dtype_t dtype, i
 // rate).
 double local_gbps_at(const LocalRates& r, int c, double f) {
     const double full = r.full[c];
+    if (full <= 0.0) {
+        // a residency only L2-tail plans reach: flat below half the slice in
+        // the tail, then along the tail levels
+        if (r.tail50[c] <= 0.0) return 0.0;
+        if (f <= 0.5) return r.tail50[c];
+        const double t75 = r.tail75[c] > 0.0 ? r.tail75[c] : r.tail50[c];
+        return std::max(0.1 * r.tail50[c], r.tail50[c] + (t75 - r.tail50[c]) * ((f - 0.5) / 0.25));
+    }
     if (f <= 0.0 || r.tail50[c] <= 0.0) return full;
     if (f <= 0.5) return full + (r.tail50[c] - full) * (f / 0.5);
     const double t75 = r.tail75[c] > 0.0 ? r.tail75[c] : r.tail50[c];
@@ -423,15 +439,15 @@ double local_gbps_at(const LocalRates& r, int c, double f) {
 }
 
 // ... at an effective residency c_eff (resident CTAs per SM, fractional):
-// linear between the measured residencies around it, proportional below one
-// CTA per SM (idle SMs stream nothing), saturated at the highest residency
-// measured.
+// linear between the measured residencies around it (for a tail plan, also
+// those only tail plans reach), proportional below one CTA per SM (idle SMs
+// stream nothing), saturated at the highest residency measured.
 double local_gbps(const LocalRates& r, double c_eff, double f) {
     if (r.full[1] <= 0.0) return 0.0;
     if (c_eff <= 1.0) return local_gbps_at(r, 1, f) * std::max(0.0, c_eff);
     int lo = 1;
     for (int c = 2; c <= kLocalMaxCps; ++c) {
-        if (r.full[c] <= 0.0) continue;
+        if (r.full[c] <= 0.0 && (f <= 0.0 || r.tail50[c] <= 0.0)) continue;
         if (c >= c_eff) {
             const double w = (c_eff - lo) / (double)(c - lo);
             return local_gbps_at(r, lo, f) * (1.0 - w) + local_gbps_at(r, c, f) * w;
@@ -613,6 +629,7 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
             // residency: CTAs per SM the footprint allows, free of clusters
             KernelKey key{(int)op, (int)dtype, pkey, true, 1};
             key.deep = deep_footprint(device, key, q.smem_bytes);
+            key.quad = quad_footprint(device, key, q.smem_bytes, q.staged_elems < q.slice_elems);
             const void* fn = cluster_kernel(key);
             int per_sm = 0;
             if (!fn || !kernel_info(device, fn, true) ||

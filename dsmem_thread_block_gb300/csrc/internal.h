@@ -36,6 +36,13 @@ __host__ __device__ constexpr bool tail_capable(int op, int dtype_bytes) {
     return op == 1 /* LayerNorm */ || op == 2 /* RMSNorm */ || (op == 0 && dtype_bytes == 2);
 }
 
+// Operators and data types with a one-row-per-cluster instantiation bounded
+// to 64 registers, four CTAs per SM, for L2-tail plans whose footprint
+// leaves room for four (bf16 softmax: no spills at that bound).
+__host__ __device__ constexpr bool quad_capable(int op, int dtype_bytes) {
+    return op == 0 && dtype_bytes == 2;
+}
+
 // Arguments of the two-pass (global re-read) kernel pair.
 struct TwoPassArgs {
     const void* x;
@@ -101,6 +108,7 @@ struct KernelKey {
     bool vec;
     int rows = 1;
     bool deep = false;  // clustered kernel for slices that leave room for <= 2 CTAs per SM
+    bool quad = false;  // clustered kernel bounded to 64 registers: four CTAs per SM
 };
 
 const void* cluster_kernel(KernelKey k);

@@ -59,6 +59,16 @@ bool deep_footprint(int dev, KernelKey k, int64_t smem_bytes) {
     return smem_bytes + ki->static_smem + d->reserved_smem > (int64_t)d->smem_per_sm / 3;
 }
 
+bool quad_footprint(int dev, KernelKey k, int64_t smem_bytes, bool tail) {
+    if (!tail || !k.vec || k.rows != 1 || !quad_capable(k.op, k.dtype == 0 ? 4 : 2)) return false;
+    const DevInfo* d = device_info(dev);
+    k.deep = false;
+    k.quad = false;
+    const KernelInfo* ki = d ? kernel_info(dev, cluster_kernel(k), true) : nullptr;
+    if (!ki) return false;
+    return smem_bytes + ki->static_smem + d->reserved_smem <= (int64_t)d->smem_per_sm / 4;
+}
+
 int64_t tail_budget_bytes(const DevInfo& d, int static_smem, int cps) {
     const int64_t per_cta = (int64_t)d.smem_per_sm / cps - d.reserved_smem;
     const int64_t kb = 1024;
@@ -215,7 +225,9 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
         }
         const int64_t pitch = row_pitch(held, es);
         const int64_t smem = staged == 1 ? round_up(held * es, 16) : staged * pitch;
-        const void* fn = cluster_kernel(KernelKey{(int)op, (int)dtype, 0, true, R});
+        KernelKey key{(int)op, (int)dtype, 0, true, R};
+        key.quad = quad_footprint(dev, key, smem, held < slice);
+        const void* fn = cluster_kernel(key);
         const KernelInfo* ki = kernel_info(dev, fn, true);
         if (!ki) return CREDIT_ERR_CUDA;
         if (smem > ki->max_dyn_smem || pitch > INT32_MAX) return CREDIT_ERR_NO_LEGAL_PLAN;

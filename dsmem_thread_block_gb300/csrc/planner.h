@@ -59,6 +59,11 @@ int64_t tail_budget_bytes(const DevInfo& d, int static_smem, int cps);
 // CTAs per SM and twice the registers.
 bool deep_footprint(int dev, KernelKey k, int64_t smem_bytes);
 
+// Does a one-row-per-cluster L2-tail launch (`tail`) of `smem_bytes` dynamic
+// shared memory leave room for four CTAs per SM, for an operator with the
+// four-CTA instantiation?  Then it takes that instantiation.
+bool quad_footprint(int dev, KernelKey k, int64_t smem_bytes, bool tail);
+
 // Staged elements per row of an L2-tail plan of cluster size P with
 // rows_per_cluster rows per cluster that lets `cps` CTAs share an SM, or 0
 // when the operator has no L2-tail form or the whole slice already fits.

@@ -5,8 +5,8 @@ softmax by default, or another operator and dtype) the cost model
 (credit_plan_profiled) predicts the time of every legal cluster size (each
 with its whole slice staged, where it fits, and with L2-tail plans) and of
 the non-DSMEM baseline and picks one; then every candidate -- every staging
-form of every legal cluster size (the whole slice, the L2-tail plans for two
-and three CTAs per SM and half the three-CTA staged length) -- is timed on
+form of every legal cluster size (the whole slice, the L2-tail plans for two,
+three and four CTAs per SM and half the three-CTA staged length) -- is timed on
 the seeded input (median of `runs` launches, CUDA events).  A point is correct when the pick's measured time is within
 max(2 %, the runs' interquartile spread) of the fastest measured candidate
 (CREDIT summary page, "C. Cost-Model Validation": profitability accuracy
@@ -95,8 +95,8 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
         return _timed(go, runs)
 
     # every candidate the model valued: per legal P its chosen staging form
-    # (measured[P]) and the other forms (whole slice, L2-tail plans for two
-    # and three CTAs per SM, half the three-CTA staged length), all timed;
+    # (measured[P]) and the other forms (whole slice, L2-tail plans for two,
+    # three and four CTAs per SM, half the three-CTA staged length), all timed;
     # forms[P] keeps the fastest form
     measured, forms = {}, {}
     for cand in rep.cand:
@@ -119,7 +119,7 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
         except C.CreditError:
             pass
         t3 = None
-        for cps in (2, 3):
+        for cps in (2, 3, 4):
             try:
                 q = C.credit_plan_tail(_OPS[op], w.rows, w.cols, _DT[dtype], device, P, cps)
                 others.append(q)

@@ -226,3 +226,28 @@ def test_footprints_of_two_ctas_per_sm(w, cases):
         assert p.smem_bytes > smem_per_sm // 3, (P, R, staged, p.smem_bytes)
         check(w, run(w, inp, p), inp)
         check(w, run(w, inp, p, in_place=True), inp)
+
+
+FOUR = [
+    # bf16 softmax L2-tail plans whose footprint leaves room for four CTAs per
+    # SM take the instantiation bounded to 64 registers
+    (wl.sweep_point(1 << 19).with_rows(5), [8, 4, 16, 5]),
+    (wl.sweep_point(1 << 20).with_rows(3), [16, 8, 12]),
+    (_custom(wl.SOFTMAX, "bf16", 4, 400008, 77, x_std=2.5, spike_frac=0.02), [7, 12]),
+]
+
+
+@pytest.mark.parametrize("w,sizes", FOUR, ids=[c[0].name for c in FOUR])
+def test_four_ctas_per_sm(w, sizes):
+    inp = w.generate()
+    dev = torch.cuda.current_device()
+    smem_per_sm = torch.cuda.get_device_properties(0).shared_memory_per_multiprocessor
+    for P in sizes:
+        p = C.credit_plan_tail(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, P, 4)
+        assert p.staged_elems < p.slice_elems and 4 * p.smem_bytes < smem_per_sm, (P, p)
+        check(w, run(w, inp, p), inp)
+        check(w, run(w, inp, p, in_place=True), inp)
+    with C.use_checked_build():
+        p = C.credit_plan_tail(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, sizes[0], 4)
+        check(w, run(w, inp, p), inp)
+        assert C.credit_get_device_error(dev) == C.OK
