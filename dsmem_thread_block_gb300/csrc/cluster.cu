@@ -342,8 +342,8 @@ static const void* pick_rows(bool vec, int rows, bool deep = false, bool quad = 
     if constexpr (kHasDeep) {
         if (deep && rows == 1) return (const void*)cluster_reduce_reuse<OP, T, PT, true, 1, true>;
     }
-    // the four-CTA instantiation: bf16 softmax (64 registers, no spills)
-    if constexpr (quad_capable(OP, (int)sizeof(T))) {
+    // the four-CTA instantiation (64 registers)
+    if constexpr (quad_capable(OP, (int)sizeof(T), (int)sizeof(PT))) {
         if (quad && rows == 1)
             return (const void*)cluster_reduce_reuse<OP, T, PT, true, 1, false, true>;
     }
@@ -356,15 +356,16 @@ static const void* pick_rows(bool vec, int rows, bool deep = false, bool quad = 
 }
 
 template <int OP, typename T>
-static const void* pick_param(int pdtype, bool vec, int rows, bool deep) {
-    return pdtype == 0 ? pick_rows<OP, T, float>(vec, rows, deep)
-                       : pick_rows<OP, T, bf16>(vec, rows, deep);
+static const void* pick_param(int pdtype, bool vec, int rows, bool deep, bool quad) {
+    return pdtype == 0 ? pick_rows<OP, T, float>(vec, rows, deep, quad)
+                       : pick_rows<OP, T, bf16>(vec, rows, deep, quad);
 }
 
 template <int OP>
-static const void* pick_dtype(int dtype, int pdtype, bool vec, int rows, bool deep = false) {
-    return dtype == 0 ? pick_param<OP, float>(pdtype, vec, rows, deep)
-                      : pick_param<OP, bf16>(pdtype, vec, rows, deep);
+static const void* pick_dtype(int dtype, int pdtype, bool vec, int rows, bool deep = false,
+                              bool quad = false) {
+    return dtype == 0 ? pick_param<OP, float>(pdtype, vec, rows, deep, quad)
+                      : pick_param<OP, bf16>(pdtype, vec, rows, deep, quad);
 }
 
 const void* cluster_kernel(KernelKey k) {
@@ -372,8 +373,10 @@ const void* cluster_kernel(KernelKey k) {
         case kSoftmax: return k.dtype == 0 ? pick_rows<kSoftmax, float, float>(k.vec, k.rows)
                                            : pick_rows<kSoftmax, bf16, float>(k.vec, k.rows,
                                                                               false, k.quad);
-        case kLayerNorm: return pick_dtype<kLayerNorm>(k.dtype, k.pdtype, k.vec, k.rows);
-        case kRMSNorm: return pick_dtype<kRMSNorm>(k.dtype, k.pdtype, k.vec, k.rows, k.deep);
+        case kLayerNorm:
+            return pick_dtype<kLayerNorm>(k.dtype, k.pdtype, k.vec, k.rows, false, k.quad);
+        case kRMSNorm:
+            return pick_dtype<kRMSNorm>(k.dtype, k.pdtype, k.vec, k.rows, k.deep, k.quad);
         case kQuant: return k.dtype == 0 ? pick_rows<kQuant, float, float>(k.vec, k.rows)
                                          : pick_rows<kQuant, bf16, float>(k.vec, k.rows);
         case kWStd: return pick_dtype<kWStd>(k.dtype, k.pdtype, k.vec, k.rows);

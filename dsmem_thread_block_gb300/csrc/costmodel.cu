@@ -276,17 +276,19 @@ int64_t staged_budget(int dev, credit_op_t op, credit_dtype_t dtype, int cps) {
 }
 
 // The L2-tail staging forms of cluster size P: the staged lengths that let
-// two, three and (bf16 softmax) four CTAs share an SM, and half the
-// three-CTA length -- a longer
-// tail that each warp writes from a ring of its freed staged tiles, whose
-// loads overlap the staging from the start (measured faster for the widest
-// bf16 softmax rows).  Empty where the operator has no L2-tail form.
+// two, three and (where the four-CTA instantiation exists) four CTAs share an
+// SM, and half the three-CTA length -- a longer tail that each warp writes
+// from a ring of its freed staged tiles, whose loads overlap the staging from
+// the start (measured faster for the widest bf16 softmax rows).  Empty where
+// the operator has no L2-tail form.
 std::vector<int64_t> tail_forms(int dev, credit_op_t op, int64_t cols, credit_dtype_t dtype,
-                                int P) {
+                                int pdt, int P) {
     std::vector<int64_t> out;
     for (int cps : {2, 3, 4}) {
         // four CTAs per SM only where the four-CTA instantiation exists
-        if (cps == 4 && !quad_capable((int)op, dtype == CREDIT_F32 ? 4 : 2)) continue;
+        if (cps == 4 &&
+            !quad_capable((int)op, dtype == CREDIT_F32 ? 4 : 2, pdt == CREDIT_BF16 ? 2 : 4))
+            continue;
         const int64_t h = tail_staged_for(dev, op, cols, dtype, P, cps);
         if (h > 0) out.push_back(h);
     }
@@ -393,7 +395,7 @@ credit_status_t local_rates_for(int dev, credit_op_t op, credit_dtype_t dtype, i
         if (st != CREDIT_OK) r.full[c] = 0.0;
         // the tail levels also where only L2-tail plans reach c CTAs per SM
         // (the four-CTA instantiation)
-        if (st != CREDIT_OK && !quad_capable((int)op, es)) continue;
+        if (st != CREDIT_OK && !quad_capable((int)op, es, pdt == CREDIT_BF16 ? 2 : 4)) continue;
         if (tails) {
             st = local_rate(dev, op, dtype, pdt, c, 1, runs, &r.tail50[c]);
             if (st != CREDIT_OK && st != CREDIT_ERR_NO_LEGAL_PLAN) return st;
@@ -619,7 +621,7 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         credit_plan_t p;
         if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1) == CREDIT_OK)
             plans.push_back(p);
-        for (int64_t held : tail_forms(device, op, cols, dtype, P)) {
+        for (int64_t held : tail_forms(device, op, cols, dtype, param_dtype, P)) {
             if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1, held) ==
                 CREDIT_OK)
                 plans.push_back(p);
@@ -721,7 +723,7 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
             if (c.plan.staged_elems < c.plan.slice_elems &&
                 make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &tp, 0, 1) == CREDIT_OK)
                 plans.push_back(tp);
-            for (int64_t held : tail_forms(device, op, cols, dtype, P)) {
+            for (int64_t held : tail_forms(device, op, cols, dtype, param_dtype, P)) {
                 if (held != c.plan.staged_elems &&
                     make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &tp, 0, 1,
                               held) == CREDIT_OK)

@@ -36,11 +36,14 @@ __host__ __device__ constexpr bool tail_capable(int op, int dtype_bytes) {
     return op == 1 /* LayerNorm */ || op == 2 /* RMSNorm */ || (op == 0 && dtype_bytes == 2);
 }
 
-// Operators and data types with a one-row-per-cluster instantiation bounded
-// to 64 registers, four CTAs per SM, for L2-tail plans whose footprint
-// leaves room for four (bf16 softmax: no spills at that bound).
-__host__ __device__ constexpr bool quad_capable(int op, int dtype_bytes) {
-    return op == 0 && dtype_bytes == 2;
+// Operators and data / parameter types with a one-row-per-cluster
+// instantiation bounded to 64 registers, four CTAs per SM, for L2-tail plans
+// whose footprint leaves room for four: bf16 softmax and LayerNorm with bf16
+// data and fp32 parameters (no spills at that bound; both measured faster).
+// RMSNorm's pipelined weight loads spill there and measured slower.
+__host__ __device__ constexpr bool quad_capable(int op, int dtype_bytes, int param_bytes) {
+    return dtype_bytes == 2 &&
+           (op == 0 /* softmax */ || (op == 1 /* LayerNorm */ && param_bytes == 4));
 }
 
 // Arguments of the two-pass (global re-read) kernel pair.

@@ -60,7 +60,9 @@ bool deep_footprint(int dev, KernelKey k, int64_t smem_bytes) {
 }
 
 bool quad_footprint(int dev, KernelKey k, int64_t smem_bytes, bool tail) {
-    if (!tail || !k.vec || k.rows != 1 || !quad_capable(k.op, k.dtype == 0 ? 4 : 2)) return false;
+    if (!tail || !k.vec || k.rows != 1 ||
+        !quad_capable(k.op, k.dtype == 0 ? 4 : 2, k.pdtype == 1 ? 2 : 4))
+        return false;
     const DevInfo* d = device_info(dev);
     k.deep = false;
     k.quad = false;

@@ -229,11 +229,16 @@ def test_footprints_of_two_ctas_per_sm(w, cases):
 
 
 FOUR = [
-    # bf16 softmax L2-tail plans whose footprint leaves room for four CTAs per
-    # SM take the instantiation bounded to 64 registers
+    # bf16 softmax and LayerNorm (bf16 data, fp32 parameters) L2-tail plans
+    # whose footprint leaves room for four CTAs per SM take the instantiation
+    # bounded to 64 registers
     (wl.sweep_point(1 << 19).with_rows(5), [8, 4, 16, 5]),
     (wl.sweep_point(1 << 20).with_rows(3), [16, 8, 12]),
     (_custom(wl.SOFTMAX, "bf16", 4, 400008, 77, x_std=2.5, spike_frac=0.02), [7, 12]),
+    (wl.LAYERNORM_BF16_1024x262144.with_rows(5), [4, 8, 6]),
+    (_custom(wl.LAYERNORM, "bf16", 3, 300008, 78, x_mean=-1.0, x_std=3.0, eps=1e-5,
+             param_dtype="f32"), [3, 5]),
+    (_custom(wl.LAYERNORM, "bf16", 3, 262144, 79, x_mean=2.0, x_std=0.5, eps=1e-5), [4]),
 ]
 
 
