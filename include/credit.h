@@ -409,14 +409,16 @@ credit_status_t credit_run_host(const credit_host_call_t *call,
  * shared memory), the warp-per-row register kernel (rows of at most 4 KiB)
  * and the two-pass global re-read pair -- and predicts every legal clustered
  * candidate (each P with its whole slice staged, where it fits, and with the
- * L2-tail plans sized for two and three CTAs per SM) from measured
- * primitives, without timing the candidate:
+ * L2-tail plans sized for two, three and -- where the four-CTA instantiation
+ * exists -- four CTAs per SM, and with half the three-CTA staged length) from
+ * measured primitives, without timing the candidate:
  *     T(P) = B_credit / (R_loc(c_eff, f) * S(P)) * q + T_ctrl(P) + T_comm(P)
  *            + T_replay(P)
  *   R_loc(c, f)  the local-work primitive: the one-CTA-per-row kernel (no
  *                DSMEM) timed once per operator and dtype on calibration
  *                rows that let c = 1..8 CTAs share an SM, fully staged and
- *                with a half and three quarters of each row an L2 tail;
+ *                with a half and three quarters of each row an L2 tail (the
+ *                tail levels also at residencies only tail plans reach);
  *                piecewise linear in c and in the tail fraction f
  *   c_eff        the CTAs per SM the candidate keeps resident: resident
  *                clusters x P / SMs, at most what its footprint allows (a
@@ -440,7 +442,8 @@ credit_status_t credit_run_host(const credit_host_call_t *call,
  * pages, the model screens and a final tuning step may pick another legal
  * size: with tune > 0 the `tune` best-predicted cluster sizes are timed (all
  * their staging forms, and the persistent and pipelined kernels of the same
- * P) and the fastest measured plan, baseline included, is chosen.
+ * P); the three fastest are timed twice more, interleaved, and the plan with
+ * the smallest mean of its three medians is chosen if it beats the baseline.
  */
 typedef struct {
     int32_t cluster_size;    /* P; 1 = the baseline */

@@ -43,7 +43,10 @@ def test_tuning_times_the_top_candidates():
                [c.persistent_us for c in timed if c.persistent_us > 0] +
                [c.pipelined_us for c in timed if c.pipelined_us > 0] +
                [c.tail_us for c in timed if c.tail_us > 0])
-    assert abs(plan.pred_us - best) <= 1e-3 * best + 1e-3  # the plan carries its measured time
+    # the plan carries its measured time: the mean of three medians of the
+    # confirmation round, which re-times the fastest plans of the first
+    assert best * 0.9 <= plan.pred_us <= best * 1.1 + 1e-3
+    assert plan.cluster_size == rep.chosen_cluster_size or plan.variant == C.TWO_PASS
 
 
 def test_softmax_sweep_profitability_and_crossover_at_full_size():
