@@ -328,8 +328,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="rmsnorm_bf16_2048x786432")
     ap.add_argument("--variant", default="auto",
-                    help="auto (cost model + tuning) | static | cluster:P[xR][:sSTAGED] | persist:P | pipe:P | "
-                         "warp_rows | two_pass")
+                    help="auto (cost model + tuning) | static | cluster:P[xR][:sSTAGED][:tTHREADS] | "
+                         "persist:P | pipe:P | warp_rows | two_pass")
     ap.add_argument("--cps", type=int, default=0, help="persistent CTAs per SM (0 = planner)")
     ap.add_argument("--exchange", default="plan", choices=["plan", "barrier", "async"],
                     help="partial exchange of a one-pass clustered plan (plan = as planned)")
@@ -411,11 +411,12 @@ def main():
         R = 0
         if "x" in P:
             P, R = P.split("x")
-        staged = int(rest[0][1:]) if rest and rest[0].startswith("s") else 0
+        staged = next((int(q[1:]) for q in rest if q.startswith("s")), 0)
+        threads = next((int(q[1:]) for q in rest if q.startswith("t")), 0)
         var = {"cluster": C.CLUSTER, "persist": C.CLUSTER_PERSISTENT,
                "pipe": C.CLUSTER_PIPELINED}[kind]
         plan = C.credit_plan_with(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, var, int(P),
-                                  rows_per_cluster=int(R), staged_elems=staged)
+                                  threads=threads, rows_per_cluster=int(R), staged_elems=staged)
     if args.cps:
         plan.ctas_per_sm = args.cps
         plan = C.Plan.from_buffer_copy(plan)

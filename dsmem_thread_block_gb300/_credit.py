@@ -356,8 +356,10 @@ def credit_plan_profiled(op: int, rows: int, cols: int, dtype: int, param_dtype:
 
 def variant_name(plan) -> str:
     """Short name of a plan's kernel and cluster size, as the benchmark
-    prints it: cluster:P[xR][:sSTAGED][:barrier], persist:P, pipe:P, warp_rows,
-    two_pass (sSTAGED: an L2-tail plan staging STAGED elements per CTA)."""
+    prints it: cluster:P[xR][:sSTAGED][:tTHREADS][:barrier], persist:P,
+    pipe:P, warp_rows, two_pass (sSTAGED: an L2-tail plan staging STAGED
+    elements per CTA; tTHREADS: an L2-tail plan with other than 256 threads
+    per CTA)."""
     if plan.variant == TWO_PASS:
         return "two_pass"
     if plan.variant == WARP_ROWS:
@@ -368,6 +370,8 @@ def variant_name(plan) -> str:
         s += f"x{plan.rows_per_cluster}"
     if plan.variant == CLUSTER and 0 < plan.staged_elems < plan.slice_elems:
         s += f":s{plan.staged_elems}"
+        if plan.threads != 256:
+            s += f":t{plan.threads}"
     if plan.variant == CLUSTER and plan.exchange == EXCHANGE_BARRIER:
         s += ":barrier"
     return s

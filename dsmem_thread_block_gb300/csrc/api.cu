@@ -454,7 +454,8 @@ credit_status_t credit_plan_for(credit_op_t op, int64_t rows, int64_t cols, cred
 credit_status_t credit_plan_tail(credit_op_t op, int64_t rows, int64_t cols, credit_dtype_t dtype,
                                  int device, int cluster_size, int ctas_per_sm,
                                  credit_plan_t* out) {
-    if (!out || rows < 1 || cols < 1 || ctas_per_sm < 1 || ctas_per_sm > 8) return CREDIT_ERR_INVALID_ARG;
+    if (!out || rows < 1 || cols < 1 || ctas_per_sm < 1 || ctas_per_sm > 32)
+        return CREDIT_ERR_INVALID_ARG;
     if (cluster_size < 1 || cluster_size > kMaxCluster) return CREDIT_ERR_NO_LEGAL_PLAN;
     if (dtype != CREDIT_F32 && dtype != CREDIT_BF16) return CREDIT_ERR_UNSUPPORTED;
     const int64_t held = tail_staged_for(device, op, cols, dtype, cluster_size, ctas_per_sm);

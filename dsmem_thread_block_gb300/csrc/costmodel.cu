@@ -275,27 +275,38 @@ int64_t staged_budget(int dev, credit_op_t op, credit_dtype_t dtype, int cps) {
     return budget / (vec * es) * vec;
 }
 
-// The L2-tail staging forms of cluster size P: the staged lengths that let
+// The L2-tail staging forms of cluster size P (staged elements per slice, and
+// threads per CTA, 0 for the planner's choice): the staged lengths that let
 // two, three and (where the four-CTA instantiation exists) four CTAs share an
-// SM, and half the three-CTA length -- a longer tail that each warp writes
-// from a ring of its freed staged tiles, whose loads overlap the staging from
-// the start (measured faster for the widest bf16 softmax rows).  Empty where
-// the operator has no L2-tail form.
-std::vector<int64_t> tail_forms(int dev, credit_op_t op, int64_t cols, credit_dtype_t dtype,
-                                int pdt, int P) {
-    std::vector<int64_t> out;
+// SM; half the three-CTA length -- a longer tail that each warp writes from
+// a ring of its freed staged tiles, whose loads overlap the staging from the
+// start (measured faster for the widest bf16 softmax rows); and, for
+// LayerNorm with the 64-register instantiation, the length for ten CTAs per
+// SM at 128 threads each: small CTAs, seven or eight resident per SM
+// (measured faster there, slower for softmax).  Empty where the operator has
+// no L2-tail form.
+struct TailForm {
+    int64_t staged;
+    int threads;
+};
+std::vector<TailForm> tail_forms(int dev, credit_op_t op, int64_t cols, credit_dtype_t dtype,
+                                 int pdt, int P) {
+    std::vector<TailForm> out;
+    const bool quad = quad_capable((int)op, dtype == CREDIT_F32 ? 4 : 2, pdt == CREDIT_BF16 ? 2 : 4);
     for (int cps : {2, 3, 4}) {
         // four CTAs per SM only where the four-CTA instantiation exists
-        if (cps == 4 &&
-            !quad_capable((int)op, dtype == CREDIT_F32 ? 4 : 2, pdt == CREDIT_BF16 ? 2 : 4))
-            continue;
+        if (cps == 4 && !quad) continue;
         const int64_t h = tail_staged_for(dev, op, cols, dtype, P, cps);
-        if (h > 0) out.push_back(h);
+        if (h > 0) out.push_back({h, 0});
     }
     const int64_t vec = dtype == CREDIT_F32 ? 4 : 8;
     const int64_t h3 = tail_staged_for(dev, op, cols, dtype, P, 3);
     const int64_t half = h3 / 2 / vec * vec;
-    if (h3 > 0 && half >= vec) out.push_back(half);
+    if (h3 > 0 && half >= vec) out.push_back({half, 0});
+    if (quad && op == CREDIT_LAYERNORM) {
+        const int64_t h10 = tail_staged_for(dev, op, cols, dtype, P, 10);
+        if (h10 > 0) out.push_back({h10, 128});
+    }
     return out;
 }
 
@@ -621,9 +632,9 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
         credit_plan_t p;
         if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1) == CREDIT_OK)
             plans.push_back(p);
-        for (int64_t held : tail_forms(device, op, cols, dtype, param_dtype, P)) {
-            if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &p, 0, 1, held) ==
-                CREDIT_OK)
+        for (const TailForm& f : tail_forms(device, op, cols, dtype, param_dtype, P)) {
+            if (make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, f.threads, 0, &p, 0, 1,
+                          f.staged) == CREDIT_OK)
                 plans.push_back(p);
         }
         for (const credit_plan_t& q : plans) {
@@ -730,10 +741,11 @@ extern "C" credit_status_t credit_plan_profiled(credit_op_t op, int64_t rows, in
             if (c.plan.staged_elems < c.plan.slice_elems &&
                 make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &tp, 0, 1) == CREDIT_OK)
                 plans.push_back(tp);
-            for (int64_t held : tail_forms(device, op, cols, dtype, param_dtype, P)) {
-                if (held != c.plan.staged_elems &&
-                    make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, 0, 0, &tp, 0, 1,
-                              held) == CREDIT_OK)
+            for (const TailForm& f : tail_forms(device, op, cols, dtype, param_dtype, P)) {
+                if ((f.staged != c.plan.staged_elems ||
+                     (f.threads != 0 && f.threads != c.plan.threads)) &&
+                    make_plan(device, op, rt, cols, dtype, CREDIT_CLUSTER, P, f.threads, 0, &tp,
+                              0, 1, f.staged) == CREDIT_OK)
                     plans.push_back(tp);
             }
             for (size_t i = 0; i < plans.size(); ++i) {

@@ -353,15 +353,21 @@ bool forced_plan(int dev, credit_op_t op, int64_t rows, int64_t cols, credit_dty
         staged = std::strtol(q, &e, 10);
         if (e == q || staged < 1) return false;
     }
+    long threads = 0;
+    if (*e == ':' && e[1] == 't') {
+        q = e + 2;
+        threads = std::strtol(q, &e, 10);
+        if (e == q || threads < 32 || threads > 1024 || threads % 32) return false;
+    }
     if (*e) return false;
     credit_variant_t v;
     if (kind == "cluster") v = CREDIT_CLUSTER;
     else if (kind == "persist") v = CREDIT_CLUSTER_PERSISTENT;
     else if (kind == "pipe") v = CREDIT_CLUSTER_PIPELINED;
     else return false;
-    if (v != CREDIT_CLUSTER && (R || staged)) return false;
-    return make_plan(dev, op, rows, cols, dtype, v, (int)P, 0, 0, out, 0, (int)R, staged) ==
-           CREDIT_OK;
+    if (v != CREDIT_CLUSTER && (R || staged || threads)) return false;
+    return make_plan(dev, op, rows, cols, dtype, v, (int)P, (int)threads, 0, out, 0, (int)R,
+                     staged) == CREDIT_OK;
 }
 
 }  // namespace credit

@@ -6,7 +6,8 @@ softmax by default, or another operator and dtype) the cost model
 with its whole slice staged, where it fits, and with L2-tail plans) and of
 the non-DSMEM baseline and picks one; then every candidate -- every staging
 form of every legal cluster size (the whole slice, the L2-tail plans for two,
-three and four CTAs per SM and half the three-CTA staged length) -- is timed on
+three and four CTAs per SM, half the three-CTA staged length, and 128-thread
+CTAs with the staged length for ten per SM) -- is timed on
 the seeded input (median of `runs` launches, CUDA events).  A point is correct when the pick's measured time is within
 max(2 %, the runs' interquartile spread) of the fastest measured candidate
 (CREDIT summary page, "C. Cost-Model Validation": profitability accuracy
@@ -96,7 +97,8 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
 
     # every candidate the model valued: per legal P its chosen staging form
     # (measured[P]) and the other forms (whole slice, L2-tail plans for two,
-    # three and four CTAs per SM, half the three-CTA staged length), all timed;
+    # three and four CTAs per SM, half the three-CTA staged length, small
+    # CTAs), all timed;
     # forms[P] keeps the fastest form
     measured, forms = {}, {}
     for cand in rep.cand:
@@ -126,6 +128,14 @@ def run_point(cols: int, runs: int = 15, device: int = 0, model_runs: int = 7,
                 t3 = q if cps == 3 else t3
             except C.CreditError:
                 pass
+        try:
+            # small CTAs: the staged length for ten CTAs per SM, 128 threads
+            t10 = C.credit_plan_tail(_OPS[op], w.rows, w.cols, _DT[dtype], device, P, 10)
+            others.append(C.credit_plan_with(_OPS[op], w.rows, w.cols, _DT[dtype], device,
+                                             C.CLUSTER, P, threads=128,
+                                             staged_elems=int(t10.staged_elems)))
+        except C.CreditError:
+            pass
         if t3 is not None and t3.staged_elems < t3.slice_elems:
             # the longer tail the cost model also considers: half the
             # three-CTA staged length

@@ -177,9 +177,10 @@ credit_status_t credit_plan(credit_op_t op, int64_t rows, int64_t cols,
 
 /*
  * The L2-tail plan of a one-row-per-cluster launch with cluster size
- * cluster_size whose staged part lets ctas_per_sm (1..8) CTAs share an SM:
+ * cluster_size whose staged part lets ctas_per_sm (1..32) CTAs share an SM:
  * staged_elems is the largest whole number of 16-byte vectors of the slice
- * that fits that share of an SM's shared memory.  CREDIT_ERR_NO_LEGAL_PLAN
+ * that fits that share of an SM's shared memory (how many CTAs are then
+ * resident also depends on threads and registers).  CREDIT_ERR_NO_LEGAL_PLAN
  * if the whole slice already fits that budget, the operator and dtype have
  * no L2-tail form (fp32 softmax, quantization, weighted standardization,
  * Pearson), or no such cluster can be resident.  Host only.
@@ -506,6 +507,7 @@ credit_status_t credit_calibrate(int device, int runs, const char *profile_path)
  *                          for the shape (else the automatic choice stands):
  *                          cluster:P, cluster:PxR (R rows per cluster),
  *                          cluster:P:sN (an L2-tail plan staging N elements),
+ *                          cluster:P:sN:tT (the same with T threads per CTA),
  *                          persist:P, pipe:P, warp_rows or twopass
  */
 typedef struct {

@@ -256,3 +256,26 @@ def test_four_ctas_per_sm(w, sizes):
         p = C.credit_plan_tail(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, sizes[0], 4)
         check(w, run(w, inp, p), inp)
         assert C.credit_get_device_error(dev) == C.OK
+
+
+SMALL = [
+    # 128-thread CTAs staging the length for ten CTAs per SM (the tuner's
+    # small-CTA form for the operators with the 64-register instantiation)
+    (wl.LAYERNORM_BF16_1024x262144.with_rows(5), [8, 4, 12]),
+    (wl.sweep_point(1 << 19).with_rows(3), [8, 16]),
+    (_custom(wl.LAYERNORM, "bf16", 3, 200008, 80, x_mean=0.3, x_std=1.7, eps=1e-5,
+             param_dtype="f32"), [5, 7]),
+]
+
+
+@pytest.mark.parametrize("w,sizes", SMALL, ids=[c[0].name for c in SMALL])
+def test_small_ctas(w, sizes):
+    inp = w.generate()
+    dev = torch.cuda.current_device()
+    for P in sizes:
+        t10 = C.credit_plan_tail(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, P, 10)
+        p = C.credit_plan_with(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.CLUSTER, P,
+                               threads=128, staged_elems=int(t10.staged_elems))
+        assert p.threads == 128 and p.staged_elems < p.slice_elems, (P, p)
+        check(w, run(w, inp, p), inp)
+        check(w, run(w, inp, p, in_place=True), inp)
