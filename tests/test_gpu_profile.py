@@ -81,9 +81,12 @@ def test_force_switch():
     assert got["variant"] == C.CLUSTER and got["cluster_size"] == 12
     got = _child({"CREDIT_FORCE": "cluster:10:s36864"})
     assert got["cluster_size"] == 10 and got["staged_elems"] == 36864
+    got = _child({"CREDIT_FORCE": "cluster:12:s8192:t128"})
+    assert got["cluster_size"] == 12 and got["staged_elems"] == 8192 and got["threads"] == 128
     got = _child({"CREDIT_FORCE": "twopass"})
     assert got["variant"] == C.TWO_PASS
     # illegal for this shape (a 1.5 MB row in one CTA) or malformed: ignored
     plain = _child({})
     assert _child({"CREDIT_FORCE": "cluster:1"}) == plain
     assert _child({"CREDIT_FORCE": "cluster:banana"}) == plain
+    assert _child({"CREDIT_FORCE": "cluster:12:s8192:t100"}) == plain  # not whole warps
