@@ -301,6 +301,26 @@ def run_reference(args, w, rank: int):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ plans
+def parse_variant(spec: str) -> dict:
+    """kind:P[xR][:sSTAGED][:tTHREADS] (the plan names variant_name prints)
+    -> {kind, P, R, staged, threads}; 0 leaves a field to the planner."""
+    kind, rest = spec.split(":", 1)
+    if kind not in ("cluster", "persist", "pipe"):
+        raise ValueError(f"unknown plan kind in {spec!r}")
+    head, *opts = rest.split(":")
+    P, R = (head.split("x") + ["0"])[:2] if "x" in head else (head, "0")
+    out = {"kind": kind, "P": int(P), "R": int(R), "staged": 0, "threads": 0}
+    for q in opts:
+        if q.startswith("s"):
+            out["staged"] = int(q[1:])
+        elif q.startswith("t"):
+            out["threads"] = int(q[1:])
+        elif q != "barrier":
+            raise ValueError(f"unknown plan option {q!r} in {spec!r}")
+    return out
+
+
 # ------------------------------------------------------------ ranks
 def max_over_ranks(x: float, world: int, device) -> float:
     """The largest of every rank's `x` (every rank calls this)."""
@@ -407,16 +427,12 @@ def main():
     elif args.variant == "warp_rows":
         plan = C.credit_plan_for(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, C.WARP_ROWS, 1)
     else:
-        kind, P, *rest = args.variant.split(":")
-        R = 0
-        if "x" in P:
-            P, R = P.split("x")
-        staged = next((int(q[1:]) for q in rest if q.startswith("s")), 0)
-        threads = next((int(q[1:]) for q in rest if q.startswith("t")), 0)
+        v = parse_variant(args.variant)
         var = {"cluster": C.CLUSTER, "persist": C.CLUSTER_PERSISTENT,
-               "pipe": C.CLUSTER_PIPELINED}[kind]
-        plan = C.credit_plan_with(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, var, int(P),
-                                  threads=threads, rows_per_cluster=int(R), staged_elems=staged)
+               "pipe": C.CLUSTER_PIPELINED}[v["kind"]]
+        plan = C.credit_plan_with(OPS[w.op], w.rows, w.cols, DT[w.dtype], dev, var, v["P"],
+                                  threads=v["threads"], rows_per_cluster=v["R"],
+                                  staged_elems=v["staged"])
     if args.cps:
         plan.ctas_per_sm = args.cps
         plan = C.Plan.from_buffer_copy(plan)

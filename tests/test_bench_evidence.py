@@ -53,3 +53,30 @@ def test_peak_from_the_measured_file_else_the_fallback(tmp_path, monkeypatch):
 def test_job_rate_uses_the_slowest_rank():
     # 2 ranks, 1 GB each per step, the slowest rank 2 ms per step: 1000 GB/s
     assert abs(bench.job_rate(1e9, 2.0, 2) - 1000.0) < 1e-9
+
+
+def test_plan_names_round_trip():
+    # the names the library's plans print are the names --variant accepts
+    from dsmem_thread_block_gb300 import _credit as C
+    p = C.Plan(variant=C.CLUSTER, cluster_size=8, threads=128, slice_elems=32768,
+               staged_elems=9728, rows_per_cluster=1)
+    assert C.variant_name(p) == "cluster:8:s9728:t128"
+    assert bench.parse_variant(C.variant_name(p)) == {
+        "kind": "cluster", "P": 8, "R": 0, "staged": 9728, "threads": 128}
+    p = C.Plan(variant=C.CLUSTER, cluster_size=12, threads=256, slice_elems=65536,
+               staged_elems=37376, rows_per_cluster=1)
+    assert C.variant_name(p) == "cluster:12:s37376"
+    p = C.Plan(variant=C.CLUSTER, cluster_size=8, threads=256, slice_elems=32768,
+               staged_elems=18432, rows_per_cluster=2)
+    assert bench.parse_variant(C.variant_name(p)) == {
+        "kind": "cluster", "P": 8, "R": 2, "staged": 18432, "threads": 0}
+    p = C.Plan(variant=C.CLUSTER, cluster_size=8, threads=128, slice_elems=16384,
+               staged_elems=16384, rows_per_cluster=1)
+    assert C.variant_name(p) == "cluster:8"  # whole slice staged: the threads are the planner's
+    assert bench.parse_variant("persist:9")["kind"] == "persist"
+    for bad in ("cluster:8:q5", "warp:3"):
+        try:
+            bench.parse_variant(bad)
+        except ValueError:
+            continue
+        raise AssertionError(bad)
