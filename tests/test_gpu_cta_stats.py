@@ -7,7 +7,8 @@ the output is only consistent across a row's slices if every CTA ends up
 with the same bits.  The checked build records, for each row and each rank,
 the combined statistics that CTA holds (credit_debug_stats).  For cluster
 sizes 2, 3 (unequal slices), 8 and 16, both exchanges, one and two rows per
-cluster, L2-tail plans, the persistent ring and the warp-specialised kernel, every
+cluster, L2-tail plans (also with small 128-thread CTAs), the persistent ring
+and the warp-specialised kernel, every
 operator: the P records of a row are bit-identical, no other rank wrote one,
 and the statistics match the oracle's fp64 values of the same row (max and
 absmax exactly).
@@ -64,6 +65,10 @@ def _plans(w, P):
             half = max(vec, out[-1][1].slice_elems // 2 // vec * vec)
             add(f"tail:{name}", C.CLUSTER, exchange=xc, staged_elems=half)
             add(f"tail2:{name}", C.CLUSTER, exchange=xc, staged_elems=half, rows_per_cluster=2)
+            # small CTAs with a long tail (the 64-register instantiation for
+            # bf16 softmax and LayerNorm)
+            add(f"small:{name}", C.CLUSTER, exchange=xc,
+                staged_elems=max(vec, half // 2 // vec * vec), threads=128)
         if w.op != wl.PEARSON:
             add(f"cluster2:{name}", C.CLUSTER, exchange=xc, rows_per_cluster=2)
         if w.op in RING_OPS:
