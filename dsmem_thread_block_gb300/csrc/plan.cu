@@ -77,6 +77,10 @@ int64_t tail_budget_bytes(const DevInfo& d, int static_smem, int cps) {
     return per_cta / kb * kb - (static_smem + kb - 1) / kb * kb - kb;
 }
 
+int64_t cluster_slice(int64_t cols, int P, int es) {
+    return round_up(ceil_div(cols, P), 128 / es);
+}
+
 int64_t tail_staged_for(int dev, credit_op_t op, int64_t cols, credit_dtype_t dtype, int P,
                         int cps, int rows_per_cluster) {
     const int es = dtype == CREDIT_F32 ? 4 : 2;
@@ -89,7 +93,7 @@ int64_t tail_staged_for(int dev, credit_op_t op, int64_t cols, credit_dtype_t dt
     const KernelInfo* ki = d ? kernel_info(dev, fn, true) : nullptr;
     if (!ki) return 0;
     const int64_t vec = 16 / es;
-    const int64_t slice = round_up(ceil_div(cols, P), vec);
+    const int64_t slice = cluster_slice(cols, P, es);
     const int64_t budget = std::min<int64_t>(tail_budget_bytes(*d, ki->static_smem, cps),
                                              ki->max_dyn_smem);
     // one row: whole 16-byte vectors; several rows: each staged slice
@@ -217,7 +221,7 @@ credit_status_t make_plan(int dev, credit_op_t op, int64_t rows, int64_t cols,
         const bool two_ops = op == CREDIT_PEARSON;
         if (two_ops && R != 1) return CREDIT_ERR_INVALID_ARG;
         const int staged = two_ops ? 2 : R;  // slices held per CTA
-        const int64_t slice = round_up(ceil_div(cols, P), vec);
+        const int64_t slice = cluster_slice(cols, P, es);
         // an L2 tail: stage only the first `held` elements of each row's
         // slice (operators without an in-place stash pass)
         int64_t held = slice;

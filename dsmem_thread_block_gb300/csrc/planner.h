@@ -64,6 +64,13 @@ bool deep_footprint(int dev, KernelKey k, int64_t smem_bytes);
 // four-CTA instantiation?  Then it takes that instantiation.
 bool quad_footprint(int dev, KernelKey k, int64_t smem_bytes, bool tail);
 
+// Columns of one CTA's slice of a row split over P CTAs of the
+// one-row-per-cluster kernel: whole 128-byte lines, so that no two CTAs share
+// a line of the row and each slice's bulk copies start on a line boundary
+// (when the row does).  The last CTA takes the remainder; trailing CTAs may
+// be empty.
+int64_t cluster_slice(int64_t cols, int P, int es);
+
 // Staged elements per row of an L2-tail plan of cluster size P with
 // rows_per_cluster rows per cluster that lets `cps` CTAs share an SM, or 0
 // when the operator has no L2-tail form or the whole slice already fits.
